@@ -1,0 +1,224 @@
+"""TurboQuant-MSE 3-bit ("TQ3") value quantisation (oracle).
+
+Source: "F5 M6 — PolyKV (shared compressed KV pool)":
+  * section "What PolyKV is (reference)": V is quantised by a fast Walsh-Hadamard
+    rotation that spreads outlier energy over the dimensions, followed by an MSE-optimal
+    Lloyd-Max quantiser;
+  * section "S2 — TurboQuant tier family": one rotation + codebook scheme,
+    parameterised by bit width;
+  * section "Phase-0 fork recon": the 3-bit block stores an fp16 norm, a 2-bit plane
+    and a 1-bit plane, and the rotation seed is 42;
+  * section "S2 perf-path Level B": the cache is read as centroid x norm in the rotated
+    domain, and the output is inverse-rotated once (Parseval keeps dot products);
+  * the bits-per-value table of section "S2 tier-family overview" (turbo3 at 0.391
+    bytes per value).
+The problem statement fixes the remaining steps: per-vector L2 norm, seeded +-1 sign
+diagonal, orthonormal FWHT over head_dim, 8-level Lloyd-Max codebook fixed by the build.
+
+Readings taken (each one is a choice the pages leave open):
+  * Transform: R = H diag(s) / sqrt(D) with H the unnormalised Sylvester-Hadamard
+    matrix over the whole head_dim (one sign vector, shared by every layer and head
+    of a given D).  The pages' 128-wide block-diagonal and two-sign variants are not
+    used.
+  * Normalisation: z = H (s * x) / ||x||, so that ||z||^2 = D and each coordinate has
+    unit variance; z is quantised with the Gaussian N(0,1) Lloyd-Max codebook.
+  * Codebook: the 8-level Lloyd-Max quantiser of N(0,1), solved in float64, with each
+    level then rounded to the nearest fp16 value (so that the levels are exact in the
+    half-precision tensor-core operands of the read path); the thresholds are the exact
+    midpoints of adjacent rounded levels.  The codebook is symmetric.
+  * Code of a coordinate: k = number of thresholds t_m with z >= t_m (ties go up).
+    Stored as a sign plane hi = (k >= 4) and a magnitude plane lo = k - 4 if hi else
+    3 - k, so level = (+1 if hi else -1) * |c|[lo].
+  * Norm: the plain L2 norm (the pages' "corrected norm" is not specified), stored as
+    fp16; decode is x_hat = (n16 / D) * s * (H c[k]).
+  * Encoder arithmetic is IEEE float32 in a fixed order: squares x_i * x_i, then a
+    halving fold (for h = D/2, ..., 1: t[i] += t[i + h]); n = sqrt(t[0]) correctly
+    rounded; the FWHT butterflies (a, b) -> (a + b, a - b) over stages h = 1, 2, ...,
+    D/2; z_i = u_i / n correctly rounded.  A zero row stores all-zero planes and a zero
+    norm.
+  * Bit order: element i lives in byte i // 4, bits 2 (i % 4) .. 2 (i % 4) + 1 of the
+    2-bit plane and in byte i // 8, bit i % 8 of the 1-bit plane.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import ndtr
+
+LEVELS = 8
+
+
+def _phi(x):
+    return np.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)
+
+
+def lloyd_max_gaussian(levels: int = LEVELS, tol: float = 1e-14, max_iter: int = 100000):
+    """Lloyd iteration for the MSE-optimal scalar quantiser of N(0, 1), in float64.
+
+    Alternates the two optimality conditions until the levels move by less than
+    ``tol``: thresholds at midpoints of adjacent levels, and each level at the
+    conditional mean of its cell, (phi(a) - phi(b)) / (Phi(b) - Phi(a)).
+    Returns ``(levels [L], thresholds [L - 1])`` in float64, ascending.
+    """
+    c = np.linspace(-2.0, 2.0, levels)
+    for _ in range(max_iter):
+        t = 0.5 * (c[:-1] + c[1:])
+        a = np.concatenate([[-np.inf], t])
+        b = np.concatenate([t, [np.inf]])
+        pa = np.where(np.isinf(a), 0.0, _phi(np.where(np.isinf(a), 0.0, a)))
+        pb = np.where(np.isinf(b), 0.0, _phi(np.where(np.isinf(b), 0.0, b)))
+        mass = ndtr(b) - ndtr(a)
+        c_new = (pa - pb) / mass
+        if np.max(np.abs(c_new - c)) < tol:
+            c = c_new
+            break
+        c = c_new
+    t = 0.5 * (c[:-1] + c[1:])
+    return c, t
+
+
+def gaussian_mse(levels: np.ndarray, thresholds: np.ndarray) -> float:
+    """Mean squared error of a scalar quantiser on N(0,1), by numerical integration."""
+    edges = np.concatenate([[-12.0], np.asarray(thresholds, dtype=np.float64), [12.0]])
+    total = 0.0
+    for k, c in enumerate(np.asarray(levels, dtype=np.float64)):
+        x = np.linspace(edges[k], edges[k + 1], 200001)
+        y = (x - c) ** 2 * _phi(x)
+        total += float(np.trapezoid(y, x))
+    return total
+
+
+def codebook():
+    """The build's fixed TQ3 codebook.
+
+    Returns ``(levels float32 [8], thresholds float32 [7])``: Lloyd-Max levels of
+    N(0,1) rounded to fp16 (held as float32), made exactly symmetric, and the exact
+    midpoints between adjacent levels.
+    """
+    c, _ = lloyd_max_gaussian(LEVELS)
+    pos = np.abs(c[LEVELS // 2:]).astype(np.float16).astype(np.float32)
+    levels = np.concatenate([-pos[::-1], pos]).astype(np.float32)
+    thresholds = ((levels[:-1] + levels[1:]) / np.float32(2.0)).astype(np.float32)
+    return levels, thresholds
+
+
+def signs_from_words(words, d: int) -> np.ndarray:
+    """Unpack the sign diagonal: bit i of word i // 32 set means s_i = -1 (float64)."""
+    w = [int(x) & 0xFFFFFFFF for x in np.asarray(words).reshape(-1).tolist()]
+    s = np.ones(d, dtype=np.float64)
+    for i in range(d):
+        if (w[i // 32] >> (i % 32)) & 1:
+            s[i] = -1.0
+    return s
+
+
+def fwht(x: np.ndarray, dtype=np.float64) -> np.ndarray:
+    """Unnormalised fast Walsh-Hadamard transform over the last axis.
+
+    Stages h = 1, 2, 4, ..., D/2; at each stage every pair (i, i + h) with i & h == 0
+    becomes (a + b, a - b), each result rounded to ``dtype``.
+    """
+    y = np.array(x, dtype=dtype, copy=True)
+    d = y.shape[-1]
+    if d & (d - 1):
+        raise ValueError("length must be a power of two")
+    lead = y.shape[:-1]
+    h = 1
+    while h < d:
+        z = y.reshape(lead + (d // (2 * h), 2, h))
+        a = z[..., 0, :]
+        b = z[..., 1, :]
+        s = (a + b).astype(dtype)
+        t = (a - b).astype(dtype)
+        y = np.stack([s, t], axis=-2).reshape(lead + (d,))
+        h *= 2
+    return y
+
+
+def _fold_sum_sq_f32(x32: np.ndarray) -> np.ndarray:
+    """Sum of squares by a halving fold: for h = D/2 .. 1, t[i] += t[i + h] (float32)."""
+    t = (x32 * x32).astype(np.float32)
+    d = t.shape[-1]
+    h = d // 2
+    while h >= 1:
+        t = (t[..., :h] + t[..., h:2 * h]).astype(np.float32)
+        h //= 2
+    return t[..., 0]
+
+
+def encode(x: np.ndarray, sign_words):
+    """Quantise fp16 rows ``x[..., D]``.
+
+    Returns ``(lo2 uint8 [..., D/4], hi1 uint8 [..., D/8], norms float16 [...])``.
+    """
+    x = np.asarray(x)
+    if x.dtype != np.float16:
+        raise TypeError("TQ3 input must be float16")
+    d = x.shape[-1]
+    if d % 32 or d & (d - 1):
+        raise ValueError("head_dim must be a power of two and a multiple of 32")
+    levels, thresholds = codebook()
+    s = signs_from_words(sign_words, d).astype(np.float32)
+    x32 = x.astype(np.float32)
+    nsq = _fold_sum_sq_f32(x32)
+    n = np.sqrt(nsq).astype(np.float32)  # correctly rounded
+    u = fwht((x32 * s).astype(np.float32), dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        z = (u / n[..., None]).astype(np.float32)
+    k = np.zeros(z.shape, dtype=np.int64)
+    for t in thresholds:
+        k += (z >= t).astype(np.int64)
+    zero = (n == 0)[..., None]
+    hi = k >= 4
+    lo = np.where(hi, k - 4, 3 - k)
+    hi = np.where(zero, False, hi)
+    lo = np.where(zero, 0, lo)
+    lo2 = pack_bits(lo.astype(np.uint8), 2)
+    hi1 = pack_bits(hi.astype(np.uint8), 1)
+    norms = n.astype(np.float16)
+    return lo2, hi1, norms
+
+
+def pack_bits(vals: np.ndarray, width: int) -> np.ndarray:
+    """Pack small unsigned fields little-endian: element i at bit width * i of the row."""
+    per = 8 // width
+    d = vals.shape[-1]
+    v = vals.reshape(vals.shape[:-1] + (d // per, per)).astype(np.uint32)
+    out = np.zeros(v.shape[:-1], dtype=np.uint32)
+    for j in range(per):
+        out |= v[..., j] << (width * j)
+    return out.astype(np.uint8)
+
+
+def unpack_bits(packed: np.ndarray, width: int, d: int) -> np.ndarray:
+    per = 8 // width
+    p = np.asarray(packed).astype(np.uint32)
+    mask = (1 << width) - 1
+    parts = [(p >> (width * j)) & mask for j in range(per)]
+    v = np.stack(parts, axis=-1)
+    return v.reshape(p.shape[:-1] + (d,)).astype(np.uint8)
+
+
+def codes_from_planes(lo2: np.ndarray, hi1: np.ndarray, d: int) -> np.ndarray:
+    """Level index k in 0..7 from the two planes."""
+    lo = unpack_bits(lo2, 2, d).astype(np.int64)
+    hi = unpack_bits(hi1, 1, d).astype(np.int64)
+    return np.where(hi == 1, 4 + lo, 3 - lo)
+
+
+def decode(lo2, hi1, norms, sign_words, d: int) -> np.ndarray:
+    """Dequantise to float64: x_hat = (n16 / D) * s * (H c[k])."""
+    levels, _ = codebook()
+    k = codes_from_planes(lo2, hi1, d)
+    ck = levels.astype(np.float64)[k]
+    s = signs_from_words(sign_words, d)
+    hc = fwht(ck, dtype=np.float64)
+    n = np.asarray(norms).astype(np.float64)[..., None]
+    return (n / d) * s * hc
+
+
+def bytes_per_value(d: int) -> float:
+    """Storage per value: 2-bit plane + 1-bit plane + one fp16 norm per vector."""
+    return (d // 4 + d // 8 + 2) / d

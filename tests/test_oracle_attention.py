@@ -1,0 +1,161 @@
+"""Pins of the attention / split / combine oracle: closed forms, library routines,
+brute force and the split identity."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import logsumexp
+
+from oracle import attention as att
+from oracle import pipeline
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def test_single_key_closed_form():
+    rng = np.random.default_rng(0)
+    q, k, v = _rand(rng, 3, 16), _rand(rng, 1, 16), _rand(rng, 1, 16)
+    o, lse = att.attend(q, k, v, 0.25)
+    assert np.allclose(o, np.repeat(v, 3, 0), atol=0)
+    assert np.allclose(lse, 0.25 * (q @ k[0]), atol=1e-15)
+
+
+def test_identical_keys_give_mean_and_log_n():
+    rng = np.random.default_rng(1)
+    n = 37
+    q = _rand(rng, 2, 8)
+    k = np.repeat(_rand(rng, 1, 8), n, 0)
+    v = _rand(rng, n, 8)
+    o, lse = att.attend(q, k, v, 0.5)
+    assert np.allclose(o, np.repeat(v.mean(0, keepdims=True), 2, 0), atol=1e-14)
+    assert np.allclose(lse, 0.5 * (q @ k[0]) + math.log(n), atol=1e-13)
+
+
+def test_zero_query_is_uniform():
+    rng = np.random.default_rng(2)
+    k, v = _rand(rng, 50, 8), _rand(rng, 50, 8)
+    o, lse = att.attend(np.zeros((1, 8)), k, v, 1.0)
+    assert np.allclose(o[0], v.mean(0), atol=1e-14) and np.isclose(lse[0], math.log(50))
+
+
+def test_empty_part():
+    o, lse = att.attend(np.ones((2, 4)), np.zeros((0, 4)), np.zeros((0, 4)), 1.0)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def test_gqa_decode_matches_torch_sdpa_and_scipy_logsumexp():
+    rng = np.random.default_rng(3)
+    hq, hkv, n, d = 8, 2, 70, 32
+    q = _rand(rng, 1, hq, d)
+    k = _rand(rng, n, hkv, d)
+    v = _rand(rng, n, hkv, d)
+    scale = 1 / math.sqrt(d)
+    o, lse = att.gqa_decode(q, k, v, scale)
+    tq = torch.tensor(q).unsqueeze(2)  # [1, hq, 1, d]
+    tk = torch.tensor(k).permute(1, 0, 2).unsqueeze(0)  # [1, hkv, n, d]
+    tv = torch.tensor(v).permute(1, 0, 2).unsqueeze(0)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale, enable_gqa=True)
+    assert np.allclose(o, ref[:, :, 0, :].numpy(), atol=1e-13)
+    g = hq // hkv
+    for h in range(hq):
+        logit = np.einsum("d,nd->n", q[0, h], k[:, h // g]) * scale
+        assert np.isclose(lse[0, h], logsumexp(logit), atol=1e-13)
+
+
+def test_gqa_group_mapping():
+    hq, hkv, n, d = 8, 4, 5, 4
+    q = np.ones((1, hq, d))
+    k = np.zeros((n, hkv, d))
+    v = np.zeros((n, hkv, d))
+    for h in range(hkv):
+        v[:, h, :] = h
+    o, _ = att.gqa_decode(q, k, v, 1.0)
+    assert np.array_equal(o[0, :, 0], np.array([h // 2 for h in range(hq)], dtype=float))
+
+
+@pytest.mark.parametrize("softcap", [0.0, 2.0])
+def test_split_equals_unsplit_for_every_window(softcap):
+    rng = np.random.default_rng(4)
+    n, d = 48, 16
+    q = _rand(rng, 1, 4, d) * 2
+    k = _rand(rng, n, 2, d)
+    v = _rand(rng, n, 2, d)
+    ref_o, ref_l = att.gqa_decode(q, k, v, 0.3, softcap)
+    for wc in range(0, n + 1):
+        tiles = [(a, min(a + 7, n)) for a in range(wc, n, 7)] or [(n, n)]
+        o, l = att.split_decode(q, k, v, wc, 0.3, softcap, tail_tiles=tiles)
+        assert np.allclose(o, ref_o, atol=1e-13) and np.allclose(l, ref_l, atol=1e-13), wc
+
+
+@pytest.mark.parametrize("softcap", [0.0, 1.5])
+def test_brute_force_loops(softcap):
+    rng = np.random.default_rng(5)
+    for n in range(1, 17):
+        q, k, v = _rand(rng, 3, 6) * 3, _rand(rng, n, 6), _rand(rng, n, 5)
+        o1, l1 = att.attend(q, k, v, 0.7, softcap)
+        o2, l2 = att.attend_loops(q, k, v, 0.7, softcap)
+        assert np.allclose(o1, o2, atol=1e-12) and np.allclose(l1, l2, atol=1e-12)
+
+
+def test_softcap_bounds_limit_and_order():
+    rng = np.random.default_rng(6)
+    q, k, v = _rand(rng, 2, 8) * 10, _rand(rng, 30, 8) * 10, _rand(rng, 30, 8)
+    s = att.logits(q, k, 1.0, 5.0)
+    assert np.all(np.abs(s) <= 5.0) and np.max(np.abs(q @ k.T)) > 50.0
+    o_inf, l_inf = att.attend(q, k, v, 1.0, 1e9)
+    o_raw, l_raw = att.attend(q, k, v, 1.0, 0.0)
+    assert np.allclose(o_inf, o_raw, atol=1e-9) and np.allclose(l_inf, l_raw, atol=1e-6)
+    # capping the logits before the softmax is not the same as not capping them
+    o_cap, l_cap = att.attend(q, k, v, 1.0, 5.0)
+    assert np.max(np.abs(o_cap - o_raw)) > 1e-2
+    # the capped result equals a softmax over explicitly capped logits
+    capped = 5.0 * np.tanh((q @ k.T) / 5.0)
+    w = np.exp(capped - capped.max(1, keepdims=True))
+    assert np.allclose(o_cap, (w @ v) / w.sum(1, keepdims=True), atol=1e-13)
+    assert np.allclose(l_cap, logsumexp(capped, axis=1), atol=1e-13)
+
+
+def test_combine_identities():
+    rng = np.random.default_rng(7)
+    o = _rand(rng, 5, 3, 4)
+    l = _rand(rng, 5, 3)
+    l[2, 1] = -np.inf
+    o_all, l_all = att.lse_combine(o, l)
+    # nested combination equals one combination
+    a = att.lse_combine(o[:2], l[:2])
+    b = att.lse_combine(o[2:], l[2:])
+    o_n, l_n = att.lse_combine(np.stack([a[0], b[0]]), np.stack([a[1], b[1]]))
+    assert np.allclose(o_all, o_n, atol=1e-14) and np.allclose(l_all, l_n, atol=1e-14)
+    # a single part is returned unchanged; all-empty gives O = 0, lse = -inf
+    o1, l1 = att.lse_combine(o[:1], l[:1])
+    assert np.allclose(o1, o[0]) and np.allclose(l1, l[0])
+    oe, le = att.lse_combine(np.zeros((3, 2, 4)), np.full((3, 2), -np.inf))
+    assert np.all(oe == 0) and np.all(np.isneginf(le))
+    # weights are softmax(lse): compare with scipy
+    w = np.exp(l - logsumexp(l, axis=0))
+    assert np.allclose(o_all, np.einsum("pr,prd->rd", w, o), atol=1e-14)
+    assert np.allclose(l_all, logsumexp(l, axis=0), atol=1e-14)
+
+
+def test_fanout_reference_equals_prefix_suffix_split():
+    rng = np.random.default_rng(8)
+    a_n, hq, hkv, d, p, s = 3, 4, 2, 32, 40, 9
+    q16 = rng.standard_normal((a_n, hq, d)).astype(np.float16)
+    pk = rng.standard_normal((p, hkv, d)).astype(np.float16)
+    pv = rng.standard_normal((p, hkv, d)).astype(np.float16)
+    sk = rng.standard_normal((a_n, s, hkv, d)).astype(np.float16)
+    sv = rng.standard_normal((a_n, s, hkv, d)).astype(np.float16)
+    words = np.array([0x12345678], dtype=np.int64)
+    o, l = pipeline.fanout_reference(q16, pk, pv, sk, sv, "q8_0", "tq3", 0.2, 0.0, words)
+    kp = pipeline.dequant("q8_0", pk)
+    vp = pipeline.dequant("tq3", pv, words)
+    pre = att.gqa_decode(q16.astype(np.float64), kp, vp, 0.2)
+    for a in range(a_n):
+        suf = att.gqa_decode(q16[a:a + 1].astype(np.float64), sk[a].astype(np.float64),
+                             sv[a].astype(np.float64), 0.2)
+        oc, lc = att.lse_combine(np.stack([pre[0][a:a + 1], suf[0]]), np.stack([pre[1][a:a + 1], suf[1]]))
+        assert np.allclose(oc[0], o[a], atol=1e-13) and np.allclose(lc[0], l[a], atol=1e-13)

@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark of one position-split decode step (window + tail ring + LSE combine).
+
+A step is one pass of the whole hot path over every layer of the workload: the
+quantised-KV decode attention of the device window, the tail streamed from pinned
+host memory through the prefetch ring, and the per-layer LSE combine.  The default
+workload is the Qwen2.5-14B-like layer stack (48 layers, 40 q / 8 KV heads, head_dim
+128, n_kv 65536, window 32768, fp16 K with 4 outlier channels per head, 3-slot ring).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn effective KV GB/s & % HBM peak; tail-hidden step ms vs max(compute,DMA)"
+UNIT = "GB/s"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="qwen14b_f16")
+    ap.add_argument("--cpu-layers", type=int, default=0, help="layers in the oracle sample (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------------
+def time_oracle(cfg, n_layers: int):
+    """Time the oracle's layer computation on ``n_layers`` layers of ``cfg`` (CPU).
+
+    Returns (KV bytes processed, seconds, sample description).  The bytes are the
+    stored KV planes of those layers, the same unit as the GPU figure."""
+    import numpy as np
+
+    import synth
+    from oracle import pipeline
+
+    signs = synth.sign_bits(cfg.d, cfg.sign_seed).numpy()
+    nbytes = 0
+    elapsed = 0.0
+    for layer in range(n_layers):
+        q = synth.query_f16(cfg, layer).numpy()
+        k = synth.kv_f16(cfg, layer, "k", cfg.n_kv).numpy()
+        v = synth.kv_f16(cfg, layer, "v", cfg.n_kv).numpy()
+        t0 = time.perf_counter()
+        pipeline.layer_reference(q, k, v, cfg.k_fmt, cfg.v_fmt, cfg.scale, cfg.softcap, signs)
+        elapsed += time.perf_counter() - t0
+        for fmt, x in ((cfg.k_fmt, k), (cfg.v_fmt, v)):
+            nbytes += sum(p.nbytes for p in pipeline.encode(fmt, x[:1], signs)) * x.shape[0]
+        del q, k, v
+    sample = (f"{n_layers} of {cfg.layers} layers of {cfg.name}, all {cfg.hq} query heads over all "
+              f"{cfg.n_kv} positions (window + tail), float64")
+    return nbytes, elapsed, sample
+
+
+def oracle_layers_for(cfg, requested: int) -> int:
+    if requested > 0:
+        return min(requested, cfg.layers)
+    return min(cfg.layers, 4 if cfg.d <= 128 else 1)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import synth
+
+    cfg = synth.by_name(args.config)
+    steps = max(1, args.steps)
+    layers = oracle_layers_for(cfg, args.cpu_layers)
+    for _ in range(max(0, min(args.warmup, 1))):
+        time_oracle(cfg, 1)
+    total_b, total_s = 0, 0.0
+    sample = ""
+    for _ in range(steps):
+        b, s, sample = time_oracle(cfg, layers)
+        total_b += b
+        total_s += s
+    value = total_b / total_s / 1e9
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total_s / steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), outlier K channels)",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "hq": cfg.hq, "hkv": cfg.hkv, "d": cfg.d,
+                   "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt, "v_fmt": cfg.v_fmt},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": sample + f", per step; CPU {cpu_model()}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.path = tempfile.mktemp(prefix="qps_clocks_", suffix=".csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------
+# measured peaks and committed ncu traffic
+# ---------------------------------------------------------------------------------
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def attention_source_sha():
+    csrc = os.path.join(ROOT, "quantized_position_split_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("attn") or name.endswith((".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    path = os.path.join(ROOT, "profiles", f"attn_window_{workload}_traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if j.get("kernel_source_sha") != attention_source_sha():
+        return None  # counters were taken on another version of the kernel
+    return j.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------------
+def measure_link(torch, device, nbytes=1 << 30):
+    """Pinned host -> device copy bandwidth (one 1 GiB cudaMemcpyAsync, best of 3), and
+    a single-thread host memcpy of the same size."""
+    import numpy as np
+
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s = torch.cuda.current_stream()
+    best = 0.0
+    for _ in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        dst.copy_(src, non_blocking=True)
+        e1.record(s)
+        e1.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    a = np.ones(nbytes // 4, dtype=np.float32)
+    b = np.empty_like(a)
+    t0 = time.perf_counter()
+    np.copyto(b, a)
+    host = a.nbytes / (time.perf_counter() - t0) / 1e9
+    del src, dst, a, b
+    return best, host
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+
+    import synth
+    import quantized_position_split_gb300 as qps
+    from quantized_position_split_gb300 import build as qbuild
+    from quantized_position_split_gb300.decode import PositionSplitDecoder
+
+    qbuild.build()
+    cfg = synth.by_name(args.config)
+    if cfg.kind != "split":
+        raise SystemExit("bench.py times the position-split workloads")
+    signs = synth.sign_bits(cfg.d, cfg.sign_seed)
+    dec = PositionSplitDecoder(layers=cfg.layers, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
+                               n_kv=cfg.n_kv, wc=cfg.wc, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
+                               scale=cfg.scale, softcap=cfg.softcap, signs=signs,
+                               ring_slots=cfg.ring_slots, tile_tokens=cfg.tile_tokens, device=device)
+    for layer in range(cfg.layers):
+        q = synth.query_f16(cfg, layer, device=device)
+        k = synth.kv_f16(cfg, layer, "k", cfg.n_kv, device=device)
+        v = synth.kv_f16(cfg, layer, "v", cfg.n_kv, device=device)
+        dec.load_layer(layer, k, v, q)
+        del q, k, v
+    dec.build()
+    torch.cuda.synchronize()
+
+    link_gbs, host_memcpy_gbs = measure_link(torch, device)
+    stream = torch.cuda.current_stream()
+    window_bytes = dec.window_bytes()
+    tail_bytes = dec.tail_bytes()
+    kv_bytes = window_bytes + tail_bytes
+
+    # per-layer timing events around the window part, one pair per (step, layer)
+    K, W, L = args.steps, args.warmup, cfg.layers
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(K)]
+    for row in ev:
+        for a, b in row:
+            a.record(stream)
+            b.record(stream)
+
+    def set_events(step_events):
+        for layer in range(L):
+            pe = dec.plan.layers[layer].part_events
+            if step_events is None:
+                pe[0] = pe[1] = None
+            else:
+                pe[0], pe[1] = step_events[layer][0].cuda_event, step_events[layer][1].cuda_event
+
+    set_events(None)
+    for _ in range(W):
+        dec.step(stream)
+    # window-only steps (ring and tail omitted) for the step criterion
+    for _ in range(2):
+        dec.window_step(stream)
+    torch.cuda.synchronize()
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for _ in range(K):
+        dec.window_step(stream)
+    w1.record(stream)
+    torch.cuda.synchronize()
+    window_step_ms = w0.elapsed_time(w1) / K
+
+    # the timed region
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    qps.launch_count(reset=True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        set_events(ev[i])
+        dec.step(stream)
+    t1.record(stream)
+    launches = qps.launch_count()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    set_events(None)
+    step_ms = t0.elapsed_time(t1) / K
+    if world > 1:
+        tt = torch.tensor([step_ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    win_ms = [ev[i][layer][0].elapsed_time(ev[i][layer][1]) for i in range(K) for layer in range(L)]
+    win_launch_ms = statistics.mean(win_ms)
+
+    # end to end through the public API with host buffers: q in, (o, lse) out each step
+    q_host = torch.empty_like(dec.q, device="cpu").pin_memory()
+    q_host.copy_(dec.q.cpu())
+    o_host = torch.empty_like(dec.o, device="cpu").pin_memory()
+    lse_host = torch.empty_like(dec.lse, device="cpu").pin_memory()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        dec.q.copy_(q_host, non_blocking=True)
+        dec.step(stream)
+        o_host.copy_(dec.o, non_blocking=True)
+        lse_host.copy_(dec.lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    h2d = q_host.numel() * q_host.element_size()
+    d2h = o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size()
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    dec.ring.sync()
+
+    # roofline of the dominant kernel: the window decode-attention launch
+    per_launch_bytes = window_bytes / L
+    rows = cfg.batch * cfg.hq
+    n_split_w = qps.attn_plan(dec.window_args[0])[0]
+    q_bytes = rows * cfg.d * 2
+    part_bytes = n_split_w * rows * (cfg.d + 1) * 4
+    algo_bytes = per_launch_bytes + q_bytes + part_bytes
+    peak, peak_kind = measured_hbm_peak()
+    achieved = algo_bytes / (win_launch_ms / 1e3) / 1e9
+    tail_dma_ms = tail_bytes / (link_gbs * 1e9) * 1e3
+    bound_ms = max(window_step_ms, tail_dma_ms)
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        b, s, sample = time_oracle(cfg, oracle_layers_for(cfg, args.cpu_layers))
+        cpu = {"value": b / s / 1e9, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": sample + f"; CPU {cpu_model()}"}
+    value = world * kv_bytes / (step_ms / 1e3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16" if cfg.k_fmt == "f16" and cfg.v_fmt == "f16" else f"{cfg.k_fmt}/{cfg.v_fmt}",
+        "data": "synthetic (seeded N(0,1) fp16, 4 outlier K channels per head x20)",
+        "config": {"workload": cfg.name, "layers": cfg.layers, "batch": cfg.batch, "hq": cfg.hq,
+                   "hkv": cfg.hkv, "d": cfg.d, "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt,
+                   "v_fmt": cfg.v_fmt, "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
+                   "tile_tokens": cfg.tile_tokens, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" %
+                         (window_bytes / 1e9, tail_bytes / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": committed_traffic(cfg.name),
+                     "kernel": "window decode attention (one launch per layer)",
+                     "algorithmic_bytes_per_launch": algo_bytes, "launch_ms": win_launch_ms,
+                     "peak_source": peak_kind},
+        "step": {"ms": step_ms, "window_only_ms": window_step_ms, "tail_dma_ms": tail_dma_ms,
+                 "bound_ms": bound_ms, "ratio_to_bound": step_ms / bound_ms,
+                 "tail_stream_gbs": tail_bytes / (step_ms / 1e3) / 1e9,
+                 "link_probe_gbs": link_gbs, "host_memcpy_1thread_gbs": host_memcpy_gbs,
+                 "steps_per_s": 1000.0 / step_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * kv_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(out), flush=True)
+    dec.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,305 @@
+/*
+ * qps.h: C ABI of the position-split, quantised-KV decode-attention library.
+ *
+ * The library computes single-token decode attention over a KV cache that is split
+ * by key position into a device-resident window [0, wc) and a host-resident tail
+ * [wc, n_kv).  Each part runs a split-KV flash-decode that emits a normalised output
+ * and its log-sum-exp (LSE); the parts are merged by an LSE combine.  K and V may be
+ * stored compressed (K: q8_0; V: q8_0 or 3-bit TurboQuant-MSE) and are dequantised on
+ * read inside the attention loop.  The tail streams from pinned host memory through a
+ * ring of device staging slots filled on a copy stream.
+ *
+ * Sources (page title, section):
+ *   [RKV]  "F5 M7 — Rolling KV: position-windowed KV residency": header status block
+ *          (position split, LSE-emitting attention) and section "Implementation
+ *          decomposition, refined (S1 -> S2 -> S3)", item S2 (per-tile O_t, lse_t and
+ *          the f32 merge; a single tile is plain attention).
+ *   [RING] "Rolling-KV: step/graph-level tail prefetch (design)", section "The fix: a
+ *          persistent, step-spanning tail-prefetch ring" (B = 2..4 slots sized once,
+ *          a flat (layer, tile) schedule kept B ahead on a copy stream, copy_done /
+ *          compute_done events instead of a per-op barrier, pre-created events).
+ *   [POLY] "F5 M6 — PolyKV (shared compressed KV pool)": section "What PolyKV is
+ *          (reference)" (K int8 / V 3-bit TurboQuant-MSE), section "S1 — SharedKVPool"
+ *          (one prefix read by many agents), section "S2 perf-path Level B" (V read as
+ *          centroid x norm in the rotated domain, output inverse-rotated once).
+ *
+ * Conventions shared by every call:
+ *   - Every call returns a qps_status; qps_last_error() gives a thread-local message
+ *     for the last failing call on the calling thread.  No call aborts, throws across
+ *     the ABI, or traps on the device.
+ *   - Pointers are raw.  "device" pointers are CUDA device memory of the current
+ *     device (the caller owns them, e.g. PyTorch tensors); "host" pointers are host
+ *     memory read synchronously during the call; "pinned" pointers are page-locked
+ *     host memory (cudaHostAlloc / cudaHostRegister / torch pin_memory).
+ *   - `stream` arguments are cudaStream_t values passed as void*; NULL is the legacy
+ *     default stream.  Calls taking a stream only enqueue work on it and return
+ *     without waiting for the device, unless stated otherwise.
+ *   - fp16 data is IEEE binary16, stored as 2-byte little-endian values.
+ *   - A "row" is one stored vector of head_dim values: one (token, KV head) of a K or
+ *     V cache.  Views address rows by strides in rows; each storage plane has its own
+ *     bytes per row (below), so one row index addresses every plane of a format.
+ *   - Unsupported shapes or formats return QPS_ERR_UNSUPPORTED; there is no fallback
+ *     path of any kind.
+ *
+ * Storage formats (bytes per row for head_dim D):
+ *   QPS_FMT_F16   data: D fp16 values (2D bytes).
+ *   QPS_FMT_Q8_0  data: D int8 codes (D bytes); aux: D/32 fp16 scales (D/16 bytes).
+ *                 Value = code * scale of its 32-value block.
+ *   QPS_FMT_TQ3   data: 2-bit magnitude plane (D/4 bytes); aux: 1-bit sign plane
+ *                 (D/8 bytes); aux2: one fp16 L2 norm (2 bytes).  Element i is at bits
+ *                 2(i%4)..2(i%4)+1 of byte i/4 and bit i%8 of byte i/8.  Level index
+ *                 k = sign ? 4 + mag : 3 - mag; value = (norm / D) * s .* (H c[k]),
+ *                 H the Sylvester-Hadamard matrix, s the seeded sign diagonal, c the
+ *                 codebook returned by qps_tq3_codebook().
+ */
+#ifndef QPS_H
+#define QPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QPS_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define QPS_API __attribute__((visibility("default")))
+#else
+#define QPS_API
+#endif
+
+typedef enum qps_status {
+  QPS_OK = 0,
+  QPS_ERR_INVALID_ARG = 1, /* a pointer, size, stride, alignment or range is invalid */
+  QPS_ERR_UNSUPPORTED = 2, /* valid but not implemented (head_dim, format pairing) */
+  QPS_ERR_CUDA = 3,        /* a CUDA runtime call failed; the message names it */
+  QPS_ERR_TIMEOUT = 4,     /* a bounded host wait ran out */
+  QPS_ERR_STATE = 5,       /* call out of order (ring schedule, destroyed object) */
+  QPS_ERR_INTERNAL = 6     /* a consistency check inside the library failed */
+} qps_status;
+
+typedef enum qps_kv_format {
+  QPS_FMT_F16 = 0,
+  QPS_FMT_Q8_0 = 1,
+  QPS_FMT_TQ3 = 2
+} qps_kv_format;
+
+/* ABI version of the loaded library (QPS_ABI_VERSION it was built with). */
+QPS_API int32_t qps_abi_version(void);
+
+/* Message of the last failing call on this thread ("" if none).  The pointer stays
+ * valid until the next failing call on the same thread. */
+QPS_API const char* qps_last_error(void);
+
+/* Constant name of a status code ("QPS_OK", ...). */
+QPS_API const char* qps_status_name(int32_t status);
+
+/* The fixed TQ3 codebook [POLY, "S2 — TurboQuant tier family"]: the 8-level Lloyd-Max
+ * quantiser of N(0,1), each level rounded to the nearest fp16 value, levels exactly
+ * symmetric, thresholds the exact midpoints of adjacent levels.  Host only; needs no
+ * GPU.  levels: host, 8 floats (ascending); thresholds: host, 7 floats.  Either may be
+ * NULL.  Errors: none. */
+QPS_API qps_status qps_tq3_codebook(float* levels, float* thresholds);
+
+/* q8_0 encode [POLY, "What PolyKV is (reference)"; problem statement: 32-value blocks,
+ * fp16 scale = absmax / 127, int8 codes].
+ *   x       device, fp16 rows [rows][D] with row stride x_row_stride (elements,
+ *           multiple of 8, >= D); 16-byte aligned.
+ *   codes   device, int8 [rows][D] contiguous; 8-byte aligned.
+ *   scales  device, fp16 [rows][D/32] contiguous; 2-byte aligned.
+ * Per block: d16 = fp16(f32(absmax) / 127); code = clamp(round_half_away(f32(x) /
+ * f32(d16)), -127, 127), all IEEE float32; a block with d16 == 0 stores zero codes.
+ * D in {32, 64, 128, 256, 512}.  rows == 0 is a no-op.
+ * Errors: INVALID_ARG (null / misaligned pointer, bad stride, rows < 0),
+ * UNSUPPORTED (D), CUDA (launch failure). */
+QPS_API qps_status qps_kv_quant_q8_0(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                             void* codes, void* scales, void* stream);
+
+/* TQ3 encode [POLY, "What PolyKV is (reference)", "S2 — TurboQuant tier family",
+ * "Phase-0 fork recon"].  Per row, in IEEE float32 with a fixed order: squares, a
+ * halving-fold sum (t[i] += t[i+h] for h = D/2 .. 1), n = sqrt; u = FWHT(s .* x)
+ * with butterflies (a+b, a-b) over stages h = 1, 2, ..., D/2; z = u / n; level index
+ * = number of codebook thresholds <= z.  Stores the planes described above and
+ * fp16(n).  A zero row stores zero planes and a zero norm.
+ *   x       device, fp16 rows [rows][D], row stride x_row_stride (elements, >= D).
+ *   signs   host, D/32 words: bit i of word i/32 set means s_i = -1.
+ *   lo2     device, [rows][D/4] bytes;  hi1 device, [rows][D/8] bytes (4-byte aligned);
+ *   norms   device, fp16 [rows].
+ * D in {32, 64, 128, 256, 512}.  rows == 0 is a no-op.
+ * Errors: INVALID_ARG, UNSUPPORTED (D), CUDA. */
+QPS_API qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* lo2, void* hi1, void* norms,
+                            void* stream);
+
+/* A K or V cache (or one of its parts) as seen by the attention calls.  Row of
+ * (token t, KV head h, batch entry b) = b*batch_stride + t*tok_stride + h*head_stride.
+ * batch_stride == 0 means every batch entry reads the same rows (a shared prefix,
+ * [POLY, "S1 — SharedKVPool"]); the attention then packs every batch entry's query
+ * rows of a KV head into one tile so the shared rows are read once. */
+typedef struct qps_kv_view {
+  int32_t fmt;         /* qps_kv_format */
+  int32_t reserved0;   /* must be 0 */
+  const void* data;    /* device: F16 values | Q8_0 codes | TQ3 2-bit plane; 16-byte aligned */
+  const void* aux;     /* device: Q8_0 scales | TQ3 1-bit plane; NULL for F16 */
+  const void* aux2;    /* device: TQ3 norms; NULL otherwise */
+  int64_t tok_stride;  /* rows between consecutive tokens (> 0) */
+  int64_t head_stride; /* rows between consecutive KV heads (>= 0) */
+  int64_t batch_stride;/* rows between consecutive batch entries; 0 = shared */
+} qps_kv_view;
+
+/* Arguments of one decode-attention part [RKV]: query rows attend key positions
+ * [kv_begin, kv_end) of (k, v).  Logit s = scale * <q, k>; with softcap c > 0,
+ * s <- c * tanh(s / c) before the softmax.  Query head h reads KV head h / (hq / hkv).
+ * The positions are cut into n_split contiguous chunks (split-KV); each chunk yields a
+ * normalised partial output and its natural-log LSE.  An empty chunk yields O = 0 and
+ * lse = -inf.
+ *
+ * Output modes:
+ *   o_parts != NULL : partials are written to part indices part_offset + s,
+ *                     s in [0, n_split), of o_parts [parts][batch*hq][D] f32 and
+ *                     lse_parts [parts][batch*hq] f32 (device); o / lse unused.
+ *                     Merge them with qps_lse_combine.
+ *   o_parts == NULL : the call merges its own chunks: o [batch*hq][D] f32 and
+ *                     lse [batch*hq] f32 (device); needs `workspace` (device, 256-byte
+ *                     aligned) of at least the size qps_attn_plan() reports.
+ * Row index of (batch entry b, query head h) is b*hq + h in every output. */
+typedef struct qps_attn_args {
+  const void* q;          /* device, fp16 [batch][hq][D], 16-byte aligned */
+  int64_t q_batch_stride; /* elements between batch entries (>= hq*D, multiple of 8) */
+  int32_t batch, hq, hkv, d;
+  qps_kv_view k, v;
+  int64_t kv_begin, kv_end; /* 0 <= kv_begin <= kv_end; tokens of the views */
+  float scale;
+  float softcap;          /* <= 0: off */
+  const uint32_t* v_signs;/* host, D/32 sign words; required iff v.fmt == QPS_FMT_TQ3 */
+  int32_t n_split;        /* > 0, or 0 = chosen by the library */
+  int32_t part_offset;
+  float* o_parts;
+  float* lse_parts;
+  float* o;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+} qps_attn_args;
+
+/* Resolve the split count and the workspace the args need (host only, no launch).
+ * n_split_out / workspace_bytes_out may be NULL.  Errors: INVALID_ARG, UNSUPPORTED. */
+QPS_API qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out,
+                         size_t* workspace_bytes_out);
+
+/* Decode attention over device-resident KV (the window [0, wc), or any device part)
+ * [RKV].  Supported: D in {64, 128, 256, 512}; K in {F16, Q8_0}; V in {F16, Q8_0, TQ3};
+ * hq a multiple of hkv.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+QPS_API qps_status qps_attn_decode_window(const qps_attn_args* a, void* stream);
+
+/* LSE combine [RKV, item S2]: M = max_t lse_t, w_t = exp(lse_t - M),
+ * o = sum_t w_t O_t / sum_t w_t, lse = M + log sum_t w_t; parts with lse = -inf weigh
+ * nothing; if all parts are empty, o = 0 and lse = -inf.
+ *   o_parts   device, f32 [n_parts][rows][D];  lse_parts device, f32 [n_parts][rows].
+ *   o         device, f32 [rows][D];           lse       device, f32 [rows].
+ * n_parts >= 1, rows >= 0, D in {32, 64, 128, 256, 512, 1024}.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+QPS_API qps_status qps_lse_combine(const float* o_parts, const float* lse_parts, int32_t n_parts,
+                           int64_t rows, int32_t d, float* o, float* lse, void* stream);
+
+/* ---- Tail-prefetch ring [RING] ------------------------------------------------ */
+
+typedef struct qps_ring qps_ring;
+
+/* Create a ring of n_slots (2..4) device staging slots of slot_bytes each on `device`,
+ * a non-blocking copy stream and pre-created copy_done / compute_done events (timing
+ * disabled).  The library owns these until qps_ring_destroy.  Makes `device` current.
+ * Errors: INVALID_ARG, CUDA (allocation). */
+QPS_API qps_status qps_ring_create(int32_t n_slots, size_t slot_bytes, int32_t device,
+                           qps_ring** out);
+
+/* Wait (bounded, 10 s) for the ring's copies, then free slots, events and the stream.
+ * NULL is a no-op.  Errors: TIMEOUT (resources leaked rather than freed in use). */
+QPS_API qps_status qps_ring_destroy(qps_ring* ring);
+
+/* One tail tile: `tokens` consecutive positions of one layer's tail, stored
+ * token-major (row = token * hkv + head) in one contiguous pinned-host range per
+ * plane.  K planes first (1 for F16, 2 for Q8_0, 3 for TQ3, in data/aux/aux2
+ * order), then V planes.  The ring places plane p at a 256-byte-aligned offset of the
+ * slot; their total must fit in slot_bytes. */
+typedef struct qps_tile_desc {
+  int32_t n_k_planes, n_v_planes;
+  const void* host_k[3];
+  size_t bytes_k[3];
+  const void* host_v[3];
+  size_t bytes_v[3];
+  int64_t tokens;
+} qps_tile_desc;
+
+/* Start a step: copy the flat (layer, tile) schedule (host array, read during the
+ * call) and enqueue the first n_slots tile copies on the copy stream; each copy
+ * first waits for the compute_done event of the slot's previous user (which may
+ * belong to the previous step).  Every host plane must be pinned.
+ * Errors: INVALID_ARG (unpinned / null plane, tile larger than a slot), STATE (a step
+ * is still open), CUDA. */
+QPS_API qps_status qps_ring_begin_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n_tiles,
+                               void* compute_stream);
+
+/* Attend tile `tile_index` of the open step [RKV, RING].  Tiles must be consumed in
+ * schedule order.  The compute stream waits for the slot's copy_done, the attention
+ * runs on the slot (the k / v views' data pointers in `a` are ignored and replaced by
+ * the slot's planes; their fmt and strides are used; kv_begin / kv_end are replaced by
+ * [0, tokens)), compute_done is recorded, and the copy of tile tile_index + n_slots
+ * into the same slot is enqueued behind it.  Output modes as for
+ * qps_attn_decode_window.  Errors: STATE (out of order, no open step), INVALID_ARG,
+ * UNSUPPORTED, CUDA. */
+QPS_API qps_status qps_attn_decode_tail(qps_ring* ring, int32_t tile_index, const qps_attn_args* a,
+                                void* compute_stream);
+
+/* Close the step (every tile must have been consumed).  Does not wait for the
+ * device.  Errors: STATE. */
+QPS_API qps_status qps_ring_end_step(qps_ring* ring);
+
+/* Wait until every copy and every tail attention issued by the ring has completed,
+ * polling with a deadline of timeout_ms (never blocks longer).  Errors: TIMEOUT,
+ * CUDA. */
+QPS_API qps_status qps_ring_sync(qps_ring* ring, int32_t timeout_ms);
+
+/* ---- Native step runner -------------------------------------------------------- */
+
+/* One layer of a decode step: device-resident parts (the window; for a shared-prefix
+ * batch the prefix and the private suffixes), then `n_tiles` consecutive ring tiles
+ * of this layer's tail attended with the `tail` template, then one LSE combine into
+ * o / lse.  The runner assigns part indices: device part i takes the next n_split
+ * indices after part i-1, then each tile its own n_split indices; the total must not
+ * exceed parts_capacity.  The o_parts / lse_parts / part_offset / o / lse fields of
+ * the per-part args are ignored (the runner sets them). */
+typedef struct qps_layer_step {
+  const qps_attn_args* device_parts; /* host array of n_device_parts args */
+  int32_t n_device_parts;
+  int32_t n_tiles;
+  const qps_attn_args* tail;         /* host; required when n_tiles > 0 */
+  float* o_parts;                    /* device, f32 [parts_capacity][batch*hq][D] */
+  float* lse_parts;                  /* device, f32 [parts_capacity][batch*hq] */
+  int32_t parts_capacity;
+  float* o;                          /* device, f32 [batch*hq][D] */
+  float* lse;                        /* device, f32 [batch*hq] */
+  void* part_events[2];              /* optional cudaEvent_t pair (caller-created, may be
+                                        NULL): recorded on the stream just before and just
+                                        after this layer's device parts, for timing them */
+} qps_layer_step;
+
+/* Run one decode step over n_layers layers on `stream` [RKV, RING]: begin the ring
+ * step with `tiles` (the concatenation of every layer's tiles, in layer order; ring
+ * may be NULL when no layer has tiles), then for each layer its device parts, its
+ * tiles and its combine, then close the ring step.  Nothing waits for the device.
+ * Errors: as the calls it makes. */
+QPS_API qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n_tiles,
+                           const qps_layer_step* layers, int32_t n_layers, void* stream);
+
+/* Number of kernel launches the calling thread has issued through this library
+ * since the last reset (reset if `reset` is non-zero).  Host only. */
+QPS_API int64_t qps_launch_count(int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QPS_H */

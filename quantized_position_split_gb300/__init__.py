@@ -1,0 +1,351 @@
+"""Position-split, quantised-KV decode attention for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``include/qps.h``: every function here only
+marshals torch tensors (device memory, pinned host memory, streams) into the ABI's
+plain pointers and sizes.  All computation runs in the library's CUDA kernels; there
+is no CPU or eager-PyTorch fallback, and a missing library raises at first use.
+
+Names follow the ABI without its ``qps_`` prefix (``kv_quant_q8_0``,
+``kv_quant_tq3``, ``attn_decode_window``, ``attn_decode_tail``, ``lse_combine``,
+``Ring`` for ``qps_ring_*``, ``StepPlan`` for ``qps_decode_step``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import _native as N
+from ._native import FMT_F16, FMT_Q8_0, FMT_TQ3, QpsError  # noqa: F401
+
+__all__ = [
+    "QpsError",
+    "KV",
+    "tq3_codebook",
+    "kv_quant_q8_0",
+    "kv_quant_tq3",
+    "encode_kv",
+    "attn_args",
+    "attn_plan",
+    "attn_decode_window",
+    "lse_combine",
+    "Ring",
+    "tile_desc",
+    "StepPlan",
+    "launch_count",
+    "lib",
+]
+
+
+def lib():
+    return N.load()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _sign_array(signs):
+    words = [int(w) & 0xFFFFFFFF for w in (signs.tolist() if hasattr(signs, "tolist") else signs)]
+    arr = (ctypes.c_uint32 * len(words))(*words)
+    return arr
+
+
+def launch_count(reset: bool = False) -> int:
+    return int(lib().qps_launch_count(1 if reset else 0))
+
+
+def tq3_codebook():
+    """The library's fixed TQ3 codebook: (8 levels, 7 thresholds) as Python floats."""
+    lv = (ctypes.c_float * 8)()
+    th = (ctypes.c_float * 7)()
+    N.check(lib().qps_tq3_codebook(lv, th))
+    return list(lv), list(th)
+
+
+def _rows2d(x: torch.Tensor):
+    if x.dtype != torch.float16 or not x.is_cuda:
+        raise QpsError(N.QPS_ERR_INVALID_ARG, "input must be a CUDA float16 tensor")
+    if x.stride(-1) != 1:
+        raise QpsError(N.QPS_ERR_INVALID_ARG, "input's last dimension must be contiguous")
+    d = x.shape[-1]
+    x2 = x.reshape(-1, d)
+    stride = x2.stride(0) if x2.shape[0] > 1 else d
+    return x2, d, stride
+
+
+def kv_quant_q8_0(x: torch.Tensor, codes=None, scales=None, stream=None):
+    """Encode fp16 rows ``x[..., D]`` as q8_0: (int8 codes [..., D], fp16 scales [..., D/32])."""
+    x2, d, stride = _rows2d(x)
+    rows = x2.shape[0]
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1] + (d // 32,), dtype=torch.float16, device=x.device)
+    N.check(lib().qps_kv_quant_q8_0(x2.data_ptr(), rows, d, stride, codes.data_ptr(),
+                                    scales.data_ptr(), _stream(stream)))
+    return codes, scales
+
+
+def kv_quant_tq3(x: torch.Tensor, signs, lo2=None, hi1=None, norms=None, stream=None):
+    """Encode fp16 rows ``x[..., D]`` as TQ3: (2-bit plane [..., D/4] u8, 1-bit plane
+    [..., D/8] u8, fp16 norms [...])."""
+    x2, d, stride = _rows2d(x)
+    rows = x2.shape[0]
+    if lo2 is None:
+        lo2 = torch.empty(x.shape[:-1] + (d // 4,), dtype=torch.uint8, device=x.device)
+    if hi1 is None:
+        hi1 = torch.empty(x.shape[:-1] + (d // 8,), dtype=torch.uint8, device=x.device)
+    if norms is None:
+        norms = torch.empty(x.shape[:-1], dtype=torch.float16, device=x.device)
+    sa = _sign_array(signs)
+    N.check(lib().qps_kv_quant_tq3(x2.data_ptr(), rows, d, stride, sa, lo2.data_ptr(),
+                                   hi1.data_ptr(), norms.data_ptr(), _stream(stream)))
+    return lo2, hi1, norms
+
+
+@dataclasses.dataclass
+class KV:
+    """A stored K or V cache: its format, its planes and how rows are addressed.
+
+    Planes are token-major tensors ``[(batch,) tokens, hkv, plane_row]``; the row of
+    (token t, KV head h, batch entry b) is b*batch_stride + t*tok_stride + h*head_stride.
+    """
+
+    fmt: str
+    planes: tuple
+    tokens: int
+    hkv: int
+    d: int
+    tok_stride: int
+    head_stride: int = 1
+    batch_stride: int = 0
+
+    def view(self) -> N.KvView:
+        ptrs = [p.data_ptr() for p in self.planes] + [None] * (3 - len(self.planes))
+        return N.KvView(N.FMT_BY_NAME[self.fmt], 0, ptrs[0], ptrs[1], ptrs[2],
+                        self.tok_stride, self.head_stride, self.batch_stride)
+
+    def nbytes(self) -> int:
+        return sum(p.numel() * p.element_size() for p in self.planes)
+
+    def token_slice(self, t0: int, t1: int) -> "KV":
+        """The positions [t0, t1) of a token-major, unbatched cache (a view, no copy)."""
+        return KV(self.fmt, tuple(p[t0:t1] for p in self.planes), t1 - t0, self.hkv, self.d,
+                  self.tok_stride, self.head_stride, self.batch_stride)
+
+    def pinned_copy(self) -> "KV":
+        """The same planes copied to pinned host memory."""
+        planes = tuple(p.detach().to("cpu").pin_memory() for p in self.planes)
+        return dataclasses.replace(self, planes=planes)
+
+
+def encode_kv(fmt: str, x: torch.Tensor, signs=None, stream=None) -> KV:
+    """Store fp16 ``x[(batch,) tokens, hkv, D]`` (CUDA) in ``fmt`` with the library's
+    encoders; the result is token-major."""
+    d = x.shape[-1]
+    hkv = x.shape[-2]
+    tokens = x.shape[-3]
+    batch_stride = tokens * hkv if x.dim() == 4 else 0
+    if fmt == "f16":
+        planes = (x.contiguous(),)
+    elif fmt == "q8_0":
+        planes = kv_quant_q8_0(x.contiguous(), stream=stream)
+    elif fmt == "tq3":
+        if signs is None:
+            raise QpsError(N.QPS_ERR_INVALID_ARG, "TQ3 needs the sign words")
+        planes = kv_quant_tq3(x.contiguous(), signs, stream=stream)
+    else:
+        raise QpsError(N.QPS_ERR_INVALID_ARG, f"unknown format {fmt}")
+    return KV(fmt, tuple(planes), tokens, hkv, d, hkv, 1, batch_stride)
+
+
+def attn_args(q: torch.Tensor, k: KV, v: KV, *, scale: float, softcap: float = 0.0,
+              kv_begin: int = 0, kv_end: Optional[int] = None, v_signs=None, n_split: int = 0,
+              shared: bool = False) -> N.AttnArgs:
+    """Build the ABI argument struct for ``q[batch, hq, D]`` against (k, v).
+
+    ``shared`` makes every batch entry read the same KV rows (batch_stride 0).  The
+    returned struct keeps a reference to the sign array it points to.
+    """
+    if q.dtype != torch.float16 or q.dim() != 3:
+        raise QpsError(N.QPS_ERR_INVALID_ARG, "q must be float16 [batch, hq, D]")
+    batch, hq, d = q.shape
+    a = N.AttnArgs()
+    a.q = q.data_ptr()
+    a.q_batch_stride = q.stride(0)
+    a.batch, a.hq, a.hkv, a.d = batch, hq, k.hkv, d
+    a.k = k.view()
+    a.v = v.view()
+    if shared:
+        a.k.batch_stride = 0
+        a.v.batch_stride = 0
+    a.kv_begin = kv_begin
+    a.kv_end = k.tokens if kv_end is None else kv_end
+    a.scale = scale
+    a.softcap = softcap
+    if v_signs is not None:
+        arr = _sign_array(v_signs)
+        a.v_signs = ctypes.cast(arr, ctypes.POINTER(ctypes.c_uint32))
+        a._keep = arr
+    a.n_split = n_split
+    return a
+
+
+def attn_plan(a: N.AttnArgs):
+    """(n_split, workspace_bytes) the library resolves for these args."""
+    n = ctypes.c_int32()
+    ws = ctypes.c_size_t()
+    N.check(lib().qps_attn_plan(ctypes.byref(a), ctypes.byref(n), ctypes.byref(ws)))
+    return n.value, ws.value
+
+
+def attn_decode_window(a: N.AttnArgs, *, o=None, lse=None, parts=None, part_offset: int = 0,
+                       workspace=None, stream=None, device=None):
+    """Run one device-resident attention part.
+
+    With ``parts=(o_parts, lse_parts)`` the split partials are written at
+    ``part_offset``; otherwise the merged (o, lse) are returned (allocated if None).
+    """
+    rows = a.batch * a.hq
+    if parts is not None:
+        a.o_parts, a.lse_parts = parts[0].data_ptr(), parts[1].data_ptr()
+        a.part_offset = part_offset
+        a.o = a.lse = None
+        N.check(lib().qps_attn_decode_window(ctypes.byref(a), _stream(stream)))
+        return parts
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    if o is None:
+        o = torch.empty((rows, a.d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=dev)
+    a.o_parts = a.lse_parts = None
+    _, ws = attn_plan(a)
+    if workspace is None or workspace.numel() < ws:
+        workspace = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
+    a.o, a.lse = o.data_ptr(), lse.data_ptr()
+    a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    N.check(lib().qps_attn_decode_window(ctypes.byref(a), _stream(stream)))
+    return o, lse
+
+
+def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, o=None, lse=None, stream=None):
+    """Merge ``o_parts[P, rows, D]`` / ``lse_parts[P, rows]`` (f32, CUDA)."""
+    p, rows, d = o_parts.shape
+    if o is None:
+        o = torch.empty((rows, d), dtype=torch.float32, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+    N.check(lib().qps_lse_combine(o_parts.data_ptr(), lse_parts.data_ptr(), p, rows, d,
+                                  o.data_ptr(), lse.data_ptr(), _stream(stream)))
+    return o, lse
+
+
+def tile_desc(k_host: KV, v_host: KV, t0: int, t1: int) -> N.TileDesc:
+    """Descriptor of positions [t0, t1) of a pinned, token-major host tail."""
+    td = N.TileDesc()
+    td.tokens = t1 - t0
+    for side, kv in (("k", k_host), ("v", v_host)):
+        hosts = getattr(td, "host_" + side)
+        sizes = getattr(td, "bytes_" + side)
+        for i, p in enumerate(kv.planes):
+            row_bytes = p[0].numel() * p.element_size() if p.shape[0] > 0 else 0
+            hosts[i] = p.data_ptr() + t0 * row_bytes
+            sizes[i] = (t1 - t0) * row_bytes
+        setattr(td, "n_%s_planes" % side, len(kv.planes))
+    return td
+
+
+class Ring:
+    """The tail-prefetch ring (``qps_ring_*``): device staging slots, a copy stream and
+    pre-created copy_done / compute_done events, owned by the library."""
+
+    def __init__(self, n_slots: int, slot_bytes: int, device: Optional[int] = None):
+        dev = torch.cuda.current_device() if device is None else device
+        h = ctypes.c_void_p()
+        N.check(lib().qps_ring_create(n_slots, slot_bytes, dev, ctypes.byref(h)))
+        self.handle = h
+        self.n_slots = n_slots
+        self.slot_bytes = slot_bytes
+        self._tiles = None
+
+    def begin_step(self, tiles: Sequence[N.TileDesc], stream=None):
+        arr = (N.TileDesc * len(tiles))(*tiles)
+        self._tiles = arr
+        N.check(lib().qps_ring_begin_step(self.handle, arr, len(tiles), _stream(stream)))
+
+    def decode_tail(self, index: int, a: N.AttnArgs, *, parts, part_offset: int, stream=None):
+        a.o_parts, a.lse_parts = parts[0].data_ptr(), parts[1].data_ptr()
+        a.part_offset = part_offset
+        N.check(lib().qps_attn_decode_tail(self.handle, index, ctypes.byref(a), _stream(stream)))
+
+    def end_step(self):
+        N.check(lib().qps_ring_end_step(self.handle))
+
+    def sync(self, timeout_ms: int = 10000):
+        N.check(lib().qps_ring_sync(self.handle, timeout_ms))
+
+    def close(self):
+        if self.handle:
+            N.check(lib().qps_ring_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StepPlan:
+    """A whole decode step prepared once and run with one ``qps_decode_step`` call.
+
+    ``layers`` is a list of dicts with keys ``device_parts`` (list of AttnArgs),
+    ``tail`` (AttnArgs or None), ``n_tiles``, ``o_parts``, ``lse_parts`` (f32 CUDA
+    tensors [capacity, rows, D] / [capacity, rows]), ``o``, ``lse`` and optionally
+    ``part_events`` (two raw cudaEvent_t handles recorded around the device parts).
+    """
+
+    def __init__(self, layers: List[dict], tiles: Sequence[N.TileDesc] = (), ring: Optional[Ring] = None):
+        self.ring = ring
+        self.tiles = (N.TileDesc * max(1, len(tiles)))(*tiles)
+        self.n_tiles = len(tiles)
+        self._keep = []
+        steps = []
+        for L in layers:
+            parts = (N.AttnArgs * max(1, len(L["device_parts"])))(*L["device_parts"])
+            tail = L.get("tail")
+            tail_ptr = None
+            if tail is not None:
+                tail_arr = (N.AttnArgs * 1)(tail)
+                tail_ptr = ctypes.cast(tail_arr, ctypes.POINTER(N.AttnArgs))
+                self._keep.append(tail_arr)
+            self._keep += [parts, L["device_parts"], tail]
+            st = N.LayerStep()
+            st.device_parts = ctypes.cast(parts, ctypes.POINTER(N.AttnArgs))
+            st.n_device_parts = len(L["device_parts"])
+            st.n_tiles = L.get("n_tiles", 0)
+            st.tail = tail_ptr
+            st.o_parts = L["o_parts"].data_ptr()
+            st.lse_parts = L["lse_parts"].data_ptr()
+            st.parts_capacity = L["o_parts"].shape[0]
+            st.o = L["o"].data_ptr()
+            st.lse = L["lse"].data_ptr()
+            ev = L.get("part_events")
+            if ev is not None:
+                st.part_events[0], st.part_events[1] = ev
+            steps.append(st)
+        self.layers = (N.LayerStep * len(steps))(*steps)
+        self.n_layers = len(steps)
+
+    def run(self, stream=None):
+        ring = self.ring.handle if self.ring is not None else None
+        N.check(lib().qps_decode_step(ring, self.tiles, self.n_tiles, self.layers, self.n_layers,
+                                      _stream(stream)))

@@ -1,0 +1,157 @@
+"""ctypes declarations of the C ABI in ``include/qps.h`` (argument marshalling only).
+
+The shared library is built in-tree by ``quantized_position_split_gb300.build``; if it
+is missing, loading fails loudly: there is no other implementation to fall back to.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqps.so")
+
+QPS_OK = 0
+QPS_ERR_INVALID_ARG = 1
+QPS_ERR_UNSUPPORTED = 2
+QPS_ERR_CUDA = 3
+QPS_ERR_TIMEOUT = 4
+QPS_ERR_STATE = 5
+QPS_ERR_INTERNAL = 6
+
+FMT_F16 = 0
+FMT_Q8_0 = 1
+FMT_TQ3 = 2
+FMT_BY_NAME = {"f16": FMT_F16, "q8_0": FMT_Q8_0, "tq3": FMT_TQ3}
+
+
+class QpsError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_name(status)}: {message}")
+        self.status = status
+
+
+class KvView(ctypes.Structure):
+    _fields_ = [
+        ("fmt", c_int32),
+        ("reserved0", c_int32),
+        ("data", c_void_p),
+        ("aux", c_void_p),
+        ("aux2", c_void_p),
+        ("tok_stride", c_int64),
+        ("head_stride", c_int64),
+        ("batch_stride", c_int64),
+    ]
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", c_void_p),
+        ("q_batch_stride", c_int64),
+        ("batch", c_int32),
+        ("hq", c_int32),
+        ("hkv", c_int32),
+        ("d", c_int32),
+        ("k", KvView),
+        ("v", KvView),
+        ("kv_begin", c_int64),
+        ("kv_end", c_int64),
+        ("scale", c_float),
+        ("softcap", c_float),
+        ("v_signs", POINTER(c_uint32)),
+        ("n_split", c_int32),
+        ("part_offset", c_int32),
+        ("o_parts", c_void_p),
+        ("lse_parts", c_void_p),
+        ("o", c_void_p),
+        ("lse", c_void_p),
+        ("workspace", c_void_p),
+        ("workspace_bytes", c_size_t),
+    ]
+
+
+class TileDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_k_planes", c_int32),
+        ("n_v_planes", c_int32),
+        ("host_k", c_void_p * 3),
+        ("bytes_k", c_size_t * 3),
+        ("host_v", c_void_p * 3),
+        ("bytes_v", c_size_t * 3),
+        ("tokens", c_int64),
+    ]
+
+
+class LayerStep(ctypes.Structure):
+    _fields_ = [
+        ("device_parts", POINTER(AttnArgs)),
+        ("n_device_parts", c_int32),
+        ("n_tiles", c_int32),
+        ("tail", POINTER(AttnArgs)),
+        ("o_parts", c_void_p),
+        ("lse_parts", c_void_p),
+        ("parts_capacity", c_int32),
+        ("o", c_void_p),
+        ("lse", c_void_p),
+        ("part_events", c_void_p * 2),
+    ]
+
+
+# (name, restype, argtypes) of every exported function, in header order.
+SIGNATURES = [
+    ("qps_abi_version", c_int32, []),
+    ("qps_last_error", c_char_p, []),
+    ("qps_status_name", c_char_p, [c_int32]),
+    ("qps_tq3_codebook", c_int32, [POINTER(c_float), POINTER(c_float)]),
+    ("qps_kv_quant_q8_0", c_int32, [c_void_p, c_int64, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
+    ("qps_kv_quant_tq3", c_int32,
+     [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p, c_void_p]),
+    ("qps_attn_plan", c_int32, [POINTER(AttnArgs), POINTER(c_int32), POINTER(c_size_t)]),
+    ("qps_attn_decode_window", c_int32, [POINTER(AttnArgs), c_void_p]),
+    ("qps_lse_combine", c_int32, [c_void_p, c_void_p, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p]),
+    ("qps_ring_create", c_int32, [c_int32, c_size_t, c_int32, POINTER(c_void_p)]),
+    ("qps_ring_destroy", c_int32, [c_void_p]),
+    ("qps_ring_begin_step", c_int32, [c_void_p, POINTER(TileDesc), c_int32, c_void_p]),
+    ("qps_attn_decode_tail", c_int32, [c_void_p, c_int32, POINTER(AttnArgs), c_void_p]),
+    ("qps_ring_end_step", c_int32, [c_void_p]),
+    ("qps_ring_sync", c_int32, [c_void_p, c_int32]),
+    ("qps_decode_step", c_int32, [c_void_p, POINTER(TileDesc), c_int32, POINTER(LayerStep), c_int32, c_void_p]),
+    ("qps_launch_count", c_int64, [c_int32]),
+]
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library once and declare every function's signature."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(
+                f"CUDA library not built: {path} is missing; run "
+                "`python -m quantized_position_split_gb300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(path)
+        for name, res, args in SIGNATURES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_name(status: int) -> str:
+    try:
+        return load().qps_status_name(status).decode()
+    except ImportError:
+        return f"status {status}"
+
+
+def check(status: int) -> None:
+    if status != QPS_OK:
+        msg = load().qps_last_error().decode(errors="replace")
+        raise QpsError(status, msg)

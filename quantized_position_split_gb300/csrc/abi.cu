@@ -1,0 +1,342 @@
+// C ABI entry points: argument validation, error reporting, the TQ3 codebook, the
+// attention plan / dispatch, the LSE combine and the native decode-step runner.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+namespace qps {
+
+// ---- errors ---------------------------------------------------------------------
+namespace {
+thread_local std::string g_last_error;
+thread_local int64_t g_launches = 0;
+}  // namespace
+
+qps_status fail(qps_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+qps_status cuda_fail(cudaError_t err, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorName(err) + " (" + cudaGetErrorString(err) + ")";
+  return QPS_ERR_CUDA;
+}
+
+void count_launch(int n) { g_launches += n; }
+
+int sm_count_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// ---- TQ3 codebook -----------------------------------------------------------------
+// Lloyd iteration for the 8-level MSE-optimal quantiser of N(0,1) in double precision
+// (thresholds at midpoints, levels at the conditional means of their cells), then each
+// level rounded to the nearest fp16 value, made exactly symmetric, and the thresholds
+// set to the exact midpoints.
+namespace {
+
+double gauss_pdf(double x) { return std::exp(-0.5 * x * x) / std::sqrt(2.0 * M_PI); }
+double gauss_cdf(double x) { return 0.5 * std::erfc(-x / std::sqrt(2.0)); }
+
+// Nearest fp16-representable value (round half to even) of a positive normal double.
+double round_to_half_grid(double x) {
+  int e = 0;
+  const double m = std::frexp(x, &e);  // x = m * 2^e, m in [0.5, 1)
+  return std::ldexp(std::nearbyint(std::ldexp(m, 11)), e - 11);
+}
+
+Codebook make_codebook() {
+  double c[8];
+  for (int i = 0; i < 8; ++i) c[i] = -2.0 + 4.0 * i / 7.0;
+  for (int it = 0; it < 100000; ++it) {
+    double t[7];
+    for (int i = 0; i < 7; ++i) t[i] = 0.5 * (c[i] + c[i + 1]);
+    double cn[8];
+    double delta = 0.0;
+    for (int k = 0; k < 8; ++k) {
+      const double pa = k == 0 ? 0.0 : gauss_pdf(t[k - 1]);
+      const double pb = k == 7 ? 0.0 : gauss_pdf(t[k]);
+      const double fa = k == 0 ? 0.0 : gauss_cdf(t[k - 1]);
+      const double fb = k == 7 ? 1.0 : gauss_cdf(t[k]);
+      cn[k] = (pa - pb) / (fb - fa);
+      delta = std::fmax(delta, std::fabs(cn[k] - c[k]));
+    }
+    for (int k = 0; k < 8; ++k) c[k] = cn[k];
+    if (delta < 1e-14) break;
+  }
+  Codebook cb{};
+  for (int i = 0; i < 4; ++i) {
+    const float pos = (float)round_to_half_grid(std::fabs(c[4 + i]));
+    cb.levels[4 + i] = pos;
+    cb.levels[3 - i] = -pos;
+  }
+  for (int i = 0; i < 7; ++i) cb.thresholds[i] = (cb.levels[i] + cb.levels[i + 1]) / 2.0f;
+  return cb;
+}
+
+}  // namespace
+
+const Codebook& tq3_codebook() {
+  static const Codebook cb = make_codebook();
+  return cb;
+}
+
+// ---- attention argument resolution ------------------------------------------------
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+qps_status check_view(const qps_kv_view& v, const char* name, bool allow_tq3) {
+  const std::string n(name);
+  if (v.reserved0 != 0) return fail(QPS_ERR_INVALID_ARG, n + ": reserved0 must be 0");
+  if (v.fmt != QPS_FMT_F16 && v.fmt != QPS_FMT_Q8_0 && v.fmt != QPS_FMT_TQ3)
+    return fail(QPS_ERR_INVALID_ARG, n + ": unknown format");
+  if (v.fmt == QPS_FMT_TQ3 && !allow_tq3)
+    return fail(QPS_ERR_UNSUPPORTED, n + ": TQ3 is supported for V only");
+  if (!v.data) return fail(QPS_ERR_INVALID_ARG, n + ": data is NULL");
+  if (!aligned(v.data, 16)) return fail(QPS_ERR_INVALID_ARG, n + ": data must be 16-byte aligned");
+  if (v.fmt != QPS_FMT_F16) {
+    if (!v.aux) return fail(QPS_ERR_INVALID_ARG, n + ": aux plane is NULL");
+    if (!aligned(v.aux, 4)) return fail(QPS_ERR_INVALID_ARG, n + ": aux must be 4-byte aligned");
+  }
+  if (v.fmt == QPS_FMT_TQ3) {
+    if (!v.aux2) return fail(QPS_ERR_INVALID_ARG, n + ": aux2 (norms) is NULL");
+    if (!aligned(v.aux2, 2)) return fail(QPS_ERR_INVALID_ARG, n + ": aux2 must be 2-byte aligned");
+  }
+  if (v.tok_stride <= 0) return fail(QPS_ERR_INVALID_ARG, n + ": tok_stride must be > 0");
+  if (v.head_stride < 0 || v.batch_stride < 0)
+    return fail(QPS_ERR_INVALID_ARG, n + ": strides must be >= 0");
+  return QPS_OK;
+}
+
+int auto_split(int64_t ntok, int ctas_per_split) {
+  const int sms = sm_count_current();
+  if (sms <= 0) return -1;
+  const int64_t min_chunk = 256;
+  const int64_t target = 4LL * sms;
+  int64_t by_occupancy = (target + ctas_per_split - 1) / ctas_per_split;
+  int64_t by_size = (ntok + min_chunk - 1) / min_chunk;
+  int64_t n = by_occupancy < by_size ? by_occupancy : by_size;
+  if (n < 1) n = 1;
+  if (n > 65535) n = 65535;
+  return (int)n;
+}
+
+}  // namespace
+
+qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out, size_t* ws_bytes) {
+  if (!a) return fail(QPS_ERR_INVALID_ARG, "attention: args is NULL");
+  if (!a->q) return fail(QPS_ERR_INVALID_ARG, "attention: q is NULL");
+  if (!aligned(a->q, 16)) return fail(QPS_ERR_INVALID_ARG, "attention: q must be 16-byte aligned");
+  if (a->batch < 1 || a->hq < 1 || a->hkv < 1)
+    return fail(QPS_ERR_INVALID_ARG, "attention: batch, hq, hkv must be >= 1");
+  if (a->hq % a->hkv) return fail(QPS_ERR_INVALID_ARG, "attention: hq must be a multiple of hkv");
+  if (a->d != 64 && a->d != 128 && a->d != 256 && a->d != 512)
+    return fail(QPS_ERR_UNSUPPORTED, "attention: head_dim must be 64, 128, 256 or 512");
+  if (a->batch > 1 && (a->q_batch_stride < (int64_t)a->hq * a->d || a->q_batch_stride % 8))
+    return fail(QPS_ERR_INVALID_ARG, "attention: q_batch_stride must be >= hq*d and a multiple of 8");
+  qps_status st = check_view(a->k, "attention k", false);
+  if (st != QPS_OK) return st;
+  st = check_view(a->v, "attention v", true);
+  if (st != QPS_OK) return st;
+  if ((a->k.batch_stride == 0) != (a->v.batch_stride == 0))
+    return fail(QPS_ERR_INVALID_ARG, "attention: k and v must both be shared (batch_stride 0) or both per-batch");
+  if (a->kv_begin < 0 || a->kv_end < a->kv_begin)
+    return fail(QPS_ERR_INVALID_ARG, "attention: need 0 <= kv_begin <= kv_end");
+  if (!std::isfinite(a->scale) || !std::isfinite(a->softcap))
+    return fail(QPS_ERR_INVALID_ARG, "attention: scale and softcap must be finite");
+  if (a->v.fmt == QPS_FMT_TQ3 && !a->v_signs)
+    return fail(QPS_ERR_INVALID_ARG, "attention: v_signs is required for a TQ3 V");
+  if (a->n_split < 0) return fail(QPS_ERR_INVALID_ARG, "attention: n_split must be >= 0");
+  const bool shared = a->k.batch_stride == 0 && a->batch > 1;
+  const int group = a->hq / a->hkv;
+  const int rows_per_cta = shared ? a->batch * group : group;
+  if (rows_per_cta > 1024) return fail(QPS_ERR_UNSUPPORTED, "attention: more than 1024 query rows per KV head");
+  const int64_t ntok = a->kv_end - a->kv_begin;
+  const int ctas_per_split = a->hkv * (shared ? 1 : a->batch);
+  int n_split = a->n_split;
+  if (n_split == 0) {
+    n_split = auto_split(ntok, ctas_per_split);
+    if (n_split < 0) return fail(QPS_ERR_CUDA, "attention: cannot query the current device's SM count");
+  }
+  if (n_split > 65535) return fail(QPS_ERR_INVALID_ARG, "attention: n_split must be <= 65535");
+  const int64_t rows_total = (int64_t)a->batch * a->hq;
+  const size_t ws = ((size_t)n_split * rows_total * (a->d + 1) * sizeof(float) + 1024 + 255) & ~(size_t)255;
+  if (n_split_out) *n_split_out = n_split;
+  if (ws_bytes) *ws_bytes = ws;
+  if (!p) return QPS_OK;
+
+  std::memset(p, 0, sizeof(*p));
+  p->q = reinterpret_cast<const __half*>(a->q);
+  p->q_bstride = a->batch > 1 ? a->q_batch_stride : (int64_t)a->hq * a->d;
+  p->batch = a->batch;
+  p->hq = a->hq;
+  p->hkv = a->hkv;
+  p->d = a->d;
+  p->group = group;
+  p->kfmt = a->k.fmt;
+  p->vfmt = a->v.fmt;
+  p->k = KvSide{a->k.data, a->k.aux, a->k.aux2, a->k.tok_stride, a->k.head_stride, a->k.batch_stride};
+  p->v = KvSide{a->v.data, a->v.aux, a->v.aux2, a->v.tok_stride, a->v.head_stride, a->v.batch_stride};
+  p->begin = a->kv_begin;
+  p->end = a->kv_end;
+  p->n_split = n_split;
+  p->chunk = ntok == 0 ? 1 : (ntok + n_split - 1) / n_split;
+  p->scale = a->scale;
+  p->softcap = a->softcap > 0.f ? a->softcap : 0.f;
+  p->shared = shared ? 1 : 0;
+  p->rows_per_cta = rows_per_cta;
+  p->rows_total = rows_total;
+  if (a->v.fmt == QPS_FMT_TQ3)
+    for (int i = 0; i < a->d / 32; ++i) p->vsigns[i] = a->v_signs[i];
+  const Codebook& cb = tq3_codebook();
+  for (int i = 0; i < 8; ++i) p->tq_levels[i] = cb.levels[i];
+  return QPS_OK;
+}
+
+qps_status launch_attn_simple(const AttnParams& p, cudaStream_t s);
+
+qps_status launch_attn(const AttnParams& p, cudaStream_t s) { return launch_attn_simple(p, s); }
+
+qps_status run_attn(const qps_attn_args* a, const AttnParams& p_in, int n_split, cudaStream_t s) {
+  AttnParams p = p_in;
+  if (a->o_parts) {
+    if (!a->lse_parts) return fail(QPS_ERR_INVALID_ARG, "attention: lse_parts is NULL");
+    if (a->part_offset < 0) return fail(QPS_ERR_INVALID_ARG, "attention: part_offset must be >= 0");
+    p.o_parts = a->o_parts;
+    p.lse_parts = a->lse_parts;
+    p.part_offset = a->part_offset;
+    return launch_attn(p, s);
+  }
+  if (!a->o || !a->lse) return fail(QPS_ERR_INVALID_ARG, "attention: o / lse are NULL and no o_parts given");
+  size_t need = 0;
+  resolve_attn(a, nullptr, nullptr, &need);
+  if (!a->workspace || a->workspace_bytes < need)
+    return fail(QPS_ERR_INVALID_ARG, "attention: workspace missing or smaller than qps_attn_plan reports");
+  if (!aligned(a->workspace, 256)) return fail(QPS_ERR_INVALID_ARG, "attention: workspace must be 256-byte aligned");
+  float* ws = reinterpret_cast<float*>(a->workspace);
+  const int64_t rows = p.rows_total;
+  p.o_parts = ws;
+  p.lse_parts = ws + (size_t)n_split * rows * p.d;
+  p.part_offset = 0;
+  qps_status st = launch_attn(p, s);
+  if (st != QPS_OK) return st;
+  return launch_combine(p.o_parts, p.lse_parts, n_split, rows, p.d, a->o, a->lse, s);
+}
+
+}  // namespace qps
+
+using namespace qps;
+
+extern "C" {
+
+int32_t qps_abi_version(void) { return QPS_ABI_VERSION; }
+
+const char* qps_last_error(void) { return g_last_error.c_str(); }
+
+const char* qps_status_name(int32_t st) {
+  switch (st) {
+    case QPS_OK: return "QPS_OK";
+    case QPS_ERR_INVALID_ARG: return "QPS_ERR_INVALID_ARG";
+    case QPS_ERR_UNSUPPORTED: return "QPS_ERR_UNSUPPORTED";
+    case QPS_ERR_CUDA: return "QPS_ERR_CUDA";
+    case QPS_ERR_TIMEOUT: return "QPS_ERR_TIMEOUT";
+    case QPS_ERR_STATE: return "QPS_ERR_STATE";
+    case QPS_ERR_INTERNAL: return "QPS_ERR_INTERNAL";
+    default: return "QPS_UNKNOWN_STATUS";
+  }
+}
+
+int64_t qps_launch_count(int32_t reset) {
+  const int64_t n = g_launches;
+  if (reset) g_launches = 0;
+  return n;
+}
+
+qps_status qps_tq3_codebook(float* levels, float* thresholds) {
+  const Codebook& cb = tq3_codebook();
+  if (levels) std::memcpy(levels, cb.levels, sizeof(cb.levels));
+  if (thresholds) std::memcpy(thresholds, cb.thresholds, sizeof(cb.thresholds));
+  return QPS_OK;
+}
+
+static qps_status check_encoder(const void* x, int64_t rows, int32_t d, int64_t stride,
+                                const char* name) {
+  const std::string n(name);
+  if (rows < 0) return fail(QPS_ERR_INVALID_ARG, n + ": rows must be >= 0");
+  if (d != 32 && d != 64 && d != 128 && d != 256 && d != 512)
+    return fail(QPS_ERR_UNSUPPORTED, n + ": head_dim must be 32, 64, 128, 256 or 512");
+  if (rows > 0 && !x) return fail(QPS_ERR_INVALID_ARG, n + ": x is NULL");
+  if (stride < d) return fail(QPS_ERR_INVALID_ARG, n + ": x_row_stride must be >= head_dim");
+  return QPS_OK;
+}
+
+qps_status qps_kv_quant_q8_0(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                             void* codes, void* scales, void* stream) {
+  qps_status st = check_encoder(x, rows, d, x_row_stride, "kv_quant_q8_0");
+  if (st != QPS_OK) return st;
+  if (rows == 0) return QPS_OK;
+  if (!codes || !scales) return fail(QPS_ERR_INVALID_ARG, "kv_quant_q8_0: codes / scales are NULL");
+  if (!aligned(x, 16) || x_row_stride % 8)
+    return fail(QPS_ERR_INVALID_ARG, "kv_quant_q8_0: x must be 16-byte aligned with a row stride multiple of 8");
+  if (!aligned(codes, 8) || !aligned(scales, 2))
+    return fail(QPS_ERR_INVALID_ARG, "kv_quant_q8_0: codes must be 8-byte and scales 2-byte aligned");
+  return launch_quant_q8_0(reinterpret_cast<const __half*>(x), rows, d, x_row_stride,
+                           reinterpret_cast<int8_t*>(codes), reinterpret_cast<__half*>(scales),
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* lo2, void* hi1, void* norms, void* stream) {
+  qps_status st = check_encoder(x, rows, d, x_row_stride, "kv_quant_tq3");
+  if (st != QPS_OK) return st;
+  if (!signs) return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq3: signs is NULL");
+  if (rows == 0) return QPS_OK;
+  if (!lo2 || !hi1 || !norms) return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq3: an output plane is NULL");
+  if (!aligned(x, 2) || !aligned(hi1, 4) || !aligned(norms, 2))
+    return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq3: x / norms must be 2-byte and hi1 4-byte aligned");
+  return launch_quant_tq3(reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs,
+                          reinterpret_cast<uint8_t*>(lo2), reinterpret_cast<uint8_t*>(hi1),
+                          reinterpret_cast<__half*>(norms), reinterpret_cast<cudaStream_t>(stream));
+}
+
+qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out, size_t* workspace_bytes_out) {
+  int n = 0;
+  size_t ws = 0;
+  qps_status st = resolve_attn(a, nullptr, &n, &ws);
+  if (st != QPS_OK) return st;
+  if (n_split_out) *n_split_out = n;
+  if (workspace_bytes_out) *workspace_bytes_out = a->o_parts ? 0 : ws;
+  return QPS_OK;
+}
+
+qps_status qps_attn_decode_window(const qps_attn_args* a, void* stream) {
+  AttnParams p;
+  int n = 0;
+  qps_status st = resolve_attn(a, &p, &n, nullptr);
+  if (st != QPS_OK) return st;
+  return run_attn(a, p, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qps_status qps_lse_combine(const float* o_parts, const float* lse_parts, int32_t n_parts,
+                           int64_t rows, int32_t d, float* o, float* lse, void* stream) {
+  if (n_parts < 1) return fail(QPS_ERR_INVALID_ARG, "lse_combine: n_parts must be >= 1");
+  if (rows < 0) return fail(QPS_ERR_INVALID_ARG, "lse_combine: rows must be >= 0");
+  if (rows == 0) return QPS_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return fail(QPS_ERR_INVALID_ARG, "lse_combine: NULL pointer");
+  if (!aligned(o_parts, 4) || !aligned(o, 4)) return fail(QPS_ERR_INVALID_ARG, "lse_combine: misaligned pointer");
+  return launch_combine(o_parts, lse_parts, n_parts, rows, d, o, lse, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "qps.h"
+
+namespace qps {
+
+// ---- error reporting ------------------------------------------------------------
+qps_status fail(qps_status st, const std::string& msg);
+qps_status cuda_fail(cudaError_t err, const char* what);
+void count_launch(int n = 1);
+
+#define QPS_CUDA_TRY(expr)                              \
+  do {                                                  \
+    cudaError_t _e = (expr);                            \
+    if (_e != cudaSuccess) return ::qps::cuda_fail(_e, #expr); \
+  } while (0)
+
+// ---- device facts -----------------------------------------------------------------
+int sm_count_current();
+
+// ---- TQ3 codebook (computed once on the host from the Gaussian density) -----------
+struct Codebook {
+  float levels[8];
+  float thresholds[7];
+};
+const Codebook& tq3_codebook();
+
+// ---- bytes per row of each storage plane ------------------------------------------
+inline int64_t plane_row_bytes(int fmt, int plane, int d) {
+  switch (fmt) {
+    case QPS_FMT_F16: return plane == 0 ? 2 * (int64_t)d : 0;
+    case QPS_FMT_Q8_0: return plane == 0 ? d : plane == 1 ? 2 * (d / 32) : 0;
+    case QPS_FMT_TQ3: return plane == 0 ? d / 4 : plane == 1 ? d / 8 : plane == 2 ? 2 : 0;
+    default: return 0;
+  }
+}
+inline int plane_count(int fmt) {
+  return fmt == QPS_FMT_F16 ? 1 : fmt == QPS_FMT_Q8_0 ? 2 : fmt == QPS_FMT_TQ3 ? 3 : 0;
+}
+
+// ---- attention kernel parameters ---------------------------------------------------
+constexpr int kMaxSignWords = 16;  // head_dim <= 512
+
+struct KvSide {
+  const void* data;
+  const void* aux;
+  const void* aux2;
+  int64_t tok, head, batch;  // strides in rows
+};
+
+struct AttnParams {
+  const __half* q;
+  int64_t q_bstride;
+  int batch, hq, hkv, d, group;
+  int kfmt, vfmt;
+  KvSide k, v;
+  int64_t begin, end;
+  int n_split;
+  int64_t chunk;       // positions per split
+  float scale, softcap;
+  int shared;          // 1: every batch entry reads the same KV rows
+  int rows_per_cta;    // shared ? batch * group : group
+  int64_t rows_total;  // batch * hq
+  float* o_parts;
+  float* lse_parts;
+  int part_offset;
+  uint32_t vsigns[kMaxSignWords];
+  float tq_levels[8];
+};
+
+// Validated, resolved form of qps_attn_args.
+qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split, size_t* ws_bytes);
+qps_status launch_attn(const AttnParams& p, cudaStream_t stream);
+qps_status launch_combine(const float* o_parts, const float* lse_parts, int n_parts,
+                          int64_t rows, int d, float* o, float* lse, cudaStream_t stream);
+// Runs a resolved attention in whichever output mode the args ask for.
+qps_status run_attn(const qps_attn_args* a, const AttnParams& p, int n_split, cudaStream_t s);
+
+qps_status launch_quant_q8_0(const __half* x, int64_t rows, int d, int64_t stride,
+                             int8_t* codes, __half* scales, cudaStream_t s);
+qps_status launch_quant_tq3(const __half* x, int64_t rows, int d, int64_t stride,
+                            const uint32_t* signs, uint8_t* lo2, uint8_t* hi1, __half* norms,
+                            cudaStream_t s);
+
+}  // namespace qps

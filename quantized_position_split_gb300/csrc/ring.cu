@@ -1,0 +1,374 @@
+// Step-spanning tail-prefetch ring and the native decode-step runner.
+//
+// Design from "Rolling-KV: step/graph-level tail prefetch (design)", section "The fix:
+// a persistent, step-spanning tail-prefetch ring": B = 2..4 device staging slots sized
+// once; one flat schedule of (layer, tile) tail reads per step, kept B tiles ahead on a
+// dedicated copy stream; each op waits for its tile's copy_done and records
+// compute_done; a slot is refilled only after its compute_done (the write-after-read
+// discipline replaces a per-op barrier); events are created once, never per op.  Each
+// tile is one bulk host-to-device transfer per plane (the tail is stored token-major,
+// so a tile is one contiguous range), after the lesson of "F5 M7 — Rolling KV:
+// position-windowed KV residency", section "2026-07-06 — bs2 tail-spill curve" (one
+// transfer per tile instead of per-head strided copies).
+//
+// Every wait is either a device-side stream/event dependency or a host poll with a
+// deadline; nothing here can block forever.
+#include <chrono>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "internal.h"
+
+struct qps_ring {
+  static constexpr uint64_t kMagic = 0x7170735f72696e67ULL;  // "qps_ring"
+  uint64_t magic = kMagic;
+  int device = 0;
+  int n_slots = 0;
+  size_t slot_bytes = 0;
+  void* slots[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaStream_t copy = nullptr;
+  cudaEvent_t copy_done[4] = {};
+  cudaEvent_t compute_done[4] = {};
+  bool compute_recorded[4] = {false, false, false, false};
+  std::vector<qps_tile_desc> tiles;
+  std::vector<size_t> offsets;  // per tile: 6 plane offsets within the slot
+  int next_consume = 0;
+  bool open = false;
+};
+
+namespace qps {
+namespace {
+
+constexpr size_t kPlaneAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool valid_ring(const qps_ring* r) { return r && r->magic == qps_ring::kMagic; }
+
+qps_status check_pinned(const void* p, const char* what) {
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(QPS_ERR_INVALID_ARG, std::string(what) + ": not a CUDA-known host pointer");
+  }
+  if (attr.type != cudaMemoryTypeHost)
+    return fail(QPS_ERR_INVALID_ARG, std::string(what) + ": tail planes must be pinned host memory");
+  return QPS_OK;
+}
+
+qps_status issue_copy(qps_ring* r, int i) {
+  const int slot = i % r->n_slots;
+  const qps_tile_desc& t = r->tiles[i];
+  if (r->compute_recorded[slot]) QPS_CUDA_TRY(cudaStreamWaitEvent(r->copy, r->compute_done[slot], 0));
+  char* base = reinterpret_cast<char*>(r->slots[slot]);
+  const size_t* off = &r->offsets[(size_t)i * 6];
+  for (int p = 0; p < t.n_k_planes; ++p)
+    if (t.bytes_k[p])
+      QPS_CUDA_TRY(cudaMemcpyAsync(base + off[p], t.host_k[p], t.bytes_k[p], cudaMemcpyHostToDevice, r->copy));
+  for (int p = 0; p < t.n_v_planes; ++p)
+    if (t.bytes_v[p])
+      QPS_CUDA_TRY(cudaMemcpyAsync(base + off[3 + p], t.host_v[p], t.bytes_v[p], cudaMemcpyHostToDevice, r->copy));
+  QPS_CUDA_TRY(cudaEventRecord(r->copy_done[slot], r->copy));
+  return QPS_OK;
+}
+
+// Bytes a view spanning `tokens` tokens of a token-major tile needs in plane `plane`.
+int64_t plane_need(const qps_kv_view& v, int plane, int d, int64_t tokens, int hkv) {
+  if (tokens == 0) return 0;
+  const int64_t rows = (tokens - 1) * v.tok_stride + (int64_t)(hkv - 1) * v.head_stride + 1;
+  return rows * plane_row_bytes(v.fmt, plane, d);
+}
+
+qps_status tail_attend(qps_ring* r, int idx, const qps_attn_args* a_in, cudaStream_t compute,
+                       int64_t parts_capacity, int* n_split_used) {
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "decode_tail: invalid or destroyed ring");
+  if (!r->open) return fail(QPS_ERR_STATE, "decode_tail: no open step");
+  if (!a_in) return fail(QPS_ERR_INVALID_ARG, "decode_tail: args is NULL");
+  if (idx != r->next_consume)
+    return fail(QPS_ERR_STATE, "decode_tail: tiles must be consumed in schedule order (expected " +
+                                   std::to_string(r->next_consume) + ", got " + std::to_string(idx) + ")");
+  const qps_tile_desc& t = r->tiles[idx];
+  const int slot = idx % r->n_slots;
+  qps_attn_args a = *a_in;
+  if (t.n_k_planes != plane_count(a.k.fmt) || t.n_v_planes != plane_count(a.v.fmt))
+    return fail(QPS_ERR_INVALID_ARG, "decode_tail: tile plane counts do not match the k / v formats");
+  char* base = reinterpret_cast<char*>(r->slots[slot]);
+  const size_t* off = &r->offsets[(size_t)idx * 6];
+  const void* kp[3] = {nullptr, nullptr, nullptr};
+  const void* vp[3] = {nullptr, nullptr, nullptr};
+  for (int p = 0; p < t.n_k_planes; ++p) {
+    kp[p] = base + off[p];
+    if (plane_need(a.k, p, a.d, t.tokens, a.hkv) > (int64_t)t.bytes_k[p])
+      return fail(QPS_ERR_INVALID_ARG, "decode_tail: a K plane of the tile is smaller than the view needs");
+  }
+  for (int p = 0; p < t.n_v_planes; ++p) {
+    vp[p] = base + off[3 + p];
+    if (plane_need(a.v, p, a.d, t.tokens, a.hkv) > (int64_t)t.bytes_v[p])
+      return fail(QPS_ERR_INVALID_ARG, "decode_tail: a V plane of the tile is smaller than the view needs");
+  }
+  a.k.data = kp[0];
+  a.k.aux = kp[1];
+  a.k.aux2 = kp[2];
+  a.v.data = vp[0];
+  a.v.aux = vp[1];
+  a.v.aux2 = vp[2];
+  a.k.batch_stride = a.v.batch_stride = 0;  // one tail tile serves every batch entry
+  a.kv_begin = 0;
+  a.kv_end = t.tokens;
+  AttnParams p;
+  int n_split = 0;
+  qps_status st = resolve_attn(&a, &p, &n_split, nullptr);
+  if (st != QPS_OK) return st;
+  if (a.o_parts && (int64_t)a.part_offset + n_split > parts_capacity)
+    return fail(QPS_ERR_INVALID_ARG, "decode_tail: parts capacity exceeded");
+  QPS_CUDA_TRY(cudaStreamWaitEvent(compute, r->copy_done[slot], 0));
+  st = run_attn(&a, p, n_split, compute);
+  if (st != QPS_OK) return st;
+  QPS_CUDA_TRY(cudaEventRecord(r->compute_done[slot], compute));
+  r->compute_recorded[slot] = true;
+  r->next_consume++;
+  if (n_split_used) *n_split_used = n_split;
+  const int next = idx + r->n_slots;
+  if (next < (int)r->tiles.size()) return issue_copy(r, next);
+  return QPS_OK;
+}
+
+qps_status ring_sync(qps_ring* r, int timeout_ms) {
+  const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+  for (;;) {
+    bool busy = false;
+    cudaError_t e = cudaStreamQuery(r->copy);
+    if (e == cudaErrorNotReady) busy = true;
+    else if (e != cudaSuccess) return cuda_fail(e, "ring_sync: cudaStreamQuery");
+    for (int s = 0; s < r->n_slots && !busy; ++s) {
+      if (!r->compute_recorded[s]) continue;
+      e = cudaEventQuery(r->compute_done[s]);
+      if (e == cudaErrorNotReady) busy = true;
+      else if (e != cudaSuccess) return cuda_fail(e, "ring_sync: cudaEventQuery");
+    }
+    if (!busy) return QPS_OK;
+    if (std::chrono::steady_clock::now() >= deadline)
+      return fail(QPS_ERR_TIMEOUT, "ring_sync: copies or tail attention still running at the deadline");
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+}  // namespace
+}  // namespace qps
+
+using namespace qps;
+
+extern "C" {
+
+qps_status qps_ring_create(int32_t n_slots, size_t slot_bytes, int32_t device, qps_ring** out) {
+  if (!out) return fail(QPS_ERR_INVALID_ARG, "ring_create: out is NULL");
+  *out = nullptr;
+  if (n_slots < 2 || n_slots > 4) return fail(QPS_ERR_INVALID_ARG, "ring_create: n_slots must be 2..4");
+  if (slot_bytes == 0) return fail(QPS_ERR_INVALID_ARG, "ring_create: slot_bytes must be > 0");
+  if (device < 0) return fail(QPS_ERR_INVALID_ARG, "ring_create: device must be >= 0");
+  QPS_CUDA_TRY(cudaSetDevice(device));
+  qps_ring* r = new qps_ring();
+  r->device = device;
+  r->n_slots = n_slots;
+  r->slot_bytes = align_up(slot_bytes, kPlaneAlign);
+  qps_status st = QPS_OK;
+  cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
+  for (int s = 0; s < n_slots && e == cudaSuccess; ++s) {
+    e = cudaMalloc(&r->slots[s], r->slot_bytes);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->copy_done[s], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->compute_done[s], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    st = cuda_fail(e, "ring_create");
+    for (int s = 0; s < 4; ++s) {
+      if (r->slots[s]) cudaFree(r->slots[s]);
+      if (r->copy_done[s]) cudaEventDestroy(r->copy_done[s]);
+      if (r->compute_done[s]) cudaEventDestroy(r->compute_done[s]);
+    }
+    if (r->copy) cudaStreamDestroy(r->copy);
+    r->magic = 0;
+    delete r;
+    return st;
+  }
+  *out = r;
+  return QPS_OK;
+}
+
+qps_status qps_ring_destroy(qps_ring* r) {
+  if (!r) return QPS_OK;
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_destroy: invalid or destroyed ring");
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(r->device);
+  qps_status st = ring_sync(r, 10000);
+  if (st != QPS_OK) {
+    cudaSetDevice(prev);
+    return st;
+  }
+  for (int s = 0; s < r->n_slots; ++s) {
+    cudaFree(r->slots[s]);
+    cudaEventDestroy(r->copy_done[s]);
+    cudaEventDestroy(r->compute_done[s]);
+  }
+  cudaStreamDestroy(r->copy);
+  r->magic = 0;
+  delete r;
+  cudaSetDevice(prev);
+  return QPS_OK;
+}
+
+qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t n_tiles,
+                               void* compute_stream) {
+  (void)compute_stream;
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_begin_step: invalid or destroyed ring");
+  if (r->open) return fail(QPS_ERR_STATE, "ring_begin_step: the previous step is still open");
+  if (n_tiles < 0 || (n_tiles > 0 && !tiles)) return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: bad tile list");
+  std::vector<size_t> offsets((size_t)n_tiles * 6, 0);
+  for (int i = 0; i < n_tiles; ++i) {
+    const qps_tile_desc& t = tiles[i];
+    if (t.n_k_planes < 1 || t.n_k_planes > 3 || t.n_v_planes < 1 || t.n_v_planes > 3 || t.tokens < 0)
+      return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: tile " + std::to_string(i) + " has bad plane counts or tokens");
+    size_t cur = 0;
+    for (int p = 0; p < 6; ++p) {
+      const bool is_k = p < 3;
+      const int pi = is_k ? p : p - 3;
+      if (pi >= (is_k ? t.n_k_planes : t.n_v_planes)) continue;
+      const void* h = is_k ? t.host_k[pi] : t.host_v[pi];
+      const size_t b = is_k ? t.bytes_k[pi] : t.bytes_v[pi];
+      if (b > 0) {
+        if (!h) return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: NULL host plane");
+        qps_status st = check_pinned(h, "ring_begin_step");
+        if (st != QPS_OK) return st;
+      }
+      offsets[(size_t)i * 6 + p] = cur;
+      cur = align_up(cur + b, kPlaneAlign);
+    }
+    if (cur > r->slot_bytes)
+      return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: tile " + std::to_string(i) + " does not fit in a slot");
+  }
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (prev != r->device) return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: the ring's device is not current");
+  r->tiles.assign(tiles, tiles + n_tiles);
+  r->offsets.swap(offsets);
+  r->next_consume = 0;
+  r->open = true;
+  const int first = n_tiles < r->n_slots ? n_tiles : r->n_slots;
+  for (int i = 0; i < first; ++i) {
+    qps_status st = issue_copy(r, i);
+    if (st != QPS_OK) {
+      r->open = false;
+      return st;
+    }
+  }
+  return QPS_OK;
+}
+
+qps_status qps_attn_decode_tail(qps_ring* r, int32_t tile_index, const qps_attn_args* a,
+                                void* compute_stream) {
+  return tail_attend(r, tile_index, a, reinterpret_cast<cudaStream_t>(compute_stream), INT64_MAX,
+                     nullptr);
+}
+
+qps_status qps_ring_end_step(qps_ring* r) {
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_end_step: invalid or destroyed ring");
+  if (!r->open) return fail(QPS_ERR_STATE, "ring_end_step: no open step");
+  if (r->next_consume != (int)r->tiles.size()) {
+    r->open = false;
+    return fail(QPS_ERR_STATE, "ring_end_step: " + std::to_string(r->tiles.size() - r->next_consume) +
+                                   " tiles were never consumed");
+  }
+  r->open = false;
+  return QPS_OK;
+}
+
+qps_status qps_ring_sync(qps_ring* r, int32_t timeout_ms) {
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_sync: invalid or destroyed ring");
+  if (timeout_ms < 0) return fail(QPS_ERR_INVALID_ARG, "ring_sync: timeout_ms must be >= 0");
+  return ring_sync(r, timeout_ms);
+}
+
+qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n_tiles,
+                           const qps_layer_step* layers, int32_t n_layers, void* stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (n_layers < 0 || (n_layers > 0 && !layers)) return fail(QPS_ERR_INVALID_ARG, "decode_step: bad layer list");
+  int64_t want_tiles = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    if (layers[l].n_tiles < 0 || layers[l].n_device_parts < 0)
+      return fail(QPS_ERR_INVALID_ARG, "decode_step: negative part or tile count");
+    if (layers[l].n_tiles > 0 && !layers[l].tail) return fail(QPS_ERR_INVALID_ARG, "decode_step: tail template missing");
+    if (layers[l].n_device_parts + layers[l].n_tiles == 0)
+      return fail(QPS_ERR_INVALID_ARG, "decode_step: a layer has no parts");
+    want_tiles += layers[l].n_tiles;
+  }
+  if (want_tiles != n_tiles) return fail(QPS_ERR_INVALID_ARG, "decode_step: tile count does not match the layers' n_tiles");
+  if (n_tiles > 0 && !ring) return fail(QPS_ERR_INVALID_ARG, "decode_step: tiles given without a ring");
+  if (ring) {
+    qps_status st = qps_ring_begin_step(ring, tiles, n_tiles, stream);
+    if (st != QPS_OK) return st;
+  }
+  qps_status st = QPS_OK;
+  int tile = 0;
+  for (int l = 0; l < n_layers && st == QPS_OK; ++l) {
+    const qps_layer_step& L = layers[l];
+    int off = 0;
+    int64_t rows = -1;
+    int d = 0;
+    if (L.part_events[0]) {
+      cudaError_t e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(L.part_events[0]), s);
+      if (e != cudaSuccess) st = cuda_fail(e, "decode_step: cudaEventRecord");
+    }
+    for (int i = 0; i < L.n_device_parts && st == QPS_OK; ++i) {
+      qps_attn_args a = L.device_parts[i];
+      a.o_parts = L.o_parts;
+      a.lse_parts = L.lse_parts;
+      a.part_offset = off;
+      AttnParams p;
+      int n = 0;
+      st = resolve_attn(&a, &p, &n, nullptr);
+      if (st != QPS_OK) break;
+      if (off + n > L.parts_capacity) {
+        st = fail(QPS_ERR_INVALID_ARG, "decode_step: parts_capacity exceeded in layer " + std::to_string(l));
+        break;
+      }
+      rows = p.rows_total;
+      d = p.d;
+      st = run_attn(&a, p, n, s);
+      off += n;
+    }
+    if (st == QPS_OK && L.part_events[1]) {
+      cudaError_t e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(L.part_events[1]), s);
+      if (e != cudaSuccess) st = cuda_fail(e, "decode_step: cudaEventRecord");
+    }
+    for (int j = 0; j < L.n_tiles && st == QPS_OK; ++j, ++tile) {
+      qps_attn_args a = *L.tail;
+      a.o_parts = L.o_parts;
+      a.lse_parts = L.lse_parts;
+      a.part_offset = off;
+      int used = 0;
+      st = tail_attend(ring, tile, &a, s, L.parts_capacity, &used);
+      if (st != QPS_OK) break;
+      rows = (int64_t)a.batch * a.hq;
+      d = a.d;
+      off += used;
+    }
+    if (st != QPS_OK) break;
+    if (!L.o || !L.lse) {
+      st = fail(QPS_ERR_INVALID_ARG, "decode_step: o / lse are NULL");
+      break;
+    }
+    st = launch_combine(L.o_parts, L.lse_parts, off, rows, d, L.o, L.lse, s);
+  }
+  if (ring) {
+    if (st != QPS_OK) {
+      ring->open = false;
+      return st;
+    }
+    return qps_ring_end_step(ring);
+  }
+  return st;
+}
+
+}  // extern "C"

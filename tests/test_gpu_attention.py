@@ -1,0 +1,131 @@
+"""GPU decode attention, split and combine vs the float64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as oatt
+from oracle import pipeline
+from tests.helpers import assert_parity, parity_report
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qps():
+    import quantized_position_split_gb300 as q
+    from quantized_position_split_gb300 import build
+    build.build()
+    return q
+
+
+def _inputs(n, hq, hkv, d, seed, outliers=True):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((1, hq, d), generator=g).half()
+    k = torch.randn((n, hkv, d), generator=g)
+    if outliers:
+        for h in range(hkv):
+            k[:, h, torch.randperm(d, generator=g)[:4]] *= 20
+    v = torch.randn((n, hkv, d), generator=g).half()
+    return q, k.half(), v
+
+
+def test_lse_combine(qps):
+    g = torch.Generator().manual_seed(0)
+    o = torch.randn((7, 33, 128), generator=g)
+    l = torch.randn((7, 33), generator=g) * 5
+    l[2, :] = -float("inf")
+    l[:, 5] = -float("inf")  # a row with every part empty
+    oo, ll = qps.lse_combine(o.cuda(), l.cuda())
+    ro, rl = oatt.lse_combine(o.numpy(), l.numpy())
+    assert np.allclose(oo.cpu().numpy(), ro, atol=2e-6)
+    assert np.allclose(ll.cpu().numpy()[np.isfinite(rl)], rl[np.isfinite(rl)], atol=2e-6)
+    assert np.all(oo.cpu().numpy()[5] == 0) and np.isneginf(ll.cpu().numpy()[5])
+
+
+FORMATS = [("f16", "f16"), ("q8_0", "q8_0"), ("q8_0", "tq3"), ("f16", "tq3"), ("q8_0", "f16")]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("kf,vf", FORMATS)
+@pytest.mark.parametrize("softcap", [0.0, 30.0])
+def test_window_attention_formats(qps, d, kf, vf, softcap):
+    hq, hkv, n = 8, 2, 1000 + 7
+    q, k, v = _inputs(n, hq, hkv, d, seed=d + len(kf) * 7 + len(vf), outliers=True)
+    words = synth.sign_bits(d, 42)
+    K = qps.encode_kv(kf, k.cuda(), words)
+    V = qps.encode_kv(vf, v.cuda(), words)
+    qc = q.cuda()
+    scale = 1.0 / np.sqrt(d)
+    ro, rl = pipeline.layer_reference(q.numpy(), k.numpy(), v.numpy(), kf, vf, scale, softcap, words.numpy())
+    for n_split in (0, 1, 5, 4000):  # 4000 > positions: most splits are empty
+        a = qps.attn_args(qc, K, V, scale=scale, softcap=softcap, v_signs=words, n_split=n_split)
+        o, lse = qps.attn_decode_window(a)
+        assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq),
+                      (d, kf, vf, softcap, n_split))
+
+
+def test_sub_range_and_empty_range(qps):
+    d, hq, hkv, n = 128, 4, 1, 300
+    q, k, v = _inputs(n, hq, hkv, d, seed=3)
+    K = qps.encode_kv("f16", k.cuda())
+    V = qps.encode_kv("f16", v.cuda())
+    a = qps.attn_args(q.cuda(), K, V, scale=0.1, kv_begin=17, kv_end=211)
+    o, lse = qps.attn_decode_window(a)
+    ro, rl = oatt.gqa_decode(q.double().numpy(), k.double().numpy(), v.double().numpy(), 0.1, 0.0, 17, 211)
+    assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq))
+    a = qps.attn_args(q.cuda(), K, V, scale=0.1, kv_begin=50, kv_end=50)
+    o, lse = qps.attn_decode_window(a)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_split_identity_every_window_length(qps):
+    """Window [0, wc) on device + tail [wc, n) through the ring, merged, equals the
+    unsplit oracle for every wc in 0..n."""
+    d, hq, hkv, n = 64, 4, 1, 64
+    q, k, v = _inputs(n, hq, hkv, d, seed=11, outliers=False)
+    ro, rl = oatt.gqa_decode(q.double().numpy(), k.double().numpy(), v.double().numpy(), 0.125)
+    K = qps.encode_kv("f16", k.cuda())
+    V = qps.encode_kv("f16", v.cuda())
+    qc = q.cuda()
+    for wc in range(0, n + 1):
+        parts = (torch.zeros((64, hq, d), device="cuda"), torch.zeros((64, hq), device="cuda"))
+        off = 0
+        a = qps.attn_args(qc, K, V, scale=0.125, kv_begin=0, kv_end=wc, n_split=2)
+        qps.attn_decode_window(a, parts=parts, part_offset=0)
+        off = 2
+        tail = [] if wc == n else [(t, min(t + 7, n)) for t in range(wc, n, 7)]
+        if tail:
+            kh, vh = K.token_slice(wc, n).pinned_copy(), V.token_slice(wc, n).pinned_copy()
+            ring = qps.Ring(2, 64 * 1024)
+            ring.begin_step([qps.tile_desc(kh, vh, a0 - wc, b0 - wc) for a0, b0 in tail])
+            for i in range(len(tail)):
+                ta = qps.attn_args(qc, kh, vh, scale=0.125, n_split=1)
+                ring.decode_tail(i, ta, parts=parts, part_offset=off)
+                off += 1
+            ring.end_step()
+        o, lse = qps.lse_combine(parts[0][:off], parts[1][:off])
+        assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq), wc)
+        if tail:
+            ring.sync()
+            ring.close()
+
+
+def test_gqa_and_shared_batch(qps):
+    """A shared prefix (batch_stride 0) read by 5 batch entries equals each entry
+    attending it alone."""
+    d, hq, hkv, n, b = 128, 8, 2, 777, 5
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn((b, hq, d), generator=g).half()
+    k = torch.randn((n, hkv, d), generator=g).half()
+    v = torch.randn((n, hkv, d), generator=g).half()
+    words = synth.sign_bits(d, 42)
+    K = qps.encode_kv("q8_0", k.cuda())
+    V = qps.encode_kv("tq3", v.cuda(), words)
+    a = qps.attn_args(q.cuda(), K, V, scale=0.09, v_signs=words, shared=True)
+    o, lse = qps.attn_decode_window(a)
+    kh = pipeline.dequant("q8_0", k.numpy())
+    vh = pipeline.dequant("tq3", v.numpy(), words.numpy())
+    ro, rl = oatt.gqa_decode(q.double().numpy(), kh, vh, 0.09)
+    assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(b * hq, d), rl.reshape(b * hq))

@@ -1,0 +1,94 @@
+"""GPU encoders vs the oracle: codes, scales, planes and norms must be bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import q8_0 as oq8
+from oracle import turboquant as otq
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qps():
+    import quantized_position_split_gb300 as q
+    from quantized_position_split_gb300 import build
+    build.build()
+    return q
+
+
+def _rows(n, d, seed, outliers=True):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((n, d), generator=g)
+    if outliers:
+        ch = torch.randperm(d, generator=g)[:4]
+        x[:, ch] *= 20
+    x[3] = 0  # a zero row
+    x[5, :32] = 0  # a zero block
+    return x.half()
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256, 512])
+def test_q8_0_bit_exact(qps, d):
+    x = _rows(1000 + 3, d, d)
+    codes, scales = qps.kv_quant_q8_0(x.cuda())
+    rc, rs = oq8.encode(x.numpy())
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), rs.view(np.uint16))
+
+
+def test_q8_0_every_fp16_value_for_fixed_amax(qps):
+    """For amax in a few values, every finite fp16 x with |x| <= amax, one block each
+    31 values plus the amax element."""
+    allv = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    allv = allv[np.isfinite(allv)]
+    for amax in [1.0, 3.140625, 0.0009765625, 65504.0]:
+        vals = allv[np.abs(allv.astype(np.float64)) <= amax]
+        pad = (-len(vals)) % 31
+        vals = np.concatenate([vals, np.zeros(pad, dtype=np.float16)]).reshape(-1, 31)
+        blocks = np.concatenate([np.full((vals.shape[0], 1), amax, dtype=np.float16), vals], axis=1)
+        x = torch.from_numpy(blocks.copy())
+        codes, scales = qps.kv_quant_q8_0(x.cuda())
+        rc, rs = oq8.encode(blocks)
+        assert np.array_equal(codes.cpu().numpy(), rc), amax
+        assert np.array_equal(scales.cpu().numpy().view(np.uint16), rs.view(np.uint16)), amax
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256, 512])
+def test_tq3_bit_exact(qps, d):
+    x = _rows(2000 + 5, d, 100 + d, outliers=(d != 64))
+    words = synth.sign_bits(d, 42)
+    lo2, hi1, n = qps.kv_quant_tq3(x.cuda(), words)
+    rlo, rhi, rn = otq.encode(x.numpy(), words.numpy())
+    glo, ghi, gn = lo2.cpu().numpy(), hi1.cpu().numpy(), n.cpu().numpy()
+    assert np.array_equal(gn.view(np.uint16), rn.view(np.uint16))
+    bad = np.nonzero((glo != rlo).any(-1) | (ghi != rhi).any(-1))[0]
+    if bad.size:
+        # report how close the disagreeing coordinates were to a threshold
+        _, thr = otq.codebook()
+        xr = x.numpy()[bad[:4]].astype(np.float64)
+        s = otq.signs_from_words(words.numpy(), d)
+        z = otq.fwht(xr * s) / np.linalg.norm(xr, axis=1, keepdims=True)
+        dist = np.min(np.abs(z[..., None] - thr.astype(np.float64)), axis=-1).min()
+        pytest.fail(f"{bad.size} rows differ; nearest threshold distance {dist:.3e}")
+
+
+def test_tq3_sign_vector_changes_codes(qps):
+    x = _rows(64, 128, 7, outliers=False).cuda()
+    a = qps.kv_quant_tq3(x, synth.sign_bits(128, 42))[0]
+    b = qps.kv_quant_tq3(x, synth.sign_bits(128, 43))[0]
+    assert not torch.equal(a, b)
+
+
+def test_encoders_row_stride(qps):
+    x = _rows(300, 256, 9)
+    xs = x[:, :128]  # a strided view: row stride 256, head_dim 128
+    c1, s1 = qps.kv_quant_q8_0(x.cuda()[:, :128])
+    rc, rs = oq8.encode(xs.contiguous().numpy())
+    assert np.array_equal(c1.cpu().numpy(), rc)
+    words = synth.sign_bits(128, 42)
+    lo2, hi1, n = qps.kv_quant_tq3(x.cuda()[:, :128], words)
+    rlo, rhi, rn = otq.encode(xs.contiguous().numpy(), words.numpy())
+    assert np.array_equal(lo2.cpu().numpy(), rlo) and np.array_equal(hi1.cpu().numpy(), rhi)

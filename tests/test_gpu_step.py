@@ -1,0 +1,116 @@
+"""Whole decode steps (window + ring tail + combine) vs the oracle, ring invariances
+and the ring's host-side error paths, at parity-sized copies of every workload."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import helpers
+from tests.helpers import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qps():
+    import quantized_position_split_gb300 as q
+    from quantized_position_split_gb300 import build
+    build.build()
+    return q
+
+
+SPLIT_CONFIGS = [c.name for c in synth.CONFIGS if c.kind == "split"]
+
+
+@pytest.mark.parametrize("name", SPLIT_CONFIGS)
+def test_workload_step_parity(qps, name):
+    cfg = synth.parity_scaled(synth.by_name(name))
+    dec, kept = helpers.build_split_decoder(cfg, keep_inputs=range(cfg.layers))
+    assert dec.n_tiles == cfg.layers * len(dec.tile_ranges()) and len(dec.tile_ranges()) >= 3
+    for _ in range(2):  # the second step reuses slots whose events belong to step one
+        dec.step()
+        torch.cuda.synchronize()
+        for layer, (q, k, v) in kept.items():
+            ro, rl = helpers.oracle_layer(cfg, q, k, v)
+            assert_parity(dec.o[layer].cpu().numpy(), dec.lse[layer].cpu().numpy(),
+                          ro.reshape(-1, cfg.d), rl.reshape(-1), (name, layer))
+    dec.ring.sync()
+    dec.close()
+
+
+def test_fanout_parity(qps):
+    from quantized_position_split_gb300.decode import FanoutDecoder
+    cfg = synth.parity_scaled(synth.by_name("fanout_prefix"))
+    ins = helpers.fanout_inputs(cfg, "cuda")
+    fd = FanoutDecoder(agents=cfg.agents, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d, k_fmt=cfg.k_fmt,
+                       v_fmt=cfg.v_fmt, scale=cfg.scale, softcap=cfg.softcap,
+                       signs=helpers.signs_for(cfg)).load(*ins).build()
+    fd.step()
+    torch.cuda.synchronize()
+    ro, rl = helpers.oracle_fanout(cfg, *ins)
+    assert_parity(fd.o.cpu().numpy(), fd.lse.cpu().numpy(), ro.reshape(-1, cfg.d), rl.reshape(-1))
+
+
+def test_ring_depth_and_tile_invariance(qps):
+    cfg = synth.parity_scaled(synth.by_name("qwen14b_q8"), layers=2)
+    outs = {}
+    for slots, tile in [(2, 512), (3, 512), (4, 512), (3, 300), (2, 2000)]:
+        dec, _ = helpers.build_split_decoder(cfg, ring_slots=slots, tile_tokens=tile)
+        dec.step()
+        torch.cuda.synchronize()
+        outs[(slots, tile)] = (dec.o.cpu().clone(), dec.lse.cpu().clone())
+        dec.ring.sync()
+        dec.close()
+    base = outs[(3, 512)]
+    for key in [(2, 512), (4, 512)]:  # same tiles: bit-identical whatever the depth
+        assert torch.equal(outs[key][0], base[0]) and torch.equal(outs[key][1], base[1]), key
+    for key in [(3, 300), (2, 2000)]:  # other tiles: same values up to rounding
+        r = helpers.parity_report(outs[key][0].numpy(), outs[key][1].numpy(),
+                                  base[0].double().numpy(), base[1].double().numpy())
+        assert r["rel_l2"] < 1e-5 and r["dlse"] < 1e-5, (key, r)
+
+
+def test_ring_host_side_errors(qps):
+    from quantized_position_split_gb300 import _native as N
+    d, hkv, hq = 128, 2, 4
+    k = torch.randn((600, hkv, d)).half()
+    K = qps.encode_kv("f16", k.cuda())
+    kh = K.pinned_copy()
+    q = torch.randn((1, hq, d)).half().cuda()
+    parts = (torch.zeros((16, hq, d), device="cuda"), torch.zeros((16, hq), device="cuda"))
+    ring = qps.Ring(2, 200 * 1024)
+    tiles = [qps.tile_desc(kh, kh, a, a + 100) for a in (0, 100, 200)]
+    ring.begin_step(tiles)
+    # a second begin while a step is open
+    with pytest.raises(N.QpsError) as e:
+        ring.begin_step(tiles)
+    assert e.value.status == N.QPS_ERR_STATE
+    # out of order
+    with pytest.raises(N.QpsError) as e:
+        ring.decode_tail(1, qps.attn_args(q, kh, kh, scale=0.1, n_split=1), parts=parts, part_offset=0)
+    assert e.value.status == N.QPS_ERR_STATE
+    ring.decode_tail(0, qps.attn_args(q, kh, kh, scale=0.1, n_split=1), parts=parts, part_offset=0)
+    # closing with unconsumed tiles
+    with pytest.raises(N.QpsError) as e:
+        ring.end_step()
+    assert e.value.status == N.QPS_ERR_STATE
+    ring.sync()
+    # unpinned (pageable) host planes are refused before any copy
+    kp = qps.KV("f16", (k.clone(),), 600, hkv, d, hkv)
+    with pytest.raises(N.QpsError) as e:
+        ring.begin_step([qps.tile_desc(kp, kp, 0, 100)])
+    assert e.value.status == N.QPS_ERR_INVALID_ARG
+    # a tile larger than a slot
+    with pytest.raises(N.QpsError) as e:
+        ring.begin_step([qps.tile_desc(kh, kh, 0, 600)])
+    assert e.value.status == N.QPS_ERR_INVALID_ARG
+    # the ring still works afterwards
+    ring.begin_step(tiles[:1])
+    ring.decode_tail(0, qps.attn_args(q, kh, kh, scale=0.1, n_split=1), parts=parts, part_offset=0)
+    ring.end_step()
+    ring.sync()
+    ring.close()
+    with pytest.raises(N.QpsError):
+        ring.handle = None
+        N.check(qps.lib().qps_ring_end_step(None))

@@ -189,6 +189,12 @@ typedef struct qps_attn_args {
 QPS_API qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out,
                          size_t* workspace_bytes_out);
 
+/* Which kernel the args select (host only): 1 = tensor-core path (every K / V plane
+ * token-contiguous, tok_stride == 1, with 16-byte-aligned bases and head / batch
+ * offsets), 0 = CUDA-core path (any other strides), negative = the args are invalid
+ * (a qps_status, negated).  Both paths compute the same attention. */
+QPS_API int32_t qps_attn_path(const qps_attn_args* a);
+
 /* Decode attention over device-resident KV (the window [0, wc), or any device part)
  * [RKV].  Supported: D in {64, 128, 256, 512}; K in {F16, Q8_0}; V in {F16, Q8_0, TQ3};
  * hq a multiple of hkv.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
@@ -203,6 +209,21 @@ QPS_API qps_status qps_attn_decode_window(const qps_attn_args* a, void* stream);
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 QPS_API qps_status qps_lse_combine(const float* o_parts, const float* lse_parts, int32_t n_parts,
                            int64_t rows, int32_t d, float* o, float* lse, void* stream);
+
+/* ---- Pinned host storage of the tail ------------------------------------------- */
+
+/* Page-locked host memory for the tail ("F5 M7 — Rolling KV: position-windowed KV
+ * residency", section "Storage layer": per-layer KV lives in pinned host memory
+ * allocated with cudaHostAlloc(cudaHostAllocPortable)).  One large arena holding every
+ * tile of the tail keeps the copy engine's reads on few, large page-locked regions.
+ *   bytes  > 0;  flags: 0 = portable, 1 = portable | write-combined;
+ *   out    receives the host pointer (256-byte aligned), owned by the caller until
+ *          qps_host_free.
+ * Errors: INVALID_ARG, CUDA (allocation failure). */
+QPS_API qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out);
+
+/* Free memory from qps_host_alloc (NULL is a no-op).  Errors: CUDA. */
+QPS_API qps_status qps_host_free(void* p);
 
 /* ---- Tail-prefetch ring [RING] ------------------------------------------------ */
 
@@ -219,11 +240,13 @@ QPS_API qps_status qps_ring_create(int32_t n_slots, size_t slot_bytes, int32_t d
  * NULL is a no-op.  Errors: TIMEOUT (resources leaked rather than freed in use). */
 QPS_API qps_status qps_ring_destroy(qps_ring* ring);
 
-/* One tail tile: `tokens` consecutive positions of one layer's tail, stored
- * token-major (row = token * hkv + head) in one contiguous pinned-host range per
- * plane.  K planes first (1 for F16, 2 for Q8_0, 3 for TQ3, in data/aux/aux2
- * order), then V planes.  The ring places plane p at a 256-byte-aligned offset of the
- * slot; their total must fit in slot_bytes. */
+/* One tail tile: `tokens` consecutive positions of one layer's tail, stored in one
+ * contiguous pinned-host range per plane, rows addressed inside the tile by
+ * row = token * tok_stride + head * head_stride (the same for every plane of K and
+ * V): token-major tiles use (hkv, 1), head-major tiles (1, padded tile length).  K
+ * planes first (1 for F16, 2 for Q8_0, 3 for TQ3, in data/aux/aux2 order), then V
+ * planes.  The ring places plane p at a 256-byte-aligned offset of the slot; their
+ * total must fit in slot_bytes. */
 typedef struct qps_tile_desc {
   int32_t n_k_planes, n_v_planes;
   const void* host_k[3];
@@ -231,6 +254,8 @@ typedef struct qps_tile_desc {
   const void* host_v[3];
   size_t bytes_v[3];
   int64_t tokens;
+  int64_t tok_stride;  /* rows; > 0 */
+  int64_t head_stride; /* rows; >= 0 */
 } qps_tile_desc;
 
 /* Start a step: copy the flat (layer, tile) schedule (host array, read during the
@@ -245,8 +270,9 @@ QPS_API qps_status qps_ring_begin_step(qps_ring* ring, const qps_tile_desc* tile
 /* Attend tile `tile_index` of the open step [RKV, RING].  Tiles must be consumed in
  * schedule order.  The compute stream waits for the slot's copy_done, the attention
  * runs on the slot (the k / v views' data pointers in `a` are ignored and replaced by
- * the slot's planes; their fmt and strides are used; kv_begin / kv_end are replaced by
- * [0, tokens)), compute_done is recorded, and the copy of tile tile_index + n_slots
+ * the slot's planes, their token / head strides by the tile's, their batch strides by
+ * 0 (one tile serves every batch entry); their fmt is used; kv_begin / kv_end are
+ * replaced by [0, tokens)), compute_done is recorded, and the copy of tile tile_index + n_slots
  * into the same slot is enqueued behind it.  Output modes as for
  * qps_attn_decode_window.  Errors: STATE (out of order, no open step), INVALID_ARG,
  * UNSUPPORTED, CUDA. */

@@ -28,10 +28,12 @@ __all__ = [
     "kv_quant_q8_0",
     "kv_quant_tq3",
     "encode_kv",
+    "encode_kv_head_major",
     "attn_args",
     "attn_plan",
     "attn_decode_window",
     "lse_combine",
+    "HostArena",
     "Ring",
     "tile_desc",
     "StepPlan",
@@ -207,6 +209,14 @@ def attn_plan(a: N.AttnArgs):
     return n.value, ws.value
 
 
+def attn_path(a: N.AttnArgs) -> str:
+    """"tensor-core" or "cuda-core": the kernel the library selects for these args."""
+    r = int(lib().qps_attn_path(ctypes.byref(a)))
+    if r < 0:
+        N.check(-r)
+    return "tensor-core" if r == 1 else "cuda-core"
+
+
 def attn_decode_window(a: N.AttnArgs, *, o=None, lse=None, parts=None, part_offset: int = 0,
                        workspace=None, stream=None, device=None):
     """Run one device-resident attention part.
@@ -248,10 +258,50 @@ def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, o=None, lse=None
     return o, lse
 
 
-def tile_desc(k_host: KV, v_host: KV, t0: int, t1: int) -> N.TileDesc:
-    """Descriptor of positions [t0, t1) of a pinned, token-major host tail."""
+def encode_kv_head_major(fmt: str, x: torch.Tensor, signs=None, pad: int = 16, stream=None) -> KV:
+    """Store fp16 ``x[(batch,) tokens, hkv, D]`` (CUDA) in ``fmt``, head-major: planes
+    ``[(batch,) hkv, tokens_pad, row]`` with tokens_pad = tokens rounded up to ``pad``
+    (the padding rows hold zeros and are never attended).  Consecutive positions of a
+    head are adjacent rows, the layout the tensor-core decode streams."""
+    batched = x.dim() == 4
+    xb = x if batched else x.unsqueeze(0)
+    b, tokens, hkv, d = xb.shape
+    tp = (tokens + pad - 1) // pad * pad
+    xt = torch.zeros((b, hkv, tp, d), dtype=x.dtype, device=x.device)
+    xt[:, :, :tokens] = xb.permute(0, 2, 1, 3)
+    kv = encode_kv(fmt, xt.reshape(b, hkv * tp, 1, d), signs, stream)
+    planes = tuple(p.reshape((b, hkv, tp) + tuple(p.shape[3:])) if batched
+                   else p.reshape((hkv, tp) + tuple(p.shape[3:])) for p in kv.planes)
+    return KV(fmt, planes, tokens, hkv, d, tok_stride=1, head_stride=tp,
+              batch_stride=hkv * tp if batched else 0)
+
+
+def tile_desc(k_host: KV, v_host: KV, t0: Optional[int] = None, t1: Optional[int] = None) -> N.TileDesc:
+    """Ring descriptor of a pinned host tile.
+
+    With ``t0, t1`` given, a token-major cache (row = token * hkv + head) is sliced to
+    positions [t0, t1).  Without them, the cache is one whole tile described as it is
+    stored (e.g. head-major, ``encode_kv_head_major``).
+    """
     td = N.TileDesc()
+    if t0 is None:
+        if (v_host.tok_stride, v_host.head_stride) != (1, k_host.head_stride):
+            raise QpsError(N.QPS_ERR_INVALID_ARG, "K and V of a tile need the same layout")
+        td.tokens = k_host.tokens
+        td.tok_stride, td.head_stride = 1, k_host.head_stride
+        for side, kv in (("k", k_host), ("v", v_host)):
+            hosts = getattr(td, "host_" + side)
+            sizes = getattr(td, "bytes_" + side)
+            for i, p in enumerate(kv.planes):
+                hosts[i] = p.data_ptr()
+                sizes[i] = p.numel() * p.element_size()
+            setattr(td, "n_%s_planes" % side, len(kv.planes))
+        return td
+    for kv in (k_host, v_host):
+        if (kv.tok_stride, kv.head_stride, kv.batch_stride) != (kv.hkv, 1, 0):
+            raise QpsError(N.QPS_ERR_INVALID_ARG, "slicing needs an unbatched token-major cache")
     td.tokens = t1 - t0
+    td.tok_stride, td.head_stride = k_host.hkv, 1
     for side, kv in (("k", k_host), ("v", v_host)):
         hosts = getattr(td, "host_" + side)
         sizes = getattr(td, "bytes_" + side)
@@ -261,6 +311,53 @@ def tile_desc(k_host: KV, v_host: KV, t0: int, t1: int) -> N.TileDesc:
             sizes[i] = (t1 - t0) * row_bytes
         setattr(td, "n_%s_planes" % side, len(kv.planes))
     return td
+
+
+class HostArena:
+    """One page-locked host region from ``qps_host_alloc``, handed out as 256-byte
+    aligned CPU tensors that alias it (no copies).  Owned until ``close()``."""
+
+    def __init__(self, nbytes: int, write_combined: bool = False):
+        p = ctypes.c_void_p()
+        N.check(lib().qps_host_alloc(max(int(nbytes), 256), 1 if write_combined else 0, ctypes.byref(p)))
+        self.ptr = p.value
+        self.nbytes = max(int(nbytes), 256)
+        self.used = 0
+        self._buf = (ctypes.c_uint8 * self.nbytes).from_address(self.ptr)
+        self.tensor = torch.frombuffer(self._buf, dtype=torch.uint8)
+
+    def take(self, shape, dtype) -> torch.Tensor:
+        n = 1
+        for s in shape:
+            n *= int(s)
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        off = (self.used + 255) // 256 * 256
+        if off + nbytes > self.nbytes:
+            raise QpsError(N.QPS_ERR_INVALID_ARG, "host arena exhausted")
+        self.used = off + nbytes
+        return self.tensor[off:off + nbytes].view(dtype).view(tuple(shape))
+
+    def copy_in(self, kv: "KV") -> "KV":
+        """A copy of ``kv`` (any device) whose planes live in this arena."""
+        planes = []
+        for p in kv.planes:
+            dst = self.take(p.shape, p.dtype)
+            dst.copy_(p)
+            planes.append(dst)
+        return dataclasses.replace(kv, planes=tuple(planes))
+
+    def close(self):
+        if self.ptr:
+            self.tensor = None
+            self._buf = None
+            N.check(lib().qps_host_free(self.ptr))
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Ring:

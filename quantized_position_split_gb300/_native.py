@@ -81,6 +81,8 @@ class TileDesc(ctypes.Structure):
         ("host_v", c_void_p * 3),
         ("bytes_v", c_size_t * 3),
         ("tokens", c_int64),
+        ("tok_stride", c_int64),
+        ("head_stride", c_int64),
     ]
 
 
@@ -109,8 +111,11 @@ SIGNATURES = [
     ("qps_kv_quant_tq3", c_int32,
      [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p, c_void_p]),
     ("qps_attn_plan", c_int32, [POINTER(AttnArgs), POINTER(c_int32), POINTER(c_size_t)]),
+    ("qps_attn_path", c_int32, [POINTER(AttnArgs)]),
     ("qps_attn_decode_window", c_int32, [POINTER(AttnArgs), c_void_p]),
     ("qps_lse_combine", c_int32, [c_void_p, c_void_p, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p]),
+    ("qps_host_alloc", c_int32, [c_size_t, c_int32, POINTER(c_void_p)]),
+    ("qps_host_free", c_int32, [c_void_p]),
     ("qps_ring_create", c_int32, [c_int32, c_size_t, c_int32, POINTER(c_void_p)]),
     ("qps_ring_destroy", c_int32, [c_void_p]),
     ("qps_ring_begin_step", c_int32, [c_void_p, POINTER(TileDesc), c_int32, c_void_p]),

@@ -206,8 +206,42 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
 }
 
 qps_status launch_attn_simple(const AttnParams& p, cudaStream_t s);
+qps_status launch_attn_mma_d64(const AttnParams& p, cudaStream_t s);
+qps_status launch_attn_mma_d128(const AttnParams& p, cudaStream_t s);
+qps_status launch_attn_mma_d256(const AttnParams& p, cudaStream_t s);
+qps_status launch_attn_mma_d512(const AttnParams& p, cudaStream_t s);
 
-qps_status launch_attn(const AttnParams& p, cudaStream_t s) { return launch_attn_simple(p, s); }
+namespace {
+
+// The tensor-core kernel stages each plane of a (KV head, batch entry) as one
+// token-contiguous range with 16-byte copies: it needs tok_stride == 1 and every
+// plane's head / batch offsets on 16-byte boundaries.
+bool side_fits_mma(const KvSide& s, int fmt, int d) {
+  if (s.tok != 1) return false;
+  const void* planes[3] = {s.data, s.aux, s.aux2};
+  for (int i = 0; i < plane_count(fmt); ++i) {
+    const int64_t rb = plane_row_bytes(fmt, i, d);
+    if (((uintptr_t)planes[i] & 15) || (s.head * rb) % 16 || (s.batch * rb) % 16) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+bool attn_uses_mma(const AttnParams& p) {
+  return side_fits_mma(p.k, p.kfmt, p.d) && side_fits_mma(p.v, p.vfmt, p.d);
+}
+
+qps_status launch_attn(const AttnParams& p, cudaStream_t s) {
+  if (!attn_uses_mma(p)) return launch_attn_simple(p, s);
+  switch (p.d) {
+    case 64: return launch_attn_mma_d64(p, s);
+    case 128: return launch_attn_mma_d128(p, s);
+    case 256: return launch_attn_mma_d256(p, s);
+    case 512: return launch_attn_mma_d512(p, s);
+    default: return fail(QPS_ERR_UNSUPPORTED, "attention: head_dim must be 64, 128, 256 or 512");
+  }
+}
 
 qps_status run_attn(const qps_attn_args* a, const AttnParams& p_in, int n_split, cudaStream_t s) {
   AttnParams p = p_in;
@@ -319,6 +353,21 @@ qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out, size_t* w
   if (n_split_out) *n_split_out = n;
   if (workspace_bytes_out) *workspace_bytes_out = a->o_parts ? 0 : ws;
   return QPS_OK;
+}
+
+int32_t qps_attn_path(const qps_attn_args* a) {
+  AttnParams p;
+  int n = 0;
+  const qps_attn_args* probe = a;
+  qps_attn_args tmp;
+  if (a && a->n_split == 0) {  // the kernel choice does not depend on the split count
+    tmp = *a;
+    tmp.n_split = 1;
+    probe = &tmp;
+  }
+  qps_status st = resolve_attn(probe, &p, &n, nullptr);
+  if (st != QPS_OK) return -(int32_t)st;
+  return attn_uses_mma(p) ? 1 : 0;
 }
 
 qps_status qps_attn_decode_window(const qps_attn_args* a, void* stream) {

@@ -1,0 +1,6 @@
+// Tensor-core decode attention instances for head_dim 512 (see attn_mma.cuh).
+#include "attn_mma.cuh"
+
+namespace qps {
+qps_status launch_attn_mma_d512(const AttnParams& p, cudaStream_t s) { return mma::launch_mma_d<512>(p, s); }
+}  // namespace qps

@@ -92,6 +92,8 @@ qps_status tail_attend(qps_ring* r, int idx, const qps_attn_args* a_in, cudaStre
   const qps_tile_desc& t = r->tiles[idx];
   const int slot = idx % r->n_slots;
   qps_attn_args a = *a_in;
+  a.k.tok_stride = a.v.tok_stride = t.tok_stride;
+  a.k.head_stride = a.v.head_stride = t.head_stride;
   if (t.n_k_planes != plane_count(a.k.fmt) || t.n_v_planes != plane_count(a.v.fmt))
     return fail(QPS_ERR_INVALID_ARG, "decode_tail: tile plane counts do not match the k / v formats");
   char* base = reinterpret_cast<char*>(r->slots[slot]);
@@ -162,6 +164,22 @@ using namespace qps;
 
 extern "C" {
 
+qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out) {
+  if (!out) return fail(QPS_ERR_INVALID_ARG, "host_alloc: out is NULL");
+  *out = nullptr;
+  if (bytes == 0) return fail(QPS_ERR_INVALID_ARG, "host_alloc: bytes must be > 0");
+  if (flags != 0 && flags != 1) return fail(QPS_ERR_INVALID_ARG, "host_alloc: flags must be 0 or 1");
+  unsigned int f = cudaHostAllocPortable | (flags == 1 ? cudaHostAllocWriteCombined : 0u);
+  QPS_CUDA_TRY(cudaHostAlloc(out, bytes, f));
+  return QPS_OK;
+}
+
+qps_status qps_host_free(void* p) {
+  if (!p) return QPS_OK;
+  QPS_CUDA_TRY(cudaFreeHost(p));
+  return QPS_OK;
+}
+
 qps_status qps_ring_create(int32_t n_slots, size_t slot_bytes, int32_t device, qps_ring** out) {
   if (!out) return fail(QPS_ERR_INVALID_ARG, "ring_create: out is NULL");
   *out = nullptr;
@@ -230,6 +248,8 @@ qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t 
     const qps_tile_desc& t = tiles[i];
     if (t.n_k_planes < 1 || t.n_k_planes > 3 || t.n_v_planes < 1 || t.n_v_planes > 3 || t.tokens < 0)
       return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: tile " + std::to_string(i) + " has bad plane counts or tokens");
+    if (t.tok_stride <= 0 || t.head_stride < 0)
+      return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: tile " + std::to_string(i) + " has bad strides");
     size_t cur = 0;
     for (int p = 0; p < 6; ++p) {
       const bool is_k = p < 3;

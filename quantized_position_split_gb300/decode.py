@@ -1,12 +1,15 @@
 """Assembly of a whole position-split decode step from per-layer fp16 K / V caches.
 
-Each layer's cache is encoded on the GPU by the library's encoders, its window
-[0, wc) stays in device memory, and its tail [wc, n_kv) is copied once to pinned host
-memory, token-major, so that a tile of consecutive positions is one contiguous range
-per plane ("Rolling-KV: step/graph-level tail prefetch (design)", section "The fix: a
-persistent, step-spanning tail-prefetch ring"; "F5 M7 — Rolling KV: position-windowed
-KV residency", header status block).  A step is one ``qps_decode_step`` call: per
-layer, the window part, the layer's ring tiles, and the LSE combine.
+Each layer's cache is encoded on the GPU by the library's encoders.  Its window
+[0, wc) stays in device memory; its tail [wc, n_kv) is cut into tiles of
+``tile_tokens`` positions, each copied once to pinned host memory as one contiguous
+range per plane ("Rolling-KV: step/graph-level tail prefetch (design)", section "The
+fix: a persistent, step-spanning tail-prefetch ring"; "F5 M7 — Rolling KV:
+position-windowed KV residency", header status block).  Both are stored head-major
+(consecutive positions of one KV head are adjacent rows, head length padded to 16) so
+that the tensor-core decode streams each head's rows as one range.  A step is one
+``qps_decode_step`` call: per layer, the window part, the layer's ring tiles, and the
+LSE combine.
 
 The shared-prefix batch ("F5 M6 — PolyKV (shared compressed KV pool)", section "S1 —
 SharedKVPool") is assembled by ``FanoutDecoder``: one compressed prefix read by every
@@ -19,7 +22,7 @@ from typing import List, Optional
 
 import torch
 
-from . import KV, Ring, StepPlan, attn_args, attn_plan, encode_kv, tile_desc
+from . import KV, HostArena, Ring, StepPlan, attn_args, attn_plan, encode_kv_head_major, tile_desc
 
 
 def _parts_buffers(capacity: int, rows: int, d: int, device):
@@ -48,8 +51,9 @@ class PositionSplitDecoder:
         self.o = torch.zeros((layers, self.rows, d), dtype=torch.float32, device=self.device)
         self.lse = torch.zeros((layers, self.rows), dtype=torch.float32, device=self.device)
         self.window: List[Optional[tuple]] = [None] * layers  # (K, V) on device
-        self.tail: List[Optional[tuple]] = [None] * layers  # (K, V) pinned host
+        self.tail: List[list] = [[] for _ in range(layers)]  # per tile: (K, V) pinned host
         self.ring: Optional[Ring] = None
+        self.arena: Optional[HostArena] = None
         self.plan: Optional[StepPlan] = None
         self.window_plan: Optional[StepPlan] = None
 
@@ -61,19 +65,39 @@ class PositionSplitDecoder:
         t = self.tile_tokens
         return [(a, min(a + t, self.tail_len)) for a in range(0, self.tail_len, t)]
 
+    def _arena_bytes(self) -> int:
+        """Pinned bytes the whole tail needs: every tile's planes, 256-byte aligned."""
+        def plane_bytes(fmt):
+            if fmt == "f16":
+                return [2 * self.d]
+            if fmt == "q8_0":
+                return [self.d, 2 * (self.d // 32)]
+            return [self.d // 4, self.d // 8, 2]
+        total = 0
+        for a, b in self.tile_ranges():
+            tp = (b - a + 15) // 16 * 16
+            for rb in plane_bytes(self.k_fmt) + plane_bytes(self.v_fmt):
+                total += (self.hkv * tp * rb + 255) // 256 * 256
+        return total * self.layers
+
     def load_layer(self, layer: int, k16: torch.Tensor, v16: torch.Tensor, q16: Optional[torch.Tensor] = None):
-        """Encode one layer's fp16 ``k16, v16[n_kv, hkv, d]`` (CUDA) and place it."""
-        k = encode_kv(self.k_fmt, k16, self.signs)
-        v = encode_kv(self.v_fmt, v16, self.signs)
-        torch.cuda.current_stream().synchronize()
-        kw, vw = k.token_slice(0, self.wc), v.token_slice(0, self.wc)
-        # the window keeps its own storage so the full-length encode can be freed
-        kw = KV(kw.fmt, tuple(p.clone() for p in kw.planes), kw.tokens, kw.hkv, kw.d, kw.tok_stride)
-        vw = KV(vw.fmt, tuple(p.clone() for p in vw.planes), vw.tokens, vw.hkv, vw.d, vw.tok_stride)
-        self.window[layer] = (kw, vw)
-        if self.tail_len > 0:
-            self.tail[layer] = (k.token_slice(self.wc, self.n_kv).pinned_copy(),
-                                v.token_slice(self.wc, self.n_kv).pinned_copy())
+        """Encode one layer's fp16 ``k16, v16[n_kv, hkv, d]`` (CUDA) and place it.
+
+        The tail tiles of every layer share one page-locked arena (``qps_host_alloc``):
+        the copy engine then reads a few large pinned regions rather than hundreds of
+        separate pinned allocations."""
+        if self.wc > 0:
+            self.window[layer] = (encode_kv_head_major(self.k_fmt, k16[:self.wc], self.signs),
+                                  encode_kv_head_major(self.v_fmt, v16[:self.wc], self.signs))
+        tiles = []
+        ranges = self.tile_ranges()
+        if ranges and self.arena is None:
+            self.arena = HostArena(self._arena_bytes())
+        for a, b in ranges:
+            kt = encode_kv_head_major(self.k_fmt, k16[self.wc + a:self.wc + b], self.signs)
+            vt = encode_kv_head_major(self.v_fmt, v16[self.wc + a:self.wc + b], self.signs)
+            tiles.append((self.arena.copy_in(kt), self.arena.copy_in(vt)))
+        self.tail[layer] = tiles
         if q16 is not None:
             self.q[layer].copy_(q16)
 
@@ -83,44 +107,43 @@ class PositionSplitDecoder:
 
     def build(self):
         """Create the ring, the flat (layer, tile) schedule and the step plans."""
-        ranges = self.tile_ranges()
         tiles = []
         slot_bytes = 0
-        if self.tail_len > 0:
-            for layer in range(self.layers):
-                kt, vt = self.tail[layer]
-                for a, b in ranges:
-                    td = tile_desc(kt, vt, a, b)
-                    tiles.append(td)
-                    need = sum((x + 255) // 256 * 256 for x in list(td.bytes_k) + list(td.bytes_v))
-                    slot_bytes = max(slot_bytes, need)
+        for layer in range(self.layers):
+            for kt, vt in self.tail[layer]:
+                td = tile_desc(kt, vt)
+                tiles.append(td)
+                need = sum((x + 255) // 256 * 256 for x in list(td.bytes_k) + list(td.bytes_v))
+                slot_bytes = max(slot_bytes, need)
+        if tiles:
             self.ring = Ring(self.ring_slots, slot_bytes, self.device.index)
         layers, wlayers = [], []
         self._keep = []
         self.window_args = []
         for layer in range(self.layers):
-            kw, vw = self.window[layer]
-            wargs = self._args(layer, kw, vw, self.n_split_window)
-            self.window_args.append(wargs)
-            n_w, _ = attn_plan(wargs)
-            cap = n_w
+            parts, cap = [], 0
+            if self.window[layer] is not None:
+                kw, vw = self.window[layer]
+                wargs = self._args(layer, kw, vw, self.n_split_window)
+                self.window_args.append(wargs)
+                parts.append(wargs)
+                cap += attn_plan(wargs)[0]
             tail_tpl = None
-            if self.tail_len > 0:
-                kt, vt = self.tail[layer]
-                # a template: the ring replaces the data pointers with its slot's planes
-                tail_tpl = self._args(layer, kt, vt, self.n_split_tail)
-                for a, b in ranges:
-                    probe = self._args(layer, kt.token_slice(a, b), vt.token_slice(a, b), self.n_split_tail)
-                    cap += attn_plan(probe)[0]
-            o_parts, lse_parts = _parts_buffers(cap, self.rows, self.d, self.device)
+            for kt, vt in self.tail[layer]:
+                probe = self._args(layer, kt, vt, self.n_split_tail)
+                cap += attn_plan(probe)[0]
+                if tail_tpl is None:
+                    # a template: the ring replaces data pointers and strides with its slot's
+                    tail_tpl = probe
+            o_parts, lse_parts = _parts_buffers(max(cap, 1), self.rows, self.d, self.device)
             self._keep += [o_parts, lse_parts]
-            layers.append(dict(device_parts=[wargs], tail=tail_tpl,
-                               n_tiles=len(ranges) if self.tail_len > 0 else 0,
+            layers.append(dict(device_parts=parts, tail=tail_tpl, n_tiles=len(self.tail[layer]),
                                o_parts=o_parts, lse_parts=lse_parts, o=self.o[layer], lse=self.lse[layer]))
-            wlayers.append(dict(device_parts=[wargs], tail=None, n_tiles=0,
-                                o_parts=o_parts, lse_parts=lse_parts, o=self.o[layer], lse=self.lse[layer]))
+            if parts:
+                wlayers.append(dict(device_parts=parts, tail=None, n_tiles=0, o_parts=o_parts,
+                                    lse_parts=lse_parts, o=self.o[layer], lse=self.lse[layer]))
         self.plan = StepPlan(layers, tiles, self.ring)
-        self.window_plan = StepPlan(wlayers)
+        self.window_plan = StepPlan(wlayers) if wlayers else None
         self.n_tiles = len(tiles)
         return self
 
@@ -129,23 +152,30 @@ class PositionSplitDecoder:
 
     def window_step(self, stream=None):
         """The same step with the ring and the tail omitted (window parts + combines)."""
-        self.window_plan.run(stream)
+        if self.window_plan is not None:
+            self.window_plan.run(stream)
 
     # algorithmic bytes: every stored plane the step must read once
     def window_bytes(self) -> int:
-        return sum(kv.nbytes() for w in self.window for kv in w)
+        return sum(kv.nbytes() for w in self.window if w is not None for kv in w)
 
     def tail_bytes(self) -> int:
-        return sum(kv.nbytes() for t in self.tail if t is not None for kv in t)
+        return sum(kv.nbytes() for t in self.tail for tile in t for kv in tile)
 
     def close(self):
+        """Release the ring (after its copies finish), the plans and the host arena."""
         if self.ring is not None:
             self.ring.close()
             self.ring = None
+        self.plan = self.window_plan = None
+        self.tail = [[] for _ in range(self.layers)]
+        if self.arena is not None:
+            self.arena.close()
+            self.arena = None
 
 
 class FanoutDecoder:
-    """One compressed prefix shared by ``agents`` query rows sets, plus private fp16
+    """One compressed prefix shared by ``agents`` sets of query rows, plus private fp16
     suffixes; one layer, all device-resident."""
 
     def __init__(self, *, agents: int, hq: int, hkv: int, d: int, k_fmt: str, v_fmt: str,
@@ -164,10 +194,10 @@ class FanoutDecoder:
     def load(self, q16, prefix_k16, prefix_v16, suffix_k16, suffix_v16):
         """q16[A, hq, d]; prefix_*[P, hkv, d]; suffix_*[A, S, hkv, d] (fp16, CUDA)."""
         self.q.copy_(q16)
-        self.pk = encode_kv(self.k_fmt, prefix_k16, self.signs)
-        self.pv = encode_kv(self.v_fmt, prefix_v16, self.signs)
-        self.sk = encode_kv("f16", suffix_k16)
-        self.sv = encode_kv("f16", suffix_v16)
+        self.pk = encode_kv_head_major(self.k_fmt, prefix_k16, self.signs)
+        self.pv = encode_kv_head_major(self.v_fmt, prefix_v16, self.signs)
+        self.sk = encode_kv_head_major("f16", suffix_k16)
+        self.sv = encode_kv_head_major("f16", suffix_v16)
         return self
 
     def build(self):

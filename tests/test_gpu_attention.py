@@ -47,23 +47,51 @@ def test_lse_combine(qps):
 FORMATS = [("f16", "f16"), ("q8_0", "q8_0"), ("q8_0", "tq3"), ("f16", "tq3"), ("q8_0", "f16")]
 
 
+def _encode(qps, layout, fmt, x, words):
+    if layout == "head":
+        return qps.encode_kv_head_major(fmt, x.cuda(), words)
+    return qps.encode_kv(fmt, x.cuda(), words)
+
+
+LAYOUT_PATH = {"head": "tensor-core", "token": "cuda-core"}
+
+
+@pytest.mark.parametrize("layout", ["head", "token"])
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
 @pytest.mark.parametrize("kf,vf", FORMATS)
 @pytest.mark.parametrize("softcap", [0.0, 30.0])
-def test_window_attention_formats(qps, d, kf, vf, softcap):
+def test_window_attention_formats(qps, layout, d, kf, vf, softcap):
     hq, hkv, n = 8, 2, 1000 + 7
     q, k, v = _inputs(n, hq, hkv, d, seed=d + len(kf) * 7 + len(vf), outliers=True)
     words = synth.sign_bits(d, 42)
-    K = qps.encode_kv(kf, k.cuda(), words)
-    V = qps.encode_kv(vf, v.cuda(), words)
+    K = _encode(qps, layout, kf, k, words)
+    V = _encode(qps, layout, vf, v, words)
     qc = q.cuda()
     scale = 1.0 / np.sqrt(d)
     ro, rl = pipeline.layer_reference(q.numpy(), k.numpy(), v.numpy(), kf, vf, scale, softcap, words.numpy())
     for n_split in (0, 1, 5, 4000):  # 4000 > positions: most splits are empty
         a = qps.attn_args(qc, K, V, scale=scale, softcap=softcap, v_signs=words, n_split=n_split)
+        assert qps.attn_path(a) == LAYOUT_PATH[layout]
         o, lse = qps.attn_decode_window(a)
         assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq),
-                      (d, kf, vf, softcap, n_split))
+                      (layout, d, kf, vf, softcap, n_split))
+
+
+@pytest.mark.parametrize("layout", ["head", "token"])
+@pytest.mark.parametrize("begin,end", [(17, 211), (0, 16), (5, 6), (31, 300), (299, 300)])
+def test_ragged_ranges(qps, layout, begin, end):
+    """Sub-ranges whose ends cut 16-token tiles, single tokens and tiny chunks."""
+    d, hq, hkv, n = 128, 5, 1, 300
+    q, k, v = _inputs(n, hq, hkv, d, seed=begin * 7 + end)
+    K = _encode(qps, layout, "q8_0", k, None)
+    V = _encode(qps, layout, "f16", v, None)
+    kh = pipeline.dequant("q8_0", k.numpy())
+    for n_split in (1, 3):
+        a = qps.attn_args(q.cuda(), K, V, scale=0.1, kv_begin=begin, kv_end=end, n_split=n_split)
+        o, lse = qps.attn_decode_window(a)
+        ro, rl = oatt.gqa_decode(q.double().numpy(), kh, v.double().numpy(), 0.1, 0.0, begin, end)
+        assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq),
+                      (layout, begin, end, n_split))
 
 
 def test_sub_range_and_empty_range(qps):
@@ -112,17 +140,19 @@ def test_split_identity_every_window_length(qps):
             ring.close()
 
 
-def test_gqa_and_shared_batch(qps):
-    """A shared prefix (batch_stride 0) read by 5 batch entries equals each entry
-    attending it alone."""
-    d, hq, hkv, n, b = 128, 8, 2, 777, 5
-    g = torch.Generator().manual_seed(5)
+@pytest.mark.parametrize("layout", ["head", "token"])
+@pytest.mark.parametrize("b", [1, 2, 5])
+def test_gqa_and_shared_batch(qps, layout, b):
+    """A shared prefix (batch_stride 0) read by b batch entries (up to 40 query rows
+    per KV head) equals each entry attending it alone."""
+    d, hq, hkv, n = 128, 16, 2, 777
+    g = torch.Generator().manual_seed(5 + b)
     q = torch.randn((b, hq, d), generator=g).half()
     k = torch.randn((n, hkv, d), generator=g).half()
     v = torch.randn((n, hkv, d), generator=g).half()
     words = synth.sign_bits(d, 42)
-    K = qps.encode_kv("q8_0", k.cuda())
-    V = qps.encode_kv("tq3", v.cuda(), words)
+    K = _encode(qps, layout, "q8_0", k, None)
+    V = _encode(qps, layout, "tq3", v, words)
     a = qps.attn_args(q.cuda(), K, V, scale=0.09, v_signs=words, shared=True)
     o, lse = qps.attn_decode_window(a)
     kh = pipeline.dequant("q8_0", k.numpy())

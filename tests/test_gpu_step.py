@@ -65,10 +65,13 @@ def test_ring_depth_and_tile_invariance(qps):
     base = outs[(3, 512)]
     for key in [(2, 512), (4, 512)]:  # same tiles: bit-identical whatever the depth
         assert torch.equal(outs[key][0], base[0]) and torch.equal(outs[key][1], base[1]), key
-    for key in [(3, 300), (2, 2000)]:  # other tiles: same values up to rounding
+    for key in [(3, 300), (2, 2000)]:
+        # other tiles: the same values up to rounding.  The LSE is fp32 throughout; O
+        # differs by the fp16 rounding of the softmax weights P, which depends on each
+        # tile's running maximum (relative 2^-12 per weight).
         r = helpers.parity_report(outs[key][0].numpy(), outs[key][1].numpy(),
                                   base[0].double().numpy(), base[1].double().numpy())
-        assert r["rel_l2"] < 1e-5 and r["dlse"] < 1e-5, (key, r)
+        assert r["rel_l2"] < 5e-4 and r["dlse"] < 1e-5, (key, r)
 
 
 def test_ring_host_side_errors(qps):

@@ -40,6 +40,8 @@ def parse_args(argv=None):
     ap.add_argument("--config", default="qwen14b_f16")
     ap.add_argument("--cpu-layers", type=int, default=0, help="layers in the oracle sample (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only this many layers (profiling of a small case; 0 = the workload's)")
     return ap.parse_args(argv)
 
 
@@ -279,6 +281,8 @@ def run_ours(args):
 
     qbuild.build()
     cfg = synth.by_name(args.config)
+    if args.layers > 0:
+        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
     if cfg.kind != "split":
         raise SystemExit("bench.py times the position-split workloads")
     signs = synth.sign_bits(cfg.d, cfg.sign_seed)

@@ -42,6 +42,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only this many layers (profiling of a small case; 0 = the workload's)")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time the window decode-attention kernel alone on one layer of every "
+                         "workload (one JSON line per workload; not the benchmark line)")
     return ap.parse_args(argv)
 
 
@@ -350,10 +353,12 @@ def run_ours(args):
     time.sleep(0.3)
     qps.launch_count(reset=True)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    bounds = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     t0.record(stream)
     for i in range(K):
         set_events(ev[i])
         dec.step(stream)
+        bounds[i].record(stream)
     t1.record(stream)
     launches = qps.launch_count()
     torch.cuda.synchronize()
@@ -368,6 +373,10 @@ def run_ours(args):
         step_ms = float(tt.item())
     win_ms = [ev[i][layer][0].elapsed_time(ev[i][layer][1]) for i in range(K) for layer in range(L)]
     win_launch_ms = statistics.mean(win_ms)
+    per_step = [t0.elapsed_time(bounds[0])] + [bounds[i - 1].elapsed_time(bounds[i]) for i in range(1, K)]
+    p50 = statistics.median(per_step)
+    step_dist = {"p50_ms": p50, "min_ms": min(per_step), "max_ms": max(per_step),
+                 "slow_steps": sum(1 for x in per_step if x > 1.25 * p50)}
 
     # end to end through the public API with host buffers: q in, (o, lse) out each step
     q_host = torch.empty_like(dec.q, device="cpu").pin_memory()
@@ -442,7 +451,7 @@ def run_ours(args):
                  "bound_ms": bound_ms, "ratio_to_bound": step_ms / bound_ms,
                  "tail_stream_gbs": tail_bytes / (step_ms / 1e3) / 1e9,
                  "link_probe_gbs": link_gbs, "host_memcpy_1thread_gbs": host_memcpy_gbs,
-                 "steps_per_s": 1000.0 / step_ms},
+                 "steps_per_s": 1000.0 / step_ms, "per_step": step_dist},
         "cpu_baseline": cpu,
         "e2e": {"value": world * kv_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -456,10 +465,71 @@ def run_ours(args):
     return 0
 
 
+def run_kernel_only(args):
+    """Per-launch time of the window decode-attention kernel on one layer of each
+    workload (or of --config), timed back to back with CUDA events; inputs > L2 except
+    the tiny and fan-out workloads (flagged)."""
+    import torch
+
+    import synth
+    import quantized_position_split_gb300 as qps
+    from quantized_position_split_gb300 import build as qbuild
+
+    qbuild.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    names = [args.config] if args.config != "qwen14b_f16" or args.layers else [c.name for c in synth.CONFIGS]
+    peak, peak_kind = measured_hbm_peak()
+    s = torch.cuda.current_stream()
+    for name in names:
+        cfg = synth.by_name(name)
+        signs = synth.sign_bits(cfg.d, cfg.sign_seed)
+        if cfg.kind == "split":
+            q = synth.query_f16(cfg, 0, device=dev)
+            k = synth.kv_f16(cfg, 0, "k", cfg.wc, device=dev)
+            v = synth.kv_f16(cfg, 0, "v", cfg.wc, device=dev)
+            K = qps.encode_kv_head_major(cfg.k_fmt, k, signs)
+            V = qps.encode_kv_head_major(cfg.v_fmt, v, signs)
+            a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs)
+            rows = cfg.batch * cfg.hq
+        else:
+            q = synth.randn_f16((cfg.agents, cfg.hq, cfg.d), cfg.seed, cfg.name, "q", device=dev)
+            pk = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "k", device=dev)
+            pv = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "v", device=dev)
+            K = qps.encode_kv_head_major(cfg.k_fmt, pk, signs)
+            V = qps.encode_kv_head_major(cfg.v_fmt, pv, signs)
+            a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs, shared=True)
+            rows = cfg.agents * cfg.hq
+        n_split, _ = qps.attn_plan(a)
+        parts = (torch.empty((n_split, rows, cfg.d), device=dev), torch.empty((n_split, rows), device=dev))
+        for _ in range(3):
+            qps.attn_decode_window(a, parts=parts)
+        n = 50
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(n):
+            qps.attn_decode_window(a, parts=parts)
+        e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / n * 1e3
+        kv = K.nbytes() + V.nbytes()
+        algo = kv + q.numel() * 2 + n_split * rows * (cfg.d + 1) * 4
+        print(json.dumps({"kernel": "attn_decode_window", "workload": name, "path": qps.attn_path(a),
+                          "n_split": n_split, "launch_us": us, "kv_bytes": kv, "algorithmic_bytes": algo,
+                          "achieved_gbs": algo / us / 1e3, "frac_of_hbm": algo / us / 1e3 / peak,
+                          "peak_gbs": peak, "peak_source": peak_kind,
+                          "l2_resident": kv < 129e6}), flush=True)
+        qps.device_status(reset=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel_only:
+        return run_kernel_only(args)
     return run_ours(args)
 
 

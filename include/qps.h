@@ -216,7 +216,9 @@ QPS_API qps_status qps_lse_combine(const float* o_parts, const float* lse_parts,
  * residency", section "Storage layer": per-layer KV lives in pinned host memory
  * allocated with cudaHostAlloc(cudaHostAllocPortable)).  One large arena holding every
  * tile of the tail keeps the copy engine's reads on few, large page-locked regions.
- *   bytes  > 0;  flags: 0 = portable, 1 = portable | write-combined;
+ *   bytes  > 0;  flags: 0 = cudaHostAlloc portable, 1 = portable | write-combined,
+ *          2 = an anonymous mapping advised to use transparent huge pages, faulted in
+ *          and registered with cudaHostRegister (portable);
  *   out    receives the host pointer (256-byte aligned), owned by the caller until
  *          qps_host_free.
  * Errors: INVALID_ARG, CUDA (allocation failure). */
@@ -319,6 +321,14 @@ typedef struct qps_layer_step {
  * Errors: as the calls it makes. */
 QPS_API qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n_tiles,
                            const qps_layer_step* layers, int32_t n_layers, void* stream);
+
+/* Device-side status of the current device.  Kernels that wait on their own
+ * asynchronous tile copies bound every wait; a wait that runs out sets a
+ * library-owned device word instead of hanging, and the kernel returns early with
+ * invalid outputs.  This call reads that word synchronously (it waits for the
+ * device's pending work to reach it on the legacy stream) and clears it if `reset`.
+ * Errors: TIMEOUT (some wait gave up since the last reset), CUDA. */
+QPS_API qps_status qps_device_status(int32_t reset);
 
 /* Number of kernel launches the calling thread has issued through this library
  * since the last reset (reset if `reset` is non-zero).  Host only. */

@@ -64,6 +64,12 @@ def launch_count(reset: bool = False) -> int:
     return int(lib().qps_launch_count(1 if reset else 0))
 
 
+def device_status(reset: bool = True) -> None:
+    """Raise QpsError(QPS_ERR_TIMEOUT) if a kernel's bounded wait gave up since the last
+    reset (synchronous)."""
+    N.check(lib().qps_device_status(1 if reset else 0))
+
+
 def tq3_codebook():
     """The library's fixed TQ3 codebook: (8 levels, 7 thresholds) as Python floats."""
     lv = (ctypes.c_float * 8)()
@@ -317,9 +323,11 @@ class HostArena:
     """One page-locked host region from ``qps_host_alloc``, handed out as 256-byte
     aligned CPU tensors that alias it (no copies).  Owned until ``close()``."""
 
-    def __init__(self, nbytes: int, write_combined: bool = False):
+    def __init__(self, nbytes: int, flags: int = 0):
+        """``flags`` as ``qps_host_alloc``: 0 cudaHostAlloc, 1 write-combined, 2 huge-page
+        backed mapping registered with CUDA."""
         p = ctypes.c_void_p()
-        N.check(lib().qps_host_alloc(max(int(nbytes), 256), 1 if write_combined else 0, ctypes.byref(p)))
+        N.check(lib().qps_host_alloc(max(int(nbytes), 256), int(flags), ctypes.byref(p)))
         self.ptr = p.value
         self.nbytes = max(int(nbytes), 256)
         self.used = 0

@@ -1,5 +1,7 @@
 // C ABI entry points: argument validation, error reporting, the TQ3 codebook, the
 // attention plan / dispatch, the LSE combine and the native decode-step runner.
+#include <cuda.h>
+
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -37,6 +39,69 @@ int sm_count_current() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+// ---- tensor maps (driver entry point looked up once through the runtime) -----------
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+}  // namespace
+
+bool encode_plane_map(TensorMap* map, const void* base, int row_bytes, int64_t tokens, int heads,
+                      int64_t head_stride_rows, int batch, int64_t batch_stride_rows, int box_bytes,
+                      int swizzle) {
+  static_assert(sizeof(TensorMap) == sizeof(CUtensorMap), "tensor map size");
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) {
+    fail(QPS_ERR_CUDA, "attention: cuTensorMapEncodeTiled is not available");
+    return false;
+  }
+  const cuuint64_t dims[4] = {(cuuint64_t)row_bytes, (cuuint64_t)(tokens > 0 ? tokens : 1), (cuuint64_t)heads,
+                              (cuuint64_t)batch};
+  const cuuint64_t hs = (cuuint64_t)(head_stride_rows > 0 ? head_stride_rows : tokens) * row_bytes;
+  const cuuint64_t bs = batch > 1 ? (cuuint64_t)batch_stride_rows * row_bytes : hs * (cuuint64_t)heads;
+  const cuuint64_t strides[3] = {(cuuint64_t)row_bytes, hs > 0 ? hs : 16, bs > 0 ? bs : 16};
+  const cuuint32_t box[4] = {(cuuint32_t)box_bytes, 16, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMapSwizzle sw = swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                          : swizzle == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                          : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = enc(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base),
+                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fail(QPS_ERR_CUDA, "attention: cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r));
+    return false;
+  }
+  return true;
+}
+
+unsigned int* device_error_word() {
+  static std::mutex mu;
+  static unsigned int* words[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!words[dev]) {
+    unsigned int* w = nullptr;
+    if (cudaMalloc(&w, sizeof(unsigned int)) != cudaSuccess) return nullptr;
+    if (cudaMemset(w, 0, sizeof(unsigned int)) != cudaSuccess) return nullptr;
+    words[dev] = w;
+  }
+  return words[dev];
 }
 
 // ---- TQ3 codebook -----------------------------------------------------------------
@@ -120,11 +185,14 @@ qps_status check_view(const qps_kv_view& v, const char* name, bool allow_tq3) {
   return QPS_OK;
 }
 
+// Split count: enough CTAs for one full wave (two resident per SM), but no chunk
+// shorter than 512 positions, so each partial amortises its merge and the combine
+// reads few parts.
 int auto_split(int64_t ntok, int ctas_per_split) {
   const int sms = sm_count_current();
   if (sms <= 0) return -1;
-  const int64_t min_chunk = 256;
-  const int64_t target = 4LL * sms;
+  const int64_t min_chunk = 512;
+  const int64_t target = 2LL * sms;
   int64_t by_occupancy = (target + ctas_per_split - 1) / ctas_per_split;
   int64_t by_size = (ntok + min_chunk - 1) / min_chunk;
   int64_t n = by_occupancy < by_size ? by_occupancy : by_size;
@@ -229,11 +297,14 @@ bool side_fits_mma(const KvSide& s, int fmt, int d) {
 }  // namespace
 
 bool attn_uses_mma(const AttnParams& p) {
-  return side_fits_mma(p.k, p.kfmt, p.d) && side_fits_mma(p.v, p.vfmt, p.d);
+  return p.end <= 0x7fffffffLL && side_fits_mma(p.k, p.kfmt, p.d) && side_fits_mma(p.v, p.vfmt, p.d);
 }
 
-qps_status launch_attn(const AttnParams& p, cudaStream_t s) {
-  if (!attn_uses_mma(p)) return launch_attn_simple(p, s);
+qps_status launch_attn(const AttnParams& p_in, cudaStream_t s) {
+  if (!attn_uses_mma(p_in)) return launch_attn_simple(p_in, s);
+  AttnParams p = p_in;
+  p.err = device_error_word();
+  if (!p.err) return fail(QPS_ERR_CUDA, "attention: cannot allocate the device error word");
   switch (p.d) {
     case 64: return launch_attn_mma_d64(p, s);
     case 128: return launch_attn_mma_d128(p, s);
@@ -290,6 +361,16 @@ const char* qps_status_name(int32_t st) {
     case QPS_ERR_INTERNAL: return "QPS_ERR_INTERNAL";
     default: return "QPS_UNKNOWN_STATUS";
   }
+}
+
+qps_status qps_device_status(int32_t reset) {
+  unsigned int* w = device_error_word();
+  if (!w) return fail(QPS_ERR_CUDA, "device_status: no device error word");
+  unsigned int v = 0;
+  QPS_CUDA_TRY(cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost));
+  if (v && reset) QPS_CUDA_TRY(cudaMemset(w, 0, sizeof(v)));
+  if (v) return fail(QPS_ERR_TIMEOUT, "device_status: a kernel's bounded wait for its tile copies gave up");
+  return QPS_OK;
 }
 
 int64_t qps_launch_count(int32_t reset) {

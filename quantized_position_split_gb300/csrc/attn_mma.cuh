@@ -19,11 +19,15 @@
 // q8_0 V value (code x scale) are rounded once to fp16.
 //
 // Data movement: the KV planes of a (KV head, batch entry) must be token-contiguous
-// (tok_stride == 1).  Each warp runs a private cp.async pipeline of STAGES tiles of 16
-// tokens over its own share of the chunk's tiles (tiles w, w + NW, ...), staging every
-// plane of the tile into shared memory with a bank-conflict-avoiding XOR swizzle; a
-// tile partly outside [t0, t1) is zero-filled past t1 and masked in the softmax.
+// (tok_stride == 1).  Each warp runs a private pipeline of STAGES tiles of 16 tokens
+// over its own share of the chunk's tiles (tiles w, w + NW, ...): every plane of a tile
+// arrives by tensor-map (TMA) boxes or, for planes under 16 bytes per token, by
+// zero-filling cp.async, all completing on the stage's mbarrier; waits are bounded and
+// report through a device error word instead of hanging.  Rows past the view's end
+// arrive as zeros; tokens outside [t0, t1) are masked in the softmax.
 #pragma once
+
+#include <cstring>
 
 #include "internal.h"
 
@@ -95,7 +99,23 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, __half2 s) {
 }
 
 // ---- tile geometry ---------------------------------------------------------------
-__host__ __device__ constexpr int r16(int x) { return (x + 15) / 16 * 16; }
+__host__ __device__ constexpr int align_to(int x, int a) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr int min_i(int a, int b) { return a < b ? a : b; }
+
+// One plane of a 16-token tile.  Planes of >= 16 bytes per token arrive as tensor-map
+// boxes of [IB bytes][16 tokens] (IB = min(row bytes, 128)); the K / V value planes use
+// the hardware XOR swizzle that matches IB so that 8 token rows read at the same column
+// fall into 8 different bank groups.  Smaller planes (fp16 norms, q8_0 scales at
+// head_dim <= 128) come by 16-byte cp.async.  Either way rows past the view's end
+// arrive as zeros.
+template <int RB, bool VALUES>
+struct PlaneG {
+  static constexpr bool TMA = RB >= 16;
+  static constexpr int IB = min_i(RB, 128);
+  static constexpr int NB = TMA ? RB / IB : 0;
+  static constexpr int SW = (VALUES && TMA) ? (IB >= 128 ? 128 : IB >= 64 ? 64 : IB >= 32 ? 32 : 0) : 0;
+  static constexpr int BYTES = kTile * RB;
+};
 
 template <int D, int KF, int VF>
 struct Geo {
@@ -104,64 +124,109 @@ struct Geo {
   static constexpr int V_RB = VF == QPS_FMT_F16 ? 2 * D : VF == QPS_FMT_Q8_0 ? D : D / 4;
   static constexpr int V_ARB = VF == QPS_FMT_Q8_0 ? D / 16 : VF == QPS_FMT_TQ3 ? D / 8 : 0;
   static constexpr int V_A2RB = VF == QPS_FMT_TQ3 ? 2 : 0;
+  using PK = PlaneG<K_RB, true>;
+  using PKA = PlaneG<K_ARB, false>;
+  using PV = PlaneG<V_RB, VF != QPS_FMT_TQ3>;
+  using PVA = PlaneG<V_ARB, false>;
+  using PVA2 = PlaneG<V_A2RB, false>;
   static constexpr int K_OFF = 0;
-  static constexpr int KA_OFF = K_OFF + kTile * K_RB;
-  static constexpr int V_OFF = KA_OFF + r16(kTile * K_ARB);
-  static constexpr int VA_OFF = V_OFF + kTile * V_RB;
-  static constexpr int VA2_OFF = VA_OFF + r16(kTile * V_ARB);
-  static constexpr int STAGE = VA2_OFF + r16(kTile * V_A2RB);
+  static constexpr int KA_OFF = align_to(K_OFF + PK::BYTES, 128);
+  static constexpr int V_OFF = align_to(KA_OFF + PKA::BYTES, 1024);
+  static constexpr int VA_OFF = align_to(V_OFF + PV::BYTES, 128);
+  static constexpr int VA2_OFF = align_to(VA_OFF + PVA::BYTES, 128);
+  static constexpr int STAGE = align_to(VA2_OFF + PVA2::BYTES, 1024);
+  // bytes the tensor-map boxes of one tile deliver
+  static constexpr int TX = PK::BYTES + (PKA::TMA ? PKA::BYTES : 0) + PV::BYTES + (PVA::TMA ? PVA::BYTES : 0) +
+                            (PVA2::TMA ? PVA2::BYTES : 0);
+  static constexpr bool SMALL = (K_ARB > 0 && !PKA::TMA) || (V_ARB > 0 && !PVA::TMA) || (V_A2RB > 0 && !PVA2::TMA);
+  static constexpr int ARRIVALS = 1 + (SMALL ? 32 : 0);  // expect_tx + one per lane's cp.async
   // warps per CTA: 4, or 2 when two stages of 4 warps would not fit in shared memory
   static constexpr int NW = 4 * 2 * STAGE <= 200 * 1024 ? 4 : 2;
-  static constexpr int STAGES_RAW = (96 * 1024) / (NW * STAGE);
+  // ~104 KB of stages per CTA: two CTAs (8 warps) per SM within its 228 KB
+  static constexpr int STAGES_RAW = (104 * 1024) / (NW * STAGE);
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 6 ? 6 : STAGES_RAW);
   static constexpr int PIPE = NW * STAGES * STAGE;
+  static constexpr int BARS = PIPE;                   // mbarriers after the stages
+  static constexpr int LUT = BARS + NW * STAGES * 8;  // TQ3 level LUT after the barriers
+  static constexpr int SMEM = 1024 + LUT + 256;       // + slack to align the base to 1024
 };
 
-// XOR swizzles of 16-byte chunks within a token row of a staged tile.
-template <int D, int FMT, bool IS_K>
-__device__ __forceinline__ int swz(int row) {
-  if constexpr (FMT == QPS_FMT_F16) {
-    return row & 7;  // ldmatrix: 8 rows x one chunk per phase
-  } else if constexpr (FMT == QPS_FMT_Q8_0) {
-    if constexpr (IS_K) return D >= 128 ? ((row & 3) << 1) : ((row & 1) << 1);
-    else return D >= 512 ? ((row >> 1) & 3) : (D >= 128 ? (row & 7) : 0);
-  } else {
-    return 0;
-  }
+// Tensor maps of one launch, one per tensor-map plane (unused ones left empty).
+struct TmaSet {
+  TensorMap k, ka, v, va;
+};
+
+// Byte offset of (token row t, byte b) of a plane staged by tensor-map boxes of IB
+// bytes with swizzle SW (the 16-byte chunk index XORed with row bits, as the hardware
+// writes it into a 1024-byte aligned region).
+template <int IB, int SW>
+__device__ __forceinline__ int soff(int t, int b) {
+  const int box = b / IB, w = b % IB;
+  int chunk = w >> 4;
+  if constexpr (SW == 128) chunk ^= (t & 7);
+  else if constexpr (SW == 64) chunk ^= ((t >> 1) & 3);
+  else if constexpr (SW == 32) chunk ^= ((t >> 2) & 1);
+  return box * (kTile * IB) + t * IB + (chunk << 4) + (w & 15);
 }
 
-// Copy one plane of a 16-token tile (token-contiguous rows of rb bytes) into shared
-// memory; rows of tokens >= valid are zero-filled without reading.
-template <int RB, int SWZ_D, int SWZ_FMT, bool SWZ_K, bool SWIZZLE>
-__device__ __forceinline__ void stage_plane(uint8_t* dst, const uint8_t* src, int valid_tokens, int lane,
-                                            const uint8_t* safe_src) {
-  constexpr int BYTES = kTile * RB;
+// ---- asynchronous copies completing on per-stage mbarriers --------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const TensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+// One poll that suspends the warp (instead of spinning on issue slots) until the phase
+// completes or about a millisecond passes.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity: false after 256 polls of at most
+// ~1 ms each, i.e. well under a second.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int it = 0; it < 256; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// A small plane's 16-token tile by 16-byte cp.async; bytes past `valid_bytes` are
+// zero-filled without being read.
+template <int BYTES>
+__device__ __forceinline__ void stage_flat_zfill(uint8_t* dst, const uint8_t* src, int valid_bytes, int lane,
+                                                 const uint8_t* safe) {
   constexpr int CHUNKS = (BYTES + 15) / 16;
-  const int valid_bytes = valid_tokens * RB;
   const uint32_t base = smem_addr(dst);
-#pragma unroll 4
   for (int ch = lane; ch < CHUNKS; ch += 32) {
-    int dch = ch;
-    if constexpr (SWIZZLE && RB >= 16) {
-      constexpr int CPR = RB / 16;  // chunks per row
-      const int row = ch / CPR, x = ch % CPR;
-      dch = row * CPR + (x ^ swz<SWZ_D, SWZ_FMT, SWZ_K>(row));
-    }
     int nb = valid_bytes - ch * 16;
     nb = nb < 0 ? 0 : (nb > 16 ? 16 : nb);
-    cp_async16(base + dch * 16, nb > 0 ? (const void*)(src + ch * 16) : (const void*)safe_src, nb);
+    cp_async16(base + ch * 16, nb > 0 ? (const void*)(src + ch * 16) : (const void*)safe, nb);
   }
-}
-
-// Where the swizzled 16-byte chunk x of row `row` lives.
-template <int RB, int D, int FMT, bool IS_K>
-__device__ __forceinline__ int chunk_off(int row, int x) {
-  return row * RB + ((x ^ swz<D, FMT, IS_K>(row)) << 4);
 }
 
 // ---- the kernel -------------------------------------------------------------------
 template <int D, int KF, int VF, int NTW>
-__global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
+    attn_mma_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TmaSet maps) {
   using G = Geo<D, KF, VF>;
   constexpr int kWarps = G::NW;
   constexpr int ROWS = 8 * NTW;  // query rows per CTA
@@ -171,9 +236,11 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
   constexpr int DT = D / 8;                  // output columns per lane group (VPERM)
   constexpr float LOG2E = 1.4426950408889634f;
 
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // swizzled boxes need a 1024-byte aligned base
+  uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint8_t* pipe = smem;
-  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + G::PIPE);  // TQ3: 64 half2
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + G::LUT);  // TQ3: 64 half2
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -241,33 +308,68 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
   // ---- plane bases of this (head, batch entry) -------------------------------------
   const int64_t krow = (p.shared ? 0 : (int64_t)bz * p.k.batch) + (int64_t)head * p.k.head;
   const int64_t vrow = (p.shared ? 0 : (int64_t)bz * p.v.batch) + (int64_t)head * p.v.head;
-  const uint8_t* kd = reinterpret_cast<const uint8_t*>(p.k.data) + krow * G::K_RB;
   const uint8_t* ka = KQ ? reinterpret_cast<const uint8_t*>(p.k.aux) + krow * G::K_ARB : nullptr;
-  const uint8_t* vd = reinterpret_cast<const uint8_t*>(p.v.data) + vrow * G::V_RB;
   const uint8_t* va = G::V_ARB ? reinterpret_cast<const uint8_t*>(p.v.aux) + vrow * G::V_ARB : nullptr;
   const uint8_t* va2 = G::V_A2RB ? reinterpret_cast<const uint8_t*>(p.v.aux2) + vrow * G::V_A2RB : nullptr;
   const uint8_t* safe = reinterpret_cast<const uint8_t*>(p.k.data);
+  const int bcoord = p.shared ? 0 : bz;  // tensor-map batch coordinate
 
   const int64_t tile0 = t0 & ~(int64_t)(kTile - 1);
   const int ntiles = (int)((t1 - tile0 + kTile - 1) / kTile);
   uint8_t* wpipe = pipe + warp * G::STAGES * G::STAGE;
 
-  auto issue = [&](int k) {  // the warp's k-th tile -> stage k % STAGES
+  const uint32_t bars = smem_addr(smem + G::BARS) + warp * G::STAGES * 8;
+  bool timed_out = false;
+
+  // The warp's k-th tile -> stage k % STAGES.  Lane 0 announces the tensor-map bytes;
+  // lanes issue one box each (K boxes from lane 0, V boxes from lane 8, the scale /
+  // bit planes from lanes 16 and 17); small planes go by zero-filling cp.async from
+  // every lane, each lane then arriving on the same mbarrier when its copies land.
+  auto issue = [&](int k) {
     const int tile = warp + k * kWarps;
-    if (tile < ntiles) {
-      uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
-      const int64_t tb = tile0 + (int64_t)tile * kTile;
-      const int valid = (int)min((int64_t)kTile, t1 - tb);
-      stage_plane<G::K_RB, D, KF, true, true>(st + G::K_OFF, kd + tb * G::K_RB, valid, lane, safe);
-      if constexpr (G::K_ARB > 0)
-        stage_plane<G::K_ARB, D, KF, true, false>(st + G::KA_OFF, ka + tb * G::K_ARB, valid, lane, safe);
-      stage_plane<G::V_RB, D, VF, false, true>(st + G::V_OFF, vd + tb * G::V_RB, valid, lane, safe);
-      if constexpr (G::V_ARB > 0)
-        stage_plane<G::V_ARB, D, VF, false, false>(st + G::VA_OFF, va + tb * G::V_ARB, valid, lane, safe);
-      if constexpr (G::V_A2RB > 0)
-        stage_plane<G::V_A2RB, D, VF, false, false>(st + G::VA2_OFF, va2 + tb * G::V_A2RB, valid, lane, safe);
+    if (tile >= ntiles) return;
+    uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
+    const int64_t tb = tile0 + (int64_t)tile * kTile;
+    const int tok = (int)tb;
+    const uint32_t bar = bars + (k % G::STAGES) * 8;
+    if (lane == 0) mbar_expect_tx(bar, G::TX);
+    __syncwarp();
+    fence_proxy_async();
+    const uint32_t sbase = smem_addr(st);
+    if (lane < G::PK::NB)
+      tma_load_4d(sbase + G::K_OFF + lane * (kTile * G::PK::IB), &maps.k, lane * G::PK::IB, tok, head, bcoord, bar);
+    if (lane >= 8 && lane < 8 + G::PV::NB) {
+      const int b = lane - 8;
+      tma_load_4d(sbase + G::V_OFF + b * (kTile * G::PV::IB), &maps.v, b * G::PV::IB, tok, head, bcoord, bar);
     }
-    cp_async_commit();
+    if constexpr (G::PKA::TMA)
+      if (lane == 16) tma_load_4d(sbase + G::KA_OFF, &maps.ka, 0, tok, head, bcoord, bar);
+    if constexpr (G::PVA::TMA)
+      if (lane == 17) tma_load_4d(sbase + G::VA_OFF, &maps.va, 0, tok, head, bcoord, bar);
+    if constexpr (G::SMALL) {
+      // rows past the view's end (kv_end) are zero-filled, like the tensor-map boxes
+      const int valid = (int)max((int64_t)0, min((int64_t)kTile, p.end - tb));
+      if constexpr (G::K_ARB > 0 && !G::PKA::TMA)
+        stage_flat_zfill<G::PKA::BYTES>(st + G::KA_OFF, ka + tb * G::K_ARB, valid * G::K_ARB, lane, safe);
+      if constexpr (G::V_ARB > 0 && !G::PVA::TMA)
+        stage_flat_zfill<G::PVA::BYTES>(st + G::VA_OFF, va + tb * G::V_ARB, valid * G::V_ARB, lane, safe);
+      if constexpr (G::V_A2RB > 0 && !G::PVA2::TMA)
+        stage_flat_zfill<G::PVA2::BYTES>(st + G::VA2_OFF, va2 + tb * G::V_A2RB, valid * G::V_A2RB, lane, safe);
+      cp_async_arrive_noinc(bar);
+    }
+  };
+
+  // Wait until the warp's k-th tile is in shared memory.
+  auto await = [&](int k) {
+    if (!mbar_wait(bars + (k % G::STAGES) * 8, (uint32_t)((k / G::STAGES) & 1))) {
+      // record the failure, then give the copies still in flight (tiles k..k+S-2 of
+      // this warp) a second bounded wait before the stage memory is reused
+      timed_out = true;
+      if (lane == 0) atomicOr(p.err, 1u);
+      for (int j = k; j < k + G::STAGES - 1 && warp + j * kWarps < ntiles; ++j)
+        mbar_wait(bars + (j % G::STAGES) * 8, (uint32_t)((j / G::STAGES) & 1));
+    }
+    __syncwarp();
   };
 
   // ---- running softmax state (log2 domain) and the O^T accumulators ---------------
@@ -283,7 +385,11 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
   const float qk_scale = p.scale;
   const float cap = p.softcap;
 
-  __syncthreads();  // the LUT is ready
+  if (lane == 0) {
+    for (int s = 0; s < G::STAGES; ++s) mbar_init(bars + s * 8, G::ARRIVALS);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();  // the LUT and the barriers are ready
 
 #pragma unroll 1
   for (int s = 0; s < G::STAGES - 1; ++s) issue(s);
@@ -291,8 +397,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
 #pragma unroll 1
   for (int k = 0; warp + k * kWarps < ntiles; ++k) {
     issue(k + G::STAGES - 1);
-    cp_async_wait<G::STAGES - 1>();
-    __syncwarp();
+    await(k);
+    if (timed_out) break;  // the error word tells the host; the outputs are not valid
     const uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
     const int64_t tb = tile0 + (int64_t)(warp + k * kWarps) * kTile;
 
@@ -304,21 +410,32 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
       const uint32_t kbase = smem_addr(st + G::K_OFF);
       const int mi = lane >> 3;
       const int trow = (lane & 7) + ((mi & 1) << 3);
+      // two independent accumulator chains (even / odd k-steps) halve the MMA latency chain
+      float sodd[NTW][4];
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) sodd[nt][0] = sodd[nt][1] = sodd[nt][2] = sodd[nt][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
         uint32_t a[4];
-        ldsm_x4(a, kbase + chunk_off<G::K_RB, D, KF, true>(trow, 2 * kk + (mi >> 1)));
+        ldsm_x4(a, kbase + soff<G::PK::IB, G::PK::SW>(trow, (2 * kk + (mi >> 1)) << 4));
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) mma16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        for (int nt = 0; nt < NTW; ++nt) {
+          if (kk & 1) mma16816(sodd[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          else mma16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
       }
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
     } else {
       const uint8_t* kc = st + G::K_OFF;
       const __half* ks = reinterpret_cast<const __half*>(st + G::KA_OFF);
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         const int x = 2 * j + (c >> 1), sub = 8 * (c & 1);
-        const uint2 wg = *reinterpret_cast<const uint2*>(kc + chunk_off<G::K_RB, D, KF, true>(g, x) + sub);
-        const uint2 wg8 = *reinterpret_cast<const uint2*>(kc + chunk_off<G::K_RB, D, KF, true>(g + 8, x) + sub);
+        const uint2 wg = *reinterpret_cast<const uint2*>(kc + soff<G::PK::IB, G::PK::SW>(g, 16 * x + sub));
+        const uint2 wg8 = *reinterpret_cast<const uint2*>(kc + soff<G::PK::IB, G::PK::SW>(g + 8, 16 * x + sub));
         uint32_t a0[4], a1[4];
         i8x4_to_h2x2(wg.x, a0[0], a0[2]);
         i8x4_to_h2x2(wg8.x, a0[1], a0[3]);
@@ -396,7 +513,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
         uint32_t a[4];
-        ldsm_x4_t(a, vbase + chunk_off<G::V_RB, D, VF, false>(trow, 2 * i + (mi & 1)));
+        ldsm_x4_t(a, vbase + soff<G::PV::IB, G::PV::SW>(trow, (2 * i + (mi & 1)) << 4));
 #pragma unroll
         for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[nt][0], pb[nt][1]);
       }
@@ -413,7 +530,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int byte = g * DT + q0;
-          const uint8_t* src = vc + chunk_off<G::V_RB, D, VF, false>(tok[u], byte >> 4) + (byte & 15);
+          const uint8_t* src = vc + soff<G::PV::IB, G::PV::SW>(tok[u], byte);
           if constexpr (CH == 16) {
             const uint4 r = *reinterpret_cast<const uint4*>(src);
             w[u][0] = r.x; w[u][1] = r.y; w[u][2] = r.z; w[u][3] = r.w;
@@ -585,22 +702,36 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2) attn_mma_kernel(co
 template <int D, int KF, int VF, int NTW>
 constexpr size_t smem_bytes() {
   using G = Geo<D, KF, VF>;
-  constexpr size_t pipe = (size_t)G::PIPE + 256;
+  constexpr size_t pipe = (size_t)G::LUT + 256;
   constexpr int ROWS = 8 * NTW;
   constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D);
-  return pipe > merge ? pipe : merge;
+  return (pipe > merge ? pipe : merge) + 1024;  // + slack for the 1024-byte base alignment
 }
 
 template <int D, int KF, int VF, int NTW>
 qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
+  using G = Geo<D, KF, VF>;
   constexpr size_t smem = smem_bytes<D, KF, VF, NTW>();
   static_assert(smem <= 227 * 1024, "tile staging exceeds the 227 KB shared memory of one CTA");
+  // tensor maps over each plane as [row bytes][tokens < kv_end][KV heads][batch]
+  TmaSet maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const int nb = p.shared ? 1 : p.batch;
+  if (!encode_plane_map(&maps.k, p.k.data, G::K_RB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PK::IB, G::PK::SW) ||
+      !encode_plane_map(&maps.v, p.v.data, G::V_RB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PV::IB, G::PV::SW))
+    return QPS_ERR_CUDA;
+  if constexpr (G::PKA::TMA)
+    if (!encode_plane_map(&maps.ka, p.k.aux, G::K_ARB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PKA::IB, 0))
+      return QPS_ERR_CUDA;
+  if constexpr (G::PVA::TMA)
+    if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, 0))
+      return QPS_ERR_CUDA;
   auto kern = attn_mma_kernel<D, KF, VF, NTW>;
   QPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   constexpr int ROWS = 8 * NTW;
   const int rgroups = (p.rows_per_cta + ROWS - 1) / ROWS;
   const dim3 grid(p.n_split, p.hkv, (p.shared ? 1 : p.batch) * rgroups);
-  kern<<<grid, Geo<D, KF, VF>::NW * 32, smem, s>>>(p);
+  kern<<<grid, G::NW * 32, smem, s>>>(p, maps);
   count_launch();
   QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;

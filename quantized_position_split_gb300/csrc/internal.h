@@ -22,8 +22,21 @@ void count_launch(int n = 1);
     if (_e != cudaSuccess) return ::qps::cuda_fail(_e, #expr); \
   } while (0)
 
+// ---- tensor memory access descriptors ----------------------------------------------
+// A byte plane seen as a 4-D tensor [row bytes][tokens][heads][batch] (innermost
+// first), loaded in boxes of [box_bytes][16 tokens][1][1].  swizzle: 0 none, 32, 64 or
+// 128 (bytes).  Returns false (with the error message set) on failure.
+struct alignas(64) TensorMap {
+  unsigned char bytes[128];
+};
+bool encode_plane_map(TensorMap* map, const void* base, int row_bytes, int64_t tokens, int heads,
+                      int64_t head_stride_rows, int batch, int64_t batch_stride_rows, int box_bytes,
+                      int swizzle);
+
 // ---- device facts -----------------------------------------------------------------
 int sm_count_current();
+// The current device's error word (library-owned, allocated on first use, zeroed).
+unsigned int* device_error_word();
 
 // ---- TQ3 codebook (computed once on the host from the Gaussian density) -----------
 struct Codebook {
@@ -71,6 +84,7 @@ struct AttnParams {
   float* o_parts;
   float* lse_parts;
   int part_offset;
+  unsigned int* err;  // device word set non-zero when a bounded in-kernel wait gives up
   uint32_t vsigns[kMaxSignWords];
   float tq_levels[8];
 };

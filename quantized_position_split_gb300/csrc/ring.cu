@@ -13,12 +13,29 @@
 //
 // Every wait is either a device-side stream/event dependency or a host poll with a
 // deadline; nothing here can block forever.
+#include <sys/mman.h>
+
 #include <chrono>
 #include <cstring>
+#include <mutex>
 #include <thread>
+#include <unordered_map>
 #include <vector>
 
 #include "internal.h"
+
+namespace {
+// Mappings made by qps_host_alloc(flags = 2): base -> length, so that qps_host_free
+// unregisters and unmaps them instead of calling cudaFreeHost.
+std::mutex& host_map_mutex() {
+  static std::mutex m;
+  return m;
+}
+std::unordered_map<void*, size_t>& host_map() {
+  static std::unordered_map<void*, size_t> m;
+  return m;
+}
+}  // namespace
 
 struct qps_ring {
   static constexpr uint64_t kMagic = 0x7170735f72696e67ULL;  // "qps_ring"
@@ -168,7 +185,26 @@ qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out) {
   if (!out) return fail(QPS_ERR_INVALID_ARG, "host_alloc: out is NULL");
   *out = nullptr;
   if (bytes == 0) return fail(QPS_ERR_INVALID_ARG, "host_alloc: bytes must be > 0");
-  if (flags != 0 && flags != 1) return fail(QPS_ERR_INVALID_ARG, "host_alloc: flags must be 0 or 1");
+  if (flags < 0 || flags > 2) return fail(QPS_ERR_INVALID_ARG, "host_alloc: flags must be 0, 1 or 2");
+  if (flags == 2) {
+    // anonymous mapping advised to use transparent huge pages, faulted in, then
+    // page-locked and registered with CUDA: fewer, larger pages for the copy engine
+    const size_t align = (size_t)2 << 20;
+    const size_t n = (bytes + align - 1) / align * align;
+    void* p = mmap(nullptr, n, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (p == MAP_FAILED) return fail(QPS_ERR_CUDA, "host_alloc: mmap failed");
+    madvise(p, n, MADV_HUGEPAGE);
+    std::memset(p, 0, n);
+    cudaError_t e = cudaHostRegister(p, n, cudaHostRegisterPortable);
+    if (e != cudaSuccess) {
+      munmap(p, n);
+      return cuda_fail(e, "host_alloc: cudaHostRegister");
+    }
+    std::lock_guard<std::mutex> lk(host_map_mutex());
+    host_map()[p] = n;
+    *out = p;
+    return QPS_OK;
+  }
   unsigned int f = cudaHostAllocPortable | (flags == 1 ? cudaHostAllocWriteCombined : 0u);
   QPS_CUDA_TRY(cudaHostAlloc(out, bytes, f));
   return QPS_OK;
@@ -176,6 +212,20 @@ qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out) {
 
 qps_status qps_host_free(void* p) {
   if (!p) return QPS_OK;
+  size_t mapped = 0;
+  {
+    std::lock_guard<std::mutex> lk(host_map_mutex());
+    auto it = host_map().find(p);
+    if (it != host_map().end()) {
+      mapped = it->second;
+      host_map().erase(it);
+    }
+  }
+  if (mapped) {
+    QPS_CUDA_TRY(cudaHostUnregister(p));
+    munmap(p, mapped);
+    return QPS_OK;
+  }
   QPS_CUDA_TRY(cudaFreeHost(p));
   return QPS_OK;
 }

@@ -36,9 +36,10 @@ class PositionSplitDecoder:
     def __init__(self, *, layers: int, batch: int, hq: int, hkv: int, d: int, n_kv: int, wc: int,
                  k_fmt: str, v_fmt: str, scale: float, softcap: float = 0.0, signs=None,
                  ring_slots: int = 3, tile_tokens: int = 8192, n_split_window: int = 0,
-                 n_split_tail: int = 0, device=None):
+                 n_split_tail: int = 0, device=None, host_alloc_flags: int = 2):
         if not 0 <= wc <= n_kv:
             raise ValueError("need 0 <= wc <= n_kv")
+        self.host_alloc_flags = host_alloc_flags
         self.layers, self.batch, self.hq, self.hkv, self.d = layers, batch, hq, hkv, d
         self.n_kv, self.wc = n_kv, wc
         self.k_fmt, self.v_fmt = k_fmt, v_fmt
@@ -83,16 +84,17 @@ class PositionSplitDecoder:
     def load_layer(self, layer: int, k16: torch.Tensor, v16: torch.Tensor, q16: Optional[torch.Tensor] = None):
         """Encode one layer's fp16 ``k16, v16[n_kv, hkv, d]`` (CUDA) and place it.
 
-        The tail tiles of every layer share one page-locked arena (``qps_host_alloc``):
-        the copy engine then reads a few large pinned regions rather than hundreds of
-        separate pinned allocations."""
+        The tail tiles of every layer share one page-locked arena (``qps_host_alloc``,
+        by default backed by transparent huge pages): the copy engine then reads a few
+        large pinned regions.  Hundreds of separate pinned allocations showed periodic
+        copy stalls of 100+ ms on GB300 hosts."""
         if self.wc > 0:
             self.window[layer] = (encode_kv_head_major(self.k_fmt, k16[:self.wc], self.signs),
                                   encode_kv_head_major(self.v_fmt, v16[:self.wc], self.signs))
         tiles = []
         ranges = self.tile_ranges()
         if ranges and self.arena is None:
-            self.arena = HostArena(self._arena_bytes())
+            self.arena = HostArena(self._arena_bytes(), self.host_alloc_flags)
         for a, b in ranges:
             kt = encode_kv_head_major(self.k_fmt, k16[self.wc + a:self.wc + b], self.signs)
             vt = encode_kv_head_major(self.v_fmt, v16[self.wc + a:self.wc + b], self.signs)

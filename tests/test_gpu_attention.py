@@ -159,3 +159,8 @@ def test_gqa_and_shared_batch(qps, layout, b):
     vh = pipeline.dequant("tq3", v.numpy(), words.numpy())
     ro, rl = oatt.gqa_decode(q.double().numpy(), kh, vh, 0.09)
     assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(b * hq, d), rl.reshape(b * hq))
+
+
+def test_zz_no_bounded_wait_gave_up(qps):
+    """Every tensor-core launch above finished its tile waits within their bounds."""
+    qps.device_status(reset=True)

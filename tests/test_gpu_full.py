@@ -53,3 +53,7 @@ def test_full_size_fanout(qps):
     torch.cuda.synchronize()
     ro, rl = helpers.oracle_fanout(cfg, *ins)
     assert_parity(fd.o.cpu().numpy(), fd.lse.cpu().numpy(), ro.reshape(-1, cfg.d), rl.reshape(-1))
+
+
+def test_zz_no_bounded_wait_gave_up(qps):
+    qps.device_status(reset=True)

@@ -117,3 +117,7 @@ def test_ring_host_side_errors(qps):
     with pytest.raises(N.QpsError):
         ring.handle = None
         N.check(qps.lib().qps_ring_end_step(None))
+
+
+def test_zz_no_bounded_wait_gave_up(qps):
+    qps.device_status(reset=True)

@@ -322,6 +322,26 @@ typedef struct qps_layer_step {
 QPS_API qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n_tiles,
                            const qps_layer_step* layers, int32_t n_layers, void* stream);
 
+/* qps_attn_decode_window in merged-output mode (o_parts == NULL, o / lse set) for
+ * callers that cannot allocate device memory on the call path: code running where
+ * cudaMalloc is forbidden or too costly (a serving loop whose device memory is owned
+ * by an external pool, a latency-critical path that must not risk the synchronisation
+ * an allocation can cause).  The pages describe no such entry point; it has no
+ * counterpart there.  It allocates nothing: instead of a caller workspace, the split
+ * partials live in a fixed 8 MiB file-scope device array that every GPU which loads
+ * the library holds until the process exits.  `workspace` is ignored.
+ *   - Requests whose partials exceed the array (n_split * batch * hq * (D + 1) floats,
+ *     plus alignment) fail with QPS_ERR_INVALID_ARG; pass a smaller n_split.
+ *   - All calls on a device share the array and leave their partials in it (each call
+ *     rewrites everything it reads); calls that overlap on the GPU race on it, so
+ *     serialise them (one stream, or events between streams).
+ *   - The first call on each device looks up the array's address and clears its error
+ *     word (a synchronising step); make that first call before any stream capture.
+ *   - A bounded in-kernel wait that gives up marks the array's error word instead of
+ *     hanging and leaves the outputs invalid; this call does not read the word back.
+ * Supported shapes, formats and other errors as qps_attn_decode_window. */
+QPS_API qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, void* stream);
+
 /* Device-side status of the current device.  Kernels that wait on their own
  * asynchronous tile copies bound every wait; a wait that runs out sets a
  * library-owned device word instead of hanging, and the kernel returns early with

@@ -252,6 +252,18 @@ def attn_decode_window(a: N.AttnArgs, *, o=None, lse=None, parts=None, part_offs
     return o, lse
 
 
+def attn_decode_window_noalloc(a: N.AttnArgs, o: torch.Tensor, lse: torch.Tensor, stream=None):
+    """Merged-output decode attention that allocates no device memory: the split
+    partials go to the library's fixed device scratch instead of a workspace.  For
+    callers that cannot allocate on the call path; ``o`` [batch*hq, D] and ``lse``
+    [batch*hq] (f32, CUDA) must be given.  Calls sharing a device must not overlap."""
+    a.o_parts = a.lse_parts = None
+    a.o, a.lse = o.data_ptr(), lse.data_ptr()
+    a.workspace, a.workspace_bytes = None, 0
+    N.check(lib().qps_attn_decode_window_noalloc(ctypes.byref(a), _stream(stream)))
+    return o, lse
+
+
 def lse_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, o=None, lse=None, stream=None):
     """Merge ``o_parts[P, rows, D]`` / ``lse_parts[P, rows]`` (f32, CUDA)."""
     p, rows, d = o_parts.shape

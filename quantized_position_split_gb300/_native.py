@@ -123,6 +123,7 @@ SIGNATURES = [
     ("qps_ring_end_step", c_int32, [c_void_p]),
     ("qps_ring_sync", c_int32, [c_void_p, c_int32]),
     ("qps_decode_step", c_int32, [c_void_p, POINTER(TileDesc), c_int32, POINTER(LayerStep), c_int32, c_void_p]),
+    ("qps_attn_decode_window_noalloc", c_int32, [POINTER(AttnArgs), c_void_p]),
     ("qps_device_status", c_int32, [c_int32]),
     ("qps_launch_count", c_int64, [c_int32]),
 ]

@@ -61,7 +61,7 @@ EncodeTiledFn tensor_map_encoder() {
 
 bool encode_plane_map(TensorMap* map, const void* base, int row_bytes, int64_t tokens, int heads,
                       int64_t head_stride_rows, int batch, int64_t batch_stride_rows, int box_bytes,
-                      int swizzle) {
+                      int swizzle, int box_rows) {
   static_assert(sizeof(TensorMap) == sizeof(CUtensorMap), "tensor map size");
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) {
@@ -73,7 +73,7 @@ bool encode_plane_map(TensorMap* map, const void* base, int row_bytes, int64_t t
   const cuuint64_t hs = (cuuint64_t)(head_stride_rows > 0 ? head_stride_rows : tokens) * row_bytes;
   const cuuint64_t bs = batch > 1 ? (cuuint64_t)batch_stride_rows * row_bytes : hs * (cuuint64_t)heads;
   const cuuint64_t strides[3] = {(cuuint64_t)row_bytes, hs > 0 ? hs : 16, bs > 0 ? bs : 16};
-  const cuuint32_t box[4] = {(cuuint32_t)box_bytes, 16, 1, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMapSwizzle sw = swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                           : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B

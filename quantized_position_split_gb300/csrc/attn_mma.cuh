@@ -108,27 +108,29 @@ __host__ __device__ constexpr int min_i(int a, int b) { return a < b ? a : b; }
 // fall into 8 different bank groups.  Smaller planes (fp16 norms, q8_0 scales at
 // head_dim <= 128) come by 16-byte cp.async.  Either way rows past the view's end
 // arrive as zeros.
-template <int RB, bool VALUES>
+template <int RB, bool VALUES, int TT>
 struct PlaneG {
   static constexpr bool TMA = RB >= 16;
   static constexpr int IB = min_i(RB, 128);
   static constexpr int NB = TMA ? RB / IB : 0;
   static constexpr int SW = (VALUES && TMA) ? (IB >= 128 ? 128 : IB >= 64 ? 64 : IB >= 32 ? 32 : 0) : 0;
-  static constexpr int BYTES = kTile * RB;
+  static constexpr int BYTES = TT * RB;
 };
 
-template <int D, int KF, int VF>
-struct Geo {
+template <int D, int KF, int VF, int TT_>
+struct GeoT {
   static constexpr int K_RB = KF == QPS_FMT_F16 ? 2 * D : D;          // K data bytes / token
   static constexpr int K_ARB = KF == QPS_FMT_Q8_0 ? D / 16 : 0;       // K scales bytes / token
   static constexpr int V_RB = VF == QPS_FMT_F16 ? 2 * D : VF == QPS_FMT_Q8_0 ? D : D / 4;
   static constexpr int V_ARB = VF == QPS_FMT_Q8_0 ? D / 16 : VF == QPS_FMT_TQ3 ? D / 8 : 0;
   static constexpr int V_A2RB = VF == QPS_FMT_TQ3 ? 2 : 0;
-  using PK = PlaneG<K_RB, true>;
-  using PKA = PlaneG<K_ARB, false>;
-  using PV = PlaneG<V_RB, VF != QPS_FMT_TQ3>;
-  using PVA = PlaneG<V_ARB, false>;
-  using PVA2 = PlaneG<V_A2RB, false>;
+  static constexpr int TT = TT_;
+  static constexpr int SUB = TT / 16;
+  using PK = PlaneG<K_RB, true, TT>;
+  using PKA = PlaneG<K_ARB, false, TT>;
+  using PV = PlaneG<V_RB, VF != QPS_FMT_TQ3, TT>;
+  using PVA = PlaneG<V_ARB, false, TT>;
+  using PVA2 = PlaneG<V_A2RB, false, TT>;
   static constexpr int K_OFF = 0;
   static constexpr int KA_OFF = align_to(K_OFF + PK::BYTES, 128);
   static constexpr int V_OFF = align_to(KA_OFF + PKA::BYTES, 1024);
@@ -151,6 +153,16 @@ struct Geo {
   static constexpr int SMEM = 1024 + LUT + 256;       // + slack to align the base to 1024
 };
 
+// Tokens per stage: two 16-token MMA sub-tiles (independent chains for latency hiding,
+// one softmax update per 32 tokens) where registers allow (head_dim <= 128) and 4 warps
+// x 2 stages of 32 tokens still leave room for two CTAs per SM; else one.
+template <int D, int KF, int VF>
+constexpr int stage_tokens() {
+  return (D <= 128 && 4 * 2 * GeoT<D, KF, VF, 32>::STAGE <= 104 * 1024) ? 32 : 16;
+}
+template <int D, int KF, int VF>
+struct Geo : GeoT<D, KF, VF, stage_tokens<D, KF, VF>()> {};
+
 // Tensor maps of one launch, one per tensor-map plane (unused ones left empty).
 struct TmaSet {
   TensorMap k, ka, v, va;
@@ -159,14 +171,14 @@ struct TmaSet {
 // Byte offset of (token row t, byte b) of a plane staged by tensor-map boxes of IB
 // bytes with swizzle SW (the 16-byte chunk index XORed with row bits, as the hardware
 // writes it into a 1024-byte aligned region).
-template <int IB, int SW>
+template <int IB, int SW, int TT>
 __device__ __forceinline__ int soff(int t, int b) {
   const int box = b / IB, w = b % IB;
   int chunk = w >> 4;
   if constexpr (SW == 128) chunk ^= (t & 7);
   else if constexpr (SW == 64) chunk ^= ((t >> 1) & 3);
   else if constexpr (SW == 32) chunk ^= ((t >> 2) & 1);
-  return box * (kTile * IB) + t * IB + (chunk << 4) + (w & 15);
+  return box * (TT * IB) + t * IB + (chunk << 4) + (w & 15);
 }
 
 // ---- asynchronous copies completing on per-stage mbarriers --------------------------
@@ -234,6 +246,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   constexpr int KQ = KF == QPS_FMT_Q8_0 ? 1 : 0;
   constexpr bool VPERM = VF != QPS_FMT_F16;  // permuted output columns (see below)
   constexpr int DT = D / 8;                  // output columns per lane group (VPERM)
+  constexpr int SUB = G::SUB, TT = G::TT;    // 16-token sub-tiles per stage, tokens per stage
   constexpr float LOG2E = 1.4426950408889634f;
 
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -314,8 +327,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   const uint8_t* safe = reinterpret_cast<const uint8_t*>(p.k.data);
   const int bcoord = p.shared ? 0 : bz;  // tensor-map batch coordinate
 
-  const int64_t tile0 = t0 & ~(int64_t)(kTile - 1);
-  const int ntiles = (int)((t1 - tile0 + kTile - 1) / kTile);
+  const int64_t tile0 = t0 & ~(int64_t)(TT - 1);
+  const int ntiles = (int)((t1 - tile0 + TT - 1) / TT);
   uint8_t* wpipe = pipe + warp * G::STAGES * G::STAGE;
 
   const uint32_t bars = smem_addr(smem + G::BARS) + warp * G::STAGES * 8;
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     const int tile = warp + k * kWarps;
     if (tile >= ntiles) return;
     uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
-    const int64_t tb = tile0 + (int64_t)tile * kTile;
+    const int64_t tb = tile0 + (int64_t)tile * TT;
     const int tok = (int)tb;
     const uint32_t bar = bars + (k % G::STAGES) * 8;
     if (lane == 0) mbar_expect_tx(bar, G::TX);
@@ -337,10 +350,10 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     fence_proxy_async();
     const uint32_t sbase = smem_addr(st);
     if (lane < G::PK::NB)
-      tma_load_4d(sbase + G::K_OFF + lane * (kTile * G::PK::IB), &maps.k, lane * G::PK::IB, tok, head, bcoord, bar);
+      tma_load_4d(sbase + G::K_OFF + lane * (TT * G::PK::IB), &maps.k, lane * G::PK::IB, tok, head, bcoord, bar);
     if (lane >= 8 && lane < 8 + G::PV::NB) {
       const int b = lane - 8;
-      tma_load_4d(sbase + G::V_OFF + b * (kTile * G::PV::IB), &maps.v, b * G::PV::IB, tok, head, bcoord, bar);
+      tma_load_4d(sbase + G::V_OFF + b * (TT * G::PV::IB), &maps.v, b * G::PV::IB, tok, head, bcoord, bar);
     }
     if constexpr (G::PKA::TMA)
       if (lane == 16) tma_load_4d(sbase + G::KA_OFF, &maps.ka, 0, tok, head, bcoord, bar);
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       if (lane == 17) tma_load_4d(sbase + G::VA_OFF, &maps.va, 0, tok, head, bcoord, bar);
     if constexpr (G::SMALL) {
       // rows past the view's end (kv_end) are zero-filled, like the tensor-map boxes
-      const int valid = (int)max((int64_t)0, min((int64_t)kTile, p.end - tb));
+      const int valid = (int)max((int64_t)0, min((int64_t)TT, p.end - tb));
       if constexpr (G::K_ARB > 0 && !G::PKA::TMA)
         stage_flat_zfill<G::PKA::BYTES>(st + G::KA_OFF, ka + tb * G::K_ARB, valid * G::K_ARB, lane, safe);
       if constexpr (G::V_ARB > 0 && !G::PVA::TMA)
@@ -400,84 +413,108 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     await(k);
     if (timed_out) break;  // the error word tells the host; the outputs are not valid
     const uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
-    const int64_t tb = tile0 + (int64_t)(warp + k * kWarps) * kTile;
+    const int64_t tb = tile0 + (int64_t)(warp + k * kWarps) * TT;
 
-    // ---- S^T = K Q^T ---------------------------------------------------------------
-    float sacc[NTW][4];
+    // ---- S^T = K Q^T for each 16-token sub-tile (independent MMA chains) ------------
+    float sacc[SUB][NTW][4];
 #pragma unroll
-    for (int nt = 0; nt < NTW; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt) sacc[sb][nt][0] = sacc[sb][nt][1] = sacc[sb][nt][2] = sacc[sb][nt][3] = 0.f;
     if constexpr (KF == QPS_FMT_F16) {
       const uint32_t kbase = smem_addr(st + G::K_OFF);
       const int mi = lane >> 3;
       const int trow = (lane & 7) + ((mi & 1) << 3);
-      // two independent accumulator chains (even / odd k-steps) halve the MMA latency chain
-      float sodd[NTW][4];
+      // per sub-tile, two accumulator chains (even / odd k-steps)
+      float sodd[SUB][NTW][4];
 #pragma unroll
-      for (int nt = 0; nt < NTW; ++nt) sodd[nt][0] = sodd[nt][1] = sodd[nt][2] = sodd[nt][3] = 0.f;
+      for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) sodd[sb][nt][0] = sodd[sb][nt][1] = sodd[sb][nt][2] = sodd[sb][nt][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
-        uint32_t a[4];
-        ldsm_x4(a, kbase + soff<G::PK::IB, G::PK::SW>(trow, (2 * kk + (mi >> 1)) << 4));
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) {
-          if (kk & 1) mma16816(sodd[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-          else mma16816(sacc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        for (int sb = 0; sb < SUB; ++sb) {
+          uint32_t a[4];
+          ldsm_x4(a, kbase + soff<G::PK::IB, G::PK::SW, TT>(trow + 16 * sb, (2 * kk + (mi >> 1)) << 4));
+#pragma unroll
+          for (int nt = 0; nt < NTW; ++nt) {
+            if (kk & 1) mma16816(sodd[sb][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+            else mma16816(sacc[sb][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          }
         }
       }
 #pragma unroll
-      for (int nt = 0; nt < NTW; ++nt)
+      for (int sb = 0; sb < SUB; ++sb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
+        for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[sb][nt][e] += sodd[sb][nt][e];
     } else {
       const uint8_t* kc = st + G::K_OFF;
       const __half* ks = reinterpret_cast<const __half*>(st + G::KA_OFF);
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         const int x = 2 * j + (c >> 1), sub = 8 * (c & 1);
-        const uint2 wg = *reinterpret_cast<const uint2*>(kc + soff<G::PK::IB, G::PK::SW>(g, 16 * x + sub));
-        const uint2 wg8 = *reinterpret_cast<const uint2*>(kc + soff<G::PK::IB, G::PK::SW>(g + 8, 16 * x + sub));
-        uint32_t a0[4], a1[4];
-        i8x4_to_h2x2(wg.x, a0[0], a0[2]);
-        i8x4_to_h2x2(wg8.x, a0[1], a0[3]);
-        i8x4_to_h2x2(wg.y, a1[0], a1[2]);
-        i8x4_to_h2x2(wg8.y, a1[1], a1[3]);
-        const float sg = __half2float(ks[g * (D / 32) + j]);
-        const float sg8 = __half2float(ks[(g + 8) * (D / 32) + j]);
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816(acc, a0, qb[nt][2 * j][0], qb[nt][2 * j][1]);
-          mma16816(acc, a1, qb[nt][2 * j + 1][0], qb[nt][2 * j + 1][1]);
-          sacc[nt][0] = fmaf(sg, acc[0], sacc[nt][0]);
-          sacc[nt][1] = fmaf(sg, acc[1], sacc[nt][1]);
-          sacc[nt][2] = fmaf(sg8, acc[2], sacc[nt][2]);
-          sacc[nt][3] = fmaf(sg8, acc[3], sacc[nt][3]);
+        for (int sb = 0; sb < SUB; ++sb) {
+          const int r0 = g + 16 * sb, r8 = r0 + 8;
+          const uint2 wg = *reinterpret_cast<const uint2*>(kc + soff<G::PK::IB, G::PK::SW, TT>(r0, 16 * x + sub));
+          const uint2 wg8 = *reinterpret_cast<const uint2*>(kc + soff<G::PK::IB, G::PK::SW, TT>(r8, 16 * x + sub));
+          uint32_t a0[4], a1[4];
+          i8x4_to_h2x2(wg.x, a0[0], a0[2]);
+          i8x4_to_h2x2(wg8.x, a0[1], a0[3]);
+          i8x4_to_h2x2(wg.y, a1[0], a1[2]);
+          i8x4_to_h2x2(wg8.y, a1[1], a1[3]);
+          const float sg = __half2float(ks[r0 * (D / 32) + j]);
+          const float sg8 = __half2float(ks[r8 * (D / 32) + j]);
+#pragma unroll
+          for (int nt = 0; nt < NTW; ++nt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(acc, a0, qb[nt][2 * j][0], qb[nt][2 * j][1]);
+            mma16816(acc, a1, qb[nt][2 * j + 1][0], qb[nt][2 * j + 1][1]);
+            sacc[sb][nt][0] = fmaf(sg, acc[0], sacc[sb][nt][0]);
+            sacc[sb][nt][1] = fmaf(sg, acc[1], sacc[sb][nt][1]);
+            sacc[sb][nt][2] = fmaf(sg8, acc[2], sacc[sb][nt][2]);
+            sacc[sb][nt][3] = fmaf(sg8, acc[3], sacc[sb][nt][3]);
+          }
         }
       }
     }
 
-    // ---- logits, masking, online softmax ---------------------------------------------
-    const bool in_g = (tb + g >= t0) && (tb + g < t1);
-    const bool in_g8 = (tb + g + 8 >= t0) && (tb + g + 8 < t1);
-    float n_g = 1.f, n_g8 = 1.f;
-    if constexpr (VF == QPS_FMT_TQ3) {
-      const __half* nrm = reinterpret_cast<const __half*>(st + G::VA2_OFF);
-      n_g = __half2float(nrm[g]);
-      n_g8 = __half2float(nrm[g + 8]);
+    // ---- logits, masking, online softmax (one update per stage) ------------------------
+    bool in_g[SUB], in_g8[SUB];
+    float n_g[SUB], n_g8[SUB];
+#pragma unroll
+    for (int sb = 0; sb < SUB; ++sb) {
+      const int64_t t_g = tb + 16 * sb + g;
+      in_g[sb] = (t_g >= t0) && (t_g < t1);
+      in_g8[sb] = (t_g + 8 >= t0) && (t_g + 8 < t1);
+      n_g[sb] = n_g8[sb] = 1.f;
+      if constexpr (VF == QPS_FMT_TQ3) {
+        const __half* nrm = reinterpret_cast<const __half*>(st + G::VA2_OFF);
+        n_g[sb] = __half2float(nrm[16 * sb + g]);
+        n_g8[sb] = __half2float(nrm[16 * sb + g + 8]);
+      }
     }
-    uint32_t pb[NTW][2];
+    uint32_t pb[SUB][NTW][2];
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt) {
-      float x[4];
+      float x[SUB][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = sacc[nt][e] * qk_scale;
-        if (cap > 0.f) v = cap * tanhf(v / cap);
-        x[e] = v * LOG2E;
+      for (int sb = 0; sb < SUB; ++sb) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float v = sacc[sb][nt][e] * qk_scale;
+          if (cap > 0.f) v = cap * tanhf(v / cap);
+          x[sb][e] = v * LOG2E;
+        }
+        if (!in_g[sb]) x[sb][0] = x[sb][1] = -INFINITY;
+        if (!in_g8[sb]) x[sb][2] = x[sb][3] = -INFINITY;
+        mx0 = fmaxf(mx0, fmaxf(x[sb][0], x[sb][2]));
+        mx1 = fmaxf(mx1, fmaxf(x[sb][1], x[sb][3]));
       }
-      if (!in_g) x[0] = x[1] = -INFINITY;
-      if (!in_g8) x[2] = x[3] = -INFINITY;
-      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -486,10 +523,18 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
       const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
       const float cr0 = exp2f(m[nt][0] - ms0), cr1 = exp2f(m[nt][1] - ms1);
-      const float p0 = exp2f(x[0] - ms0), p1 = exp2f(x[1] - ms1);
-      const float p2 = exp2f(x[2] - ms0), p3 = exp2f(x[3] - ms1);
-      l[nt][0] = l[nt][0] * cr0 + (p0 + p2);
-      l[nt][1] = l[nt][1] * cr1 + (p1 + p3);
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int sb = 0; sb < SUB; ++sb) {
+        const float p0 = exp2f(x[sb][0] - ms0), p1 = exp2f(x[sb][1] - ms1);
+        const float p2 = exp2f(x[sb][2] - ms0), p3 = exp2f(x[sb][3] - ms1);
+        sum0 += p0 + p2;
+        sum1 += p1 + p3;
+        pb[sb][nt][0] = movmatrix_t(pack_h2(p0 * n_g[sb], p1 * n_g[sb]));
+        pb[sb][nt][1] = movmatrix_t(pack_h2(p2 * n_g8[sb], p3 * n_g8[sb]));
+      }
+      l[nt][0] = l[nt][0] * cr0 + sum0;
+      l[nt][1] = l[nt][1] * cr1 + sum1;
       m[nt][0] = mn0;
       m[nt][1] = mn1;
       if (__any_sync(0xffffffffu, cr0 != 1.f || cr1 != 1.f)) {
@@ -501,8 +546,6 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
           o[i][nt][3] *= cr1;
         }
       }
-      pb[nt][0] = movmatrix_t(pack_h2(p0 * n_g, p1 * n_g));
-      pb[nt][1] = movmatrix_t(pack_h2(p2 * n_g8, p3 * n_g8));
     }
 
     // ---- O^T += V^T P^T ---------------------------------------------------------------
@@ -512,10 +555,13 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       const int trow = (lane & 7) + ((mi & 2) << 2);
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
-        uint32_t a[4];
-        ldsm_x4_t(a, vbase + soff<G::PV::IB, G::PV::SW>(trow, (2 * i + (mi & 1)) << 4));
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[nt][0], pb[nt][1]);
+        for (int sb = 0; sb < SUB; ++sb) {
+          uint32_t a[4];
+          ldsm_x4_t(a, vbase + soff<G::PV::IB, G::PV::SW, TT>(trow + 16 * sb, (2 * i + (mi & 1)) << 4));
+#pragma unroll
+          for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[sb][nt][0], pb[sb][nt][1]);
+        }
       }
     } else if constexpr (VF == QPS_FMT_Q8_0) {
       // lane group g owns output columns [g*DT, g*DT + DT); tokens 2c, 2c+1, 2c+8, 2c+9
@@ -523,44 +569,47 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       const __half* vs = reinterpret_cast<const __half*>(st + G::VA_OFF);
       constexpr int CH = DT >= 16 ? 16 : DT;  // bytes per read
 #pragma unroll
-      for (int q0 = 0; q0 < DT; q0 += CH) {
-        uint32_t w[4][CH / 4];
-        const int tok[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-        const int blk = (g * DT + q0) / 32;
+      for (int sb = 0; sb < SUB; ++sb) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int byte = g * DT + q0;
-          const uint8_t* src = vc + soff<G::PV::IB, G::PV::SW>(tok[u], byte);
-          if constexpr (CH == 16) {
-            const uint4 r = *reinterpret_cast<const uint4*>(src);
-            w[u][0] = r.x; w[u][1] = r.y; w[u][2] = r.z; w[u][3] = r.w;
-          } else {
-            const uint2 r = *reinterpret_cast<const uint2*>(src);
-            w[u][0] = r.x; w[u][1] = r.y;
-          }
-        }
-        __half2 sc[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sc[u] = __half2half2(vs[tok[u] * (D / 32) + blk]);
-#pragma unroll
-        for (int wi = 0; wi < CH / 4; ++wi) {
-          uint32_t hv[4][2];
+        for (int q0 = 0; q0 < DT; q0 += CH) {
+          uint32_t w[4][CH / 4];
+          const int tok[4] = {16 * sb + 2 * c, 16 * sb + 2 * c + 1, 16 * sb + 2 * c + 8, 16 * sb + 2 * c + 9};
+          const int blk = (g * DT + q0) / 32;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            i8x4_to_h2x2(w[u][wi], hv[u][0], hv[u][1]);
-            hv[u][0] = hmul2_u(hv[u][0], sc[u]);
-            hv[u][1] = hmul2_u(hv[u][1], sc[u]);
+            const int byte = g * DT + q0;
+            const uint8_t* src = vc + soff<G::PV::IB, G::PV::SW, TT>(tok[u], byte);
+            if constexpr (CH == 16) {
+              const uint4 r = *reinterpret_cast<const uint4*>(src);
+              w[u][0] = r.x; w[u][1] = r.y; w[u][2] = r.z; w[u][3] = r.w;
+            } else {
+              const uint2 r = *reinterpret_cast<const uint2*>(src);
+              w[u][0] = r.x; w[u][1] = r.y;
+            }
           }
+          __half2 sc[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int i = (q0 + 4 * wi) / 2 + hh;  // m-tile: output columns base + 2i, +1
-            uint32_t a[4];
-            a[0] = __byte_perm(hv[0][hh], hv[1][hh], 0x5410);
-            a[1] = __byte_perm(hv[0][hh], hv[1][hh], 0x7632);
-            a[2] = __byte_perm(hv[2][hh], hv[3][hh], 0x5410);
-            a[3] = __byte_perm(hv[2][hh], hv[3][hh], 0x7632);
+          for (int u = 0; u < 4; ++u) sc[u] = __half2half2(vs[tok[u] * (D / 32) + blk]);
 #pragma unroll
-            for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[nt][0], pb[nt][1]);
+          for (int wi = 0; wi < CH / 4; ++wi) {
+            uint32_t hv[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              i8x4_to_h2x2(w[u][wi], hv[u][0], hv[u][1]);
+              hv[u][0] = hmul2_u(hv[u][0], sc[u]);
+              hv[u][1] = hmul2_u(hv[u][1], sc[u]);
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int i = (q0 + 4 * wi) / 2 + hh;  // m-tile: output columns base + 2i, +1
+              uint32_t a[4];
+              a[0] = __byte_perm(hv[0][hh], hv[1][hh], 0x5410);
+              a[1] = __byte_perm(hv[0][hh], hv[1][hh], 0x7632);
+              a[2] = __byte_perm(hv[2][hh], hv[3][hh], 0x5410);
+              a[3] = __byte_perm(hv[2][hh], hv[3][hh], 0x7632);
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[sb][nt][0], pb[sb][nt][1]);
+            }
           }
         }
       }
@@ -569,38 +618,41 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       const uint8_t* hi1 = st + G::VA_OFF;
       constexpr int LB = D / 32;  // 2-bit plane bytes per lane group and token
 #pragma unroll
-      for (int e0 = 0; e0 < DT; e0 += 16) {  // 16 elements = one 32-bit word of lo2
-        uint32_t L[4], H[4];
-        const int tok[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+      for (int sb = 0; sb < SUB; ++sb) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int lb = tok[u] * (D / 4) + g * LB + e0 / 4;
-          const int hb = tok[u] * (D / 8) + g * (LB / 2) + e0 / 8;
-          if constexpr (DT >= 16) {
-            L[u] = *reinterpret_cast<const uint32_t*>(lo2 + lb);
-            H[u] = *reinterpret_cast<const uint16_t*>(hi1 + hb);
-          } else {  // D = 64: 8 elements per lane group
-            L[u] = *reinterpret_cast<const uint16_t*>(lo2 + lb);
-            H[u] = *reinterpret_cast<const uint8_t*>(hi1 + hb);
+        for (int e0 = 0; e0 < DT; e0 += 16) {  // 16 elements = one 32-bit word of lo2
+          uint32_t L[4], H[4];
+          const int tok[4] = {16 * sb + 2 * c, 16 * sb + 2 * c + 1, 16 * sb + 2 * c + 8, 16 * sb + 2 * c + 9};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int lb = tok[u] * (D / 4) + g * LB + e0 / 4;
+            const int hb = tok[u] * (D / 8) + g * (LB / 2) + e0 / 8;
+            if constexpr (DT >= 16) {
+              L[u] = *reinterpret_cast<const uint32_t*>(lo2 + lb);
+              H[u] = *reinterpret_cast<const uint16_t*>(hi1 + hb);
+            } else {  // D = 64: 8 elements per lane group
+              L[u] = *reinterpret_cast<const uint16_t*>(lo2 + lb);
+              H[u] = *reinterpret_cast<const uint8_t*>(hi1 + hb);
+            }
           }
-        }
-        constexpr int NE = DT >= 16 ? 16 : DT;
+          constexpr int NE = DT >= 16 ? 16 : DT;
 #pragma unroll
-        for (int e = 0; e < NE; e += 2) {
-          const int i = (e0 + e) / 2;
-          uint32_t a[4];
+          for (int e = 0; e < NE; e += 2) {
+            const int i = (e0 + e) / 2;
+            uint32_t a[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int ee = e + hh;
-            const uint32_t i01 = ((L[0] >> (2 * ee)) & 3u) | (((L[1] >> (2 * ee)) & 3u) << 2) |
-                                 (((H[0] >> ee) & 1u) << 4) | (((H[1] >> ee) & 1u) << 5);
-            const uint32_t i89 = ((L[2] >> (2 * ee)) & 3u) | (((L[3] >> (2 * ee)) & 3u) << 2) |
-                                 (((H[2] >> ee) & 1u) << 4) | (((H[3] >> ee) & 1u) << 5);
-            a[hh] = lut[i01];
-            a[2 + hh] = lut[i89];
+            for (int hh = 0; hh < 2; ++hh) {
+              const int ee = e + hh;
+              const uint32_t i01 = ((L[0] >> (2 * ee)) & 3u) | (((L[1] >> (2 * ee)) & 3u) << 2) |
+                                   (((H[0] >> ee) & 1u) << 4) | (((H[1] >> ee) & 1u) << 5);
+              const uint32_t i89 = ((L[2] >> (2 * ee)) & 3u) | (((L[3] >> (2 * ee)) & 3u) << 2) |
+                                   (((H[2] >> ee) & 1u) << 4) | (((H[3] >> ee) & 1u) << 5);
+              a[hh] = lut[i01];
+              a[2 + hh] = lut[i89];
+            }
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[sb][nt][0], pb[sb][nt][1]);
           }
-#pragma unroll
-          for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[nt][0], pb[nt][1]);
         }
       }
     }
@@ -717,14 +769,14 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
   TmaSet maps;
   std::memset(&maps, 0, sizeof(maps));
   const int nb = p.shared ? 1 : p.batch;
-  if (!encode_plane_map(&maps.k, p.k.data, G::K_RB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PK::IB, G::PK::SW) ||
-      !encode_plane_map(&maps.v, p.v.data, G::V_RB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PV::IB, G::PV::SW))
+  if (!encode_plane_map(&maps.k, p.k.data, G::K_RB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PK::IB, G::PK::SW, G::TT) ||
+      !encode_plane_map(&maps.v, p.v.data, G::V_RB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PV::IB, G::PV::SW, G::TT))
     return QPS_ERR_CUDA;
   if constexpr (G::PKA::TMA)
-    if (!encode_plane_map(&maps.ka, p.k.aux, G::K_ARB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PKA::IB, 0))
+    if (!encode_plane_map(&maps.ka, p.k.aux, G::K_ARB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PKA::IB, 0, G::TT))
       return QPS_ERR_CUDA;
   if constexpr (G::PVA::TMA)
-    if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, 0))
+    if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, 0, G::TT))
       return QPS_ERR_CUDA;
   auto kern = attn_mma_kernel<D, KF, VF, NTW>;
   QPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));

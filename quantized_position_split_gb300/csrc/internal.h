@@ -24,14 +24,14 @@ void count_launch(int n = 1);
 
 // ---- tensor memory access descriptors ----------------------------------------------
 // A byte plane seen as a 4-D tensor [row bytes][tokens][heads][batch] (innermost
-// first), loaded in boxes of [box_bytes][16 tokens][1][1].  swizzle: 0 none, 32, 64 or
+// first), loaded in boxes of [box_bytes][box_rows tokens][1][1].  swizzle: 0 none, 32, 64 or
 // 128 (bytes).  Returns false (with the error message set) on failure.
 struct alignas(64) TensorMap {
   unsigned char bytes[128];
 };
 bool encode_plane_map(TensorMap* map, const void* base, int row_bytes, int64_t tokens, int heads,
                       int64_t head_stride_rows, int batch, int64_t batch_stride_rows, int box_bytes,
-                      int swizzle);
+                      int swizzle, int box_rows);
 
 // ---- device facts -----------------------------------------------------------------
 int sm_count_current();

@@ -102,12 +102,12 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, __half2 s) {
 __host__ __device__ constexpr int align_to(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ constexpr int min_i(int a, int b) { return a < b ? a : b; }
 
-// One plane of a 16-token tile.  Planes of >= 16 bytes per token arrive as tensor-map
-// boxes of [IB bytes][16 tokens] (IB = min(row bytes, 128)); the K / V value planes use
-// the hardware XOR swizzle that matches IB so that 8 token rows read at the same column
-// fall into 8 different bank groups.  Smaller planes (fp16 norms, q8_0 scales at
-// head_dim <= 128) come by 16-byte cp.async.  Either way rows past the view's end
-// arrive as zeros.
+// One plane of a TT-token stage.  Planes of >= 16 bytes per token arrive as tensor-map
+// boxes of [IB bytes][TT tokens] (IB = min(row bytes, 128)); the K / V value planes
+// (and the TQ3 sign plane) use the hardware XOR swizzle that matches IB so that token
+// rows read at the same column fall into different bank groups.  Smaller planes (fp16
+// norms, q8_0 scales at head_dim <= 128) come by 16-byte cp.async.  Either way rows past
+// the view's end arrive as zeros.
 template <int RB, bool VALUES, int TT>
 struct PlaneG {
   static constexpr bool TMA = RB >= 16;
@@ -128,13 +128,13 @@ struct GeoT {
   static constexpr int SUB = TT / 16;
   using PK = PlaneG<K_RB, true, TT>;
   using PKA = PlaneG<K_ARB, false, TT>;
-  using PV = PlaneG<V_RB, VF != QPS_FMT_TQ3, TT>;
-  using PVA = PlaneG<V_ARB, false, TT>;
+  using PV = PlaneG<V_RB, true, TT>;
+  using PVA = PlaneG<V_ARB, VF == QPS_FMT_TQ3, TT>;  // the TQ3 sign plane is read like values
   using PVA2 = PlaneG<V_A2RB, false, TT>;
   static constexpr int K_OFF = 0;
   static constexpr int KA_OFF = align_to(K_OFF + PK::BYTES, 128);
   static constexpr int V_OFF = align_to(KA_OFF + PKA::BYTES, 1024);
-  static constexpr int VA_OFF = align_to(V_OFF + PV::BYTES, 128);
+  static constexpr int VA_OFF = align_to(V_OFF + PV::BYTES, PVA::SW ? 1024 : 128);
   static constexpr int VA2_OFF = align_to(VA_OFF + PVA::BYTES, 128);
   static constexpr int STAGE = align_to(VA2_OFF + PVA2::BYTES, 1024);
   // bytes the tensor-map boxes of one tile deliver
@@ -149,8 +149,8 @@ struct GeoT {
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 6 ? 6 : STAGES_RAW);
   static constexpr int PIPE = NW * STAGES * STAGE;
   static constexpr int BARS = PIPE;                   // mbarriers after the stages
-  static constexpr int LUT = BARS + NW * STAGES * 8;  // TQ3 level LUT after the barriers
-  static constexpr int SMEM = 1024 + LUT + 256;       // + slack to align the base to 1024
+  static constexpr int END = BARS + NW * STAGES * 8;  // end of the barriers
+  static constexpr int SMEM = 1024 + END;             // + slack to align the base to 1024
 };
 
 // Tokens per stage: two 16-token MMA sub-tiles (independent chains for latency hiding,
@@ -235,6 +235,14 @@ __device__ __forceinline__ void stage_flat_zfill(uint8_t* dst, const uint8_t* sr
   }
 }
 
+// Output column (within a lane group's DT columns) of row g (hh = 0) or g + 8 (hh = 1)
+// of the TQ3 PV m-tile i: word k = i / 8 covers 16 columns, its m-tile 2j + h takes
+// columns j + 8h and j + 8h + 4 (DT = 8: one half-word, m-tile j takes j and j + 4).
+template <int DT>
+__host__ __device__ constexpr int tq_col(int i, int hh) {
+  return DT >= 16 ? 16 * (i >> 3) + ((i >> 1) & 3) + 8 * (i & 1) + 4 * hh : i + 4 * hh;
+}
+
 // ---- the kernel -------------------------------------------------------------------
 template <int D, int KF, int VF, int NTW>
 __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
@@ -253,7 +261,6 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   // swizzled boxes need a 1024-byte aligned base
   uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint8_t* pipe = smem;
-  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + G::LUT);  // TQ3: 64 half2
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -282,12 +289,11 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     return;
   }
 
+  // TQ3 magnitudes as fp16 (exact): level 4 + m in bytes 2m, 2m + 1 of {tq_lo, tq_hi}
+  uint32_t tq_lo = 0u, tq_hi = 0u;
   if constexpr (VF == QPS_FMT_TQ3) {
-    // index = mag_a | mag_b << 2 | sign_a << 4 | sign_b << 5 -> half2(level_a, level_b)
-    for (int i = threadIdx.x; i < 64; i += blockDim.x) {
-      const float ma = p.tq_levels[4 + (i & 3)], mb = p.tq_levels[4 + ((i >> 2) & 3)];
-      lut[i] = pack_h2((i & 16) ? ma : -ma, (i & 32) ? mb : -mb);
-    }
+    tq_lo = pack_h2(p.tq_levels[4], p.tq_levels[5]);
+    tq_hi = pack_h2(p.tq_levels[6], p.tq_levels[7]);
   }
 
   // ---- query fragments (B operand of S^T), one set per 8-row n-tile --------------
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     for (int s = 0; s < G::STAGES; ++s) mbar_init(bars + s * 8, G::ARRIVALS);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  __syncthreads();  // the LUT and the barriers are ready
+  __syncthreads();  // the barriers are ready
 
 #pragma unroll 1
   for (int s = 0; s < G::STAGES - 1; ++s) issue(s);
@@ -613,45 +619,75 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
           }
         }
       }
-    } else {  // TQ3: levels through the LUT, tokens paired (2c, 2c+1) and (2c+8, 2c+9)
+    } else {
+      // TQ3.  Word k of a lane group's 2-bit plane holds 16 of its output columns; the
+      // codes of the two tokens of a pair are interleaved byte by byte, spread to one
+      // code per byte and turned into byte-permute selectors over the fp16 magnitude
+      // table; the sign plane supplies bit 15 of each half.  m-tile i of word k takes
+      // columns tq_col(i, 0) and tq_col(i, 1) (see the epilogue).
+      constexpr int LB = DT / 4;                   // 2-bit plane bytes per lane group, token
+      constexpr int HB = DT / 8;                   // sign plane bytes per lane group, token
+      constexpr int NWD = DT >= 16 ? DT / 16 : 1;  // 16-column words
+      constexpr int NH = DT >= 16 ? 2 : 1;         // 8-column halves of a word
       const uint8_t* lo2 = st + G::V_OFF;
       const uint8_t* hi1 = st + G::VA_OFF;
-      constexpr int LB = D / 32;  // 2-bit plane bytes per lane group and token
 #pragma unroll
       for (int sb = 0; sb < SUB; ++sb) {
+        const int tk[4] = {16 * sb + 2 * c, 16 * sb + 2 * c + 1, 16 * sb + 2 * c + 8, 16 * sb + 2 * c + 9};
+        uint32_t L[4][NWD];
 #pragma unroll
-        for (int e0 = 0; e0 < DT; e0 += 16) {  // 16 elements = one 32-bit word of lo2
-          uint32_t L[4], H[4];
-          const int tok[4] = {16 * sb + 2 * c, 16 * sb + 2 * c + 1, 16 * sb + 2 * c + 8, 16 * sb + 2 * c + 9};
+        for (int u = 0; u < 4; ++u) {
+          const uint8_t* ls = lo2 + soff<G::PV::IB, G::PV::SW, TT>(tk[u], g * LB);
+          if constexpr (LB == 16) {
+            const uint4 r = *reinterpret_cast<const uint4*>(ls);
+            L[u][0] = r.x; L[u][1] = r.y; L[u][2] = r.z; L[u][3] = r.w;
+          } else if constexpr (LB == 8) {
+            const uint2 r = *reinterpret_cast<const uint2*>(ls);
+            L[u][0] = r.x; L[u][1] = r.y;
+          } else if constexpr (LB == 4) {
+            L[u][0] = *reinterpret_cast<const uint32_t*>(ls);
+          } else {
+            L[u][0] = *reinterpret_cast<const uint16_t*>(ls);
+          }
+        }
+        uint32_t H[4];  // sign bits of 32 columns (fewer at head_dim <= 128) per token
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int lb = tok[u] * (D / 4) + g * LB + e0 / 4;
-            const int hb = tok[u] * (D / 8) + g * (LB / 2) + e0 / 8;
-            if constexpr (DT >= 16) {
-              L[u] = *reinterpret_cast<const uint32_t*>(lo2 + lb);
-              H[u] = *reinterpret_cast<const uint16_t*>(hi1 + hb);
-            } else {  // D = 64: 8 elements per lane group
-              L[u] = *reinterpret_cast<const uint16_t*>(lo2 + lb);
-              H[u] = *reinterpret_cast<const uint8_t*>(hi1 + hb);
+        for (int k = 0; k < NWD; ++k) {
+          if ((k & 1) == 0) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint8_t* hs = hi1 + soff<G::PVA::IB, G::PVA::SW, TT>(tk[u], g * HB + 2 * k);
+              if constexpr (HB >= 4) H[u] = *reinterpret_cast<const uint32_t*>(hs);
+              else if constexpr (HB == 2) H[u] = *reinterpret_cast<const uint16_t*>(hs);
+              else H[u] = *hs;
             }
           }
-          constexpr int NE = DT >= 16 ? 16 : DT;
+          // sign bits of word k: token a of the pair in bits 0..15, token b in 16..31
+          const uint32_t hsel = (k & 1) ? 0x7632u : 0x5410u;
+          const uint32_t hab[2] = {__byte_perm(H[0], H[1], hsel), __byte_perm(H[2], H[3], hsel)};
 #pragma unroll
-          for (int e = 0; e < NE; e += 2) {
-            const int i = (e0 + e) / 2;
-            uint32_t a[4];
+          for (int h = 0; h < NH; ++h) {
+            // bytes: (a, b) codes of columns 8h .. 8h + 3, then of 8h + 4 .. 8h + 7
+            const uint32_t ysel = h ? 0x7362u : 0x5140u;
+            const uint32_t y[2] = {__byte_perm(L[0][k], L[1][k], ysel), __byte_perm(L[2][k], L[3][k], ysel)};
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int ee = e + hh;
-              const uint32_t i01 = ((L[0] >> (2 * ee)) & 3u) | (((L[1] >> (2 * ee)) & 3u) << 2) |
-                                   (((H[0] >> ee) & 1u) << 4) | (((H[1] >> ee) & 1u) << 5);
-              const uint32_t i89 = ((L[2] >> (2 * ee)) & 3u) | (((L[3] >> (2 * ee)) & 3u) << 2) |
-                                   (((H[2] >> ee) & 1u) << 4) | (((H[3] >> ee) & 1u) << 5);
-              a[hh] = lut[i01];
-              a[2 + hh] = lut[i89];
+            for (int j = 0; j < 4; ++j) {
+              const int i = DT >= 16 ? 8 * k + 2 * j + h : j;  // m-tile
+              const int e0 = j + 8 * h, e1 = e0 + 4;           // columns within the word
+              uint32_t a[4];
+#pragma unroll
+              for (int pr = 0; pr < 2; ++pr) {
+                // one code per byte, then the selector nibbles (2m, 2m + 1) of level 4 + m
+                const uint32_t sel = ((y[pr] >> (2 * j)) & 0x03030303u) * 0x22u + 0x10101010u;
+                const uint32_t m0 = __byte_perm(tq_lo, tq_hi, sel);
+                const uint32_t m1 = __byte_perm(tq_lo, tq_hi, sel >> 16);
+                // a clear sign bit stores a negative level
+                a[2 * pr] = m0 | (~(hab[pr] << (15 - e0)) & 0x80008000u);
+                a[2 * pr + 1] = m1 | (~(hab[pr] << (15 - e1)) & 0x80008000u);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[sb][nt][0], pb[sb][nt][1]);
             }
-#pragma unroll
-            for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[sb][nt][0], pb[sb][nt][1]);
           }
         }
       }
@@ -682,7 +718,10 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
       int d0, d1;
-      if constexpr (VPERM) {
+      if constexpr (VF == QPS_FMT_TQ3) {
+        d0 = g * DT + tq_col<DT>(i, 0);
+        d1 = g * DT + tq_col<DT>(i, 1);
+      } else if constexpr (VPERM) {
         d0 = g * DT + 2 * i;
         d1 = d0 + 1;
       } else {
@@ -754,7 +793,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
 template <int D, int KF, int VF, int NTW>
 constexpr size_t smem_bytes() {
   using G = Geo<D, KF, VF>;
-  constexpr size_t pipe = (size_t)G::LUT + 256;
+  constexpr size_t pipe = (size_t)G::END;
   constexpr int ROWS = 8 * NTW;
   constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D);
   return (pipe > merge ? pipe : merge) + 1024;  // + slack for the 1024-byte base alignment
@@ -776,7 +815,7 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
     if (!encode_plane_map(&maps.ka, p.k.aux, G::K_ARB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PKA::IB, 0, G::TT))
       return QPS_ERR_CUDA;
   if constexpr (G::PVA::TMA)
-    if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, 0, G::TT))
+    if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, G::PVA::SW, G::TT))
       return QPS_ERR_CUDA;
   auto kern = attn_mma_kernel<D, KF, VF, NTW>;
   QPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));

@@ -61,8 +61,10 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
                : "r"(addr));
 }
 
+// Register-only operations are plain asm so that the compiler may interleave them;
+// shared-memory reads stay volatile behind the barrier waits.
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -71,7 +73,7 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
 
@@ -96,6 +98,16 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
 __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, __half2 s) {
   __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
   return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Logit softcap c * tanh(x / c) through tanh(y) = 1 - 2 / (1 + e^(2y)), with the
+// hardware base-2 exponential and reciprocal; k = 2 log2(e) / c.  Its absolute error
+// is a few 1e-7 x c (the 1 - 2r cancellation near 0), and it saturates to +-c.
+__device__ __forceinline__ float softcap_tanh(float x, float c, float k) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * k));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return fmaf(-2.f * c, r, c);
 }
 
 // ---- tile geometry ---------------------------------------------------------------
@@ -131,11 +143,13 @@ struct GeoT {
   using PV = PlaneG<V_RB, true, TT>;
   using PVA = PlaneG<V_ARB, VF == QPS_FMT_TQ3, TT>;  // the TQ3 sign plane is read like values
   using PVA2 = PlaneG<V_A2RB, false, TT>;
+  // swizzled planes first (each on a 1024-byte boundary), then the small ones
   static constexpr int K_OFF = 0;
-  static constexpr int KA_OFF = align_to(K_OFF + PK::BYTES, 128);
-  static constexpr int V_OFF = align_to(KA_OFF + PKA::BYTES, 1024);
-  static constexpr int VA_OFF = align_to(V_OFF + PV::BYTES, PVA::SW ? 1024 : 128);
-  static constexpr int VA2_OFF = align_to(VA_OFF + PVA::BYTES, 128);
+  static constexpr int V_OFF = align_to(K_OFF + PK::BYTES, 1024);
+  static constexpr int AFTER_V = V_OFF + PV::BYTES;
+  static constexpr int KA_OFF = align_to(PVA::SW ? align_to(AFTER_V, 1024) + PVA::BYTES : AFTER_V, 128);
+  static constexpr int VA_OFF = PVA::SW ? align_to(AFTER_V, 1024) : align_to(KA_OFF + PKA::BYTES, 128);
+  static constexpr int VA2_OFF = align_to(PVA::SW ? KA_OFF + PKA::BYTES : VA_OFF + PVA::BYTES, 128);
   static constexpr int STAGE = align_to(VA2_OFF + PVA2::BYTES, 1024);
   // bytes the tensor-map boxes of one tile deliver
   static constexpr int TX = PK::BYTES + (PKA::TMA ? PKA::BYTES : 0) + PV::BYTES + (PVA::TMA ? PVA::BYTES : 0) +
@@ -150,7 +164,6 @@ struct GeoT {
   static constexpr int PIPE = NW * STAGES * STAGE;
   static constexpr int BARS = PIPE;                   // mbarriers after the stages
   static constexpr int END = BARS + NW * STAGES * 8;  // end of the barriers
-  static constexpr int SMEM = 1024 + END;             // + slack to align the base to 1024
 };
 
 // Tokens per stage: two 16-token MMA sub-tiles (independent chains for latency hiding,
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   };
 
   if (t0 >= t1) {  // an empty chunk: O = 0, lse = -inf
-    for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < nrows * D; idx += G::NW * 32) {
       const int r = idx / D, dd = idx % D;
       const int64_t row = out_row(row0 + r);
       p.o_parts[((int64_t)part * p.rows_total + row) * D + dd] = 0.f;
@@ -340,10 +353,9 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   const uint32_t bars = smem_addr(smem + G::BARS) + warp * G::STAGES * 8;
   bool timed_out = false;
 
-  // The warp's k-th tile -> stage k % STAGES.  Lane 0 announces the tensor-map bytes;
-  // lanes issue one box each (K boxes from lane 0, V boxes from lane 8, the scale /
-  // bit planes from lanes 16 and 17); small planes go by zero-filling cp.async from
-  // every lane, each lane then arriving on the same mbarrier when its copies land.
+  // The warp's k-th tile -> stage k % STAGES.  Lane 0 announces the tensor-map bytes; lanes issue one box each; small planes go by
+  // zero-filling cp.async from every lane, each lane then arriving on the same mbarrier
+  // when its copies land.
   auto issue = [&](int k) {
     const int tile = warp + k * kWarps;
     if (tile >= ntiles) return;
@@ -355,16 +367,25 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     __syncwarp();
     fence_proxy_async();
     const uint32_t sbase = smem_addr(st);
-    if (lane < G::PK::NB)
-      tma_load_4d(sbase + G::K_OFF + lane * (TT * G::PK::IB), &maps.k, lane * G::PK::IB, tok, head, bcoord, bar);
-    if (lane >= 8 && lane < 8 + G::PV::NB) {
-      const int b = lane - 8;
-      tma_load_4d(sbase + G::V_OFF + b * (TT * G::PV::IB), &maps.v, b * G::PV::IB, tok, head, bcoord, bar);
+    // one box per lane: K boxes, then V boxes, then the K-scale and V-aux planes
+    constexpr int NKB = G::PK::NB, NVB = G::PV::NB;
+    constexpr int NBOX = NKB + NVB + (G::PKA::TMA ? 1 : 0) + (G::PVA::TMA ? 1 : 0);
+    static_assert(NBOX <= 32, "one tensor-map box per lane");
+    if (lane < NBOX) {
+      const TensorMap* mp = &maps.k;
+      int dst = G::K_OFF + lane * (TT * G::PK::IB), x = lane * G::PK::IB;
+      if (lane >= NKB && lane < NKB + NVB) {
+        mp = &maps.v;
+        dst = G::V_OFF + (lane - NKB) * (TT * G::PV::IB);
+        x = (lane - NKB) * G::PV::IB;
+      } else if (lane >= NKB + NVB) {
+        const bool ka = G::PKA::TMA && lane == NKB + NVB;
+        mp = ka ? &maps.ka : &maps.va;
+        dst = ka ? G::KA_OFF : G::VA_OFF;
+        x = 0;
+      }
+      tma_load_4d(sbase + dst, mp, x, tok, head, bcoord, bar);
     }
-    if constexpr (G::PKA::TMA)
-      if (lane == 16) tma_load_4d(sbase + G::KA_OFF, &maps.ka, 0, tok, head, bcoord, bar);
-    if constexpr (G::PVA::TMA)
-      if (lane == 17) tma_load_4d(sbase + G::VA_OFF, &maps.va, 0, tok, head, bcoord, bar);
     if constexpr (G::SMALL) {
       // rows past the view's end (kv_end) are zero-filled, like the tensor-map boxes
       const int valid = (int)max((int64_t)0, min((int64_t)TT, p.end - tb));
@@ -403,6 +424,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   }
   const float qk_scale = p.scale;
   const float cap = p.softcap;
+  const float cap_k = cap > 0.f ? 2.f * 1.4426950408889634f / cap : 0.f;  // 2 log2(e) / cap
 
   if (lane == 0) {
     for (int s = 0; s < G::STAGES; ++s) mbar_init(bars + s * 8, G::ARRIVALS);
@@ -410,19 +432,22 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   }
   __syncthreads();  // the barriers are ready
 
-#pragma unroll 1
-  for (int s = 0; s < G::STAGES - 1; ++s) issue(s);
+  // ---- per-tile work ------------------------------------------------------------------
+  // per-lane stage offsets that do not change from tile to tile
+  const int ks_lane = g * (D / 32);                        // K scale of (row g, block 0)
+  int tq_lo2[4] = {0, 0, 0, 0}, tq_sgn[4] = {0, 0, 0, 0};   // TQ3 plane offsets, tokens 2c..
+  if constexpr (VF == QPS_FMT_TQ3) {
+    const int tk0[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      tq_lo2[u] = soff<G::PV::IB, G::PV::SW, TT>(tk0[u], g * (DT / 4));
+      tq_sgn[u] = soff<G::PVA::IB, G::PVA::SW, TT>(tk0[u], g * (DT / 8));
+    }
+  }
 
-#pragma unroll 1
-  for (int k = 0; warp + k * kWarps < ntiles; ++k) {
-    issue(k + G::STAGES - 1);
-    await(k);
-    if (timed_out) break;  // the error word tells the host; the outputs are not valid
-    const uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
-    const int64_t tb = tile0 + (int64_t)(warp + k * kWarps) * TT;
-
+  // S^T = K Q^T over this warp's columns, for each 16-token sub-tile
+  auto k_part = [&](const uint8_t* st, float (&sacc)[SUB][NTW][4]) {
     // ---- S^T = K Q^T for each 16-token sub-tile (independent MMA chains) ------------
-    float sacc[SUB][NTW][4];
 #pragma unroll
     for (int sb = 0; sb < SUB; ++sb)
 #pragma unroll
@@ -458,7 +483,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
           for (int e = 0; e < 4; ++e) sacc[sb][nt][e] += sodd[sb][nt][e];
     } else {
       const uint8_t* kc = st + G::K_OFF;
-      const __half* ks = reinterpret_cast<const __half*>(st + G::KA_OFF);
+      const __half* ks = reinterpret_cast<const __half*>(st + G::KA_OFF) + ks_lane;
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         const int x = 2 * j + (c >> 1), sub = 8 * (c & 1);
@@ -472,8 +497,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
           i8x4_to_h2x2(wg8.x, a0[1], a0[3]);
           i8x4_to_h2x2(wg.y, a1[0], a1[2]);
           i8x4_to_h2x2(wg8.y, a1[1], a1[3]);
-          const float sg = __half2float(ks[r0 * (D / 32) + j]);
-          const float sg8 = __half2float(ks[r8 * (D / 32) + j]);
+          const float sg = __half2float(ks[16 * sb * (D / 32) + j]);
+          const float sg8 = __half2float(ks[(16 * sb + 8) * (D / 32) + j]);
 #pragma unroll
           for (int nt = 0; nt < NTW; ++nt) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -488,6 +513,10 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       }
     }
 
+  };
+
+  // logits of the stage starting at token tb, online softmax, O^T += V^T P^T
+  auto attend_tile = [&](const uint8_t* st, int64_t tb, float (&sacc)[SUB][NTW][4]) {
     // ---- logits, masking, online softmax (one update per stage) ------------------------
     bool in_g[SUB], in_g8[SUB];
     float n_g[SUB], n_g8[SUB];
@@ -513,7 +542,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float v = sacc[sb][nt][e] * qk_scale;
-          if (cap > 0.f) v = cap * tanhf(v / cap);
+          if (cap > 0.f) v = softcap_tanh(v, cap, cap_k);
           x[sb][e] = v * LOG2E;
         }
         if (!in_g[sb]) x[sb][0] = x[sb][1] = -INFINITY;
@@ -633,11 +662,10 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       const uint8_t* hi1 = st + G::VA_OFF;
 #pragma unroll
       for (int sb = 0; sb < SUB; ++sb) {
-        const int tk[4] = {16 * sb + 2 * c, 16 * sb + 2 * c + 1, 16 * sb + 2 * c + 8, 16 * sb + 2 * c + 9};
         uint32_t L[4][NWD];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint8_t* ls = lo2 + soff<G::PV::IB, G::PV::SW, TT>(tk[u], g * LB);
+          const uint8_t* ls = lo2 + tq_lo2[u] + 16 * sb * G::PV::IB;  // swizzle repeats every 8 rows
           if constexpr (LB == 16) {
             const uint4 r = *reinterpret_cast<const uint4*>(ls);
             L[u][0] = r.x; L[u][1] = r.y; L[u][2] = r.z; L[u][3] = r.w;
@@ -656,7 +684,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
           if ((k & 1) == 0) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const uint8_t* hs = hi1 + soff<G::PVA::IB, G::PVA::SW, TT>(tk[u], g * HB + 2 * k);
+              // (2k stays inside the lane's 16-byte chunk: HB = 8 puts its 8 bytes in one)
+              const uint8_t* hs = hi1 + tq_sgn[u] + 16 * sb * G::PVA::IB + 2 * k;
               if constexpr (HB >= 4) H[u] = *reinterpret_cast<const uint32_t*>(hs);
               else if constexpr (HB == 2) H[u] = *reinterpret_cast<const uint16_t*>(hs);
               else H[u] = *hs;
@@ -692,16 +721,30 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
         }
       }
     }
+  };
+
+  // ---- the warp's tiles: a private pipeline, no cross-warp traffic ---------------------
+#pragma unroll 1
+  for (int s = 0; s < G::STAGES - 1; ++s) issue(s);
+#pragma unroll 1
+  for (int k = 0; warp + k * kWarps < ntiles; ++k) {
+    issue(k + G::STAGES - 1);  // stage (k - 1) % STAGES is free
+    await(k);
+    if (timed_out) break;  // the error word tells the host; the outputs are not valid
+    const uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
+    float sacc[SUB][NTW][4];
+    k_part(st, sacc);
+    attend_tile(st, tile0 + (int64_t)(warp + k * kWarps) * TT, sacc);
     __syncwarp();
   }
   cp_async_wait<0>();
   __syncthreads();
 
   // ---- merge the warps' states, then the chunk's partial ------------------------------
-  float* mw = reinterpret_cast<float*>(smem);            // [kWarps][ROWS]
-  float* lw = mw + kWarps * ROWS;                         // [kWarps][ROWS]
-  float* ow = lw + kWarps * ROWS;                         // [kWarps][ROWS][D]
-  float* fin = ow + kWarps * ROWS * D;                    // [ROWS][D]
+  float* mw = reinterpret_cast<float*>(smem);  // [kWarps][ROWS]
+  float* lw = mw + kWarps * ROWS;              // [kWarps][ROWS]
+  float* ow = lw + kWarps * ROWS;              // [kWarps][ROWS][D]
+  float* fin = ow + kWarps * ROWS * D;         // [ROWS][D]
 #pragma unroll
   for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
@@ -736,7 +779,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < ROWS * D; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < ROWS * D; idx += G::NW * 32) {
     const int r = idx / D, dd = idx % D;
     float mx = -INFINITY;
 #pragma unroll
@@ -753,10 +796,13 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   }
   __syncthreads();
   if constexpr (VF == QPS_FMT_TQ3) {  // inverse rotation x = s .* (H y) / D, in place
-    for (int h = 1; h < D; h <<= 1) {
-      for (int pid = threadIdx.x; pid < ROWS * (D / 2); pid += blockDim.x) {
+#pragma unroll
+    for (int lh = 0; (1 << lh) < D; ++lh) {  // butterflies of span h = 2^lh
+      const int h = 1 << lh;
+#pragma unroll 4
+      for (int pid = threadIdx.x; pid < ROWS * (D / 2); pid += G::NW * 32) {
         const int r = pid / (D / 2), j = pid % (D / 2);
-        const int i = (j / h) * 2 * h + (j % h);
+        const int i = ((j >> lh) << (lh + 1)) | (j & (h - 1));
         const float a = fin[r * D + i], b = fin[r * D + i + h];
         fin[r * D + i] = a + b;
         fin[r * D + i + h] = a - b;
@@ -764,7 +810,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       __syncthreads();
     }
   }
-  for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < nrows * D; idx += G::NW * 32) {
     const int r = idx / D, dd = idx % D;
     float mx = -INFINITY;
 #pragma unroll
@@ -804,6 +850,10 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
   using G = Geo<D, KF, VF>;
   constexpr size_t smem = smem_bytes<D, KF, VF, NTW>();
   static_assert(smem <= 227 * 1024, "tile staging exceeds the 227 KB shared memory of one CTA");
+  // two CTAs per SM (the launch bound the registers are sized for: 228 KB less 1 KB
+  // reserved per CTA), unless the stages are already at their minimum of two (fp16
+  // planes at head_dim >= 256, which then run one CTA per SM)
+  static_assert(2 * (smem + 1024) <= 228 * 1024 || G::STAGES == 2, "two CTAs per SM no longer fit");
   // tensor maps over each plane as [row bytes][tokens < kv_end][KV heads][batch]
   TmaSet maps;
   std::memset(&maps, 0, sizeof(maps));

@@ -79,19 +79,23 @@ def test_window_attention_formats(qps, layout, d, kf, vf, softcap):
 
 @pytest.mark.parametrize("layout", ["head", "token"])
 @pytest.mark.parametrize("begin,end", [(17, 211), (0, 16), (5, 6), (31, 300), (299, 300)])
-def test_ragged_ranges(qps, layout, begin, end):
-    """Sub-ranges whose ends cut 16-token tiles, single tokens and tiny chunks."""
-    d, hq, hkv, n = 128, 5, 1, 300
+@pytest.mark.parametrize("d,vf", [(128, "f16"), (512, "tq3")])
+def test_ragged_ranges(qps, layout, begin, end, d, vf):
+    """Sub-ranges whose ends cut 16-token tiles, single tokens and tiny chunks (at
+    head_dim 512 several warps share each tile)."""
+    hq, hkv, n = 5, 1, 300
     q, k, v = _inputs(n, hq, hkv, d, seed=begin * 7 + end)
+    words = synth.sign_bits(d, 5) if vf == "tq3" else None
     K = _encode(qps, layout, "q8_0", k, None)
-    V = _encode(qps, layout, "f16", v, None)
+    V = _encode(qps, layout, vf, v, words)
     kh = pipeline.dequant("q8_0", k.numpy())
+    vh = pipeline.dequant(vf, v.numpy(), None if words is None else words.numpy())
     for n_split in (1, 3):
-        a = qps.attn_args(q.cuda(), K, V, scale=0.1, kv_begin=begin, kv_end=end, n_split=n_split)
+        a = qps.attn_args(q.cuda(), K, V, scale=0.1, kv_begin=begin, kv_end=end, n_split=n_split, v_signs=words)
         o, lse = qps.attn_decode_window(a)
-        ro, rl = oatt.gqa_decode(q.double().numpy(), kh, v.double().numpy(), 0.1, 0.0, begin, end)
+        ro, rl = oatt.gqa_decode(q.double().numpy(), kh, vh, 0.1, 0.0, begin, end)
         assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq),
-                      (layout, begin, end, n_split))
+                      (layout, begin, end, n_split, d))
 
 
 def test_sub_range_and_empty_range(qps):

@@ -354,12 +354,14 @@ def run_ours(args):
     qps.launch_count(reset=True)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     bounds = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.nvtx.range_push("qps_timed")  # lets a profiler select the timed launches
     t0.record(stream)
     for i in range(K):
         set_events(ev[i])
         dec.step(stream)
         bounds[i].record(stream)
     t1.record(stream)
+    torch.cuda.nvtx.range_pop()
     launches = qps.launch_count()
     torch.cuda.synchronize()
     if world > 1:

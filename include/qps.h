@@ -247,8 +247,10 @@ QPS_API qps_status qps_ring_destroy(qps_ring* ring);
  * row = token * tok_stride + head * head_stride (the same for every plane of K and
  * V): token-major tiles use (hkv, 1), head-major tiles (1, padded tile length).  K
  * planes first (1 for F16, 2 for Q8_0, 3 for TQ3, in data/aux/aux2 order), then V
- * planes.  The ring places plane p at a 256-byte-aligned offset of the slot; their
- * total must fit in slot_bytes. */
+ * planes.  The ring places each plane at the next 256-byte-aligned offset of the slot
+ * (in that order); their total must fit in slot_bytes.  When the host planes already
+ * sit at those offsets from the first K plane (a tail packed tile by tile), the whole
+ * tile moves in one copy; otherwise each plane is its own copy. */
 typedef struct qps_tile_desc {
   int32_t n_k_planes, n_v_planes;
   const void* host_k[3];

@@ -24,6 +24,7 @@ qps_status fail(qps_status st, const std::string& msg) {
 
 qps_status cuda_fail(cudaError_t err, const char* what) {
   g_last_error = std::string(what) + ": " + cudaGetErrorName(err) + " (" + cudaGetErrorString(err) + ")";
+  cudaGetLastError();  // the status carries the error: leave no non-sticky error behind
   return QPS_ERR_CUDA;
 }
 
@@ -191,7 +192,7 @@ qps_status check_view(const qps_kv_view& v, const char* name, bool allow_tq3) {
 int auto_split(int64_t ntok, int ctas_per_split) {
   const int sms = sm_count_current();
   if (sms <= 0) return -1;
-  const int64_t min_chunk = 512;
+  const int64_t min_chunk = 256;  // positions per split at least (16 tiles of 16)
   const int64_t target = 2LL * sms;
   int64_t by_occupancy = (target + ctas_per_split - 1) / ctas_per_split;
   int64_t by_size = (ntok + min_chunk - 1) / min_chunk;

@@ -6,10 +6,10 @@
 // dedicated copy stream; each op waits for its tile's copy_done and records
 // compute_done; a slot is refilled only after its compute_done (the write-after-read
 // discipline replaces a per-op barrier); events are created once, never per op.  Each
-// tile is one bulk host-to-device transfer per plane (the tail is stored token-major,
-// so a tile is one contiguous range), after the lesson of "F5 M7 — Rolling KV:
-// position-windowed KV residency", section "2026-07-06 — bs2 tail-spill curve" (one
-// transfer per tile instead of per-head strided copies).
+// tile is one bulk host-to-device transfer per plane, or a single transfer when its
+// planes are packed in host memory as they are in the slot, after the lesson of "F5
+// M7 — Rolling KV: position-windowed KV residency", section "2026-07-06 — bs2
+// tail-spill curve" (one transfer per tile instead of per-head strided copies).
 //
 // Every wait is either a device-side stream/event dependency or a host poll with a
 // deadline; nothing here can block forever.
@@ -19,21 +19,35 @@
 #include <cstring>
 #include <mutex>
 #include <thread>
-#include <unordered_map>
+#include <map>
 #include <vector>
 
 #include "internal.h"
 
 namespace {
-// Mappings made by qps_host_alloc(flags = 2): base -> length, so that qps_host_free
-// unregisters and unmaps them instead of calling cudaFreeHost.
+// Every allocation made by qps_host_alloc: base -> (length, made by mmap).  qps_host_free
+// unregisters and unmaps the mappings (flags = 2) instead of calling cudaFreeHost, and
+// the ring copies a packed tile in one transfer only when it lies in one of them.
+struct HostAlloc {
+  size_t bytes;
+  bool mapped;
+};
 std::mutex& host_map_mutex() {
   static std::mutex m;
   return m;
 }
-std::unordered_map<void*, size_t>& host_map() {
-  static std::unordered_map<void*, size_t> m;
+std::map<uintptr_t, HostAlloc>& host_map() {
+  static std::map<uintptr_t, HostAlloc> m;
   return m;
+}
+// True when [p, p + n) lies inside one qps_host_alloc allocation.
+bool in_one_host_alloc(const void* p, size_t n) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  std::lock_guard<std::mutex> lk(host_map_mutex());
+  auto it = host_map().upper_bound(a);
+  if (it == host_map().begin()) return false;
+  --it;
+  return a - it->first <= it->second.bytes && n <= it->second.bytes - (a - it->first);
 }
 }  // namespace
 
@@ -50,6 +64,7 @@ struct qps_ring {
   bool compute_recorded[4] = {false, false, false, false};
   std::vector<qps_tile_desc> tiles;
   std::vector<size_t> offsets;  // per tile: 6 plane offsets within the slot
+  std::vector<size_t> span;     // per tile: bytes of one copy covering every plane, or 0
   int next_consume = 0;
   bool open = false;
 };
@@ -81,12 +96,16 @@ qps_status issue_copy(qps_ring* r, int i) {
   if (r->compute_recorded[slot]) QPS_CUDA_TRY(cudaStreamWaitEvent(r->copy, r->compute_done[slot], 0));
   char* base = reinterpret_cast<char*>(r->slots[slot]);
   const size_t* off = &r->offsets[(size_t)i * 6];
-  for (int p = 0; p < t.n_k_planes; ++p)
-    if (t.bytes_k[p])
-      QPS_CUDA_TRY(cudaMemcpyAsync(base + off[p], t.host_k[p], t.bytes_k[p], cudaMemcpyHostToDevice, r->copy));
-  for (int p = 0; p < t.n_v_planes; ++p)
-    if (t.bytes_v[p])
-      QPS_CUDA_TRY(cudaMemcpyAsync(base + off[3 + p], t.host_v[p], t.bytes_v[p], cudaMemcpyHostToDevice, r->copy));
+  if (r->span[i]) {  // the planes sit in host memory exactly as in the slot: one copy
+    QPS_CUDA_TRY(cudaMemcpyAsync(base, t.host_k[0], r->span[i], cudaMemcpyHostToDevice, r->copy));
+  } else {
+    for (int p = 0; p < t.n_k_planes; ++p)
+      if (t.bytes_k[p])
+        QPS_CUDA_TRY(cudaMemcpyAsync(base + off[p], t.host_k[p], t.bytes_k[p], cudaMemcpyHostToDevice, r->copy));
+    for (int p = 0; p < t.n_v_planes; ++p)
+      if (t.bytes_v[p])
+        QPS_CUDA_TRY(cudaMemcpyAsync(base + off[3 + p], t.host_v[p], t.bytes_v[p], cudaMemcpyHostToDevice, r->copy));
+  }
   QPS_CUDA_TRY(cudaEventRecord(r->copy_done[slot], r->copy));
   return QPS_OK;
 }
@@ -201,12 +220,14 @@ qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out) {
       return cuda_fail(e, "host_alloc: cudaHostRegister");
     }
     std::lock_guard<std::mutex> lk(host_map_mutex());
-    host_map()[p] = n;
+    host_map()[reinterpret_cast<uintptr_t>(p)] = HostAlloc{n, true};
     *out = p;
     return QPS_OK;
   }
   unsigned int f = cudaHostAllocPortable | (flags == 1 ? cudaHostAllocWriteCombined : 0u);
   QPS_CUDA_TRY(cudaHostAlloc(out, bytes, f));
+  std::lock_guard<std::mutex> lk(host_map_mutex());
+  host_map()[reinterpret_cast<uintptr_t>(*out)] = HostAlloc{bytes, false};
   return QPS_OK;
 }
 
@@ -215,9 +236,9 @@ qps_status qps_host_free(void* p) {
   size_t mapped = 0;
   {
     std::lock_guard<std::mutex> lk(host_map_mutex());
-    auto it = host_map().find(p);
+    auto it = host_map().find(reinterpret_cast<uintptr_t>(p));
     if (it != host_map().end()) {
-      mapped = it->second;
+      if (it->second.mapped) mapped = it->second.bytes;
       host_map().erase(it);
     }
   }
@@ -293,7 +314,7 @@ qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t 
   if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_begin_step: invalid or destroyed ring");
   if (r->open) return fail(QPS_ERR_STATE, "ring_begin_step: the previous step is still open");
   if (n_tiles < 0 || (n_tiles > 0 && !tiles)) return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: bad tile list");
-  std::vector<size_t> offsets((size_t)n_tiles * 6, 0);
+  std::vector<size_t> offsets((size_t)n_tiles * 6, 0), span((size_t)n_tiles, 0);
   for (int i = 0; i < n_tiles; ++i) {
     const qps_tile_desc& t = tiles[i];
     if (t.n_k_planes < 1 || t.n_k_planes > 3 || t.n_v_planes < 1 || t.n_v_planes > 3 || t.tokens < 0)
@@ -317,12 +338,31 @@ qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t 
     }
     if (cur > r->slot_bytes)
       return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: tile " + std::to_string(i) + " does not fit in a slot");
+    // one copy suffices when every plane starts at its slot offset from the first
+    // plane's host address (the tail packed tile by tile, planes 256-byte aligned) and
+    // the whole span lies in one allocation of this library (a copy may not cross
+    // separately pinned ranges)
+    bool contiguous = t.bytes_k[0] > 0;
+    size_t end = 0;
+    const char* h0 = reinterpret_cast<const char*>(t.host_k[0]);
+    for (int p = 0; p < 6 && contiguous; ++p) {
+      const bool is_k = p < 3;
+      const int pi = is_k ? p : p - 3;
+      if (pi >= (is_k ? t.n_k_planes : t.n_v_planes)) continue;
+      const char* h = reinterpret_cast<const char*>(is_k ? t.host_k[pi] : t.host_v[pi]);
+      const size_t b = is_k ? t.bytes_k[pi] : t.bytes_v[pi];
+      if (b == 0) continue;
+      contiguous = h >= h0 && (size_t)(h - h0) == offsets[(size_t)i * 6 + p];
+      end = offsets[(size_t)i * 6 + p] + b;
+    }
+    span[i] = contiguous && in_one_host_alloc(h0, end) ? end : 0;
   }
   int prev = 0;
   cudaGetDevice(&prev);
   if (prev != r->device) return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: the ring's device is not current");
   r->tiles.assign(tiles, tiles + n_tiles);
   r->offsets.swap(offsets);
+  r->span.swap(span);
   r->next_consume = 0;
   r->open = true;
   const int first = n_tiles < r->n_slots ? n_tiles : r->n_slots;

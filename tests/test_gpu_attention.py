@@ -31,11 +31,14 @@ def _inputs(n, hq, hkv, d, seed, outliers=True):
     return q, k.half(), v
 
 
-def test_lse_combine(qps):
-    g = torch.Generator().manual_seed(0)
-    o = torch.randn((7, 33, 128), generator=g)
-    l = torch.randn((7, 33), generator=g) * 5
-    l[2, :] = -float("inf")
+@pytest.mark.parametrize("n_parts,d", [(7, 128), (1, 32), (201, 512), (64, 1024)])
+def test_lse_combine(qps, n_parts, d):
+    """Several part counts around the 64 parts a CTA has in flight, every head_dim slice
+    count, an empty part and a row whose parts are all empty."""
+    g = torch.Generator().manual_seed(n_parts * 7 + d)
+    o = torch.randn((n_parts, 33, d), generator=g)
+    l = torch.randn((n_parts, 33), generator=g) * 5
+    l[min(2, n_parts - 1), :7] = -float("inf")
     l[:, 5] = -float("inf")  # a row with every part empty
     oo, ll = qps.lse_combine(o.cuda(), l.cuda())
     ro, rl = oatt.lse_combine(o.numpy(), l.numpy())

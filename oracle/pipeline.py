@@ -56,6 +56,22 @@ def layer_reference(q16, k16, v16, k_fmt: str, v_fmt: str, scale: float, softcap
     return attention.gqa_decode(np.asarray(q16, dtype=np.float64), kh, vh, scale, softcap)
 
 
+def mixed_layer_reference(q16, k16, v16, wc: int, k_fmt: str, v_fmt: str, tail_k_fmt: str,
+                          tail_v_fmt: str, scale: float, softcap: float, sign_words=None):
+    """Expected outputs of one layer whose tail carries other storage formats.
+
+    "F5 M7 — Rolling KV: position-windowed KV residency", section "2026-07-12 — #582-P2
+    SHIPPED: position-axis mixed KV (compressed tail, -ctkt/-ctvt)": the positions
+    [0, wc) keep the window's K / V formats, the positions [wc, n) are stored in the
+    tail's (more compressed) formats, and each part is read at its own format.  The
+    expected output is plain attention over the concatenation of the two dequantised
+    ranges; with the tail formats equal to the window's it is ``layer_reference``.
+    """
+    kh = np.concatenate([dequant(k_fmt, k16[:wc], sign_words), dequant(tail_k_fmt, k16[wc:], sign_words)], axis=0)
+    vh = np.concatenate([dequant(v_fmt, v16[:wc], sign_words), dequant(tail_v_fmt, v16[wc:], sign_words)], axis=0)
+    return attention.gqa_decode(np.asarray(q16, dtype=np.float64), kh, vh, scale, softcap)
+
+
 def fanout_reference(q16, prefix_k16, prefix_v16, suffix_k16, suffix_v16,
                      k_fmt: str, v_fmt: str, scale: float, softcap: float = 0.0,
                      sign_words=None):

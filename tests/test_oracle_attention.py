@@ -159,3 +159,63 @@ def test_fanout_reference_equals_prefix_suffix_split():
                              sv[a].astype(np.float64), 0.2)
         oc, lc = att.lse_combine(np.stack([pre[0][a:a + 1], suf[0]]), np.stack([pre[1][a:a + 1], suf[1]]))
         assert np.allclose(oc[0], o[a], atol=1e-13) and np.allclose(lc[0], l[a], atol=1e-13)
+
+
+def _mixed_inputs(seed, n=37, hq=4, hkv=2, d=32):
+    rng = np.random.default_rng(seed)
+    q16 = (rng.standard_normal((1, hq, d)) * 2).astype(np.float16)
+    k16 = rng.standard_normal((n, hkv, d)).astype(np.float16)
+    v16 = rng.standard_normal((n, hkv, d)).astype(np.float16)
+    return q16, k16, v16, np.array([0x9E3779B9], dtype=np.int64)
+
+
+def test_mixed_reference_reduces_to_uniform():
+    """Tail formats equal to the window's, and the two extreme window lengths, give
+    exactly the uniform-format reference."""
+    q16, k16, v16, w = _mixed_inputs(11)
+    n = k16.shape[0]
+    ref = pipeline.layer_reference(q16, k16, v16, "q8_0", "tq3", 0.25, 0.0, w)
+    for wc in (0, 13, n):
+        o, l = pipeline.mixed_layer_reference(q16, k16, v16, wc, "q8_0", "tq3", "q8_0", "tq3", 0.25, 0.0, w)
+        assert np.array_equal(o, ref[0]) and np.array_equal(l, ref[1]), wc
+    tail_only = pipeline.layer_reference(q16, k16, v16, "f16", "q8_0", 0.25, 0.0, w)
+    o, l = pipeline.mixed_layer_reference(q16, k16, v16, 0, "q8_0", "tq3", "f16", "q8_0", 0.25, 0.0, w)
+    assert np.array_equal(o, tail_only[0]) and np.array_equal(l, tail_only[1])
+    window_only = pipeline.layer_reference(q16, k16, v16, "q8_0", "tq3", 0.25, 0.0, w)
+    o, l = pipeline.mixed_layer_reference(q16, k16, v16, n, "q8_0", "tq3", "f16", "q8_0", 0.25, 0.0, w)
+    assert np.array_equal(o, window_only[0]) and np.array_equal(l, window_only[1])
+
+
+@pytest.mark.parametrize("wc", [1, 16, 36])
+def test_mixed_reference_brute_force_per_position(wc):
+    """Each position read at the format of its own range, checked by explicit loops
+    (a swapped range or an off-by-one at wc changes the result)."""
+    q16, k16, v16, w = _mixed_inputs(12 + wc)
+    n, hkv = k16.shape[0], k16.shape[1]
+    hq = q16.shape[1]
+    o, l = pipeline.mixed_layer_reference(q16, k16, v16, wc, "f16", "f16", "q8_0", "tq3", 0.3, 2.0, w)
+    for h in range(hq):
+        g = h // (hq // hkv)
+        ks, vs = [], []
+        for t in range(n):
+            kf, vf = ("f16", "f16") if t < wc else ("q8_0", "tq3")
+            ks.append(pipeline.dequant(kf, k16[t:t + 1, g], w)[0])
+            vs.append(pipeline.dequant(vf, v16[t:t + 1, g], w)[0])
+        ob, lb = att.attend_loops(q16[0, h:h + 1].astype(np.float64), np.array(ks), np.array(vs), 0.3, 2.0)
+        assert np.allclose(o[0, h], ob[0], atol=1e-12) and abs(l[0, h] - lb[0]) < 1e-12
+    # and the tail really is read at its own format: with the tail at fp16 the output moves
+    o2, _ = pipeline.mixed_layer_reference(q16, k16, v16, wc, "f16", "f16", "f16", "f16", 0.3, 2.0, w)
+    assert not np.allclose(o, o2, atol=1e-6)
+
+
+def test_mixed_reference_is_the_combine_of_its_two_parts():
+    """The position-split method: window part at the window formats, tail part at the
+    tail formats, merged by the LSE combine, equals the mixed reference."""
+    q16, k16, v16, w = _mixed_inputs(21)
+    wc = 19
+    o, l = pipeline.mixed_layer_reference(q16, k16, v16, wc, "q8_0", "q8_0", "q8_0", "tq3", 0.2, 0.0, w)
+    q = q16.astype(np.float64)
+    pw = att.gqa_decode(q, pipeline.dequant("q8_0", k16[:wc]), pipeline.dequant("q8_0", v16[:wc]), 0.2)
+    pt = att.gqa_decode(q, pipeline.dequant("q8_0", k16[wc:]), pipeline.dequant("tq3", v16[wc:], w), 0.2)
+    oc, lc = att.lse_combine(np.stack([pw[0], pt[0]]), np.stack([pw[1], pt[1]]))
+    assert np.allclose(oc, o, atol=1e-13) and np.allclose(lc, l, atol=1e-13)

@@ -94,10 +94,13 @@ def time_oracle(cfg, n_layers: int):
         k = synth.kv_f16(cfg, layer, "k", cfg.n_kv).numpy()
         v = synth.kv_f16(cfg, layer, "v", cfg.n_kv).numpy()
         t0 = time.perf_counter()
-        pipeline.layer_reference(q, k, v, cfg.k_fmt, cfg.v_fmt, cfg.scale, cfg.softcap, signs)
+        pipeline.mixed_layer_reference(q, k, v, cfg.wc, cfg.k_fmt, cfg.v_fmt, cfg.tk_fmt, cfg.tv_fmt,
+                                       cfg.scale, cfg.softcap, signs)
         elapsed += time.perf_counter() - t0
-        for fmt, x in ((cfg.k_fmt, k), (cfg.v_fmt, v)):
-            nbytes += sum(p.nbytes for p in pipeline.encode(fmt, x[:1], signs)) * x.shape[0]
+        for fmt, x in ((cfg.k_fmt, k[:cfg.wc]), (cfg.v_fmt, v[:cfg.wc]), (cfg.tk_fmt, k[cfg.wc:]),
+                       (cfg.tv_fmt, v[cfg.wc:])):
+            if x.shape[0]:
+                nbytes += sum(p.nbytes for p in pipeline.encode(fmt, x[:1], signs)) * x.shape[0]
         del q, k, v
     sample = (f"{n_layers} of {cfg.layers} layers of {cfg.name}, all {cfg.hq} query heads over all "
               f"{cfg.n_kv} positions (window + tail), float64")
@@ -292,7 +295,8 @@ def run_ours(args):
     dec = PositionSplitDecoder(layers=cfg.layers, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
                                n_kv=cfg.n_kv, wc=cfg.wc, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
                                scale=cfg.scale, softcap=cfg.softcap, signs=signs,
-                               ring_slots=cfg.ring_slots, tile_tokens=cfg.tile_tokens, device=device)
+                               ring_slots=cfg.ring_slots, tile_tokens=cfg.tile_tokens, device=device,
+                               tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt)
     for layer in range(cfg.layers):
         q = synth.query_f16(cfg, layer, device=device)
         k = synth.kv_f16(cfg, layer, "k", cfg.n_kv, device=device)
@@ -436,11 +440,13 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16" if cfg.k_fmt == "f16" and cfg.v_fmt == "f16" else f"{cfg.k_fmt}/{cfg.v_fmt}",
+        "dtype": ("f16" if cfg.k_fmt == "f16" and cfg.v_fmt == "f16" else f"{cfg.k_fmt}/{cfg.v_fmt}") +
+                 (f" window, {cfg.tk_fmt}/{cfg.tv_fmt} tail" if cfg.mixed else ""),
         "data": "synthetic (seeded N(0,1) fp16, 4 outlier K channels per head x20)",
         "config": {"workload": cfg.name, "layers": cfg.layers, "batch": cfg.batch, "hq": cfg.hq,
                    "hkv": cfg.hkv, "d": cfg.d, "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt,
-                   "v_fmt": cfg.v_fmt, "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
+                   "v_fmt": cfg.v_fmt, "tail_k_fmt": cfg.tk_fmt, "tail_v_fmt": cfg.tv_fmt,
+                   "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
                    "tile_tokens": cfg.tile_tokens, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" %
                          (window_bytes / 1e9, tail_bytes / 1e9)},
@@ -480,7 +486,9 @@ def run_kernel_only(args):
     qbuild.build()
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    names = [args.config] if args.config != "qwen14b_f16" or args.layers else [c.name for c in synth.CONFIGS]
+    # (the mixed-tail workloads share their window kernel with the uniform ones)
+    names = [args.config] if args.config != "qwen14b_f16" or args.layers else [
+        c.name for c in synth.CONFIGS if not c.mixed]
     peak, peak_kind = measured_hbm_peak()
     s = torch.cuda.current_stream()
     for name in names:

@@ -31,18 +31,28 @@ def _parts_buffers(capacity: int, rows: int, d: int, device):
 
 
 class PositionSplitDecoder:
-    """Decode attention of ``layers`` layers over a KV cache split at ``wc``."""
+    """Decode attention of ``layers`` layers over a KV cache split at ``wc``.
+
+    ``tail_k_fmt`` / ``tail_v_fmt`` store the tail in other (normally more compressed)
+    formats than the window ("F5 M7 — Rolling KV: position-windowed KV residency",
+    section "2026-07-12 — #582-P2 SHIPPED: position-axis mixed KV (compressed tail,
+    -ctkt/-ctvt)"): the recent positions keep the window's formats on the device, the
+    tail ships fewer bytes per step, and each part is read at its own format.  Unset,
+    the tail uses the window's formats."""
 
     def __init__(self, *, layers: int, batch: int, hq: int, hkv: int, d: int, n_kv: int, wc: int,
                  k_fmt: str, v_fmt: str, scale: float, softcap: float = 0.0, signs=None,
                  ring_slots: int = 3, tile_tokens: int = 8192, n_split_window: int = 0,
-                 n_split_tail: int = 0, device=None, host_alloc_flags: int = 2):
+                 n_split_tail: int = 0, device=None, host_alloc_flags: int = 2,
+                 tail_k_fmt: Optional[str] = None, tail_v_fmt: Optional[str] = None):
         if not 0 <= wc <= n_kv:
             raise ValueError("need 0 <= wc <= n_kv")
         self.host_alloc_flags = host_alloc_flags
         self.layers, self.batch, self.hq, self.hkv, self.d = layers, batch, hq, hkv, d
         self.n_kv, self.wc = n_kv, wc
         self.k_fmt, self.v_fmt = k_fmt, v_fmt
+        self.tail_k_fmt = k_fmt if tail_k_fmt is None else tail_k_fmt
+        self.tail_v_fmt = v_fmt if tail_v_fmt is None else tail_v_fmt
         self.scale, self.softcap, self.signs = scale, softcap, signs
         self.ring_slots, self.tile_tokens = ring_slots, tile_tokens
         self.n_split_window, self.n_split_tail = n_split_window, n_split_tail
@@ -77,7 +87,7 @@ class PositionSplitDecoder:
         total = 0
         for a, b in self.tile_ranges():
             tp = (b - a + 15) // 16 * 16
-            for rb in plane_bytes(self.k_fmt) + plane_bytes(self.v_fmt):
+            for rb in plane_bytes(self.tail_k_fmt) + plane_bytes(self.tail_v_fmt):
                 total += (self.hkv * tp * rb + 255) // 256 * 256
         return total * self.layers
 
@@ -96,8 +106,8 @@ class PositionSplitDecoder:
         if ranges and self.arena is None:
             self.arena = HostArena(self._arena_bytes(), self.host_alloc_flags)
         for a, b in ranges:
-            kt = encode_kv_head_major(self.k_fmt, k16[self.wc + a:self.wc + b], self.signs)
-            vt = encode_kv_head_major(self.v_fmt, v16[self.wc + a:self.wc + b], self.signs)
+            kt = encode_kv_head_major(self.tail_k_fmt, k16[self.wc + a:self.wc + b], self.signs)
+            vt = encode_kv_head_major(self.tail_v_fmt, v16[self.wc + a:self.wc + b], self.signs)
             tiles.append((self.arena.copy_in(kt), self.arena.copy_in(vt)))
         self.tail[layer] = tiles
         if q16 is not None:

@@ -1,4 +1,4 @@
-"""Workload shapes: the five decode configurations and their parity-sized copies.
+"""Workload shapes: the decode configurations and their parity-sized copies.
 
 Every field is a plain shape or format name; nothing here computes anything.
 """
@@ -24,6 +24,8 @@ class Workload:
     k_fmt: str  # "f16" | "q8_0"
     v_fmt: str  # "f16" | "q8_0" | "tq3"
     softcap: float = 0.0  # <= 0: off
+    tail_k_fmt: Optional[str] = None  # split: the tail's K format (None: k_fmt)
+    tail_v_fmt: Optional[str] = None  # split: the tail's V format (None: v_fmt)
     k_outliers: int = 0  # channels per (layer, KV head) scaled by outlier_scale
     outlier_scale: float = 20.0
     ring_slots: int = 3
@@ -40,6 +42,18 @@ class Workload:
     @property
     def group(self) -> int:
         return self.hq // self.hkv
+
+    @property
+    def tk_fmt(self) -> str:
+        return self.k_fmt if self.tail_k_fmt is None else self.tail_k_fmt
+
+    @property
+    def tv_fmt(self) -> str:
+        return self.v_fmt if self.tail_v_fmt is None else self.tail_v_fmt
+
+    @property
+    def mixed(self) -> bool:
+        return (self.tk_fmt, self.tv_fmt) != (self.k_fmt, self.v_fmt)
 
     @property
     def tail_len(self) -> int:
@@ -113,6 +127,44 @@ CONFIGS = [
         k_outliers=4,
         ring_slots=3,
         tile_tokens=16384,
+    ),
+    # the same Qwen-like stacks with a more compressed tail than window (the tail's own
+    # K / V storage formats)
+    Workload(
+        name="qwen14b_f16_q8tail",
+        kind="split",
+        layers=48,
+        batch=1,
+        hq=40,
+        hkv=8,
+        d=128,
+        n_kv=65536,
+        wc=32768,
+        k_fmt="f16",
+        v_fmt="f16",
+        tail_k_fmt="q8_0",
+        tail_v_fmt="q8_0",
+        k_outliers=4,
+        ring_slots=3,
+        tile_tokens=8192,
+    ),
+    Workload(
+        name="qwen14b_q8_tq3vtail",
+        kind="split",
+        layers=48,
+        batch=1,
+        hq=40,
+        hkv=8,
+        d=128,
+        n_kv=131072,
+        wc=98304,
+        k_fmt="q8_0",
+        v_fmt="q8_0",
+        tail_k_fmt="q8_0",
+        tail_v_fmt="tq3",
+        k_outliers=4,
+        ring_slots=3,
+        tile_tokens=8192,
     ),
     Workload(
         name="fanout_prefix",

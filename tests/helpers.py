@@ -46,6 +46,10 @@ def layer_inputs(cfg, layer, device):
 
 
 def oracle_layer(cfg, q, k, v):
+    if cfg.mixed:
+        return pipeline.mixed_layer_reference(q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy(), cfg.wc,
+                                              cfg.k_fmt, cfg.v_fmt, cfg.tk_fmt, cfg.tv_fmt, cfg.scale,
+                                              cfg.softcap, signs_for(cfg).numpy())
     return pipeline.layer_reference(q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy(),
                                     cfg.k_fmt, cfg.v_fmt, cfg.scale, cfg.softcap,
                                     signs_for(cfg).numpy())
@@ -62,7 +66,8 @@ def build_split_decoder(cfg, device="cuda", keep_inputs=(), **kw):
                                n_kv=cfg.n_kv, wc=cfg.wc, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
                                scale=cfg.scale, softcap=cfg.softcap, signs=signs_for(cfg),
                                ring_slots=kw.pop("ring_slots", cfg.ring_slots),
-                               tile_tokens=kw.pop("tile_tokens", cfg.tile_tokens), device=device, **kw)
+                               tile_tokens=kw.pop("tile_tokens", cfg.tile_tokens), device=device,
+                               tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt, **kw)
     kept = {}
     for layer in range(cfg.layers):
         q, k, v = layer_inputs(cfg, layer, device)

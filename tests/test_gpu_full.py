@@ -26,6 +26,8 @@ def qps():
     ("qwen14b_f16", (0, 47)),
     ("qwen14b_q8", (13,)),
     ("gemma_global_q8k_tq3v", (4,)),
+    ("qwen14b_f16_q8tail", (5,)),
+    ("qwen14b_q8_tq3vtail", (40,)),
 ])
 def test_full_size_split_workload(qps, name, sample):
     cfg = synth.by_name(name)

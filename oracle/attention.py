@@ -80,6 +80,31 @@ def gqa_decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     return o, lse
 
 
+def multi_query_decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                       softcap: float = 0.0, begin: int = 0, end=None, q_pos=None):
+    """Attention of ``n_q`` query tokens of one sequence, ``q[n_q, Hq, D]``, over
+    token-major ``k, v[n, Hkv, D]`` (positions [begin, end)).
+
+    The verify batch of "F5 M6 — PolyKV (shared compressed KV pool)", section "S2
+    perf-path — turbo-MMA verify kernel + scalar-K/turbo-V fused decode" (n_q > 1 query
+    tokens checked in one pass over the cache).  With ``q_pos`` given, query token i
+    sits at position ``q_pos + i`` of the same index space and sees only the positions
+    p <= q_pos + i (the cache up to and including itself); without it every query sees
+    all of [begin, end).  Returns ``(O [n_q, Hq, D], lse [n_q, Hq])``; a query that sees
+    no position gets O = 0, lse = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n_q = q.shape[0]
+    end = k.shape[0] if end is None else end
+    o = np.zeros((n_q,) + q.shape[1:2] + (v.shape[-1],))
+    lse = np.zeros(q.shape[:2])
+    for i in range(n_q):
+        e = end if q_pos is None else min(end, max(begin, q_pos + i + 1))
+        oi, li = gqa_decode(q[i:i + 1], k, v, scale, softcap, begin, e)
+        o[i], lse[i] = oi[0], li[0]
+    return o, lse
+
+
 def lse_combine(o_parts: np.ndarray, lse_parts: np.ndarray):
     """Merge normalised partial outputs by their log-sum-exp.
 

@@ -219,3 +219,61 @@ def test_mixed_reference_is_the_combine_of_its_two_parts():
     pt = att.gqa_decode(q, pipeline.dequant("q8_0", k16[wc:]), pipeline.dequant("tq3", v16[wc:], w), 0.2)
     oc, lc = att.lse_combine(np.stack([pw[0], pt[0]]), np.stack([pw[1], pt[1]]))
     assert np.allclose(oc, o, atol=1e-13) and np.allclose(lc, l, atol=1e-13)
+
+
+def _mq_inputs(seed, n_q=4, n=29, hq=6, hkv=2, d=16):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((n_q, hq, d)) * 1.5, rng.standard_normal((n, hkv, d)),
+            rng.standard_normal((n, hkv, d)))
+
+
+def test_multi_query_single_token_and_no_limit_reduce_to_decode():
+    q, k, v = _mq_inputs(31)
+    o, l = att.multi_query_decode(q[:1], k, v, 0.4)
+    r = att.gqa_decode(q[:1], k, v, 0.4)
+    assert np.array_equal(o, r[0]) and np.array_equal(l, r[1])
+    # a causal limit at or past the end changes nothing
+    o1, l1 = att.multi_query_decode(q, k, v, 0.4, 1.0)
+    o2, l2 = att.multi_query_decode(q, k, v, 0.4, 1.0, q_pos=k.shape[0] - 1)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("q_pos,begin,end", [(20, 0, 29), (3, 0, 29), (10, 5, 25), (-2, 0, 29)])
+def test_multi_query_causal_matches_sdpa_mask_and_loops(q_pos, begin, end):
+    """Query token i sees positions p in [begin, end) with p <= q_pos + i: checked
+    against torch SDPA with an explicit boolean mask (float64) and against loops."""
+    q, k, v = _mq_inputs(32 + q_pos)
+    n_q, hq = q.shape[0], q.shape[1]
+    g = hq // k.shape[1]
+    o, l = att.multi_query_decode(q, k, v, 0.35, 0.0, begin, end, q_pos)
+    pos = torch.arange(k.shape[0])
+    for h in range(hq):
+        kk = torch.from_numpy(k[:, h // g]).double()
+        vv = torch.from_numpy(v[:, h // g]).double()
+        qq = torch.from_numpy(q[:, h]).double()
+        mask = (pos[None, :] >= begin) & (pos[None, :] < end) & (pos[None, :] <= q_pos + torch.arange(n_q)[:, None])
+        for i in range(n_q):
+            vis = mask[i]
+            if not bool(vis.any()):
+                assert np.all(o[i, h] == 0) and np.isneginf(l[i, h])
+                continue
+            ref = torch.nn.functional.scaled_dot_product_attention(qq[i:i + 1][None], kk[None], vv[None],
+                                                                   attn_mask=vis[None, None], scale=0.35)[0, 0]
+            assert np.allclose(o[i, h], ref.numpy(), atol=1e-12)
+            s = (qq[i] @ kk[vis].T).numpy() * 0.35
+            assert abs(l[i, h] - logsumexp(s)) < 1e-12
+            ob, lb = att.attend_loops(q[i:i + 1, h], k[vis.numpy(), h // g], v[vis.numpy(), h // g], 0.35)
+            assert np.allclose(o[i, h], ob[0], atol=1e-12) and abs(l[i, h] - lb[0]) < 1e-12
+
+
+def test_multi_query_causal_split_identity():
+    """Position-split with a causal limit: the parts [0, m) and [m, n) each masked by
+    the same absolute q_pos, merged, equal the unsplit result for every m."""
+    q, k, v = _mq_inputs(40, n_q=5, n=23)
+    n = k.shape[0]
+    ref = att.multi_query_decode(q, k, v, 0.3, 0.0, q_pos=n - 5)
+    for m in range(0, n + 1):
+        a = att.multi_query_decode(q, k, v, 0.3, 0.0, 0, m, q_pos=n - 5)
+        b = att.multi_query_decode(q, k, v, 0.3, 0.0, m, n, q_pos=n - 5)
+        oc, lc = att.lse_combine(np.stack([a[0], b[0]]), np.stack([a[1], b[1]]))
+        assert np.allclose(oc, ref[0], atol=1e-13) and np.allclose(lc, ref[1], atol=1e-13), m

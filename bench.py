@@ -510,28 +510,40 @@ def run_kernel_only(args):
             V = qps.encode_kv_head_major(cfg.v_fmt, pv, signs)
             a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs, shared=True)
             rows = cfg.agents * cfg.hq
-        n_split, _ = qps.attn_plan(a)
-        parts = (torch.empty((n_split, rows, cfg.d), device=dev), torch.empty((n_split, rows), device=dev))
-        for _ in range(3):
-            qps.attn_decode_window(a, parts=parts)
-        n = 50
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(s)
-        for _ in range(n):
-            qps.attn_decode_window(a, parts=parts)
-        e1.record(s)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) / n * 1e3
-        kv = K.nbytes() + V.nbytes()
-        algo = kv + q.numel() * 2 + n_split * rows * (cfg.d + 1) * 4
-        print(json.dumps({"kernel": "attn_decode_window", "workload": name, "path": qps.attn_path(a),
-                          "n_split": n_split, "launch_us": us, "kv_bytes": kv, "algorithmic_bytes": algo,
-                          "achieved_gbs": algo / us / 1e3, "frac_of_hbm": algo / us / 1e3 / peak,
-                          "peak_gbs": peak, "peak_source": peak_kind,
-                          "l2_resident": kv < 129e6}), flush=True)
+        for n_q in ([1, 4] if name == "qwen14b_q8" and cfg.kind == "split" else [1]):
+            if n_q > 1:  # a verify batch: 4 query tokens at the end of the window, causal
+                q4 = synth.randn_f16((cfg.batch, n_q, cfg.hq, cfg.d), cfg.seed, cfg.name, "verify", device=dev)
+                a = qps.attn_args(q4, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs,
+                                  q_pos=cfg.wc - n_q)
+                rows = cfg.batch * n_q * cfg.hq
+            _time_window_launch(qps, torch, a, name if n_q == 1 else f"{name} verify n_q={n_q} causal",
+                                rows, cfg, K, V, dev, s, peak, peak_kind)
         qps.device_status(reset=True)
     return 0
+
+
+def _time_window_launch(qps, torch, a, label, rows, cfg, K, V, dev, s, peak, peak_kind):
+    """Per-launch time of one window attention (50 launches back to back, CUDA events)."""
+    n_split, _ = qps.attn_plan(a)
+    parts = (torch.empty((n_split, rows, cfg.d), device=dev), torch.empty((n_split, rows), device=dev))
+    for _ in range(3):
+        qps.attn_decode_window(a, parts=parts)
+    n = 50
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(n):
+        qps.attn_decode_window(a, parts=parts)
+    e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / n * 1e3
+    kv = K.nbytes() + V.nbytes()
+    algo = kv + rows * cfg.d * 2 + n_split * rows * (cfg.d + 1) * 4
+    print(json.dumps({"kernel": "attn_decode_window", "workload": label, "path": qps.attn_path(a),
+                      "n_split": n_split, "launch_us": us, "kv_bytes": kv, "algorithmic_bytes": algo,
+                      "achieved_gbs": algo / us / 1e3, "frac_of_hbm": algo / us / 1e3 / peak,
+                      "peak_gbs": peak, "peak_source": peak_kind,
+                      "l2_resident": kv < 129e6}), flush=True)
 
 
 def main(argv=None):

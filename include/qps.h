@@ -1,7 +1,8 @@
 /*
  * qps.h: C ABI of the position-split, quantised-KV decode-attention library.
  *
- * The library computes single-token decode attention over a KV cache that is split
+ * The library computes decode attention (one, or a few verify, query tokens per
+ * sequence) over a KV cache that is split
  * by key position into a device-resident window [0, wc) and a host-resident tail
  * [wc, n_kv).  Each part runs a split-KV flash-decode that emits a normalised output
  * and its log-sum-exp (LSE); the parts are merged by an LSE combine.  K and V may be
@@ -21,7 +22,10 @@
  *   [POLY] "F5 M6 — PolyKV (shared compressed KV pool)": section "What PolyKV is
  *          (reference)" (K int8 / V 3-bit TurboQuant-MSE), section "S1 — SharedKVPool"
  *          (one prefix read by many agents), section "S2 perf-path Level B" (V read as
- *          centroid x norm in the rotated domain, output inverse-rotated once).
+ *          centroid x norm in the rotated domain, output inverse-rotated once), and
+ *          section "S2 perf-path — turbo-MMA verify kernel + scalar-K/turbo-V fused
+ *          decode" (n_q > 1 query tokens per sequence on tensor cores, K / V
+ *          dequantised in the tile).
  *
  * Conventions shared by every call:
  *   - Every call returns a qps_status; qps_last_error() gives a thread-local message
@@ -62,7 +66,7 @@
 extern "C" {
 #endif
 
-#define QPS_ABI_VERSION 1
+#define QPS_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define QPS_API __attribute__((visibility("default")))
@@ -182,6 +186,20 @@ typedef struct qps_attn_args {
   float* lse;
   void* workspace;
   size_t workspace_bytes;
+  /* Multi-query decode (verify batches) [POLY, "S2 perf-path — turbo-MMA verify
+   * kernel"]: n_q query tokens per batch entry; 0 or 1 is single-token decode.  With
+   * n_q > 1, q is fp16 [batch][n_q][hq][D] (q_batch_stride >= n_q*hq*D) and the output
+   * row of (batch entry b, query token i, head h) is (b*n_q + i)*hq + h.
+   * causal != 0: query token i sees only the view positions p <= q_pos + i (positions
+   * counted like kv_begin / kv_end); a token that sees none of [kv_begin, kv_end) gets
+   * O = 0 and lse = -inf.  n_q > 1 or causal needs the tensor-core path (see
+   * qps_attn_path) and per-entry KV rows (batch_stride != 0 or batch == 1); the
+   * decode-step ring (qps_attn_decode_tail, qps_decode_step tails) takes n_q > 1 but
+   * not causal, since its tiles carry no position.  Zero-initialised fields keep the
+   * single-token behaviour. */
+  int32_t n_q;
+  int32_t causal;
+  int64_t q_pos;
 } qps_attn_args;
 
 /* Resolve the split count and the workspace the args need (host only, no launch).

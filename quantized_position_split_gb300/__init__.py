@@ -177,19 +177,31 @@ def encode_kv(fmt: str, x: torch.Tensor, signs=None, stream=None) -> KV:
 
 def attn_args(q: torch.Tensor, k: KV, v: KV, *, scale: float, softcap: float = 0.0,
               kv_begin: int = 0, kv_end: Optional[int] = None, v_signs=None, n_split: int = 0,
-              shared: bool = False) -> N.AttnArgs:
+              shared: bool = False, q_pos: Optional[int] = None) -> N.AttnArgs:
     """Build the ABI argument struct for ``q[batch, hq, D]`` against (k, v).
 
+    A 4-D ``q[batch, n_q, hq, D]`` asks for multi-query (verify-batch) decode: n_q
+    query tokens per batch entry, output rows ordered (batch, token, head).  With
+    ``q_pos``, query token i sees only the positions <= q_pos + i (causal).
     ``shared`` makes every batch entry read the same KV rows (batch_stride 0).  The
     returned struct keeps a reference to the sign array it points to.
     """
-    if q.dtype != torch.float16 or q.dim() != 3:
-        raise QpsError(N.QPS_ERR_INVALID_ARG, "q must be float16 [batch, hq, D]")
-    batch, hq, d = q.shape
+    if q.dtype != torch.float16 or q.dim() not in (3, 4):
+        raise QpsError(N.QPS_ERR_INVALID_ARG, "q must be float16 [batch, hq, D] or [batch, n_q, hq, D]")
+    if q.dim() == 3:
+        batch, hq, d = q.shape
+        n_q = 1
+    else:
+        batch, n_q, hq, d = q.shape
+        if q.stride(1) != hq * d or q.stride(2) != d or q.stride(3) != 1:
+            raise QpsError(N.QPS_ERR_INVALID_ARG, "q [batch, n_q, hq, D] must be contiguous per batch entry")
     a = N.AttnArgs()
     a.q = q.data_ptr()
     a.q_batch_stride = q.stride(0)
     a.batch, a.hq, a.hkv, a.d = batch, hq, k.hkv, d
+    a.n_q = n_q
+    if q_pos is not None:
+        a.causal, a.q_pos = 1, q_pos
     a.k = k.view()
     a.v = v.view()
     if shared:
@@ -230,7 +242,7 @@ def attn_decode_window(a: N.AttnArgs, *, o=None, lse=None, parts=None, part_offs
     With ``parts=(o_parts, lse_parts)`` the split partials are written at
     ``part_offset``; otherwise the merged (o, lse) are returned (allocated if None).
     """
-    rows = a.batch * a.hq
+    rows = a.batch * max(1, a.n_q) * a.hq
     if parts is not None:
         a.o_parts, a.lse_parts = parts[0].data_ptr(), parts[1].data_ptr()
         a.part_offset = part_offset

@@ -69,6 +69,9 @@ class AttnArgs(ctypes.Structure):
         ("lse", c_void_p),
         ("workspace", c_void_p),
         ("workspace_bytes", c_size_t),
+        ("n_q", c_int32),
+        ("causal", c_int32),
+        ("q_pos", c_int64),
     ]
 
 

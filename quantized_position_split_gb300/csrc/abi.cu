@@ -2,6 +2,7 @@
 // attention plan / dispatch, the LSE combine and the native decode-step runner.
 #include <cuda.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -189,14 +190,15 @@ qps_status check_view(const qps_kv_view& v, const char* name, bool allow_tq3) {
 // Split count: enough CTAs for one full wave (two resident per SM), but no chunk
 // shorter than 512 positions, so each partial amortises its merge and the combine
 // reads few parts.
+// Enough chunks for two CTAs per SM (one wave), each chunk at least 512 positions, or
+// 256 when 512-position chunks would leave SMs without a CTA (a short tail tile).
 int auto_split(int64_t ntok, int ctas_per_split) {
   const int sms = sm_count_current();
   if (sms <= 0) return -1;
-  const int64_t min_chunk = 256;  // positions per split at least (16 tiles of 16)
   const int64_t target = 2LL * sms;
-  int64_t by_occupancy = (target + ctas_per_split - 1) / ctas_per_split;
-  int64_t by_size = (ntok + min_chunk - 1) / min_chunk;
-  int64_t n = by_occupancy < by_size ? by_occupancy : by_size;
+  const int64_t by_occupancy = (target + ctas_per_split - 1) / ctas_per_split;
+  int64_t n = std::min(by_occupancy, (ntok + 511) / 512);
+  if (n * ctas_per_split < sms) n = std::min(by_occupancy, (ntok + 255) / 256);
   if (n < 1) n = 1;
   if (n > 65535) n = 65535;
   return (int)n;
@@ -213,8 +215,10 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   if (a->hq % a->hkv) return fail(QPS_ERR_INVALID_ARG, "attention: hq must be a multiple of hkv");
   if (a->d != 64 && a->d != 128 && a->d != 256 && a->d != 512)
     return fail(QPS_ERR_UNSUPPORTED, "attention: head_dim must be 64, 128, 256 or 512");
-  if (a->batch > 1 && (a->q_batch_stride < (int64_t)a->hq * a->d || a->q_batch_stride % 8))
-    return fail(QPS_ERR_INVALID_ARG, "attention: q_batch_stride must be >= hq*d and a multiple of 8");
+  if (a->n_q < 0 || a->n_q > 64) return fail(QPS_ERR_INVALID_ARG, "attention: n_q must be in [0, 64]");
+  const int n_q = a->n_q < 1 ? 1 : a->n_q;
+  if (a->batch > 1 && (a->q_batch_stride < (int64_t)n_q * a->hq * a->d || a->q_batch_stride % 8))
+    return fail(QPS_ERR_INVALID_ARG, "attention: q_batch_stride must be >= n_q*hq*d and a multiple of 8");
   qps_status st = check_view(a->k, "attention k", false);
   if (st != QPS_OK) return st;
   st = check_view(a->v, "attention v", true);
@@ -229,18 +233,22 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
     return fail(QPS_ERR_INVALID_ARG, "attention: v_signs is required for a TQ3 V");
   if (a->n_split < 0) return fail(QPS_ERR_INVALID_ARG, "attention: n_split must be >= 0");
   const bool shared = a->k.batch_stride == 0 && a->batch > 1;
+  if (shared && n_q > 1)
+    return fail(QPS_ERR_UNSUPPORTED, "attention: multi-query decode needs per-entry KV rows (batch_stride != 0)");
   const int group = a->hq / a->hkv;
-  const int rows_per_cta = shared ? a->batch * group : group;
+  const int rows_per_cta = shared ? a->batch * group : n_q * group;
   if (rows_per_cta > 1024) return fail(QPS_ERR_UNSUPPORTED, "attention: more than 1024 query rows per KV head");
   const int64_t ntok = a->kv_end - a->kv_begin;
-  const int ctas_per_split = a->hkv * (shared ? 1 : a->batch);
+  // CTAs per chunk: one per (KV head, batch entry) and row group of the tensor-core tile
+  const int tile_rows = mma_tile_rows(a->d, rows_per_cta, shared);
+  const int ctas_per_split = a->hkv * (shared ? 1 : a->batch) * ((rows_per_cta + tile_rows - 1) / tile_rows);
   int n_split = a->n_split;
   if (n_split == 0) {
     n_split = auto_split(ntok, ctas_per_split);
     if (n_split < 0) return fail(QPS_ERR_CUDA, "attention: cannot query the current device's SM count");
   }
   if (n_split > 65535) return fail(QPS_ERR_INVALID_ARG, "attention: n_split must be <= 65535");
-  const int64_t rows_total = (int64_t)a->batch * a->hq;
+  const int64_t rows_total = (int64_t)a->batch * n_q * a->hq;
   const size_t ws = ((size_t)n_split * rows_total * (a->d + 1) * sizeof(float) + 1024 + 255) & ~(size_t)255;
   if (n_split_out) *n_split_out = n_split;
   if (ws_bytes) *ws_bytes = ws;
@@ -248,7 +256,7 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
 
   std::memset(p, 0, sizeof(*p));
   p->q = reinterpret_cast<const __half*>(a->q);
-  p->q_bstride = a->batch > 1 ? a->q_batch_stride : (int64_t)a->hq * a->d;
+  p->q_bstride = a->batch > 1 ? a->q_batch_stride : (int64_t)n_q * a->hq * a->d;
   p->batch = a->batch;
   p->hq = a->hq;
   p->hkv = a->hkv;
@@ -265,6 +273,9 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   p->scale = a->scale;
   p->softcap = a->softcap > 0.f ? a->softcap : 0.f;
   p->shared = shared ? 1 : 0;
+  p->n_q = n_q;
+  p->causal = a->causal ? 1 : 0;
+  p->q_pos = a->q_pos;
   p->rows_per_cta = rows_per_cta;
   p->rows_total = rows_total;
   if (a->v.fmt == QPS_FMT_TQ3)
@@ -302,7 +313,12 @@ bool attn_uses_mma(const AttnParams& p) {
 }
 
 qps_status launch_attn(const AttnParams& p_in, cudaStream_t s) {
-  if (!attn_uses_mma(p_in)) return launch_attn_simple(p_in, s);
+  if (!attn_uses_mma(p_in)) {
+    if (p_in.n_q > 1 || p_in.causal)
+      return fail(QPS_ERR_UNSUPPORTED, "attention: multi-query / causal decode needs the tensor-core path "
+                                       "(token-contiguous planes, see qps_attn_path)");
+    return launch_attn_simple(p_in, s);
+  }
   AttnParams p = p_in;
   p.err = device_error_word();
   if (!p.err) return fail(QPS_ERR_CUDA, "attention: cannot allocate the device error word");

@@ -257,7 +257,9 @@ __host__ __device__ constexpr int tq_col(int i, int hh) {
 }
 
 // ---- the kernel -------------------------------------------------------------------
-template <int D, int KF, int VF, int NTW>
+// CAUSAL: the verify batch's causal limit (a separate instance, so that single-token
+// decode compiles without it).
+template <int D, int KF, int VF, int NTW, bool CAUSAL>
 __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     attn_mma_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TmaSet maps) {
   using G = Geo<D, KF, VF>;
@@ -277,19 +279,23 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int split = blockIdx.x, head = blockIdx.y;
+  // the row groups of one (chunk, KV head) are adjacent CTAs, so they stream the same
+  // KV rows at about the same time and all but the first read come from L2
   const int rgroups = (p.rows_per_cta + ROWS - 1) / ROWS;
-  const int rg = blockIdx.z % rgroups, bz = blockIdx.z / rgroups;
+  const int split = blockIdx.x / rgroups, rg = blockIdx.x % rgroups;
+  const int head = blockIdx.y, bz = blockIdx.z;
   const int row0 = rg * ROWS;
   const int nrows = min(ROWS, p.rows_per_cta - row0);
   const int64_t t0 = p.begin + (int64_t)split * p.chunk;
   const int64_t t1 = min(p.end, t0 + p.chunk);
   const int part = p.part_offset + split;
 
+  // CTA row rr: (batch entry, head) in a shared tile; (query token rr / group, head)
+  // of batch entry bz otherwise
   auto out_row = [&](int rr) -> int64_t {
-    const int b = p.shared ? rr / p.group : bz;
-    const int h = head * p.group + (p.shared ? rr % p.group : rr);
-    return (int64_t)b * p.hq + h;
+    const int h = head * p.group + rr % p.group;
+    if (p.shared) return (int64_t)(rr / p.group) * p.hq + h;
+    return ((int64_t)bz * p.n_q + rr / p.group) * p.hq + h;
   };
 
   if (t0 >= t1) {  // an empty chunk: O = 0, lse = -inf
@@ -317,9 +323,9 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     const bool valid = rr < p.rows_per_cta;
     const __half* qrow = nullptr;
     if (valid) {
-      const int b = p.shared ? rr / p.group : bz;
-      const int h = head * p.group + (p.shared ? rr % p.group : rr);
-      qrow = p.q + (int64_t)b * p.q_bstride + (int64_t)h * D;
+      const int h = head * p.group + rr % p.group;
+      qrow = p.shared ? p.q + (int64_t)(rr / p.group) * p.q_bstride + (int64_t)h * D
+                      : p.q + (int64_t)bz * p.q_bstride + ((int64_t)(rr / p.group) * p.hq + h) * D;
     }
 #pragma unroll
     for (int kk = 0; kk < MT; ++kk) {
@@ -433,6 +439,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   __syncthreads();  // the barriers are ready
 
   // ---- per-tile work ------------------------------------------------------------------
+
   // per-lane stage offsets that do not change from tile to tile
   const int ks_lane = g * (D / 32);                        // K scale of (row g, block 0)
   int tq_lo2[4] = {0, 0, 0, 0}, tq_sgn[4] = {0, 0, 0, 0};   // TQ3 plane offsets, tokens 2c..
@@ -547,6 +554,18 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
         }
         if (!in_g[sb]) x[sb][0] = x[sb][1] = -INFINITY;
         if (!in_g8[sb]) x[sb][2] = x[sb][3] = -INFINITY;
+        if constexpr (CAUSAL) {
+          // position t is visible to CTA row r (query token r / group) iff
+          // t - q_pos <= r / group, i.e. (t - q_pos) * group <= r; t - q_pos is clamped
+          // so the product stays in 32 bits (rows are < 1024)
+          const int64_t rel64 = tb + 16 * sb + g - p.q_pos;
+          const int rel = (int)max((int64_t)-2048, min((int64_t)2048, rel64)) * p.group;
+          const int r0 = row0 + nt * 8 + 2 * c, r8 = rel + 8 * p.group;
+          if (rel > r0) x[sb][0] = -INFINITY;
+          if (rel > r0 + 1) x[sb][1] = -INFINITY;
+          if (r8 > r0) x[sb][2] = -INFINITY;
+          if (r8 > r0 + 1) x[sb][3] = -INFINITY;
+        }
         mx0 = fmaxf(mx0, fmaxf(x[sb][0], x[sb][2]));
         mx1 = fmaxf(mx1, fmaxf(x[sb][1], x[sb][3]));
       }
@@ -745,6 +764,11 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   float* lw = mw + kWarps * ROWS;              // [kWarps][ROWS]
   float* ow = lw + kWarps * ROWS;              // [kWarps][ROWS][D]
   float* fin = ow + kWarps * ROWS * D;         // [ROWS][D]
+  int64_t* orow = reinterpret_cast<int64_t*>(fin + ROWS * D);  // [ROWS] output row index
+  float* wgt = reinterpret_cast<float*>(orow + ROWS);             // [kWarps][ROWS] warp weights
+  float* rmx = wgt + kWarps * ROWS;                                // [ROWS] row maximum (log2)
+  float* rden = rmx + ROWS;                                        // [ROWS] row denominator
+  if (threadIdx.x < nrows) orow[threadIdx.x] = out_row(row0 + threadIdx.x);
 #pragma unroll
   for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
@@ -779,19 +803,30 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < ROWS * D; idx += G::NW * 32) {
-    const int r = idx / D, dd = idx % D;
+  // per row: the maximum over the warps, each warp's weight 2^(m_w - max) (0 for a warp
+  // that saw nothing of the row) and the merged denominator
+  if (threadIdx.x < ROWS) {
+    const int r = threadIdx.x;
     float mx = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, mw[w * ROWS + r]);
-    float acc = 0.f;
-    if (mx != -INFINITY) {
+    float den = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mv = mw[w * ROWS + r];
-        if (mv != -INFINITY) acc += ow[(w * ROWS + r) * D + dd] * exp2f(mv - mx);
-      }
+    for (int w = 0; w < kWarps; ++w) {
+      const float mv = mw[w * ROWS + r];
+      const float f = (mx != -INFINITY && mv != -INFINITY) ? exp2f(mv - mx) : 0.f;
+      wgt[w * ROWS + r] = f;
+      den += lw[w * ROWS + r] * f;
     }
+    rmx[r] = mx;
+    rden[r] = den;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < ROWS * D; idx += G::NW * 32) {
+    const int r = idx / D, dd = idx % D;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) acc += ow[(w * ROWS + r) * D + dd] * wgt[w * ROWS + r];
     fin[idx] = acc;
   }
   __syncthreads();
@@ -812,23 +847,13 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
   }
   for (int idx = threadIdx.x; idx < nrows * D; idx += G::NW * 32) {
     const int r = idx / D, dd = idx % D;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, mw[w * ROWS + r]);
-    float den = 0.f;
-    if (mx != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mv = mw[w * ROWS + r];
-        if (mv != -INFINITY) den += lw[w * ROWS + r] * exp2f(mv - mx);
-      }
-    }
+    const float mx = rmx[r], den = rden[r];
     float val = fin[r * D + dd];
     if constexpr (VF == QPS_FMT_TQ3) {
       val *= 1.0f / (float)D;
       if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) val = -val;
     }
-    const int64_t row = out_row(row0 + r);
+    const int64_t row = orow[r];
     const bool empty = !(den > 0.f);
     p.o_parts[((int64_t)part * p.rows_total + row) * D + dd] = empty ? 0.f : val / den;
     if (dd == 0)
@@ -841,11 +866,12 @@ constexpr size_t smem_bytes() {
   using G = Geo<D, KF, VF>;
   constexpr size_t pipe = (size_t)G::END;
   constexpr int ROWS = 8 * NTW;
-  constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D);
+  constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D) +
+                           sizeof(int64_t) * ROWS + sizeof(float) * ((size_t)G::NW * ROWS + 2 * ROWS);
   return (pipe > merge ? pipe : merge) + 1024;  // + slack for the 1024-byte base alignment
 }
 
-template <int D, int KF, int VF, int NTW>
+template <int D, int KF, int VF, int NTW, bool CAUSAL>
 qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
   using G = Geo<D, KF, VF>;
   constexpr size_t smem = smem_bytes<D, KF, VF, NTW>();
@@ -867,24 +893,29 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
   if constexpr (G::PVA::TMA)
     if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, G::PVA::SW, G::TT))
       return QPS_ERR_CUDA;
-  auto kern = attn_mma_kernel<D, KF, VF, NTW>;
+  auto kern = attn_mma_kernel<D, KF, VF, NTW, CAUSAL>;
   QPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   constexpr int ROWS = 8 * NTW;
   const int rgroups = (p.rows_per_cta + ROWS - 1) / ROWS;
-  const dim3 grid(p.n_split, p.hkv, (p.shared ? 1 : p.batch) * rgroups);
+  const dim3 grid(p.n_split * rgroups, p.hkv, p.shared ? 1 : p.batch);
   kern<<<grid, G::NW * 32, smem, s>>>(p, maps);
   count_launch();
   QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;
 }
 
-template <int D>
+// Every format pairing and n-tile count of one head_dim, with or without the causal
+// limit (the two halves live in separate translation units).
+template <int D, bool CAUSAL>
 qps_status launch_mma_d(const AttnParams& p, cudaStream_t s) {
-  // two 8-row n-tiles per warp only where the accumulators still fit in registers
-  const bool wide = p.rows_per_cta > 8 && D <= 128;
+  // 8-row n-tiles per warp: more only where the accumulators still fit in registers
+  const int ntw = mma_tile_rows(D, p.rows_per_cta, p.shared != 0) / 8;
 #define QPS_MMA_CASE(KF, VF)                                                       \
-  if (p.kfmt == KF && p.vfmt == VF)                                                \
-    return wide ? launch_mma_t<D, KF, VF, (D <= 128 ? 2 : 1)>(p, s) : launch_mma_t<D, KF, VF, 1>(p, s);
+  if (p.kfmt == KF && p.vfmt == VF) {                                              \
+    if (ntw == 3) return launch_mma_t<D, KF, VF, (D <= 128 ? 3 : 1), CAUSAL>(p, s); \
+    if (ntw == 2) return launch_mma_t<D, KF, VF, (D <= 128 ? 2 : 1), CAUSAL>(p, s); \
+    return launch_mma_t<D, KF, VF, 1, CAUSAL>(p, s);                                \
+  }
   QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_F16)
   QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_Q8_0)
   QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_TQ3)

@@ -1,6 +1,10 @@
-// Tensor-core decode attention instances for head_dim 128 (see attn_mma.cuh).
+// Tensor-core decode attention instances for head_dim 128 (see attn_mma.cuh); the
+// causal (verify-batch) instances are in attn_mma_d128_causal.cu.
 #include "attn_mma.cuh"
 
 namespace qps {
-qps_status launch_attn_mma_d128(const AttnParams& p, cudaStream_t s) { return mma::launch_mma_d<128>(p, s); }
+qps_status launch_attn_mma_d128_causal(const AttnParams& p, cudaStream_t s);
+qps_status launch_attn_mma_d128(const AttnParams& p, cudaStream_t s) {
+  return p.causal ? launch_attn_mma_d128_causal(p, s) : mma::launch_mma_d<128, false>(p, s);
+}
 }  // namespace qps

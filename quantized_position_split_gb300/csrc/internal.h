@@ -79,8 +79,11 @@ struct AttnParams {
   int64_t chunk;       // positions per split
   float scale, softcap;
   int shared;          // 1: every batch entry reads the same KV rows
-  int rows_per_cta;    // shared ? batch * group : group
-  int64_t rows_total;  // batch * hq
+  int n_q;             // query tokens per batch entry (>= 1)
+  int causal;          // 1: query token i sees only positions <= q_pos + i
+  int64_t q_pos;
+  int rows_per_cta;    // shared ? batch * group : n_q * group
+  int64_t rows_total;  // batch * n_q * hq
   float* o_parts;
   float* lse_parts;
   int part_offset;
@@ -88,6 +91,15 @@ struct AttnParams {
   uint32_t vsigns[kMaxSignWords];
   float tq_levels[8];
 };
+
+// Query rows one tensor-core CTA holds (8 per n-tile): at head_dim <= 128, where the
+// accumulators still fit in registers, up to 2 n-tiles, or 3 for per-entry rows (a
+// verify batch: each row group would dequantise the same tiles again); a shared prefix
+// is cheap to re-read from L2, so its rows keep the smaller tiles and more CTAs.
+inline int mma_tile_rows(int d, int rows_per_cta, bool shared) {
+  if (d > 128 || rows_per_cta <= 8) return 8;
+  return (rows_per_cta <= 16 || shared) ? 16 : 24;
+}
 
 // Validated, resolved form of qps_attn_args.
 qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split, size_t* ws_bytes);

@@ -122,6 +122,7 @@ qps_status tail_attend(qps_ring* r, int idx, const qps_attn_args* a_in, cudaStre
   if (!valid_ring(r)) return fail(QPS_ERR_STATE, "decode_tail: invalid or destroyed ring");
   if (!r->open) return fail(QPS_ERR_STATE, "decode_tail: no open step");
   if (!a_in) return fail(QPS_ERR_INVALID_ARG, "decode_tail: args is NULL");
+  if (a_in->causal) return fail(QPS_ERR_UNSUPPORTED, "decode_tail: ring tiles carry no position; causal is not supported");
   if (idx != r->next_consume)
     return fail(QPS_ERR_STATE, "decode_tail: tiles must be consumed in schedule order (expected " +
                                    std::to_string(r->next_consume) + ", got " + std::to_string(idx) + ")");
@@ -460,7 +461,7 @@ qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n
       int used = 0;
       st = tail_attend(ring, tile, &a, s, L.parts_capacity, &used);
       if (st != QPS_OK) break;
-      rows = (int64_t)a.batch * a.hq;
+      rows = (int64_t)a.batch * (a.n_q > 1 ? a.n_q : 1) * a.hq;
       d = a.d;
       off += used;
     }

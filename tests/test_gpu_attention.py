@@ -168,6 +168,81 @@ def test_gqa_and_shared_batch(qps, layout, b):
     assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(b * hq, d), rl.reshape(b * hq))
 
 
+MQ_FORMATS = [(128, "q8_0", "q8_0", 0.0), (128, "f16", "f16", 0.0), (512, "q8_0", "tq3", 50.0),
+              (64, "f16", "tq3", 0.0), (256, "q8_0", "f16", 30.0)]
+
+
+@pytest.mark.parametrize("d,kf,vf,softcap", MQ_FORMATS)
+@pytest.mark.parametrize("n_q", [2, 4, 5])
+@pytest.mark.parametrize("batch", [1, 2])
+def test_multi_query_verify_batch(qps, d, kf, vf, softcap, n_q, batch):
+    """n_q query tokens per sequence (verify batch) on the tensor cores, with and
+    without the causal limit, several split counts; some causal rows see no position
+    of some chunks, and with q_pos below kv_begin the first tokens see none at all."""
+    hq, hkv, n = 10 if d <= 128 else 8, 2, 611
+    g = torch.Generator().manual_seed(d + 7 * n_q + 31 * batch)
+    q = torch.randn((batch, n_q, hq, d), generator=g).half()
+    k = torch.randn((batch, n, hkv, d), generator=g).half()
+    v = torch.randn((batch, n, hkv, d), generator=g).half()
+    words = synth.sign_bits(d, 42)
+    K = qps.encode_kv_head_major(kf, k.cuda(), words)
+    V = qps.encode_kv_head_major(vf, v.cuda(), words)
+    scale = 1.0 / np.sqrt(d)
+    for begin, end, q_pos in [(0, n, None), (0, n, n - n_q), (37, 400, 120), (100, 300, 98)]:
+        for n_split in (0, 1, 7):
+            a = qps.attn_args(q.cuda(), K, V, scale=scale, softcap=softcap, v_signs=words, kv_begin=begin,
+                              kv_end=end, n_split=n_split, q_pos=q_pos)
+            assert qps.attn_path(a) == "tensor-core"
+            o, lse = qps.attn_decode_window(a)
+            o, lse = o.cpu().numpy(), lse.cpu().numpy()
+            for b in range(batch):
+                kh = pipeline.dequant(kf, k[b].numpy(), words.numpy())
+                vh = pipeline.dequant(vf, v[b].numpy(), words.numpy())
+                ro, rl = oatt.multi_query_decode(q[b].double().numpy(), kh, vh, scale, softcap, begin, end, q_pos)
+                rows = slice(b * n_q * hq, (b + 1) * n_q * hq)
+                assert_parity(o[rows], lse[rows], ro.reshape(n_q * hq, d), rl.reshape(n_q * hq),
+                              (d, kf, vf, n_q, batch, begin, end, q_pos, n_split))
+
+
+def test_multi_query_paths_that_refuse(qps):
+    """Multi-query needs the tensor-core path and per-entry KV; the ring refuses a
+    causal limit (its tiles carry no position)."""
+    from quantized_position_split_gb300 import _native as N
+    d, hq, hkv, n = 128, 4, 1, 64
+    q = torch.randn((1, 3, hq, d)).half().cuda()
+    k = torch.randn((n, hkv, d)).half().cuda()
+    k2 = torch.randn((n, 2, d)).half().cuda()  # token-major, 2 heads: not token-contiguous
+    Kt2 = qps.encode_kv("f16", k2)
+    a = qps.attn_args(torch.randn((1, 3, 2, d)).half().cuda(), Kt2, Kt2, scale=0.1)
+    assert qps.attn_path(a) == "cuda-core"
+    with pytest.raises(N.QpsError) as e:
+        qps.attn_decode_window(a)
+    assert e.value.status == N.QPS_ERR_UNSUPPORTED
+    Kh = qps.encode_kv_head_major("f16", k)
+    a = qps.attn_args(torch.randn((2, 3, hq, d)).half().cuda(), Kh, Kh, scale=0.1, shared=True)
+    with pytest.raises(N.QpsError) as e:
+        qps.attn_plan(a)
+    assert e.value.status == N.QPS_ERR_UNSUPPORTED
+    kh = Kh.pinned_copy()
+    ring = qps.Ring(2, 1 << 20)
+    ring.begin_step([qps.tile_desc(kh, kh)])
+    ta = qps.attn_args(q, kh, kh, scale=0.1, q_pos=10)
+    parts = (torch.zeros((8, 3 * hq, d), device="cuda"), torch.zeros((8, 3 * hq), device="cuda"))
+    with pytest.raises(N.QpsError) as e:
+        ring.decode_tail(0, ta, parts=parts, part_offset=0)
+    assert e.value.status == N.QPS_ERR_UNSUPPORTED
+    ta = qps.attn_args(q, kh, kh, scale=0.1)  # n_q > 1 without the causal limit is fine
+    ring.decode_tail(0, ta, parts=parts, part_offset=0)
+    ring.end_step()
+    ring.sync()
+    ring.close()
+    n_split = qps.attn_plan(ta)[0]
+    o, lse = qps.lse_combine(parts[0][:n_split], parts[1][:n_split])
+    ro, rl = oatt.multi_query_decode(q[0].double().cpu().numpy(), k.double().cpu().numpy(),
+                                     k.double().cpu().numpy(), 0.1)
+    assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(3 * hq, d), rl.reshape(3 * hq))
+
+
 def test_zz_no_bounded_wait_gave_up(qps):
     """Every tensor-core launch above finished its tile waits within their bounds."""
     qps.device_status(reset=True)

@@ -42,6 +42,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only this many layers (profiling of a small case; 0 = the workload's)")
+    ap.add_argument("--auto-ring", action="store_true",
+                    help="size the ring (slots, tile tokens) from the measured link and attention time "
+                         "instead of the workload's fixed values")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the window decode-attention kernel alone on one layer of every "
                          "workload (one JSON line per workload; not the benchmark line)")
@@ -292,6 +295,22 @@ def run_ours(args):
     if cfg.kind != "split":
         raise SystemExit("bench.py times the position-split workloads")
     signs = synth.sign_bits(cfg.d, cfg.sign_seed)
+    ring_plan = None
+    if args.auto_ring:
+        from quantized_position_split_gb300 import autosize
+        link, host = autosize.measure_link(device)
+        bw_eff = link  # pinned host -> device through the copy engine: the tail's own path
+        att_ms = autosize.attention_ms(cfg.k_fmt, cfg.v_fmt, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
+                                       n_kv=cfg.n_kv, scale=cfg.scale, softcap=cfg.softcap, signs=signs,
+                                       device=device)
+        row = {"f16": 2 * cfg.d, "q8_0": cfg.d + cfg.d // 16, "tq3": cfg.d // 4 + cfg.d // 8 + 2}
+        ptb = cfg.hkv * (row[cfg.tk_fmt] + row[cfg.tv_fmt])
+        slot_budget = 4.0 * (1 << 30)  # device memory set aside for the ring's slots
+        rp = qps.plan_ring(att_ms, bw_eff, slot_budget, float(cfg.tail_len * ptb))
+        tile_tokens = max(16, int(rp["tile_bytes"] // ptb) // 16 * 16)
+        ring_plan = dict(rp, link_gbs=link, host_memcpy_gbs=host, bw_eff_gbs=bw_eff, attention_ms=att_ms,
+                         slot_budget_bytes=slot_budget, tile_tokens=tile_tokens)
+        cfg = cfg.replace(ring_slots=rp["n_slots"], tile_tokens=tile_tokens)
     dec = PositionSplitDecoder(layers=cfg.layers, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
                                n_kv=cfg.n_kv, wc=cfg.wc, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
                                scale=cfg.scale, softcap=cfg.softcap, signs=signs,
@@ -447,7 +466,7 @@ def run_ours(args):
                    "hkv": cfg.hkv, "d": cfg.d, "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt,
                    "v_fmt": cfg.v_fmt, "tail_k_fmt": cfg.tk_fmt, "tail_v_fmt": cfg.tv_fmt,
                    "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
-                   "tile_tokens": cfg.tile_tokens, "parallelism": f"replicas x{world}",
+                   "tile_tokens": cfg.tile_tokens, "ring_plan": ring_plan, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" %
                          (window_bytes / 1e9, tail_bytes / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

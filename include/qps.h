@@ -26,6 +26,10 @@
  *          section "S2 perf-path — turbo-MMA verify kernel + scalar-K/turbo-V fused
  *          decode" (n_q > 1 query tokens per sequence on tensor cores, K / V
  *          dequantised in the tile).
+ *   [TSTAR] "T*-aware auto rolling-KV spill (HAL #582 P1+, #621 follow-on)": sections
+ *          "The decision (fit-condition reformulation)" and "T* — the negligible-drop
+ *          tail band" (per-token drop of a streamed tail, the largest tail T* within a
+ *          target drop, the first storage tier that fits budget + T*).
  *
  * Conventions shared by every call:
  *   - Every call returns a qps_status; qps_last_error() gives a thread-local message
@@ -373,6 +377,34 @@ QPS_API qps_status qps_device_status(int32_t reset);
 /* Number of kernel launches the calling thread has issued through this library
  * since the last reset (reset if `reset` is non-zero).  Host only. */
 QPS_API int64_t qps_launch_count(int32_t reset);
+
+/* ---- Residency and ring sizing policy (host arithmetic only) ------------------- */
+
+/* Ring sizing [RKV, sections "Slot pool" and "Auto-adapt loop"]: the largest tile the
+ * link moves while one layer's attention runs,
+ *   tile_bytes_max = compute_ms_per_layer * 1e-3 * bw_eff_gbs * 1e9 * 0.8,
+ * n_slots = clamp(floor(slot_budget_bytes / tile_bytes_max), 2, 4); a layer's tail is
+ * cut into the fewest equal tiles of at most tile_bytes_max (tiles_per_layer, tile_bytes
+ * rounded up; both 0 without a tail).  Inputs > 0 (per_layer_tail_bytes >= 0), finite;
+ * any output pointer may be NULL.  Errors: INVALID_ARG. */
+QPS_API qps_status qps_plan_ring(double compute_ms_per_layer, double bw_eff_gbs, double slot_budget_bytes,
+                                 double per_layer_tail_bytes, int32_t* n_slots, int32_t* tiles_per_layer,
+                                 double* tile_bytes, double* tile_bytes_max);
+
+/* The negligible-drop tail band [TSTAR]: streaming a tail of B bytes slows a token by
+ * (c_engage_ms + B / bw_eff) / t_resident_ms; the largest tail within target_drop is
+ *   T* = (target_drop * t_resident_ms - c_engage_ms) * 1e-3 * bw_eff_gbs * 1e9,
+ * reported as 0 when negative (never spill: compress instead).  t_resident_ms,
+ * bw_eff_gbs > 0; c_engage_ms >= 0; 0 < target_drop < 1.  Errors: INVALID_ARG. */
+QPS_API qps_status qps_tail_band(double t_resident_ms, double c_engage_ms, double bw_eff_gbs,
+                                 double target_drop, double* t_star_bytes);
+
+/* Storage tier choice [TSTAR, "The decision"]: the index of the first tier (ordered from
+ * least to most compressing) whose KV bytes are <= budget_bytes + t_star_bytes, or the
+ * last tier when none is (the rolling window then spills the rest).  n_tiers >= 1.
+ * Errors: INVALID_ARG. */
+QPS_API qps_status qps_choose_tier(const double* kv_bytes_per_tier, int32_t n_tiers, double budget_bytes,
+                                   double t_star_bytes, int32_t* tier);
 
 #ifdef __cplusplus
 }

@@ -478,3 +478,30 @@ class StepPlan:
         ring = self.ring.handle if self.ring is not None else None
         N.check(lib().qps_decode_step(ring, self.tiles, self.n_tiles, self.layers, self.n_layers,
                                       _stream(stream)))
+
+
+# ---- residency and ring sizing policy (host arithmetic in the library) -------------
+def plan_ring(compute_ms_per_layer: float, bw_eff_gbs: float, slot_budget_bytes: float,
+              per_layer_tail_bytes: float) -> dict:
+    """Ring slots and tail tiling from one layer's attention time and the link
+    bandwidth (``qps_plan_ring``)."""
+    n, t = ctypes.c_int32(), ctypes.c_int32()
+    tb, tmax = ctypes.c_double(), ctypes.c_double()
+    N.check(lib().qps_plan_ring(compute_ms_per_layer, bw_eff_gbs, slot_budget_bytes, per_layer_tail_bytes,
+                                ctypes.byref(n), ctypes.byref(t), ctypes.byref(tb), ctypes.byref(tmax)))
+    return {"n_slots": n.value, "tiles_per_layer": t.value, "tile_bytes": tb.value, "tile_bytes_max": tmax.value}
+
+
+def tail_band(t_resident_ms: float, c_engage_ms: float, bw_eff_gbs: float, target_drop: float = 0.20) -> float:
+    """T*: the largest streamed tail (bytes) within ``target_drop`` (``qps_tail_band``)."""
+    out = ctypes.c_double()
+    N.check(lib().qps_tail_band(t_resident_ms, c_engage_ms, bw_eff_gbs, target_drop, ctypes.byref(out)))
+    return out.value
+
+
+def choose_tier(kv_bytes_per_tier, budget_bytes: float, t_star_bytes: float) -> int:
+    """The first storage tier whose bytes fit budget + T* (``qps_choose_tier``)."""
+    arr = (ctypes.c_double * len(kv_bytes_per_tier))(*[float(x) for x in kv_bytes_per_tier])
+    out = ctypes.c_int32()
+    N.check(lib().qps_choose_tier(arr, len(kv_bytes_per_tier), budget_bytes, t_star_bytes, ctypes.byref(out)))
+    return out.value

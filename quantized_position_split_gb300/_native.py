@@ -9,7 +9,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
-from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+from ctypes import POINTER, c_char_p, c_double, c_float, c_int32, c_int64, c_size_t, c_uint32, c_void_p
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqps.so")
 
@@ -129,6 +129,10 @@ SIGNATURES = [
     ("qps_attn_decode_window_noalloc", c_int32, [POINTER(AttnArgs), c_void_p]),
     ("qps_device_status", c_int32, [c_int32]),
     ("qps_launch_count", c_int64, [c_int32]),
+    ("qps_plan_ring", c_int32, [c_double, c_double, c_double, c_double, POINTER(c_int32), POINTER(c_int32),
+                                POINTER(c_double), POINTER(c_double)]),
+    ("qps_tail_band", c_int32, [c_double, c_double, c_double, c_double, POINTER(c_double)]),
+    ("qps_choose_tier", c_int32, [POINTER(c_double), c_int32, c_double, c_double, POINTER(c_int32)]),
 ]
 
 _lib = None

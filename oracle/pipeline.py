@@ -27,6 +27,9 @@ def encode(fmt: str, x16: np.ndarray, sign_words=None):
         return q8_0.encode(x16)
     if fmt == "tq3":
         return turboquant.encode(x16, sign_words)
+    if fmt in ("tq2", "tq4"):
+        planes, norms = turboquant.encode_tier(x16, sign_words, int(fmt[2]))
+        return planes + (norms,)
     raise ValueError(fmt)
 
 
@@ -41,6 +44,10 @@ def dequant(fmt: str, x16: np.ndarray, sign_words=None) -> np.ndarray:
     if fmt == "tq3":
         lo2, hi1, n = turboquant.encode(x16, sign_words)
         return turboquant.decode(lo2, hi1, n, sign_words, d)
+    if fmt in ("tq2", "tq4"):
+        bits = int(fmt[2])
+        planes, n = turboquant.encode_tier(x16, sign_words, bits)
+        return turboquant.decode_tier(planes, n, sign_words, d, bits)
     raise ValueError(fmt)
 
 

@@ -38,6 +38,16 @@ Readings taken (each one is a choice the pages leave open):
     norm.
   * Bit order: element i lives in byte i // 4, bits 2 (i % 4) .. 2 (i % 4) + 1 of the
     2-bit plane and in byte i // 8, bit i % 8 of the 1-bit plane.
+
+The tier ladder of section "S2 — TurboQuant tier family" (one rotation + codebook
+scheme at several bit widths) adds a 2-bit and a 4-bit tier with the same transform and
+norm; their codebooks are the 4- and 16-level Lloyd-Max quantisers of N(0,1), rounded
+and made symmetric the same way.  A level index k of a b-bit tier (L = 2^b levels) is
+stored as sign = (k >= L/2) and magnitude m = k - L/2 if sign else L/2 - 1 - k:
+  * TQ2: a 1-bit magnitude plane (element i at bit i % 8 of byte i / 8) and the 1-bit
+    sign plane;
+  * TQ3: the 2-bit magnitude plane and the 1-bit sign plane (above);
+  * TQ4: a 2-bit plane of m & 3, and a 2-bit plane of (m >> 2) | (sign << 1).
 """
 
 from __future__ import annotations
@@ -90,15 +100,15 @@ def gaussian_mse(levels: np.ndarray, thresholds: np.ndarray) -> float:
     return total
 
 
-def codebook():
-    """The build's fixed TQ3 codebook.
+def codebook(levels: int = LEVELS):
+    """The build's fixed codebook of ``levels`` levels (8 for TQ3; 4, 16 for TQ2, TQ4).
 
-    Returns ``(levels float32 [8], thresholds float32 [7])``: Lloyd-Max levels of
+    Returns ``(levels float32 [L], thresholds float32 [L - 1])``: Lloyd-Max levels of
     N(0,1) rounded to fp16 (held as float32), made exactly symmetric, and the exact
     midpoints between adjacent levels.
     """
-    c, _ = lloyd_max_gaussian(LEVELS)
-    pos = np.abs(c[LEVELS // 2:]).astype(np.float16).astype(np.float32)
+    c, _ = lloyd_max_gaussian(levels)
+    pos = np.abs(c[levels // 2:]).astype(np.float16).astype(np.float32)
     levels = np.concatenate([-pos[::-1], pos]).astype(np.float32)
     thresholds = ((levels[:-1] + levels[1:]) / np.float32(2.0)).astype(np.float32)
     return levels, thresholds
@@ -148,18 +158,15 @@ def _fold_sum_sq_f32(x32: np.ndarray) -> np.ndarray:
     return t[..., 0]
 
 
-def encode(x: np.ndarray, sign_words):
-    """Quantise fp16 rows ``x[..., D]``.
-
-    Returns ``(lo2 uint8 [..., D/4], hi1 uint8 [..., D/8], norms float16 [...])``.
-    """
+def level_index(x: np.ndarray, sign_words, levels: int = LEVELS):
+    """Codebook index k [..., D] (0 for a zero row) and fp16 norms of fp16 rows."""
     x = np.asarray(x)
     if x.dtype != np.float16:
-        raise TypeError("TQ3 input must be float16")
+        raise TypeError("TurboQuant input must be float16")
     d = x.shape[-1]
     if d % 32 or d & (d - 1):
         raise ValueError("head_dim must be a power of two and a multiple of 32")
-    levels, thresholds = codebook()
+    _, thresholds = codebook(levels)
     s = signs_from_words(sign_words, d).astype(np.float32)
     x32 = x.astype(np.float32)
     nsq = _fold_sum_sq_f32(x32)
@@ -171,13 +178,69 @@ def encode(x: np.ndarray, sign_words):
     for t in thresholds:
         k += (z >= t).astype(np.int64)
     zero = (n == 0)[..., None]
-    hi = k >= 4
-    lo = np.where(hi, k - 4, 3 - k)
-    hi = np.where(zero, False, hi)
-    lo = np.where(zero, 0, lo)
-    lo2 = pack_bits(lo.astype(np.uint8), 2)
-    hi1 = pack_bits(hi.astype(np.uint8), 1)
-    norms = n.astype(np.float16)
+    k = np.where(zero, levels // 2 - 1, k)  # stores sign 0, magnitude 0
+    return k, n.astype(np.float16)
+
+
+def _sign_magnitude(k, levels):
+    half = levels // 2
+    sign = k >= half
+    mag = np.where(sign, k - half, half - 1 - k)
+    return sign.astype(np.uint8), mag.astype(np.uint8)
+
+
+def encode_tier(x: np.ndarray, sign_words, bits: int):
+    """Quantise fp16 rows ``x[..., D]`` with the ``bits``-bit tier (2, 3 or 4).
+
+    Returns ``(planes tuple of uint8 arrays, norms float16 [...])``; the planes are
+    TQ2: (magnitude 1-bit, sign 1-bit); TQ3: (magnitude 2-bit, sign 1-bit);
+    TQ4: (magnitude low 2 bits, magnitude bit 2 | sign << 1).
+    """
+    levels = 1 << bits
+    k, norms = level_index(x, sign_words, levels)
+    sign, mag = _sign_magnitude(k, levels)
+    if bits == 2:
+        return (pack_bits(mag, 1), pack_bits(sign, 1)), norms
+    if bits == 3:
+        return (pack_bits(mag, 2), pack_bits(sign, 1)), norms
+    if bits == 4:
+        return (pack_bits(mag & 3, 2), pack_bits((mag >> 2) | (sign << 1), 2)), norms
+    raise ValueError("bits must be 2, 3 or 4")
+
+
+def codes_from_tier_planes(planes, d: int, bits: int) -> np.ndarray:
+    """Level index k in 0..2^bits - 1 from a tier's planes."""
+    half = 1 << (bits - 1)
+    if bits == 2:
+        mag = unpack_bits(planes[0], 1, d).astype(np.int64)
+        sign = unpack_bits(planes[1], 1, d).astype(np.int64)
+    elif bits == 3:
+        mag = unpack_bits(planes[0], 2, d).astype(np.int64)
+        sign = unpack_bits(planes[1], 1, d).astype(np.int64)
+    elif bits == 4:
+        hi = unpack_bits(planes[1], 2, d).astype(np.int64)
+        mag = unpack_bits(planes[0], 2, d).astype(np.int64) | ((hi & 1) << 2)
+        sign = hi >> 1
+    else:
+        raise ValueError("bits must be 2, 3 or 4")
+    return np.where(sign == 1, half + mag, half - 1 - mag)
+
+
+def decode_tier(planes, norms, sign_words, d: int, bits: int) -> np.ndarray:
+    """Dequantise a tier to float64: x_hat = (n16 / D) * s * (H c[k])."""
+    levels, _ = codebook(1 << bits)
+    ck = levels.astype(np.float64)[codes_from_tier_planes(planes, d, bits)]
+    s = signs_from_words(sign_words, d)
+    n = np.asarray(norms).astype(np.float64)[..., None]
+    return (n / d) * s * fwht(ck, dtype=np.float64)
+
+
+def encode(x: np.ndarray, sign_words):
+    """Quantise fp16 rows ``x[..., D]`` with TQ3.
+
+    Returns ``(lo2 uint8 [..., D/4], hi1 uint8 [..., D/8], norms float16 [...])``.
+    """
+    (lo2, hi1), norms = encode_tier(x, sign_words, 3)
     return lo2, hi1, norms
 
 
@@ -202,10 +265,8 @@ def unpack_bits(packed: np.ndarray, width: int, d: int) -> np.ndarray:
 
 
 def codes_from_planes(lo2: np.ndarray, hi1: np.ndarray, d: int) -> np.ndarray:
-    """Level index k in 0..7 from the two planes."""
-    lo = unpack_bits(lo2, 2, d).astype(np.int64)
-    hi = unpack_bits(hi1, 1, d).astype(np.int64)
-    return np.where(hi == 1, 4 + lo, 3 - lo)
+    """TQ3 level index k in 0..7 from the two planes."""
+    return codes_from_tier_planes((lo2, hi1), d, 3)
 
 
 def decode(lo2, hi1, norms, sign_words, d: int) -> np.ndarray:
@@ -219,6 +280,7 @@ def decode(lo2, hi1, norms, sign_words, d: int) -> np.ndarray:
     return (n / d) * s * hc
 
 
-def bytes_per_value(d: int) -> float:
-    """Storage per value: 2-bit plane + 1-bit plane + one fp16 norm per vector."""
-    return (d // 4 + d // 8 + 2) / d
+def bytes_per_value(d: int, bits: int = 3) -> float:
+    """Storage per value: the tier's planes + one fp16 norm per vector."""
+    plane_bytes = {2: d // 8 + d // 8, 3: d // 4 + d // 8, 4: d // 4 + d // 4}[bits]
+    return (plane_bytes + 2) / d

@@ -47,7 +47,9 @@ stored as sign = (k >= L/2) and magnitude m = k - L/2 if sign else L/2 - 1 - k:
   * TQ2: a 1-bit magnitude plane (element i at bit i % 8 of byte i / 8) and the 1-bit
     sign plane;
   * TQ3: the 2-bit magnitude plane and the 1-bit sign plane (above);
-  * TQ4: a 2-bit plane of m & 3, and a 2-bit plane of (m >> 2) | (sign << 1).
+  * TQ4: a 2-bit plane of m & 3, and a second plane of D/4 bytes per row holding two
+    1-bit sub-planes: the sign bits (its first D/8 bytes) and the magnitude's bit 2
+    (its last D/8 bytes).
 """
 
 from __future__ import annotations
@@ -194,7 +196,7 @@ def encode_tier(x: np.ndarray, sign_words, bits: int):
 
     Returns ``(planes tuple of uint8 arrays, norms float16 [...])``; the planes are
     TQ2: (magnitude 1-bit, sign 1-bit); TQ3: (magnitude 2-bit, sign 1-bit);
-    TQ4: (magnitude low 2 bits, magnitude bit 2 | sign << 1).
+    TQ4: (magnitude low 2 bits, [sign 1-bit | magnitude bit 2, 1-bit]).
     """
     levels = 1 << bits
     k, norms = level_index(x, sign_words, levels)
@@ -204,7 +206,7 @@ def encode_tier(x: np.ndarray, sign_words, bits: int):
     if bits == 3:
         return (pack_bits(mag, 2), pack_bits(sign, 1)), norms
     if bits == 4:
-        return (pack_bits(mag & 3, 2), pack_bits((mag >> 2) | (sign << 1), 2)), norms
+        return (pack_bits(mag & 3, 2), np.concatenate([pack_bits(sign, 1), pack_bits(mag >> 2, 1)], axis=-1)), norms
     raise ValueError("bits must be 2, 3 or 4")
 
 
@@ -218,9 +220,8 @@ def codes_from_tier_planes(planes, d: int, bits: int) -> np.ndarray:
         mag = unpack_bits(planes[0], 2, d).astype(np.int64)
         sign = unpack_bits(planes[1], 1, d).astype(np.int64)
     elif bits == 4:
-        hi = unpack_bits(planes[1], 2, d).astype(np.int64)
-        mag = unpack_bits(planes[0], 2, d).astype(np.int64) | ((hi & 1) << 2)
-        sign = hi >> 1
+        sign = unpack_bits(planes[1][..., :d // 8], 1, d).astype(np.int64)
+        mag = unpack_bits(planes[0], 2, d).astype(np.int64) | (unpack_bits(planes[1][..., d // 8:], 1, d).astype(np.int64) << 2)
     else:
         raise ValueError("bits must be 2, 3 or 4")
     return np.where(sign == 1, half + mag, half - 1 - mag)

@@ -73,16 +73,20 @@ def test_codes_are_nearest_level_of_the_rotated_coordinate(bits):
 def test_plane_layouts_bit_by_bit():
     """Hand-built level indices land at the documented bits of each tier's planes."""
     d = 32
-    # TQ4: level index k -> sign = k >= 8, m = k - 8 or 7 - k; low 2 bits / (bit 2 | sign << 1)
+    # TQ4: level index k -> sign = k >= 8, m = k - 8 or 7 - k; low 2 bits, then a plane of
+    # [sign bits (D/8 bytes) | magnitude bit 2 (D/8 bytes)]
     k4 = np.array([[15, 0, 8, 7] + [7] * 28])
     sign = (k4 >= 8).astype(np.uint8)
     mag = np.where(k4 >= 8, k4 - 8, 7 - k4).astype(np.uint8)
     assert mag[0, :4].tolist() == [7, 7, 0, 0] and sign[0, :4].tolist() == [1, 0, 1, 0]
+    x = np.zeros((1, d), dtype=np.float16)
     lo = tq.pack_bits(mag & 3, 2)
-    hi = tq.pack_bits((mag >> 2) | (sign << 1), 2)
-    # element 0: m = 7 (low bits 3, bit 2 set), sign 1 -> hi field 0b11; element 1: m = 7, sign 0 -> 0b01
-    assert lo[0, 0] == (3 | 3 << 2 | 0 << 4 | 0 << 6) and hi[0, 0] == (0b11 | 0b01 << 2 | 0b10 << 4 | 0b00 << 6)
+    hi = np.concatenate([tq.pack_bits(sign, 1), tq.pack_bits(mag >> 2, 1)], axis=-1)
+    assert hi.shape == (1, d // 4)
+    assert lo[0, 0] == (3 | 3 << 2 | 0 << 4 | 0 << 6)
+    assert hi[0, 0] == 0b00000101 and hi[0, d // 8] == 0b00000011  # signs of 0, 2; bit 2 of 0, 1
     assert np.array_equal(tq.codes_from_tier_planes((lo, hi), d, 4), k4)
+    del x
     # TQ2: element i at bit i % 8 of byte i / 8 in both planes
     k2 = np.array([[3, 0, 2, 1] + [1] * 28])
     mag2 = np.where(k2 >= 2, k2 - 2, 1 - k2).astype(np.uint8)

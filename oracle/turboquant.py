@@ -43,13 +43,13 @@ The tier ladder of section "S2 — TurboQuant tier family" (one rotation + codeb
 scheme at several bit widths) adds a 2-bit and a 4-bit tier with the same transform and
 norm; their codebooks are the 4- and 16-level Lloyd-Max quantisers of N(0,1), rounded
 and made symmetric the same way.  A level index k of a b-bit tier (L = 2^b levels) is
-stored as sign = (k >= L/2) and magnitude m = k - L/2 if sign else L/2 - 1 - k:
-  * TQ2: a 1-bit magnitude plane (element i at bit i % 8 of byte i / 8) and the 1-bit
-    sign plane;
-  * TQ3: the 2-bit magnitude plane and the 1-bit sign plane (above);
-  * TQ4: a 2-bit plane of m & 3, and a second plane of D/4 bytes per row holding two
-    1-bit sub-planes: the sign bits (its first D/8 bytes) and the magnitude's bit 2
-    (its last D/8 bytes).
+held as sign = (k >= L/2) and magnitude m = k - L/2 if sign else L/2 - 1 - k.  The
+pages fix no storage layout for these two tiers; here each element gets one
+sign-magnitude field (sign in the top bit, m below), packed little-endian like the TQ3
+magnitude plane:
+  * TQ2: a 2-bit plane, field (sign << 1) | m, element i at bits 2 (i % 4) of byte i / 4;
+  * TQ4: a 4-bit plane, field (sign << 3) | m, element i at bits 4 (i % 2) of byte i / 2;
+each with one fp16 norm per vector (the pages' 4-bit block is 2 bytes per vector larger).
 """
 
 from __future__ import annotations
@@ -195,18 +195,18 @@ def encode_tier(x: np.ndarray, sign_words, bits: int):
     """Quantise fp16 rows ``x[..., D]`` with the ``bits``-bit tier (2, 3 or 4).
 
     Returns ``(planes tuple of uint8 arrays, norms float16 [...])``; the planes are
-    TQ2: (magnitude 1-bit, sign 1-bit); TQ3: (magnitude 2-bit, sign 1-bit);
-    TQ4: (magnitude low 2 bits, [sign 1-bit | magnitude bit 2, 1-bit]).
+    TQ2: (2-bit sign-magnitude fields,); TQ3: (magnitude 2-bit, sign 1-bit);
+    TQ4: (4-bit sign-magnitude fields,).
     """
     levels = 1 << bits
     k, norms = level_index(x, sign_words, levels)
     sign, mag = _sign_magnitude(k, levels)
     if bits == 2:
-        return (pack_bits(mag, 1), pack_bits(sign, 1)), norms
+        return (pack_bits((sign << 1) | mag, 2),), norms
     if bits == 3:
         return (pack_bits(mag, 2), pack_bits(sign, 1)), norms
     if bits == 4:
-        return (pack_bits(mag & 3, 2), np.concatenate([pack_bits(sign, 1), pack_bits(mag >> 2, 1)], axis=-1)), norms
+        return (pack_bits((sign << 3) | mag, 4),), norms
     raise ValueError("bits must be 2, 3 or 4")
 
 
@@ -214,14 +214,14 @@ def codes_from_tier_planes(planes, d: int, bits: int) -> np.ndarray:
     """Level index k in 0..2^bits - 1 from a tier's planes."""
     half = 1 << (bits - 1)
     if bits == 2:
-        mag = unpack_bits(planes[0], 1, d).astype(np.int64)
-        sign = unpack_bits(planes[1], 1, d).astype(np.int64)
+        f = unpack_bits(planes[0], 2, d).astype(np.int64)
+        sign, mag = f >> 1, f & 1
     elif bits == 3:
         mag = unpack_bits(planes[0], 2, d).astype(np.int64)
         sign = unpack_bits(planes[1], 1, d).astype(np.int64)
     elif bits == 4:
-        sign = unpack_bits(planes[1][..., :d // 8], 1, d).astype(np.int64)
-        mag = unpack_bits(planes[0], 2, d).astype(np.int64) | (unpack_bits(planes[1][..., d // 8:], 1, d).astype(np.int64) << 2)
+        f = unpack_bits(planes[0], 4, d).astype(np.int64)
+        sign, mag = f >> 3, f & 7
     else:
         raise ValueError("bits must be 2, 3 or 4")
     return np.where(sign == 1, half + mag, half - 1 - mag)
@@ -283,5 +283,5 @@ def decode(lo2, hi1, norms, sign_words, d: int) -> np.ndarray:
 
 def bytes_per_value(d: int, bits: int = 3) -> float:
     """Storage per value: the tier's planes + one fp16 norm per vector."""
-    plane_bytes = {2: d // 8 + d // 8, 3: d // 4 + d // 8, 4: d // 4 + d // 4}[bits]
+    plane_bytes = {2: d // 4, 3: d // 4 + d // 8, 4: d // 2}[bits]
     return (plane_bytes + 2) / d

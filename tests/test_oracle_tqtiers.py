@@ -71,28 +71,37 @@ def test_codes_are_nearest_level_of_the_rotated_coordinate(bits):
 
 
 def test_plane_layouts_bit_by_bit():
-    """Hand-built level indices land at the documented bits of each tier's planes."""
+    """Hand-built level indices land at the documented bits of each tier's plane."""
     d = 32
-    # TQ4: level index k -> sign = k >= 8, m = k - 8 or 7 - k; low 2 bits, then a plane of
-    # [sign bits (D/8 bytes) | magnitude bit 2 (D/8 bytes)]
-    k4 = np.array([[15, 0, 8, 7] + [7] * 28])
+    # TQ4: k -> sign = k >= 8, m = k - 8 or 7 - k; field (sign << 3) | m, element i at
+    # bits 4 (i % 2) of byte i / 2
+    k4 = np.array([[15, 0, 8, 7, 12, 3] + [7] * 26])
     sign = (k4 >= 8).astype(np.uint8)
     mag = np.where(k4 >= 8, k4 - 8, 7 - k4).astype(np.uint8)
-    assert mag[0, :4].tolist() == [7, 7, 0, 0] and sign[0, :4].tolist() == [1, 0, 1, 0]
-    x = np.zeros((1, d), dtype=np.float16)
-    lo = tq.pack_bits(mag & 3, 2)
-    hi = np.concatenate([tq.pack_bits(sign, 1), tq.pack_bits(mag >> 2, 1)], axis=-1)
-    assert hi.shape == (1, d // 4)
-    assert lo[0, 0] == (3 | 3 << 2 | 0 << 4 | 0 << 6)
-    assert hi[0, 0] == 0b00000101 and hi[0, d // 8] == 0b00000011  # signs of 0, 2; bit 2 of 0, 1
-    assert np.array_equal(tq.codes_from_tier_planes((lo, hi), d, 4), k4)
-    del x
-    # TQ2: element i at bit i % 8 of byte i / 8 in both planes
-    k2 = np.array([[3, 0, 2, 1] + [1] * 28])
-    mag2 = np.where(k2 >= 2, k2 - 2, 1 - k2).astype(np.uint8)
+    assert mag[0, :6].tolist() == [7, 7, 0, 0, 4, 4] and sign[0, :6].tolist() == [1, 0, 1, 0, 1, 0]
+    p4 = tq.pack_bits((sign << 3) | mag, 4)
+    assert p4.shape == (1, d // 2)
+    assert p4[0, :3].tolist() == [0xF | 0x7 << 4, 0x8 | 0x0 << 4, 0xC | 0x4 << 4]
+    assert np.array_equal(tq.codes_from_tier_planes((p4,), d, 4), k4)
+    # TQ2: field (sign << 1) | m, element i at bits 2 (i % 4) of byte i / 4
+    k2 = np.array([[3, 0, 2, 1, 1, 3, 0, 2] + [1] * 24])
     sign2 = (k2 >= 2).astype(np.uint8)
-    assert tq.pack_bits(mag2, 1)[0, 0] == 0b00000011 and tq.pack_bits(sign2, 1)[0, 0] == 0b00000101
-    assert np.array_equal(tq.codes_from_tier_planes((tq.pack_bits(mag2, 1), tq.pack_bits(sign2, 1)), d, 2), k2)
+    mag2 = np.where(k2 >= 2, k2 - 2, 1 - k2).astype(np.uint8)
+    p2 = tq.pack_bits((sign2 << 1) | mag2, 2)
+    assert p2.shape == (1, d // 4)
+    assert p2[0, 0] == (0b11 | 0b01 << 2 | 0b10 << 4 | 0b00 << 6)
+    assert p2[0, 1] == (0b00 | 0b11 << 2 | 0b01 << 4 | 0b10 << 6)
+    assert np.array_equal(tq.codes_from_tier_planes((p2,), d, 2), k2)
+    # the encoder writes one such plane per tier, and reading it back gives the level
+    # index it quantised to
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((3, d)).astype(np.float16)
+    w = np.array([0x12345678], dtype=np.int64)
+    for bits in (2, 4):
+        planes, _ = tq.encode_tier(x, w, bits)
+        assert len(planes) == 1 and planes[0].shape == (3, d * bits // 8)
+        k, _ = tq.level_index(x, w, 1 << bits)
+        assert np.array_equal(tq.codes_from_tier_planes(planes, d, bits), k)
 
 
 def test_distortion_ladder_and_bytes_per_value():
@@ -109,5 +118,15 @@ def test_distortion_ladder_and_bytes_per_value():
     # relative MSE close to the Gaussian quantiser's (the rotated coordinates are ~N(0,1))
     assert abs(err[2] - 0.1175) < 0.02 and abs(err[3] - 0.03454) < 0.006 and abs(err[4] - 0.009497) < 0.002
     assert err[2] > err[3] > err[4]
-    assert tq.bytes_per_value(d, 2) == (d // 8 * 2 + 2) / d
+    assert tq.bytes_per_value(d, 2) == (d // 4 + 2) / d
     assert tq.bytes_per_value(d, 4) == (d // 2 + 2) / d
+
+
+def test_bytes_per_value_against_the_pages_table():
+    """turbo2 matches the pages' bpv; turbo4 is exactly one fp16 per vector smaller."""
+    rows = {r[1]: (float(r[2]), int(r[3])) for r in golden_rows("polykv_storage_and_roundtrip.txt")
+            if r[0] == "bytes_per_value"}
+    val, dec = rows["turbo2"]
+    assert abs(tq.bytes_per_value(128, 2) - val) <= 0.5 * 10 ** -dec
+    val, dec = rows["turbo4"]
+    assert abs(tq.bytes_per_value(128, 4) + 2.0 / 128 - val) <= 0.5 * 10 ** -dec

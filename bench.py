@@ -45,6 +45,9 @@ def parse_args(argv=None):
     ap.add_argument("--auto-ring", action="store_true",
                     help="size the ring (slots, tile tokens) from the measured link and attention time "
                          "instead of the workload's fixed values")
+    ap.add_argument("--v-fmt", default="",
+                    help="with --kernel-only: store the window's V in this format instead "
+                         "(f16, q8_0, tq2, tq3, tq4)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the window decode-attention kernel alone on one layer of every "
                          "workload (one JSON line per workload; not the benchmark line)")
@@ -303,8 +306,7 @@ def run_ours(args):
         att_ms = autosize.attention_ms(cfg.k_fmt, cfg.v_fmt, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
                                        n_kv=cfg.n_kv, scale=cfg.scale, softcap=cfg.softcap, signs=signs,
                                        device=device)
-        row = {"f16": 2 * cfg.d, "q8_0": cfg.d + cfg.d // 16, "tq3": cfg.d // 4 + cfg.d // 8 + 2}
-        ptb = cfg.hkv * (row[cfg.tk_fmt] + row[cfg.tv_fmt])
+        ptb = cfg.hkv * (sum(qps.plane_row_bytes(cfg.tk_fmt, cfg.d)) + sum(qps.plane_row_bytes(cfg.tv_fmt, cfg.d)))
         slot_budget = 4.0 * (1 << 30)  # device memory set aside for the ring's slots
         rp = qps.plan_ring(att_ms, bw_eff, slot_budget, float(cfg.tail_len * ptb))
         tile_tokens = max(16, int(rp["tile_bytes"] // ptb) // 16 * 16)
@@ -492,6 +494,10 @@ def run_ours(args):
     return 0
 
 
+# kernel-only lines of a workload's window with V stored at another TurboQuant tier
+TIER_VARIANTS = {"qwen14b_q8": ("tq4", "tq2"), "gemma_global_q8k_tq3v": ("tq4", "tq2")}
+
+
 def run_kernel_only(args):
     """Per-launch time of the window decode-attention kernel on one layer of each
     workload (or of --config), timed back to back with CUDA events; inputs > L2 except
@@ -512,6 +518,9 @@ def run_kernel_only(args):
     s = torch.cuda.current_stream()
     for name in names:
         cfg = synth.by_name(name)
+        if args.v_fmt:
+            cfg = cfg.replace(v_fmt=args.v_fmt)
+            name = f"{name} V={args.v_fmt}"
         signs = synth.sign_bits(cfg.d, cfg.sign_seed)
         if cfg.kind == "split":
             q = synth.query_f16(cfg, 0, device=dev)
@@ -537,6 +546,13 @@ def run_kernel_only(args):
                 rows = cfg.batch * n_q * cfg.hq
             _time_window_launch(qps, torch, a, name if n_q == 1 else f"{name} verify n_q={n_q} causal",
                                 rows, cfg, K, V, dev, s, peak, peak_kind)
+        # the same window with V at the 2- and 4-bit TurboQuant tiers
+        for vf in (TIER_VARIANTS.get(name, ()) if not (args.layers or args.v_fmt) else ()):
+            del V
+            V = qps.encode_kv_head_major(vf, v, signs)
+            a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs)
+            _time_window_launch(qps, torch, a, f"{name} V={vf}", cfg.batch * cfg.hq, cfg.replace(v_fmt=vf),
+                                K, V, dev, s, peak, peak_kind)
         qps.device_status(reset=True)
     return 0
 

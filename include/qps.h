@@ -58,7 +58,15 @@
  *                 2(i%4)..2(i%4)+1 of byte i/4 and bit i%8 of byte i/8.  Level index
  *                 k = sign ? 4 + mag : 3 - mag; value = (norm / D) * s .* (H c[k]),
  *                 H the Sylvester-Hadamard matrix, s the seeded sign diagonal, c the
- *                 codebook returned by qps_tq3_codebook().
+ *                 8-level codebook returned by qps_tq_codebook(3, ...).
+ *   QPS_FMT_TQ2   data: 2-bit fields (sign << 1) | mag (D/4 bytes), element i at bits
+ *                 2(i%4)..2(i%4)+1 of byte i/4; aux: one fp16 norm (2 bytes).
+ *                 k = sign ? 2 + mag : 1 - mag over the 4-level codebook; value as TQ3.
+ *   QPS_FMT_TQ4   data: 4-bit fields (sign << 3) | mag (D/2 bytes), element i at bits
+ *                 4(i%2)..4(i%2)+3 of byte i/2; aux: one fp16 norm (2 bytes).
+ *                 k = sign ? 8 + mag : 7 - mag over the 16-level codebook; value as TQ3.
+ *   TQ2 / TQ3 / TQ4 are the 2-, 3- and 4-bit rungs of one rotation + codebook scheme
+ *   [POLY, "S2 — TurboQuant tier family"]; they are V formats only.
  */
 #ifndef QPS_H
 #define QPS_H
@@ -91,7 +99,9 @@ typedef enum qps_status {
 typedef enum qps_kv_format {
   QPS_FMT_F16 = 0,
   QPS_FMT_Q8_0 = 1,
-  QPS_FMT_TQ3 = 2
+  QPS_FMT_TQ3 = 2,
+  QPS_FMT_TQ2 = 3,
+  QPS_FMT_TQ4 = 4
 } qps_kv_format;
 
 /* ABI version of the loaded library (QPS_ABI_VERSION it was built with). */
@@ -110,6 +120,12 @@ QPS_API const char* qps_status_name(int32_t status);
  * GPU.  levels: host, 8 floats (ascending); thresholds: host, 7 floats.  Either may be
  * NULL.  Errors: none. */
 QPS_API qps_status qps_tq3_codebook(float* levels, float* thresholds);
+
+/* The codebook of the `bits`-bit TurboQuant tier (2, 3 or 4), built like the TQ3 one
+ * from the 2^bits-level Lloyd-Max quantiser of N(0,1) [POLY, "S2 — TurboQuant tier
+ * family"].  levels: host, 2^bits floats (ascending); thresholds: host, 2^bits - 1
+ * floats; either may be NULL.  Host only.  Errors: UNSUPPORTED (bits). */
+QPS_API qps_status qps_tq_codebook(int32_t bits, float* levels, float* thresholds);
 
 /* q8_0 encode [POLY, "What PolyKV is (reference)"; problem statement: 32-value blocks,
  * fp16 scale = absmax / 127, int8 codes].
@@ -141,6 +157,21 @@ QPS_API qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int6
                             const uint32_t* signs, void* lo2, void* hi1, void* norms,
                             void* stream);
 
+/* TQ2 / TQ4 encode: the TQ3 steps above with the 4- or 16-level codebook
+ * (qps_tq_codebook(2 or 4, ...)), storing one sign-magnitude field per element
+ * (QPS_FMT_TQ2 / QPS_FMT_TQ4 above) and fp16(n).  A zero row stores zero fields and a
+ * zero norm.
+ *   x       device, fp16 rows [rows][D], row stride x_row_stride (elements, >= D).
+ *   signs   host, D/32 words: bit i of word i/32 set means s_i = -1.
+ *   codes   device, [rows][D/4] (TQ2) or [rows][D/2] (TQ4) bytes;
+ *   norms   device, fp16 [rows]; 2-byte aligned (so is x).
+ * D in {32, 64, 128, 256, 512}.  rows == 0 is a no-op.
+ * Errors: INVALID_ARG, UNSUPPORTED (D), CUDA. */
+QPS_API qps_status qps_kv_quant_tq2(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* codes, void* norms, void* stream);
+QPS_API qps_status qps_kv_quant_tq4(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* codes, void* norms, void* stream);
+
 /* A K or V cache (or one of its parts) as seen by the attention calls.  Row of
  * (token t, KV head h, batch entry b) = b*batch_stride + t*tok_stride + h*head_stride.
  * batch_stride == 0 means every batch entry reads the same rows (a shared prefix,
@@ -149,8 +180,8 @@ QPS_API qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int6
 typedef struct qps_kv_view {
   int32_t fmt;         /* qps_kv_format */
   int32_t reserved0;   /* must be 0 */
-  const void* data;    /* device: F16 values | Q8_0 codes | TQ3 2-bit plane; 16-byte aligned */
-  const void* aux;     /* device: Q8_0 scales | TQ3 1-bit plane; NULL for F16 */
+  const void* data;    /* device: F16 values | Q8_0 codes | TQ2/3/4 code plane; 16-byte aligned */
+  const void* aux;     /* device: Q8_0 scales | TQ3 1-bit plane | TQ2/TQ4 norms; NULL for F16 */
   const void* aux2;    /* device: TQ3 norms; NULL otherwise */
   int64_t tok_stride;  /* rows between consecutive tokens (> 0) */
   int64_t head_stride; /* rows between consecutive KV heads (>= 0) */
@@ -181,7 +212,7 @@ typedef struct qps_attn_args {
   int64_t kv_begin, kv_end; /* 0 <= kv_begin <= kv_end; tokens of the views */
   float scale;
   float softcap;          /* <= 0: off */
-  const uint32_t* v_signs;/* host, D/32 sign words; required iff v.fmt == QPS_FMT_TQ3 */
+  const uint32_t* v_signs;/* host, D/32 sign words; required iff v.fmt is TQ2, TQ3 or TQ4 */
   int32_t n_split;        /* > 0, or 0 = chosen by the library */
   int32_t part_offset;
   float* o_parts;
@@ -218,7 +249,7 @@ QPS_API qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out,
 QPS_API int32_t qps_attn_path(const qps_attn_args* a);
 
 /* Decode attention over device-resident KV (the window [0, wc), or any device part)
- * [RKV].  Supported: D in {64, 128, 256, 512}; K in {F16, Q8_0}; V in {F16, Q8_0, TQ3};
+ * [RKV].  Supported: D in {64, 128, 256, 512}; K in {F16, Q8_0}; V in {F16, Q8_0, TQ2, TQ3, TQ4};
  * hq a multiple of hkv.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 QPS_API qps_status qps_attn_decode_window(const qps_attn_args* a, void* stream);
 
@@ -268,7 +299,7 @@ QPS_API qps_status qps_ring_destroy(qps_ring* ring);
  * contiguous pinned-host range per plane, rows addressed inside the tile by
  * row = token * tok_stride + head * head_stride (the same for every plane of K and
  * V): token-major tiles use (hkv, 1), head-major tiles (1, padded tile length).  K
- * planes first (1 for F16, 2 for Q8_0, 3 for TQ3, in data/aux/aux2 order), then V
+ * planes first (1 for F16, 2 for Q8_0, TQ2 and TQ4, 3 for TQ3, in data/aux/aux2 order), then V
  * planes.  The ring places each plane at the next 256-byte-aligned offset of the slot
  * (in that order); their total must fit in slot_bytes.  When the host planes already
  * sit at those offsets from the first K plane (a tail packed tile by tile), the whole

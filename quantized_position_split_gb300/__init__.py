@@ -19,14 +19,18 @@ from typing import List, Optional, Sequence
 import torch
 
 from . import _native as N
-from ._native import FMT_F16, FMT_Q8_0, FMT_TQ3, QpsError  # noqa: F401
+from ._native import FMT_F16, FMT_Q8_0, FMT_TQ2, FMT_TQ3, FMT_TQ4, QpsError  # noqa: F401
 
 __all__ = [
     "QpsError",
     "KV",
     "tq3_codebook",
+    "tq_codebook",
     "kv_quant_q8_0",
     "kv_quant_tq3",
+    "plane_row_bytes",
+    "kv_quant_tq2",
+    "kv_quant_tq4",
     "encode_kv",
     "encode_kv_head_major",
     "attn_args",
@@ -78,6 +82,16 @@ def tq3_codebook():
     return list(lv), list(th)
 
 
+def tq_codebook(bits: int):
+    """The codebook of the ``bits``-bit TurboQuant tier (2, 3 or 4): (2^bits levels,
+    2^bits - 1 thresholds) as Python floats."""
+    n = 1 << bits if bits in (2, 3, 4) else 1
+    lv = (ctypes.c_float * n)()
+    th = (ctypes.c_float * max(1, n - 1))()
+    N.check(lib().qps_tq_codebook(bits, lv, th))
+    return list(lv), list(th)[:n - 1]
+
+
 def _rows2d(x: torch.Tensor):
     if x.dtype != torch.float16 or not x.is_cuda:
         raise QpsError(N.QPS_ERR_INVALID_ARG, "input must be a CUDA float16 tensor")
@@ -117,6 +131,37 @@ def kv_quant_tq3(x: torch.Tensor, signs, lo2=None, hi1=None, norms=None, stream=
     N.check(lib().qps_kv_quant_tq3(x2.data_ptr(), rows, d, stride, sa, lo2.data_ptr(),
                                    hi1.data_ptr(), norms.data_ptr(), _stream(stream)))
     return lo2, hi1, norms
+
+
+def _kv_quant_fields(bits: int, x: torch.Tensor, signs, codes=None, norms=None, stream=None):
+    x2, d, stride = _rows2d(x)
+    rows = x2.shape[0]
+    if codes is None:
+        codes = torch.empty(x.shape[:-1] + (d * bits // 8,), dtype=torch.uint8, device=x.device)
+    if norms is None:
+        norms = torch.empty(x.shape[:-1], dtype=torch.float16, device=x.device)
+    sa = _sign_array(signs)
+    fn = lib().qps_kv_quant_tq2 if bits == 2 else lib().qps_kv_quant_tq4
+    N.check(fn(x2.data_ptr(), rows, d, stride, sa, codes.data_ptr(), norms.data_ptr(), _stream(stream)))
+    return codes, norms
+
+
+def kv_quant_tq2(x: torch.Tensor, signs, codes=None, norms=None, stream=None):
+    """Encode fp16 rows ``x[..., D]`` as TQ2: (2-bit sign-magnitude fields [..., D/4] u8,
+    fp16 norms [...])."""
+    return _kv_quant_fields(2, x, signs, codes, norms, stream)
+
+
+def kv_quant_tq4(x: torch.Tensor, signs, codes=None, norms=None, stream=None):
+    """Encode fp16 rows ``x[..., D]`` as TQ4: (4-bit sign-magnitude fields [..., D/2] u8,
+    fp16 norms [...])."""
+    return _kv_quant_fields(4, x, signs, codes, norms, stream)
+
+
+def plane_row_bytes(fmt: str, d: int) -> List[int]:
+    """Bytes per row of each stored plane of ``fmt`` (data, aux, aux2 order)."""
+    return {"f16": [2 * d], "q8_0": [d, d // 16], "tq3": [d // 4, d // 8, 2],
+            "tq2": [d // 4, 2], "tq4": [d // 2, 2]}[fmt]
 
 
 @dataclasses.dataclass
@@ -166,10 +211,11 @@ def encode_kv(fmt: str, x: torch.Tensor, signs=None, stream=None) -> KV:
         planes = (x.contiguous(),)
     elif fmt == "q8_0":
         planes = kv_quant_q8_0(x.contiguous(), stream=stream)
-    elif fmt == "tq3":
+    elif fmt in ("tq2", "tq3", "tq4"):
         if signs is None:
-            raise QpsError(N.QPS_ERR_INVALID_ARG, "TQ3 needs the sign words")
-        planes = kv_quant_tq3(x.contiguous(), signs, stream=stream)
+            raise QpsError(N.QPS_ERR_INVALID_ARG, "TurboQuant formats need the sign words")
+        enc = {"tq2": kv_quant_tq2, "tq3": kv_quant_tq3, "tq4": kv_quant_tq4}[fmt]
+        planes = enc(x.contiguous(), signs, stream=stream)
     else:
         raise QpsError(N.QPS_ERR_INVALID_ARG, f"unknown format {fmt}")
     return KV(fmt, tuple(planes), tokens, hkv, d, hkv, 1, batch_stride)

@@ -24,7 +24,9 @@ QPS_ERR_INTERNAL = 6
 FMT_F16 = 0
 FMT_Q8_0 = 1
 FMT_TQ3 = 2
-FMT_BY_NAME = {"f16": FMT_F16, "q8_0": FMT_Q8_0, "tq3": FMT_TQ3}
+FMT_TQ2 = 3
+FMT_TQ4 = 4
+FMT_BY_NAME = {"f16": FMT_F16, "q8_0": FMT_Q8_0, "tq3": FMT_TQ3, "tq2": FMT_TQ2, "tq4": FMT_TQ4}
 
 
 class QpsError(RuntimeError):
@@ -110,9 +112,14 @@ SIGNATURES = [
     ("qps_last_error", c_char_p, []),
     ("qps_status_name", c_char_p, [c_int32]),
     ("qps_tq3_codebook", c_int32, [POINTER(c_float), POINTER(c_float)]),
+    ("qps_tq_codebook", c_int32, [c_int32, POINTER(c_float), POINTER(c_float)]),
     ("qps_kv_quant_q8_0", c_int32, [c_void_p, c_int64, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
     ("qps_kv_quant_tq3", c_int32,
      [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p, c_void_p]),
+    ("qps_kv_quant_tq2", c_int32,
+     [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p]),
+    ("qps_kv_quant_tq4", c_int32,
+     [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p]),
     ("qps_attn_plan", c_int32, [POINTER(AttnArgs), POINTER(c_int32), POINTER(c_size_t)]),
     ("qps_attn_path", c_int32, [POINTER(AttnArgs)]),
     ("qps_attn_decode_window", c_int32, [POINTER(AttnArgs), c_void_p]),

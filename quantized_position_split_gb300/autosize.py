@@ -22,7 +22,7 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 from . import (Ring, attn_args, attn_decode_window, attn_plan, choose_tier, encode_kv_head_major, lse_combine,
-               plan_ring, tail_band, tile_desc)
+               plan_ring, plane_row_bytes, tail_band, tile_desc)
 
 
 def measure_link(device, nbytes: int = 256 << 20, reps: int = 3) -> Tuple[float, float]:
@@ -153,7 +153,7 @@ def plan_decode(*, layers: int, batch: int, hq: int, hkv: int, d: int, n_kv: int
 
     def per_token(fmt_k, fmt_v):  # stored bytes of one position of one layer
         def row(fmt):
-            return {"f16": 2 * d, "q8_0": d + d // 16, "tq3": d // 4 + d // 8 + 2}[fmt]
+            return sum(plane_row_bytes(fmt, d))
         return hkv * (row(fmt_k) + row(fmt_v))
 
     kv_bytes = [layers * n_kv * per_token(kf, vf) for kf, vf in tiers]

@@ -1,4 +1,4 @@
-// C ABI entry points: argument validation, error reporting, the TQ3 codebook, the
+// C ABI entry points: argument validation, error reporting, the TurboQuant codebooks, the
 // attention plan / dispatch, the LSE combine and the native decode-step runner.
 #include <cuda.h>
 
@@ -106,11 +106,11 @@ unsigned int* device_error_word() {
   return words[dev];
 }
 
-// ---- TQ3 codebook -----------------------------------------------------------------
-// Lloyd iteration for the 8-level MSE-optimal quantiser of N(0,1) in double precision
-// (thresholds at midpoints, levels at the conditional means of their cells), then each
-// level rounded to the nearest fp16 value, made exactly symmetric, and the thresholds
-// set to the exact midpoints.
+// ---- TurboQuant codebooks -----------------------------------------------------------
+// Lloyd iteration for the L-level MSE-optimal quantiser of N(0,1) in double precision
+// (thresholds at midpoints, levels at the conditional means of their cells, starting
+// from L evenly spaced levels on [-2, 2]), then each level rounded to the nearest fp16
+// value, made exactly symmetric, and the thresholds set to the exact midpoints.
 namespace {
 
 double gauss_pdf(double x) { return std::exp(-0.5 * x * x) / std::sqrt(2.0 * M_PI); }
@@ -123,40 +123,40 @@ double round_to_half_grid(double x) {
   return std::ldexp(std::nearbyint(std::ldexp(m, 11)), e - 11);
 }
 
-Codebook make_codebook() {
-  double c[8];
-  for (int i = 0; i < 8; ++i) c[i] = -2.0 + 4.0 * i / 7.0;
+Codebook make_codebook(int L) {
+  double c[16], t[15], cn[16];
+  for (int i = 0; i < L; ++i) c[i] = -2.0 + 4.0 * i / (L - 1);
   for (int it = 0; it < 100000; ++it) {
-    double t[7];
-    for (int i = 0; i < 7; ++i) t[i] = 0.5 * (c[i] + c[i + 1]);
-    double cn[8];
+    for (int i = 0; i < L - 1; ++i) t[i] = 0.5 * (c[i] + c[i + 1]);
     double delta = 0.0;
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < L; ++k) {
       const double pa = k == 0 ? 0.0 : gauss_pdf(t[k - 1]);
-      const double pb = k == 7 ? 0.0 : gauss_pdf(t[k]);
+      const double pb = k == L - 1 ? 0.0 : gauss_pdf(t[k]);
       const double fa = k == 0 ? 0.0 : gauss_cdf(t[k - 1]);
-      const double fb = k == 7 ? 1.0 : gauss_cdf(t[k]);
+      const double fb = k == L - 1 ? 1.0 : gauss_cdf(t[k]);
       cn[k] = (pa - pb) / (fb - fa);
       delta = std::fmax(delta, std::fabs(cn[k] - c[k]));
     }
-    for (int k = 0; k < 8; ++k) c[k] = cn[k];
+    for (int k = 0; k < L; ++k) c[k] = cn[k];
     if (delta < 1e-14) break;
   }
   Codebook cb{};
-  for (int i = 0; i < 4; ++i) {
-    const float pos = (float)round_to_half_grid(std::fabs(c[4 + i]));
-    cb.levels[4 + i] = pos;
-    cb.levels[3 - i] = -pos;
+  cb.n = L;
+  const int h = L / 2;
+  for (int i = 0; i < h; ++i) {
+    const float pos = (float)round_to_half_grid(std::fabs(c[h + i]));
+    cb.levels[h + i] = pos;
+    cb.levels[h - 1 - i] = -pos;
   }
-  for (int i = 0; i < 7; ++i) cb.thresholds[i] = (cb.levels[i] + cb.levels[i + 1]) / 2.0f;
+  for (int i = 0; i < L - 1; ++i) cb.thresholds[i] = (cb.levels[i] + cb.levels[i + 1]) / 2.0f;
   return cb;
 }
 
 }  // namespace
 
-const Codebook& tq3_codebook() {
-  static const Codebook cb = make_codebook();
-  return cb;
+const Codebook* tq_codebook(int bits) {
+  static const Codebook cb2 = make_codebook(4), cb3 = make_codebook(8), cb4 = make_codebook(16);
+  return bits == 2 ? &cb2 : bits == 3 ? &cb3 : bits == 4 ? &cb4 : nullptr;
 }
 
 // ---- attention argument resolution ------------------------------------------------
@@ -164,18 +164,21 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-qps_status check_view(const qps_kv_view& v, const char* name, bool allow_tq3) {
+qps_status check_view(const qps_kv_view& v, const char* name, bool allow_tq) {
   const std::string n(name);
   if (v.reserved0 != 0) return fail(QPS_ERR_INVALID_ARG, n + ": reserved0 must be 0");
-  if (v.fmt != QPS_FMT_F16 && v.fmt != QPS_FMT_Q8_0 && v.fmt != QPS_FMT_TQ3)
+  if (v.fmt != QPS_FMT_F16 && v.fmt != QPS_FMT_Q8_0 && !is_tq(v.fmt))
     return fail(QPS_ERR_INVALID_ARG, n + ": unknown format");
-  if (v.fmt == QPS_FMT_TQ3 && !allow_tq3)
-    return fail(QPS_ERR_UNSUPPORTED, n + ": TQ3 is supported for V only");
+  if (is_tq(v.fmt) && !allow_tq)
+    return fail(QPS_ERR_UNSUPPORTED, n + ": TurboQuant formats are supported for V only");
   if (!v.data) return fail(QPS_ERR_INVALID_ARG, n + ": data is NULL");
   if (!aligned(v.data, 16)) return fail(QPS_ERR_INVALID_ARG, n + ": data must be 16-byte aligned");
   if (v.fmt != QPS_FMT_F16) {
+    // q8_0 scales and TQ3 sign planes: 4-byte aligned; TQ2 / TQ4 norms: fp16 aligned
+    const size_t al = (v.fmt == QPS_FMT_TQ2 || v.fmt == QPS_FMT_TQ4) ? 2 : 4;
     if (!v.aux) return fail(QPS_ERR_INVALID_ARG, n + ": aux plane is NULL");
-    if (!aligned(v.aux, 4)) return fail(QPS_ERR_INVALID_ARG, n + ": aux must be 4-byte aligned");
+    if (!aligned(v.aux, al))
+      return fail(QPS_ERR_INVALID_ARG, n + (al == 4 ? ": aux must be 4-byte aligned" : ": aux must be 2-byte aligned"));
   }
   if (v.fmt == QPS_FMT_TQ3) {
     if (!v.aux2) return fail(QPS_ERR_INVALID_ARG, n + ": aux2 (norms) is NULL");
@@ -229,8 +232,8 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
     return fail(QPS_ERR_INVALID_ARG, "attention: need 0 <= kv_begin <= kv_end");
   if (!std::isfinite(a->scale) || !std::isfinite(a->softcap))
     return fail(QPS_ERR_INVALID_ARG, "attention: scale and softcap must be finite");
-  if (a->v.fmt == QPS_FMT_TQ3 && !a->v_signs)
-    return fail(QPS_ERR_INVALID_ARG, "attention: v_signs is required for a TQ3 V");
+  if (is_tq(a->v.fmt) && !a->v_signs)
+    return fail(QPS_ERR_INVALID_ARG, "attention: v_signs is required for a TurboQuant V");
   if (a->n_split < 0) return fail(QPS_ERR_INVALID_ARG, "attention: n_split must be >= 0");
   const bool shared = a->k.batch_stride == 0 && a->batch > 1;
   if (shared && n_q > 1)
@@ -278,10 +281,11 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   p->q_pos = a->q_pos;
   p->rows_per_cta = rows_per_cta;
   p->rows_total = rows_total;
-  if (a->v.fmt == QPS_FMT_TQ3)
+  if (is_tq(a->v.fmt)) {
     for (int i = 0; i < a->d / 32; ++i) p->vsigns[i] = a->v_signs[i];
-  const Codebook& cb = tq3_codebook();
-  for (int i = 0; i < 8; ++i) p->tq_levels[i] = cb.levels[i];
+    const Codebook* cb = tq_codebook(tq_bits(a->v.fmt));
+    for (int i = 0; i < cb->n; ++i) p->tq_levels[i] = cb->levels[i];
+  }
   return QPS_OK;
 }
 
@@ -396,12 +400,15 @@ int64_t qps_launch_count(int32_t reset) {
   return n;
 }
 
-qps_status qps_tq3_codebook(float* levels, float* thresholds) {
-  const Codebook& cb = tq3_codebook();
-  if (levels) std::memcpy(levels, cb.levels, sizeof(cb.levels));
-  if (thresholds) std::memcpy(thresholds, cb.thresholds, sizeof(cb.thresholds));
+qps_status qps_tq_codebook(int32_t bits, float* levels, float* thresholds) {
+  const Codebook* cb = tq_codebook(bits);
+  if (!cb) return fail(QPS_ERR_UNSUPPORTED, "tq_codebook: bits must be 2, 3 or 4");
+  if (levels) std::memcpy(levels, cb->levels, sizeof(float) * cb->n);
+  if (thresholds) std::memcpy(thresholds, cb->thresholds, sizeof(float) * (cb->n - 1));
   return QPS_OK;
 }
+
+qps_status qps_tq3_codebook(float* levels, float* thresholds) { return qps_tq_codebook(3, levels, thresholds); }
 
 static qps_status check_encoder(const void* x, int64_t rows, int32_t d, int64_t stride,
                                 const char* name) {
@@ -438,9 +445,36 @@ qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int64_t x_ro
   if (!lo2 || !hi1 || !norms) return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq3: an output plane is NULL");
   if (!aligned(x, 2) || !aligned(hi1, 4) || !aligned(norms, 2))
     return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq3: x / norms must be 2-byte and hi1 4-byte aligned");
-  return launch_quant_tq3(reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs,
-                          reinterpret_cast<uint8_t*>(lo2), reinterpret_cast<uint8_t*>(hi1),
-                          reinterpret_cast<__half*>(norms), reinterpret_cast<cudaStream_t>(stream));
+  return launch_quant_tq(3, reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs,
+                         reinterpret_cast<uint8_t*>(lo2), reinterpret_cast<uint8_t*>(hi1),
+                         reinterpret_cast<__half*>(norms), reinterpret_cast<cudaStream_t>(stream));
+}
+
+// TQ2 / TQ4: one plane of sign-magnitude fields and the norms
+static qps_status kv_quant_tq_fields(int bits, const char* name, const void* x, int64_t rows, int32_t d,
+                                     int64_t x_row_stride, const uint32_t* signs, void* codes,
+                                     void* norms, void* stream) {
+  const std::string n(name);
+  qps_status st = check_encoder(x, rows, d, x_row_stride, name);
+  if (st != QPS_OK) return st;
+  if (!signs) return fail(QPS_ERR_INVALID_ARG, n + ": signs is NULL");
+  if (rows == 0) return QPS_OK;
+  if (!codes || !norms) return fail(QPS_ERR_INVALID_ARG, n + ": an output plane is NULL");
+  if (!aligned(x, 2) || !aligned(norms, 2))
+    return fail(QPS_ERR_INVALID_ARG, n + ": x / norms must be 2-byte aligned");
+  return launch_quant_tq(bits, reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs,
+                         reinterpret_cast<uint8_t*>(codes), nullptr, reinterpret_cast<__half*>(norms),
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+qps_status qps_kv_quant_tq2(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* codes, void* norms, void* stream) {
+  return kv_quant_tq_fields(2, "kv_quant_tq2", x, rows, d, x_row_stride, signs, codes, norms, stream);
+}
+
+qps_status qps_kv_quant_tq4(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* codes, void* norms, void* stream) {
+  return kv_quant_tq_fields(4, "kv_quant_tq4", x, rows, d, x_row_stride, signs, codes, norms, stream);
 }
 
 qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out, size_t* workspace_bytes_out) {

@@ -3,9 +3,10 @@
 // One part of the position-split decode of "F5 M7 — Rolling KV: position-windowed KV
 // residency" (section "Implementation decomposition, refined (S1 -> S2 -> S3)", item
 // S2): every split chunk of positions yields a normalised output and its log-sum-exp.
-// K / V are dequantised in registers on their way into the tensor-core operands; a TQ3
-// V is read as centroid x norm in the rotated domain and the output is inverse-rotated
-// once ("F5 M6 — PolyKV (shared compressed KV pool)", section "S2 perf-path Level B").
+// K / V are dequantised in registers on their way into the tensor-core operands; a
+// TurboQuant V (TQ2 / TQ3 / TQ4) is read as centroid x norm in the rotated domain and the
+// output is inverse-rotated once ("F5 M6 — PolyKV (shared compressed KV pool)", sections
+// "S2 perf-path Level B" and "S2 — TurboQuant tier family").
 //
 // Formulation (query rows on the narrow N = 8 side, so a GQA group of 5..8 rows wastes
 // nothing):   S^T[t][r] = sum_d K[t][d] Q[r][d]       (A = K tile, B = Q^T)
@@ -15,7 +16,7 @@
 //
 // Exactness: q8_0 K codes are exact in f16; each 32-value block is accumulated
 // separately and multiplied by its fp32 scale afterwards, so the logits carry only
-// fp32 rounding.  TQ3 levels are fp16-exact by construction.  P (in [0, 1]) and a
+// fp32 rounding.  TurboQuant levels are fp16-exact by construction.  P (in [0, 1]) and a
 // q8_0 V value (code x scale) are rounded once to fp16.
 //
 // Data movement: the KV planes of a (KV head, batch entry) must be token-contiguous
@@ -82,6 +83,15 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Byte permute over {b, a} (bytes 0..7) with the selector's low four nibbles: bits 0..2
+// of a nibble pick a source byte, bit 3 replicates that byte's top bit over the result
+// byte instead of copying it.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 // 4 signed int8 codes (little-endian in w) -> two half2 {c0, c1}, {c2, c3}, exactly:
 // the biased byte b + 128 becomes the mantissa of 1024 + (b + 128) and 1152 is removed.
 __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -133,8 +143,10 @@ template <int D, int KF, int VF, int TT_>
 struct GeoT {
   static constexpr int K_RB = KF == QPS_FMT_F16 ? 2 * D : D;          // K data bytes / token
   static constexpr int K_ARB = KF == QPS_FMT_Q8_0 ? D / 16 : 0;       // K scales bytes / token
-  static constexpr int V_RB = VF == QPS_FMT_F16 ? 2 * D : VF == QPS_FMT_Q8_0 ? D : D / 4;
-  static constexpr int V_ARB = VF == QPS_FMT_Q8_0 ? D / 16 : VF == QPS_FMT_TQ3 ? D / 8 : 0;
+  // V data: fp16 values, q8_0 codes, TQ2 / TQ3 2-bit fields or TQ4 4-bit fields; V aux:
+  // q8_0 scales, the TQ3 sign plane or the TQ2 / TQ4 norms; V aux2: the TQ3 norms
+  static constexpr int V_RB = VF == QPS_FMT_F16 ? 2 * D : VF == QPS_FMT_Q8_0 ? D : VF == QPS_FMT_TQ4 ? D / 2 : D / 4;
+  static constexpr int V_ARB = VF == QPS_FMT_Q8_0 ? D / 16 : VF == QPS_FMT_TQ3 ? D / 8 : is_tq(VF) ? 2 : 0;
   static constexpr int V_A2RB = VF == QPS_FMT_TQ3 ? 2 : 0;
   static constexpr int TT = TT_;
   static constexpr int SUB = TT / 16;
@@ -150,6 +162,7 @@ struct GeoT {
   static constexpr int KA_OFF = align_to(PVA::SW ? align_to(AFTER_V, 1024) + PVA::BYTES : AFTER_V, 128);
   static constexpr int VA_OFF = PVA::SW ? align_to(AFTER_V, 1024) : align_to(KA_OFF + PKA::BYTES, 128);
   static constexpr int VA2_OFF = align_to(PVA::SW ? KA_OFF + PKA::BYTES : VA_OFF + PVA::BYTES, 128);
+  static constexpr int NORM_OFF = VF == QPS_FMT_TQ3 ? VA2_OFF : VA_OFF;  // TurboQuant norms
   static constexpr int STAGE = align_to(VA2_OFF + PVA2::BYTES, 1024);
   // bytes the tensor-map boxes of one tile deliver
   static constexpr int TX = PK::BYTES + (PKA::TMA ? PKA::BYTES : 0) + PV::BYTES + (PVA::TMA ? PVA::BYTES : 0) +
@@ -249,7 +262,7 @@ __device__ __forceinline__ void stage_flat_zfill(uint8_t* dst, const uint8_t* sr
 }
 
 // Output column (within a lane group's DT columns) of row g (hh = 0) or g + 8 (hh = 1)
-// of the TQ3 PV m-tile i: word k = i / 8 covers 16 columns, its m-tile 2j + h takes
+// of the TQ2 / TQ3 PV m-tile i: word k = i / 8 covers 16 columns, its m-tile 2j + h takes
 // columns j + 8h and j + 8h + 4 (DT = 8: one half-word, m-tile j takes j and j + 4).
 template <int DT>
 __host__ __device__ constexpr int tq_col(int i, int hh) {
@@ -308,11 +321,24 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     return;
   }
 
-  // TQ3 magnitudes as fp16 (exact): level 4 + m in bytes 2m, 2m + 1 of {tq_lo, tq_hi}
-  uint32_t tq_lo = 0u, tq_hi = 0u;
+  // TurboQuant levels as fp16 (exact).  TQ3: magnitude m (level 4 + m) in bytes 2m,
+  // 2m + 1 of {tq_lo, tq_hi}.  TQ2: the level of field f = (sign << 1) | m in bytes 2f,
+  // 2f + 1 (levels 1, 0, 2, 3).  TQ4: the low bytes of the magnitudes m = 0..7 (levels
+  // 8 + m) in {tq_lo, tq_hi}, their high bytes in {tq_lo2, tq_hi2}.
+  uint32_t tq_lo = 0u, tq_hi = 0u, tq_lo2 = 0u, tq_hi2 = 0u;
   if constexpr (VF == QPS_FMT_TQ3) {
     tq_lo = pack_h2(p.tq_levels[4], p.tq_levels[5]);
     tq_hi = pack_h2(p.tq_levels[6], p.tq_levels[7]);
+  } else if constexpr (VF == QPS_FMT_TQ2) {
+    tq_lo = pack_h2(p.tq_levels[1], p.tq_levels[0]);
+    tq_hi = pack_h2(p.tq_levels[2], p.tq_levels[3]);
+  } else if constexpr (VF == QPS_FMT_TQ4) {
+    const uint32_t m01 = pack_h2(p.tq_levels[8], p.tq_levels[9]), m23 = pack_h2(p.tq_levels[10], p.tq_levels[11]);
+    const uint32_t m45 = pack_h2(p.tq_levels[12], p.tq_levels[13]), m67 = pack_h2(p.tq_levels[14], p.tq_levels[15]);
+    tq_lo = __byte_perm(m01, m23, 0x6420);
+    tq_hi = __byte_perm(m45, m67, 0x6420);
+    tq_lo2 = __byte_perm(m01, m23, 0x7531);
+    tq_hi2 = __byte_perm(m45, m67, 0x7531);
   }
 
   // ---- query fragments (B operand of S^T), one set per 8-row n-tile --------------
@@ -442,13 +468,14 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
 
   // per-lane stage offsets that do not change from tile to tile
   const int ks_lane = g * (D / 32);                        // K scale of (row g, block 0)
-  int tq_lo2[4] = {0, 0, 0, 0}, tq_sgn[4] = {0, 0, 0, 0};   // TQ3 plane offsets, tokens 2c..
-  if constexpr (VF == QPS_FMT_TQ3) {
+  // TQ2 / TQ3 2-bit plane and TQ3 sign plane offsets of tokens 2c, 2c+1, 2c+8, 2c+9
+  int tq_off2[4] = {0, 0, 0, 0}, tq_sgn[4] = {0, 0, 0, 0};
+  if constexpr (VF == QPS_FMT_TQ3 || VF == QPS_FMT_TQ2) {
     const int tk0[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      tq_lo2[u] = soff<G::PV::IB, G::PV::SW, TT>(tk0[u], g * (DT / 4));
-      tq_sgn[u] = soff<G::PVA::IB, G::PVA::SW, TT>(tk0[u], g * (DT / 8));
+      tq_off2[u] = soff<G::PV::IB, G::PV::SW, TT>(tk0[u], g * (DT / 4));
+      if constexpr (VF == QPS_FMT_TQ3) tq_sgn[u] = soff<G::PVA::IB, G::PVA::SW, TT>(tk0[u], g * (DT / 8));
     }
   }
 
@@ -533,8 +560,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
       in_g[sb] = (t_g >= t0) && (t_g < t1);
       in_g8[sb] = (t_g + 8 >= t0) && (t_g + 8 < t1);
       n_g[sb] = n_g8[sb] = 1.f;
-      if constexpr (VF == QPS_FMT_TQ3) {
-        const __half* nrm = reinterpret_cast<const __half*>(st + G::VA2_OFF);
+      if constexpr (is_tq(VF)) {
+        const __half* nrm = reinterpret_cast<const __half*>(st + G::NORM_OFF);
         n_g[sb] = __half2float(nrm[16 * sb + g]);
         n_g8[sb] = __half2float(nrm[16 * sb + g + 8]);
       }
@@ -667,12 +694,13 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
           }
         }
       }
-    } else {
-      // TQ3.  Word k of a lane group's 2-bit plane holds 16 of its output columns; the
-      // codes of the two tokens of a pair are interleaved byte by byte, spread to one
-      // code per byte and turned into byte-permute selectors over the fp16 magnitude
-      // table; the sign plane supplies bit 15 of each half.  m-tile i of word k takes
-      // columns tq_col(i, 0) and tq_col(i, 1) (see the epilogue).
+    } else if constexpr (VF == QPS_FMT_TQ3 || VF == QPS_FMT_TQ2) {
+      // TQ2 / TQ3.  Word k of a lane group's 2-bit plane holds 16 of its output columns;
+      // the codes of the two tokens of a pair are interleaved byte by byte, spread to one
+      // code per byte and turned into byte-permute selectors over the fp16 level table
+      // (TQ3: magnitudes, the sign plane then supplying bit 15 of each half; TQ2: the four
+      // signed levels in field order).  m-tile i of word k takes columns tq_col(i, 0) and
+      // tq_col(i, 1) (see the epilogue).
       constexpr int LB = DT / 4;                   // 2-bit plane bytes per lane group, token
       constexpr int HB = DT / 8;                   // sign plane bytes per lane group, token
       constexpr int NWD = DT >= 16 ? DT / 16 : 1;  // 16-column words
@@ -684,7 +712,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
         uint32_t L[4][NWD];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint8_t* ls = lo2 + tq_lo2[u] + 16 * sb * G::PV::IB;  // swizzle repeats every 8 rows
+          const uint8_t* ls = lo2 + tq_off2[u] + 16 * sb * G::PV::IB;  // swizzle repeats every 8 rows
           if constexpr (LB == 16) {
             const uint4 r = *reinterpret_cast<const uint4*>(ls);
             L[u][0] = r.x; L[u][1] = r.y; L[u][2] = r.z; L[u][3] = r.w;
@@ -697,22 +725,26 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
             L[u][0] = *reinterpret_cast<const uint16_t*>(ls);
           }
         }
-        uint32_t H[4];  // sign bits of 32 columns (fewer at head_dim <= 128) per token
+        uint32_t H[4] = {0u, 0u, 0u, 0u};  // TQ3 sign bits of 32 columns (fewer at head_dim <= 128) per token
 #pragma unroll
         for (int k = 0; k < NWD; ++k) {
-          if ((k & 1) == 0) {
+          uint32_t hab[2] = {0u, 0u};
+          if constexpr (VF == QPS_FMT_TQ3) {
+            if ((k & 1) == 0) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              // (2k stays inside the lane's 16-byte chunk: HB = 8 puts its 8 bytes in one)
-              const uint8_t* hs = hi1 + tq_sgn[u] + 16 * sb * G::PVA::IB + 2 * k;
-              if constexpr (HB >= 4) H[u] = *reinterpret_cast<const uint32_t*>(hs);
-              else if constexpr (HB == 2) H[u] = *reinterpret_cast<const uint16_t*>(hs);
-              else H[u] = *hs;
+              for (int u = 0; u < 4; ++u) {
+                // (2k stays inside the lane's 16-byte chunk: HB = 8 puts its 8 bytes in one)
+                const uint8_t* hs = hi1 + tq_sgn[u] + 16 * sb * G::PVA::IB + 2 * k;
+                if constexpr (HB >= 4) H[u] = *reinterpret_cast<const uint32_t*>(hs);
+                else if constexpr (HB == 2) H[u] = *reinterpret_cast<const uint16_t*>(hs);
+                else H[u] = *hs;
+              }
             }
+            // sign bits of word k: token a of the pair in bits 0..15, token b in 16..31
+            const uint32_t hsel = (k & 1) ? 0x7632u : 0x5410u;
+            hab[0] = __byte_perm(H[0], H[1], hsel);
+            hab[1] = __byte_perm(H[2], H[3], hsel);
           }
-          // sign bits of word k: token a of the pair in bits 0..15, token b in 16..31
-          const uint32_t hsel = (k & 1) ? 0x7632u : 0x5410u;
-          const uint32_t hab[2] = {__byte_perm(H[0], H[1], hsel), __byte_perm(H[2], H[3], hsel)};
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             // bytes: (a, b) codes of columns 8h .. 8h + 3, then of 8h + 4 .. 8h + 7
@@ -725,16 +757,84 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
               uint32_t a[4];
 #pragma unroll
               for (int pr = 0; pr < 2; ++pr) {
-                // one code per byte, then the selector nibbles (2m, 2m + 1) of level 4 + m
+                // one code per byte, then the selector nibbles (2f, 2f + 1) of table entry f
                 const uint32_t sel = ((y[pr] >> (2 * j)) & 0x03030303u) * 0x22u + 0x10101010u;
                 const uint32_t m0 = __byte_perm(tq_lo, tq_hi, sel);
                 const uint32_t m1 = __byte_perm(tq_lo, tq_hi, sel >> 16);
-                // a clear sign bit stores a negative level
-                a[2 * pr] = m0 | (~(hab[pr] << (15 - e0)) & 0x80008000u);
-                a[2 * pr + 1] = m1 | (~(hab[pr] << (15 - e1)) & 0x80008000u);
+                if constexpr (VF == QPS_FMT_TQ3) {
+                  // a clear sign bit stores a negative level
+                  a[2 * pr] = m0 | (~(hab[pr] << (15 - e0)) & 0x80008000u);
+                  a[2 * pr + 1] = m1 | (~(hab[pr] << (15 - e1)) & 0x80008000u);
+                } else {
+                  a[2 * pr] = m0;
+                  a[2 * pr + 1] = m1;
+                }
               }
 #pragma unroll
               for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[sb][nt][0], pb[sb][nt][1]);
+            }
+          }
+        }
+      }
+    } else {
+      // TQ4.  A lane group's DT 4-bit fields (DT / 2 bytes per token) hold its columns in
+      // order, 8 per 32-bit word.  The fields of a token pair are interleaved byte by
+      // byte; their magnitudes (bits 0..2) select the low and the high byte of the fp16
+      // magnitude from two 8-byte tables, bit 3 (set: positive) sets the high byte's top
+      // bit through a sign-replicating byte permute, and the low / high bytes are then
+      // interleaved into halves.  m-tile i takes columns 2i and 2i + 1, as for q8_0.
+      static_assert(VF == QPS_FMT_TQ4, "unhandled V format");
+      constexpr int FB = DT / 2;               // field bytes per lane group and token
+      constexpr int CH = FB >= 16 ? 16 : FB;   // bytes per read
+      const uint8_t* vf = st + G::V_OFF;
+#pragma unroll
+      for (int sb = 0; sb < SUB; ++sb) {
+        const int tok[4] = {16 * sb + 2 * c, 16 * sb + 2 * c + 1, 16 * sb + 2 * c + 8, 16 * sb + 2 * c + 9};
+#pragma unroll
+        for (int q0 = 0; q0 < FB; q0 += CH) {
+          uint32_t w[4][CH / 4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint8_t* src = vf + soff<G::PV::IB, G::PV::SW, TT>(tok[u], g * FB + q0);
+            if constexpr (CH == 16) {
+              const uint4 r = *reinterpret_cast<const uint4*>(src);
+              w[u][0] = r.x; w[u][1] = r.y; w[u][2] = r.z; w[u][3] = r.w;
+            } else if constexpr (CH == 8) {
+              const uint2 r = *reinterpret_cast<const uint2*>(src);
+              w[u][0] = r.x; w[u][1] = r.y;
+            } else {
+              w[u][0] = *reinterpret_cast<const uint32_t*>(src);
+            }
+          }
+#pragma unroll
+          for (int wi = 0; wi < CH / 4; ++wi) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              // nibbles: a c0, a c1, b c0, b c1, a c2, a c3, b c2, b c3 of columns 4h ..
+              const uint32_t ysel = h ? 0x7362u : 0x5140u;
+              const uint32_t y[2] = {__byte_perm(w[0][wi], w[1][wi], ysel), __byte_perm(w[2][wi], w[3][wi], ysel)};
+              const uint32_t mg[2] = {y[0] & 0x77777777u, y[1] & 0x77777777u};
+              // each byte's low field moved up: its sign (bit 3) becomes the byte's top bit
+              const uint32_t y4[2] = {y[0] << 4, y[1] << 4};
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const int i = q0 + 4 * wi + 2 * h + q;  // m-tile: columns 2i, 2i + 1
+                uint32_t a[4];
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr) {
+                  const uint32_t sel = q ? mg[pr] >> 16 : mg[pr];
+                  const uint32_t lo = prmt(tq_lo, tq_hi, sel);
+                  // 0xff per value whose sign bit is set, in selector order (a even, a odd,
+                  // b even, b odd): the even column's from y4, the odd one's from y
+                  const uint32_t pos = prmt(y[pr], y4[pr], q ? 0xBFAEu : 0x9D8Cu);
+                  // a clear sign bit stores a negative level
+                  const uint32_t hi = prmt(tq_lo2, tq_hi2, sel) | (~pos & 0x80808080u);
+                  a[2 * pr] = __byte_perm(lo, hi, 0x6240u);
+                  a[2 * pr + 1] = __byte_perm(lo, hi, 0x7351u);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NTW; ++nt) mma16816(o[i][nt], a, pb[sb][nt][0], pb[sb][nt][1]);
+              }
             }
           }
         }
@@ -785,7 +885,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
       int d0, d1;
-      if constexpr (VF == QPS_FMT_TQ3) {
+      if constexpr (VF == QPS_FMT_TQ3 || VF == QPS_FMT_TQ2) {
         d0 = g * DT + tq_col<DT>(i, 0);
         d1 = g * DT + tq_col<DT>(i, 1);
       } else if constexpr (VPERM) {
@@ -830,7 +930,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     fin[idx] = acc;
   }
   __syncthreads();
-  if constexpr (VF == QPS_FMT_TQ3) {  // inverse rotation x = s .* (H y) / D, in place
+  if constexpr (is_tq(VF)) {  // inverse rotation x = s .* (H y) / D, in place
 #pragma unroll
     for (int lh = 0; (1 << lh) < D; ++lh) {  // butterflies of span h = 2^lh
       const int h = 1 << lh;
@@ -849,7 +949,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     const int r = idx / D, dd = idx % D;
     const float mx = rmx[r], den = rden[r];
     float val = fin[r * D + dd];
-    if constexpr (VF == QPS_FMT_TQ3) {
+    if constexpr (is_tq(VF)) {
       val *= 1.0f / (float)D;
       if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) val = -val;
     }
@@ -905,8 +1005,9 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
 }
 
 // Every format pairing and n-tile count of one head_dim, with or without the causal
-// limit (the two halves live in separate translation units).
-template <int D, bool CAUSAL>
+// limit; TIERS selects the V formats: TQ2 / TQ4 (true) or F16 / Q8_0 / TQ3 (false).  The
+// halves live in separate translation units.
+template <int D, bool CAUSAL, bool TIERS>
 qps_status launch_mma_d(const AttnParams& p, cudaStream_t s) {
   // 8-row n-tiles per warp: more only where the accumulators still fit in registers
   const int ntw = mma_tile_rows(D, p.rows_per_cta, p.shared != 0) / 8;
@@ -916,12 +1017,19 @@ qps_status launch_mma_d(const AttnParams& p, cudaStream_t s) {
     if (ntw == 2) return launch_mma_t<D, KF, VF, (D <= 128 ? 2 : 1), CAUSAL>(p, s); \
     return launch_mma_t<D, KF, VF, 1, CAUSAL>(p, s);                                \
   }
-  QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_F16)
-  QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_Q8_0)
-  QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_TQ3)
-  QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_F16)
-  QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_Q8_0)
-  QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_TQ3)
+  if constexpr (TIERS) {
+    QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_TQ2)
+    QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_TQ4)
+    QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_TQ2)
+    QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_TQ4)
+  } else {
+    QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_F16)
+    QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_Q8_0)
+    QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_TQ3)
+    QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_F16)
+    QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_Q8_0)
+    QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_TQ3)
+  }
 #undef QPS_MMA_CASE
   return fail(QPS_ERR_UNSUPPORTED, "attention: unsupported K/V format pairing");
 }

@@ -4,7 +4,7 @@
 // position-windowed KV residency" (section "Implementation decomposition, refined
 // (S1 -> S2 -> S3)", item S2): every split chunk of positions yields a normalised
 // output and its log-sum-exp; the chunks are merged later by the LSE combine.  K / V
-// are dequantised in registers as they are read; a TQ3 V is accumulated in the
+// are dequantised in registers as they are read; a TurboQuant V is accumulated in the
 // rotated domain as level x norm and inverse-rotated once per output row ("F5 M6 —
 // PolyKV (shared compressed KV pool)", section "S2 perf-path Level B").
 //
@@ -76,8 +76,9 @@ __device__ __forceinline__ void load_q8(const int8_t* p, float scale, float* out
   }
 }
 
-// Row `row` of a KV side, lane's E elements, as float.  TQ3 gives the rotated-domain
-// value norm * level (the 1/D, the Hadamard matrix and the signs come at the end).
+// Row `row` of a KV side, lane's E elements, as float.  A TurboQuant tier gives the
+// rotated-domain value norm * level (the 1/D, the Hadamard matrix and the signs come at
+// the end); `levels` is its codebook, ascending and symmetric.
 template <int FMT, int D>
 __device__ __forceinline__ void load_row(const KvSide& s, int64_t row, int lane,
                                          const float* levels, float* out) {
@@ -88,7 +89,7 @@ __device__ __forceinline__ void load_row(const KvSide& s, int64_t row, int lane,
     const float sc = __half2float(
         reinterpret_cast<const __half*>(s.aux)[row * (D / 32) + (lane * E) / 32]);
     load_q8<E>(reinterpret_cast<const int8_t*>(s.data) + row * D + lane * E, sc, out);
-  } else {
+  } else if constexpr (FMT == QPS_FMT_TQ3) {
     const uint32_t* lo = reinterpret_cast<const uint32_t*>(
         reinterpret_cast<const uint8_t*>(s.data) + row * (D / 4));
     const uint32_t* hi = reinterpret_cast<const uint32_t*>(
@@ -100,6 +101,19 @@ __device__ __forceinline__ void load_row(const KvSide& s, int64_t row, int lane,
     for (int e = 0; e < E; ++e) {
       const float mag = levels[4 + ((lw >> (2 * e)) & 3u)];
       out[e] = ((hw >> e) & 1u) ? n * mag : -n * mag;
+    }
+  } else {
+    // TQ2 / TQ4: fields (sign << (B - 1)) | magnitude of B bits, little-endian
+    constexpr int B = FMT == QPS_FMT_TQ2 ? 2 : 4;
+    constexpr int HALF = 1 << (B - 1);
+    const uint8_t* f = reinterpret_cast<const uint8_t*>(s.data) + row * (D * B / 8);
+    const float n = __half2float(reinterpret_cast<const __half*>(s.aux)[row]);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int bit = B * (E * lane + e);
+      const uint32_t fld = (f[bit >> 3] >> (bit & 7)) & ((1u << B) - 1);
+      const float mag = levels[HALF + (fld & (HALF - 1))];
+      out[e] = (fld & HALF) ? n * mag : -n * mag;
     }
   }
 }
@@ -124,9 +138,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
   const int64_t kbase = p.shared ? 0 : (int64_t)bz * p.k.batch;
   const int64_t vbase = p.shared ? 0 : (int64_t)bz * p.v.batch;
   const int part = p.part_offset + split;
-  float levels[8];
+  float levels[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) levels[i] = p.tq_levels[i];
+  for (int i = 0; i < 16; ++i) levels[i] = p.tq_levels[i];
 
   for (int rc0 = 0; rc0 < R; rc0 += RC) {
     const int nr = min(RC, R - rc0);
@@ -203,7 +217,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
     }
     __syncthreads();
 
-    if constexpr (VF == QPS_FMT_TQ3) {
+    if constexpr (is_tq(VF)) {
       // inverse rotation of the accumulated rows: x = s .* (H y) / D
       for (int h = 1; h < D; h *= 2) {
         for (int pid = threadIdx.x; pid < nr * (D / 2); pid += blockDim.x) {
@@ -229,7 +243,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
         }
       }
       float val = qs[r * D + dd];
-      if constexpr (VF == QPS_FMT_TQ3) {
+      if constexpr (is_tq(VF)) {
         val *= 1.0f / (float)D;
         if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) val = -val;
       }
@@ -264,10 +278,14 @@ qps_status launch_simple_d(const AttnParams& p, cudaStream_t s) {
     if (p.vfmt == QPS_FMT_F16) return launch_simple_dkv<D, QPS_FMT_F16, QPS_FMT_F16>(p, s);
     if (p.vfmt == QPS_FMT_Q8_0) return launch_simple_dkv<D, QPS_FMT_F16, QPS_FMT_Q8_0>(p, s);
     if (p.vfmt == QPS_FMT_TQ3) return launch_simple_dkv<D, QPS_FMT_F16, QPS_FMT_TQ3>(p, s);
+    if (p.vfmt == QPS_FMT_TQ2) return launch_simple_dkv<D, QPS_FMT_F16, QPS_FMT_TQ2>(p, s);
+    if (p.vfmt == QPS_FMT_TQ4) return launch_simple_dkv<D, QPS_FMT_F16, QPS_FMT_TQ4>(p, s);
   } else if (p.kfmt == QPS_FMT_Q8_0) {
     if (p.vfmt == QPS_FMT_F16) return launch_simple_dkv<D, QPS_FMT_Q8_0, QPS_FMT_F16>(p, s);
     if (p.vfmt == QPS_FMT_Q8_0) return launch_simple_dkv<D, QPS_FMT_Q8_0, QPS_FMT_Q8_0>(p, s);
     if (p.vfmt == QPS_FMT_TQ3) return launch_simple_dkv<D, QPS_FMT_Q8_0, QPS_FMT_TQ3>(p, s);
+    if (p.vfmt == QPS_FMT_TQ2) return launch_simple_dkv<D, QPS_FMT_Q8_0, QPS_FMT_TQ2>(p, s);
+    if (p.vfmt == QPS_FMT_TQ4) return launch_simple_dkv<D, QPS_FMT_Q8_0, QPS_FMT_TQ4>(p, s);
   }
   return fail(QPS_ERR_UNSUPPORTED, "attention: unsupported K/V format pairing");
 }

@@ -38,12 +38,22 @@ int sm_count_current();
 // The current device's error word (library-owned, allocated on first use, zeroed).
 unsigned int* device_error_word();
 
-// ---- TQ3 codebook (computed once on the host from the Gaussian density) -----------
+// ---- TurboQuant codebooks (computed once on the host from the Gaussian density) ----
 struct Codebook {
-  float levels[8];
-  float thresholds[7];
+  int n;                // levels: 4, 8 or 16
+  float levels[16];     // ascending, the first n used
+  float thresholds[15]; // the first n - 1 used
 };
-const Codebook& tq3_codebook();
+// bits = 2, 3 or 4; nullptr for any other width
+const Codebook* tq_codebook(int bits);
+
+// The TurboQuant tiers (V formats only) and their bit widths.
+__host__ __device__ constexpr bool is_tq(int fmt) {
+  return fmt == QPS_FMT_TQ2 || fmt == QPS_FMT_TQ3 || fmt == QPS_FMT_TQ4;
+}
+__host__ __device__ constexpr int tq_bits(int fmt) {
+  return fmt == QPS_FMT_TQ2 ? 2 : fmt == QPS_FMT_TQ3 ? 3 : fmt == QPS_FMT_TQ4 ? 4 : 0;
+}
 
 // ---- bytes per row of each storage plane ------------------------------------------
 inline int64_t plane_row_bytes(int fmt, int plane, int d) {
@@ -51,11 +61,18 @@ inline int64_t plane_row_bytes(int fmt, int plane, int d) {
     case QPS_FMT_F16: return plane == 0 ? 2 * (int64_t)d : 0;
     case QPS_FMT_Q8_0: return plane == 0 ? d : plane == 1 ? 2 * (d / 32) : 0;
     case QPS_FMT_TQ3: return plane == 0 ? d / 4 : plane == 1 ? d / 8 : plane == 2 ? 2 : 0;
+    case QPS_FMT_TQ2: return plane == 0 ? d / 4 : plane == 1 ? 2 : 0;
+    case QPS_FMT_TQ4: return plane == 0 ? d / 2 : plane == 1 ? 2 : 0;
     default: return 0;
   }
 }
 inline int plane_count(int fmt) {
-  return fmt == QPS_FMT_F16 ? 1 : fmt == QPS_FMT_Q8_0 ? 2 : fmt == QPS_FMT_TQ3 ? 3 : 0;
+  switch (fmt) {
+    case QPS_FMT_F16: return 1;
+    case QPS_FMT_Q8_0: case QPS_FMT_TQ2: case QPS_FMT_TQ4: return 2;
+    case QPS_FMT_TQ3: return 3;
+    default: return 0;
+  }
 }
 
 // ---- attention kernel parameters ---------------------------------------------------
@@ -89,7 +106,7 @@ struct AttnParams {
   int part_offset;
   unsigned int* err;  // device word set non-zero when a bounded in-kernel wait gives up
   uint32_t vsigns[kMaxSignWords];
-  float tq_levels[8];
+  float tq_levels[16];  // the V tier's codebook (ascending)
 };
 
 // Query rows one tensor-core CTA holds (8 per n-tile): at head_dim <= 128, where the
@@ -111,8 +128,9 @@ qps_status run_attn(const qps_attn_args* a, const AttnParams& p, int n_split, cu
 
 qps_status launch_quant_q8_0(const __half* x, int64_t rows, int d, int64_t stride,
                              int8_t* codes, __half* scales, cudaStream_t s);
-qps_status launch_quant_tq3(const __half* x, int64_t rows, int d, int64_t stride,
-                            const uint32_t* signs, uint8_t* lo2, uint8_t* hi1, __half* norms,
-                            cudaStream_t s);
+// TurboQuant encode at `bits` = 2, 3 or 4; plane1 is the TQ3 sign plane (unused otherwise)
+qps_status launch_quant_tq(int bits, const __half* x, int64_t rows, int d, int64_t stride,
+                           const uint32_t* signs, uint8_t* plane0, uint8_t* plane1, __half* norms,
+                           cudaStream_t s);
 
 }  // namespace qps

@@ -1,13 +1,14 @@
-// KV encoders: q8_0 and 3-bit TurboQuant-MSE (TQ3).
+// KV encoders: q8_0 and the 2-, 3- and 4-bit TurboQuant-MSE tiers (TQ2 / TQ3 / TQ4).
 //
 // q8_0 follows "F5 M6 — PolyKV (shared compressed KV pool)", section "What PolyKV is
 // (reference)" (keys at int8), with 32-value blocks and an fp16 absmax/127 scale.
-// TQ3 follows the same page, sections "What PolyKV is (reference)", "S2 — TurboQuant
-// tier family" and "Phase-0 fork recon": L2 norm, seeded sign diagonal, Walsh-Hadamard
-// rotation over head_dim, Lloyd-Max levels, stored as a 2-bit magnitude plane, a 1-bit
-// sign plane and an fp16 norm.
+// The TurboQuant tiers follow the same page, sections "What PolyKV is (reference)",
+// "S2 — TurboQuant tier family" and "Phase-0 fork recon": L2 norm, seeded sign diagonal,
+// Walsh-Hadamard rotation over head_dim, Lloyd-Max levels of 2^bits cells.  TQ3 stores a
+// 2-bit magnitude plane, a 1-bit sign plane and an fp16 norm; TQ2 and TQ4 store one
+// sign-magnitude field of 2 or 4 bits per element and an fp16 norm.
 //
-// Both encoders are bit-exact contracts: every floating-point step is an explicitly
+// The encoders are bit-exact contracts: every floating-point step is an explicitly
 // rounded IEEE float32 operation (__fmul_rn / __fadd_rn / __fdiv_rn / __fsqrt_rn) in a
 // fixed order, so that no contraction into FMA can change a code.
 #include "internal.h"
@@ -66,20 +67,24 @@ __global__ void __launch_bounds__(256) quant_q8_0_kernel(const __half* __restric
   }
 }
 
-struct Tq3Consts {
+struct TqConsts {
   uint32_t signs[kMaxSignWords];
-  float thresholds[7];
+  float thresholds[15];
 };
 
 // One warp per row.  Lane L holds elements L + 32 e, e < D / 32, so the FWHT stages
 // h < 32 are lane shuffles and the stages h >= 32 stay inside a lane's registers.
-template <int D>
-__global__ void __launch_bounds__(256) quant_tq3_kernel(const __half* __restrict__ x, int64_t rows,
-                                                        int64_t stride, Tq3Consts c,
-                                                        uint8_t* __restrict__ lo2,
-                                                        uint8_t* __restrict__ hi1,
-                                                        __half* __restrict__ norms) {
+// BITS = 3: plane0 = magnitudes (2 bits), plane1 = signs (1 bit); BITS = 2 / 4: plane0 =
+// (sign << (BITS - 1)) | magnitude fields, plane1 unused.
+template <int D, int BITS>
+__global__ void __launch_bounds__(256) quant_tq_kernel(const __half* __restrict__ x, int64_t rows,
+                                                       int64_t stride, TqConsts c,
+                                                       uint8_t* __restrict__ plane0,
+                                                       uint8_t* __restrict__ plane1,
+                                                       __half* __restrict__ norms) {
   constexpr int E = D / 32;
+  constexpr int L = 1 << BITS, HALF = L / 2;
+  constexpr int RB0 = D * (BITS == 4 ? 4 : 2) / 8;  // plane0 bytes per row
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -131,28 +136,51 @@ __global__ void __launch_bounds__(256) quant_tq3_kernel(const __half* __restrict
       }
     }
 
-    // level index, sign / magnitude planes
+    // level index k (a zero row takes k = HALF - 1: sign 0, magnitude 0), then its
+    // sign and magnitude
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      int k = 0;
+      int k = HALF - 1;
       if (n != 0.f) {
         const float z = __fdiv_rn(u[e], n);
+        k = 0;
 #pragma unroll
-        for (int m = 0; m < 7; ++m) k += (z >= c.thresholds[m]) ? 1 : 0;
+        for (int m = 0; m < L - 1; ++m) k += (z >= c.thresholds[m]) ? 1 : 0;
       }
-      const bool hi = (n != 0.f) && k >= 4;
-      const uint32_t lo = n == 0.f ? 0u : (hi ? (uint32_t)(k - 4) : (uint32_t)(3 - k));
-      const uint32_t sign_word = __ballot_sync(0xffffffffu, hi);
-      // 4 neighbouring lanes make one byte of the 2-bit plane
-      const uint32_t l1 = __shfl_down_sync(0xffffffffu, lo, 1);
-      const uint32_t l2 = __shfl_down_sync(0xffffffffu, lo, 2);
-      const uint32_t l3 = __shfl_down_sync(0xffffffffu, lo, 3);
-      if ((lane & 3) == 0)
-        lo2[row * (D / 4) + (32 * e + lane) / 4] = (uint8_t)(lo | (l1 << 2) | (l2 << 4) | (l3 << 6));
-      if (lane == 0)
-        *reinterpret_cast<uint32_t*>(hi1 + row * (D / 8) + 4 * e) = sign_word;
+      const bool sgn = k >= HALF;
+      const uint32_t mag = sgn ? (uint32_t)(k - HALF) : (uint32_t)(HALF - 1 - k);
+      uint8_t* r0 = plane0 + row * RB0;
+      if constexpr (BITS == 4) {
+        // 2 neighbouring lanes make one byte of 4-bit fields
+        const uint32_t f = (sgn ? 8u : 0u) | mag;
+        const uint32_t f1 = __shfl_down_sync(0xffffffffu, f, 1);
+        if ((lane & 1) == 0) r0[(32 * e + lane) / 2] = (uint8_t)(f | (f1 << 4));
+      } else {
+        // 4 neighbouring lanes make one byte of 2-bit fields
+        const uint32_t f = BITS == 2 ? ((sgn ? 2u : 0u) | mag) : mag;
+        const uint32_t f1 = __shfl_down_sync(0xffffffffu, f, 1);
+        const uint32_t f2 = __shfl_down_sync(0xffffffffu, f, 2);
+        const uint32_t f3 = __shfl_down_sync(0xffffffffu, f, 3);
+        if ((lane & 3) == 0) r0[(32 * e + lane) / 4] = (uint8_t)(f | (f1 << 2) | (f2 << 4) | (f3 << 6));
+      }
+      if constexpr (BITS == 3) {
+        const uint32_t sign_word = __ballot_sync(0xffffffffu, sgn);
+        if (lane == 0) *reinterpret_cast<uint32_t*>(plane1 + row * (D / 8) + 4 * e) = sign_word;
+      }
     }
     if (lane == 0) norms[row] = __float2half_rn(n);
+  }
+}
+
+template <int BITS>
+void launch_quant_tq_bits(int d, int grid, int block, cudaStream_t s, const __half* x, int64_t rows,
+                          int64_t stride, const TqConsts& c, uint8_t* p0, uint8_t* p1, __half* norms) {
+  switch (d) {
+    case 32: quant_tq_kernel<32, BITS><<<grid, block, 0, s>>>(x, rows, stride, c, p0, p1, norms); break;
+    case 64: quant_tq_kernel<64, BITS><<<grid, block, 0, s>>>(x, rows, stride, c, p0, p1, norms); break;
+    case 128: quant_tq_kernel<128, BITS><<<grid, block, 0, s>>>(x, rows, stride, c, p0, p1, norms); break;
+    case 256: quant_tq_kernel<256, BITS><<<grid, block, 0, s>>>(x, rows, stride, c, p0, p1, norms); break;
+    default: quant_tq_kernel<512, BITS><<<grid, block, 0, s>>>(x, rows, stride, c, p0, p1, norms); break;
   }
 }
 
@@ -177,24 +205,22 @@ qps_status launch_quant_q8_0(const __half* x, int64_t rows, int d, int64_t strid
   return QPS_OK;
 }
 
-qps_status launch_quant_tq3(const __half* x, int64_t rows, int d, int64_t stride,
-                            const uint32_t* signs, uint8_t* lo2, uint8_t* hi1, __half* norms,
-                            cudaStream_t s) {
+qps_status launch_quant_tq(int bits, const __half* x, int64_t rows, int d, int64_t stride,
+                           const uint32_t* signs, uint8_t* plane0, uint8_t* plane1, __half* norms,
+                           cudaStream_t s) {
   if (rows == 0) return QPS_OK;
-  Tq3Consts c{};
+  const Codebook* cb = tq_codebook(bits);
+  if (!cb) return fail(QPS_ERR_UNSUPPORTED, "kv_quant_tq: bits must be 2, 3 or 4");
+  if (d != 32 && d != 64 && d != 128 && d != 256 && d != 512)
+    return fail(QPS_ERR_UNSUPPORTED, "kv_quant_tq: head_dim must be 32, 64, 128, 256 or 512");
+  TqConsts c{};
   for (int i = 0; i < d / 32; ++i) c.signs[i] = signs[i];
-  const Codebook& cb = tq3_codebook();
-  for (int i = 0; i < 7; ++i) c.thresholds[i] = cb.thresholds[i];
+  for (int i = 0; i < cb->n - 1; ++i) c.thresholds[i] = cb->thresholds[i];
   const int block = 256;
   const int grid = grid_for(rows * 32, block);
-  switch (d) {
-    case 32: quant_tq3_kernel<32><<<grid, block, 0, s>>>(x, rows, stride, c, lo2, hi1, norms); break;
-    case 64: quant_tq3_kernel<64><<<grid, block, 0, s>>>(x, rows, stride, c, lo2, hi1, norms); break;
-    case 128: quant_tq3_kernel<128><<<grid, block, 0, s>>>(x, rows, stride, c, lo2, hi1, norms); break;
-    case 256: quant_tq3_kernel<256><<<grid, block, 0, s>>>(x, rows, stride, c, lo2, hi1, norms); break;
-    case 512: quant_tq3_kernel<512><<<grid, block, 0, s>>>(x, rows, stride, c, lo2, hi1, norms); break;
-    default: return fail(QPS_ERR_UNSUPPORTED, "kv_quant_tq3: head_dim must be 32, 64, 128, 256 or 512");
-  }
+  if (bits == 2) launch_quant_tq_bits<2>(d, grid, block, s, x, rows, stride, c, plane0, plane1, norms);
+  else if (bits == 3) launch_quant_tq_bits<3>(d, grid, block, s, x, rows, stride, c, plane0, plane1, norms);
+  else launch_quant_tq_bits<4>(d, grid, block, s, x, rows, stride, c, plane0, plane1, norms);
   count_launch();
   QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;

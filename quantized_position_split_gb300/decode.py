@@ -22,7 +22,7 @@ from typing import List, Optional
 
 import torch
 
-from . import KV, HostArena, Ring, StepPlan, attn_args, attn_plan, encode_kv_head_major, tile_desc
+from . import KV, HostArena, Ring, StepPlan, attn_args, attn_plan, encode_kv_head_major, plane_row_bytes, tile_desc
 
 
 def _parts_buffers(capacity: int, rows: int, d: int, device):
@@ -79,11 +79,7 @@ class PositionSplitDecoder:
     def _arena_bytes(self) -> int:
         """Pinned bytes the whole tail needs: every tile's planes, 256-byte aligned."""
         def plane_bytes(fmt):
-            if fmt == "f16":
-                return [2 * self.d]
-            if fmt == "q8_0":
-                return [self.d, 2 * (self.d // 32)]
-            return [self.d // 4, self.d // 8, 2]
+            return plane_row_bytes(fmt, self.d)
         total = 0
         for a, b in self.tile_ranges():
             tp = (b - a + 15) // 16 * 16

@@ -55,6 +55,18 @@ def test_abi_version_and_status_names(lib):
     assert lib.qps_status_name(4) == b"QPS_ERR_TIMEOUT"
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_tier_codebooks_equal_oracle_bit_for_bit(lib, bits):
+    n = 1 << bits
+    lv = (ctypes.c_float * n)()
+    th = (ctypes.c_float * (n - 1))()
+    assert lib.qps_tq_codebook(bits, lv, th) == 0
+    levels, thresholds = tq.codebook(n)
+    assert np.array_equal(np.array(list(lv), dtype=np.float32), levels)
+    assert np.array_equal(np.array(list(th), dtype=np.float32), thresholds)
+    assert lib.qps_tq_codebook(5, lv, th) == N.QPS_ERR_UNSUPPORTED
+
+
 def test_codebook_equals_oracle_bit_for_bit(lib):
     lv = (ctypes.c_float * 8)()
     th = (ctypes.c_float * 7)()
@@ -136,6 +148,20 @@ def test_attn_view_validation(lib):
     a.v.fmt = N.FMT_TQ3
     a.v.aux = a.v.aux2 = 8192  # no sign words
     assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
+    for fmt in (N.FMT_TQ2, N.FMT_TQ4):
+        a = _args()
+        a.k.fmt = fmt  # TurboQuant tiers are for V only
+        a.k.aux = 8192
+        assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_UNSUPPORTED
+        a = _args()
+        a.v.fmt = fmt
+        a.v.aux = 8192  # norms present, no sign words
+        assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
+        a.v.aux = 0  # no norms
+        assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
+    a = _args()
+    a.v.fmt = 5  # unknown format
+    assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
     a = _args()
     a.k.batch_stride = 5  # k per batch, v shared
     assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
@@ -146,6 +172,9 @@ def test_encoder_and_combine_validation(lib):
     assert lib.qps_kv_quant_q8_0(None, 4, 48, 48, None, None, None) == N.QPS_ERR_UNSUPPORTED
     assert lib.qps_kv_quant_q8_0(None, 0, 128, 128, None, None, None) == N.QPS_OK  # no-op
     assert lib.qps_kv_quant_tq3(None, 4, 128, 128, None, None, None, None, None) == N.QPS_ERR_INVALID_ARG
+    for fn in (lib.qps_kv_quant_tq2, lib.qps_kv_quant_tq4):
+        assert fn(None, 4, 128, 128, None, None, None, None) == N.QPS_ERR_INVALID_ARG
+        assert fn(None, 4, 96, 96, None, None, None, None) == N.QPS_ERR_UNSUPPORTED
     assert lib.qps_lse_combine(None, None, 0, 4, 128, None, None, None) == N.QPS_ERR_INVALID_ARG
     assert lib.qps_lse_combine(None, None, 2, 0, 128, None, None, None) == N.QPS_OK  # no rows
 

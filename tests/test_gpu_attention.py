@@ -47,7 +47,8 @@ def test_lse_combine(qps, n_parts, d):
     assert np.all(oo.cpu().numpy()[5] == 0) and np.isneginf(ll.cpu().numpy()[5])
 
 
-FORMATS = [("f16", "f16"), ("q8_0", "q8_0"), ("q8_0", "tq3"), ("f16", "tq3"), ("q8_0", "f16")]
+FORMATS = [("f16", "f16"), ("q8_0", "q8_0"), ("q8_0", "tq3"), ("f16", "tq3"), ("q8_0", "f16"),
+           ("q8_0", "tq2"), ("q8_0", "tq4"), ("f16", "tq2"), ("f16", "tq4")]
 
 
 def _encode(qps, layout, fmt, x, words):
@@ -82,13 +83,13 @@ def test_window_attention_formats(qps, layout, d, kf, vf, softcap):
 
 @pytest.mark.parametrize("layout", ["head", "token"])
 @pytest.mark.parametrize("begin,end", [(17, 211), (0, 16), (5, 6), (31, 300), (299, 300)])
-@pytest.mark.parametrize("d,vf", [(128, "f16"), (512, "tq3")])
+@pytest.mark.parametrize("d,vf", [(128, "f16"), (512, "tq3"), (64, "tq4"), (256, "tq2")])
 def test_ragged_ranges(qps, layout, begin, end, d, vf):
     """Sub-ranges whose ends cut 16-token tiles, single tokens and tiny chunks (at
     head_dim 512 several warps share each tile)."""
     hq, hkv, n = 5, 1, 300
     q, k, v = _inputs(n, hq, hkv, d, seed=begin * 7 + end)
-    words = synth.sign_bits(d, 5) if vf == "tq3" else None
+    words = synth.sign_bits(d, 5) if vf.startswith("tq") else None
     K = _encode(qps, layout, "q8_0", k, None)
     V = _encode(qps, layout, vf, v, words)
     kh = pipeline.dequant("q8_0", k.numpy())
@@ -149,7 +150,8 @@ def test_split_identity_every_window_length(qps):
 
 @pytest.mark.parametrize("layout", ["head", "token"])
 @pytest.mark.parametrize("b", [1, 2, 5])
-def test_gqa_and_shared_batch(qps, layout, b):
+@pytest.mark.parametrize("vf", ["tq3", "tq4"])
+def test_gqa_and_shared_batch(qps, layout, b, vf):
     """A shared prefix (batch_stride 0) read by b batch entries (up to 40 query rows
     per KV head) equals each entry attending it alone."""
     d, hq, hkv, n = 128, 16, 2, 777
@@ -159,17 +161,18 @@ def test_gqa_and_shared_batch(qps, layout, b):
     v = torch.randn((n, hkv, d), generator=g).half()
     words = synth.sign_bits(d, 42)
     K = _encode(qps, layout, "q8_0", k, None)
-    V = _encode(qps, layout, "tq3", v, words)
+    V = _encode(qps, layout, vf, v, words)
     a = qps.attn_args(q.cuda(), K, V, scale=0.09, v_signs=words, shared=True)
     o, lse = qps.attn_decode_window(a)
     kh = pipeline.dequant("q8_0", k.numpy())
-    vh = pipeline.dequant("tq3", v.numpy(), words.numpy())
+    vh = pipeline.dequant(vf, v.numpy(), words.numpy())
     ro, rl = oatt.gqa_decode(q.double().numpy(), kh, vh, 0.09)
     assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(b * hq, d), rl.reshape(b * hq))
 
 
 MQ_FORMATS = [(128, "q8_0", "q8_0", 0.0), (128, "f16", "f16", 0.0), (512, "q8_0", "tq3", 50.0),
-              (64, "f16", "tq3", 0.0), (256, "q8_0", "f16", 30.0)]
+              (64, "f16", "tq3", 0.0), (256, "q8_0", "f16", 30.0), (128, "q8_0", "tq2", 0.0),
+              (256, "q8_0", "tq4", 0.0), (64, "q8_0", "tq4", 30.0), (512, "f16", "tq2", 0.0)]
 
 
 @pytest.mark.parametrize("d,kf,vf,softcap", MQ_FORMATS)

@@ -75,6 +75,28 @@ def test_tq3_bit_exact(qps, d):
         pytest.fail(f"{bad.size} rows differ; nearest threshold distance {dist:.3e}")
 
 
+@pytest.mark.parametrize("d", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_tq_tier_bit_exact(qps, d, bits):
+    """TQ2 / TQ4 fields and norms equal the oracle's, zero row and zero block included."""
+    x = _rows(2000 + 5, d, 200 + d + bits, outliers=(d != 64))
+    words = synth.sign_bits(d, 42)
+    enc = qps.kv_quant_tq2 if bits == 2 else qps.kv_quant_tq4
+    codes, n = enc(x.cuda(), words)
+    (rc,), rn = otq.encode_tier(x.numpy(), words.numpy(), bits)
+    assert codes.shape == (x.shape[0], d * bits // 8)
+    assert np.array_equal(n.cpu().numpy().view(np.uint16), rn.view(np.uint16))
+    bad = np.nonzero((codes.cpu().numpy() != rc).any(-1))[0]
+    if bad.size:
+        _, thr = otq.codebook(1 << bits)
+        xr = x.numpy()[bad[:4]].astype(np.float64)
+        s = otq.signs_from_words(words.numpy(), d)
+        z = otq.fwht(xr * s) / np.linalg.norm(xr, axis=1, keepdims=True)
+        dist = np.min(np.abs(z[..., None] - thr.astype(np.float64)), axis=-1).min()
+        pytest.fail(f"{bad.size} rows differ; nearest threshold distance {dist:.3e}")
+    assert not codes[3].any() and float(n[3]) == 0.0  # the zero row
+
+
 def test_tq3_sign_vector_changes_codes(qps):
     x = _rows(64, 128, 7, outliers=False).cuda()
     a = qps.kv_quant_tq3(x, synth.sign_bits(128, 42))[0]

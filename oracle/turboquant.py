@@ -50,6 +50,16 @@ magnitude plane:
   * TQ2: a 2-bit plane, field (sign << 1) | m, element i at bits 2 (i % 4) of byte i / 4;
   * TQ4: a 4-bit plane, field (sign << 3) | m, element i at bits 4 (i % 2) of byte i / 2;
 each with one fp16 norm per vector (the pages' 4-bit block is 2 bytes per vector larger).
+
+The rotation has a second form, the one the pages' fork runs (sections "S2 perf-path
+Level B" and the head_dim-512 note after it: the Walsh-Hadamard transform is
+block-diagonal over 128-wide blocks, with a sign vector before and another after it):
+R = diag(s2) blockdiag(H_G) diag(s1) / sqrt(G) for a block width G dividing D.  The
+first form is G = D with s2 = 1.  A ``Rotation(signs1, signs2, block)`` stands wherever
+sign words are accepted.  Encoder order: u = FWHT stages h = 1 .. G/2 of s1 .* x (fp32),
+then u = s2 .* u (exact), then z = fp32(fp32(u * kappa) / n) with kappa = the float32
+square root of D / G (1 when G = D, which leaves the first form unchanged).  Decode:
+x_hat = n * s1 .* blockdiag(H_G) (s2 .* c[k]) / sqrt(D G).
 """
 
 from __future__ import annotations
@@ -116,6 +126,27 @@ def codebook(levels: int = LEVELS):
     return levels, thresholds
 
 
+class Rotation:
+    """The transform's parameters: sign words s1 (D/32 words), optional second sign
+    words s2 (None: all +1) and the Hadamard block width (None: head_dim)."""
+
+    def __init__(self, signs1, signs2=None, block=None):
+        self.signs1 = signs1
+        self.signs2 = signs2
+        self.block = block
+
+
+def _rotation(sign_words, d: int):
+    """(s1, s2 or None, G) as float64 sign vectors and the block width."""
+    if isinstance(sign_words, Rotation):
+        g = d if sign_words.block is None else int(sign_words.block)
+        if g < 32 or g > d or d % g or g & (g - 1):
+            raise ValueError("block must be a power of two in [32, head_dim]")
+        s2 = None if sign_words.signs2 is None else signs_from_words(sign_words.signs2, d)
+        return signs_from_words(sign_words.signs1, d), s2, g
+    return signs_from_words(sign_words, d), None, d
+
+
 def signs_from_words(words, d: int) -> np.ndarray:
     """Unpack the sign diagonal: bit i of word i // 32 set means s_i = -1 (float64)."""
     w = [int(x) & 0xFFFFFFFF for x in np.asarray(words).reshape(-1).tolist()]
@@ -126,19 +157,21 @@ def signs_from_words(words, d: int) -> np.ndarray:
     return s
 
 
-def fwht(x: np.ndarray, dtype=np.float64) -> np.ndarray:
+def fwht(x: np.ndarray, dtype=np.float64, block=None) -> np.ndarray:
     """Unnormalised fast Walsh-Hadamard transform over the last axis.
 
     Stages h = 1, 2, 4, ..., D/2; at each stage every pair (i, i + h) with i & h == 0
-    becomes (a + b, a - b), each result rounded to ``dtype``.
+    becomes (a + b, a - b), each result rounded to ``dtype``.  With ``block`` = G the
+    stages stop at G/2: an independent transform of each G-wide block.
     """
     y = np.array(x, dtype=dtype, copy=True)
     d = y.shape[-1]
     if d & (d - 1):
         raise ValueError("length must be a power of two")
+    g = d if block is None else block
     lead = y.shape[:-1]
     h = 1
-    while h < d:
+    while h < g:
         z = y.reshape(lead + (d // (2 * h), 2, h))
         a = z[..., 0, :]
         b = z[..., 1, :]
@@ -169,13 +202,16 @@ def level_index(x: np.ndarray, sign_words, levels: int = LEVELS):
     if d % 32 or d & (d - 1):
         raise ValueError("head_dim must be a power of two and a multiple of 32")
     _, thresholds = codebook(levels)
-    s = signs_from_words(sign_words, d).astype(np.float32)
+    s1, s2, g = _rotation(sign_words, d)
     x32 = x.astype(np.float32)
     nsq = _fold_sum_sq_f32(x32)
     n = np.sqrt(nsq).astype(np.float32)  # correctly rounded
-    u = fwht((x32 * s).astype(np.float32), dtype=np.float32)
+    u = fwht((x32 * s1.astype(np.float32)).astype(np.float32), dtype=np.float32, block=g)
+    if s2 is not None:
+        u = (u * s2.astype(np.float32)).astype(np.float32)
+    kappa = np.sqrt(np.float32(d // g), dtype=np.float32)  # correctly rounded; 1 when g = d
     with np.errstate(divide="ignore", invalid="ignore"):
-        z = (u / n[..., None]).astype(np.float32)
+        z = ((u * kappa).astype(np.float32) / n[..., None]).astype(np.float32)
     k = np.zeros(z.shape, dtype=np.int64)
     for t in thresholds:
         k += (z >= t).astype(np.int64)
@@ -228,12 +264,15 @@ def codes_from_tier_planes(planes, d: int, bits: int) -> np.ndarray:
 
 
 def decode_tier(planes, norms, sign_words, d: int, bits: int) -> np.ndarray:
-    """Dequantise a tier to float64: x_hat = (n16 / D) * s * (H c[k])."""
+    """Dequantise a tier to float64: x_hat = n16 * s1 .* blockdiag(H_G)(s2 .* c[k]) /
+    sqrt(D G), which is (n16 / D) * s .* (H c[k]) for the first form."""
     levels, _ = codebook(1 << bits)
     ck = levels.astype(np.float64)[codes_from_tier_planes(planes, d, bits)]
-    s = signs_from_words(sign_words, d)
+    s1, s2, g = _rotation(sign_words, d)
+    if s2 is not None:
+        ck = ck * s2
     n = np.asarray(norms).astype(np.float64)[..., None]
-    return (n / d) * s * fwht(ck, dtype=np.float64)
+    return (n / np.sqrt(float(d) * g)) * s1 * fwht(ck, dtype=np.float64, block=g)
 
 
 def encode(x: np.ndarray, sign_words):
@@ -271,14 +310,8 @@ def codes_from_planes(lo2: np.ndarray, hi1: np.ndarray, d: int) -> np.ndarray:
 
 
 def decode(lo2, hi1, norms, sign_words, d: int) -> np.ndarray:
-    """Dequantise to float64: x_hat = (n16 / D) * s * (H c[k])."""
-    levels, _ = codebook()
-    k = codes_from_planes(lo2, hi1, d)
-    ck = levels.astype(np.float64)[k]
-    s = signs_from_words(sign_words, d)
-    hc = fwht(ck, dtype=np.float64)
-    n = np.asarray(norms).astype(np.float64)[..., None]
-    return (n / d) * s * hc
+    """Dequantise TQ3 to float64 (see ``decode_tier``)."""
+    return decode_tier((lo2, hi1), norms, sign_words, d, 3)
 
 
 def bytes_per_value(d: int, bits: int = 3) -> float:

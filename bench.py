@@ -82,6 +82,12 @@ def cpu_model() -> str:
 # ---------------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline leg)
 # ---------------------------------------------------------------------------------
+def _lib_signs(qps, synth, cfg):
+    """The workload's TurboQuant sign words, or its Rotation, for the library."""
+    w1, w2, block = synth.rotation_words(cfg)
+    return w1 if w2 is None and block == 0 else qps.Rotation(w1, w2, block)
+
+
 def time_oracle(cfg, n_layers: int):
     """Time the oracle's layer computation on ``n_layers`` layers of ``cfg`` (CPU).
 
@@ -92,7 +98,10 @@ def time_oracle(cfg, n_layers: int):
     import synth
     from oracle import pipeline
 
-    signs = synth.sign_bits(cfg.d, cfg.sign_seed).numpy()
+    from oracle import turboquant
+    w1, w2, block = synth.rotation_words(cfg)
+    signs = w1.numpy() if w2 is None and block == 0 else turboquant.Rotation(
+        w1.numpy(), None if w2 is None else w2.numpy(), block or None)
     nbytes = 0
     elapsed = 0.0
     for layer in range(n_layers):
@@ -297,7 +306,7 @@ def run_ours(args):
         cfg = cfg.replace(layers=min(args.layers, cfg.layers))
     if cfg.kind != "split":
         raise SystemExit("bench.py times the position-split workloads")
-    signs = synth.sign_bits(cfg.d, cfg.sign_seed)
+    signs = _lib_signs(qps, synth, cfg)
     ring_plan = None
     if args.auto_ring:
         from quantized_position_split_gb300 import autosize
@@ -521,7 +530,7 @@ def run_kernel_only(args):
         if args.v_fmt:
             cfg = cfg.replace(v_fmt=args.v_fmt)
             name = f"{name} V={args.v_fmt}"
-        signs = synth.sign_bits(cfg.d, cfg.sign_seed)
+        signs = _lib_signs(qps, synth, cfg)
         if cfg.kind == "split":
             q = synth.query_f16(cfg, 0, device=dev)
             k = synth.kv_f16(cfg, 0, "k", cfg.wc, device=dev)

@@ -78,7 +78,7 @@
 extern "C" {
 #endif
 
-#define QPS_ABI_VERSION 2
+#define QPS_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define QPS_API __attribute__((visibility("default")))
@@ -167,6 +167,21 @@ QPS_API qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int6
  *   norms   device, fp16 [rows]; 2-byte aligned (so is x).
  * D in {32, 64, 128, 256, 512}.  rows == 0 is a no-op.
  * Errors: INVALID_ARG, UNSUPPORTED (D), CUDA. */
+/* TurboQuant encode at any tier and with either rotation form [POLY, "S2 —
+ * TurboQuant tier family", "S2 perf-path Level B"]: R = diag(s2) blockdiag(H_G)
+ * diag(s1) / sqrt(G).  Per row, in IEEE float32 with a fixed order: the norm as for
+ * TQ3; u = FWHT stages h = 1 .. G/2 of s1 .* x; u = s2 .* u; z = (u * kappa) / n with
+ * kappa = sqrtf(D / G) correctly rounded (1 when G = D); level index = number of
+ * codebook thresholds <= z.  bits = 2, 3, 4 store the planes of QPS_FMT_TQ2 / TQ3 /
+ * TQ4: plane0 = the data plane, plane1 = the TQ3 sign plane (4-byte aligned; NULL for
+ * TQ2 / TQ4), norms = fp16 [rows].  signs1: host, D/32 words; signs2: host, D/32 words
+ * or NULL; block: G (0 = D).  With signs2 = NULL and block = 0 this is
+ * qps_kv_quant_tq2 / tq3 / tq4.  Errors: INVALID_ARG, UNSUPPORTED (D, bits), CUDA. */
+QPS_API qps_status qps_kv_quant_tq_rot(int32_t bits, const void* x, int64_t rows, int32_t d,
+                               int64_t x_row_stride, const uint32_t* signs1,
+                               const uint32_t* signs2, int32_t block, void* plane0,
+                               void* plane1, void* norms, void* stream);
+
 QPS_API qps_status qps_kv_quant_tq2(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
                             const uint32_t* signs, void* codes, void* norms, void* stream);
 QPS_API qps_status qps_kv_quant_tq4(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
@@ -235,6 +250,15 @@ typedef struct qps_attn_args {
   int32_t n_q;
   int32_t causal;
   int64_t q_pos;
+  /* The TurboQuant V rotation's second form [POLY, "S2 perf-path Level B" and its
+   * head_dim-512 note]: R = diag(s2) blockdiag(H_G) diag(s1) / sqrt(G), s1 = v_signs.
+   * v_signs2: host, D/32 words (bit set: -1) applied after the transform; NULL = none.
+   * v_block: G, a power of two in [32, D] dividing D; 0 = D.  The V cache must have
+   * been encoded with the same rotation (qps_kv_quant_tq_rot).  Zero-initialised
+   * fields keep the first form R = H diag(s1) / sqrt(D). */
+  const uint32_t* v_signs2;
+  int32_t v_block;
+  int32_t reserved1;      /* must be 0 */
 } qps_attn_args;
 
 /* Resolve the split count and the workspace the args need (host only, no launch).

@@ -29,6 +29,7 @@ __all__ = [
     "kv_quant_q8_0",
     "kv_quant_tq3",
     "plane_row_bytes",
+    "Rotation",
     "kv_quant_tq2",
     "kv_quant_tq4",
     "encode_kv",
@@ -62,6 +63,30 @@ def _sign_array(signs):
     words = [int(w) & 0xFFFFFFFF for w in (signs.tolist() if hasattr(signs, "tolist") else signs)]
     arr = (ctypes.c_uint32 * len(words))(*words)
     return arr
+
+
+@dataclasses.dataclass(frozen=True)
+class Rotation:
+    """A TurboQuant rotation R = diag(s2) blockdiag(H_block) diag(s1) / sqrt(block):
+    sign words ``signs1`` (D/32), optional ``signs2`` and the Hadamard block width
+    (0 = head_dim).  Accepted wherever TurboQuant sign words are; plain sign words mean
+    ``Rotation(signs)``."""
+
+    signs1: object
+    signs2: object = None
+    block: int = 0
+
+
+def _rotation(signs) -> Rotation:
+    return signs if isinstance(signs, Rotation) else Rotation(signs)
+
+
+def _tq_encode_rot(bits: int, x2, rows: int, d: int, stride: int, rot: Rotation, p0, p1, norms, stream):
+    s1 = _sign_array(rot.signs1)
+    s2 = _sign_array(rot.signs2) if rot.signs2 is not None else None
+    N.check(lib().qps_kv_quant_tq_rot(bits, x2.data_ptr(), rows, d, stride, s1, s2, int(rot.block),
+                                      p0.data_ptr(), None if p1 is None else p1.data_ptr(),
+                                      norms.data_ptr(), _stream(stream)))
 
 
 def launch_count(reset: bool = False) -> int:
@@ -127,6 +152,9 @@ def kv_quant_tq3(x: torch.Tensor, signs, lo2=None, hi1=None, norms=None, stream=
         hi1 = torch.empty(x.shape[:-1] + (d // 8,), dtype=torch.uint8, device=x.device)
     if norms is None:
         norms = torch.empty(x.shape[:-1], dtype=torch.float16, device=x.device)
+    if isinstance(signs, Rotation):
+        _tq_encode_rot(3, x2, rows, d, stride, signs, lo2, hi1, norms, stream)
+        return lo2, hi1, norms
     sa = _sign_array(signs)
     N.check(lib().qps_kv_quant_tq3(x2.data_ptr(), rows, d, stride, sa, lo2.data_ptr(),
                                    hi1.data_ptr(), norms.data_ptr(), _stream(stream)))
@@ -140,6 +168,9 @@ def _kv_quant_fields(bits: int, x: torch.Tensor, signs, codes=None, norms=None, 
         codes = torch.empty(x.shape[:-1] + (d * bits // 8,), dtype=torch.uint8, device=x.device)
     if norms is None:
         norms = torch.empty(x.shape[:-1], dtype=torch.float16, device=x.device)
+    if isinstance(signs, Rotation):
+        _tq_encode_rot(bits, x2, rows, d, stride, signs, codes, None, norms, stream)
+        return codes, norms
     sa = _sign_array(signs)
     fn = lib().qps_kv_quant_tq2 if bits == 2 else lib().qps_kv_quant_tq4
     N.check(fn(x2.data_ptr(), rows, d, stride, sa, codes.data_ptr(), norms.data_ptr(), _stream(stream)))
@@ -229,8 +260,9 @@ def attn_args(q: torch.Tensor, k: KV, v: KV, *, scale: float, softcap: float = 0
     A 4-D ``q[batch, n_q, hq, D]`` asks for multi-query (verify-batch) decode: n_q
     query tokens per batch entry, output rows ordered (batch, token, head).  With
     ``q_pos``, query token i sees only the positions <= q_pos + i (causal).
-    ``shared`` makes every batch entry read the same KV rows (batch_stride 0).  The
-    returned struct keeps a reference to the sign array it points to.
+    ``shared`` makes every batch entry read the same KV rows (batch_stride 0).
+    ``v_signs``: a TurboQuant V's sign words or ``Rotation``.  The returned struct keeps
+    a reference to the sign arrays it points to.
     """
     if q.dtype != torch.float16 or q.dim() not in (3, 4):
         raise QpsError(N.QPS_ERR_INVALID_ARG, "q must be float16 [batch, hq, D] or [batch, n_q, hq, D]")
@@ -258,9 +290,16 @@ def attn_args(q: torch.Tensor, k: KV, v: KV, *, scale: float, softcap: float = 0
     a.scale = scale
     a.softcap = softcap
     if v_signs is not None:
-        arr = _sign_array(v_signs)
+        rot = _rotation(v_signs)
+        arr = _sign_array(rot.signs1)
         a.v_signs = ctypes.cast(arr, ctypes.POINTER(ctypes.c_uint32))
-        a._keep = arr
+        keep = [arr]
+        if rot.signs2 is not None:
+            arr2 = _sign_array(rot.signs2)
+            a.v_signs2 = ctypes.cast(arr2, ctypes.POINTER(ctypes.c_uint32))
+            keep.append(arr2)
+        a.v_block = int(rot.block)
+        a._keep = keep
     a.n_split = n_split
     return a
 

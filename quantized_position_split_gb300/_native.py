@@ -74,6 +74,9 @@ class AttnArgs(ctypes.Structure):
         ("n_q", c_int32),
         ("causal", c_int32),
         ("q_pos", c_int64),
+        ("v_signs2", POINTER(c_uint32)),
+        ("v_block", c_int32),
+        ("reserved1", c_int32),
     ]
 
 
@@ -116,6 +119,9 @@ SIGNATURES = [
     ("qps_kv_quant_q8_0", c_int32, [c_void_p, c_int64, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
     ("qps_kv_quant_tq3", c_int32,
      [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p, c_void_p]),
+    ("qps_kv_quant_tq_rot", c_int32,
+     [c_int32, c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), POINTER(c_uint32), c_int32, c_void_p,
+      c_void_p, c_void_p, c_void_p]),
     ("qps_kv_quant_tq2", c_int32,
      [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p]),
     ("qps_kv_quant_tq4", c_int32,

@@ -190,15 +190,14 @@ qps_status check_view(const qps_kv_view& v, const char* name, bool allow_tq) {
   return QPS_OK;
 }
 
-// Split count: enough CTAs for one full wave (two resident per SM), but no chunk
-// shorter than 512 positions, so each partial amortises its merge and the combine
-// reads few parts.
-// Enough chunks for two CTAs per SM (one wave), each chunk at least 512 positions, or
-// 256 when 512-position chunks would leave SMs without a CTA (a short tail tile).
-int auto_split(int64_t ntok, int ctas_per_split) {
+// Split count: enough chunks for one full wave (ctas_per_sm resident CTAs on every SM),
+// each chunk at least 512 positions, so each partial amortises its merge and the
+// combine reads few parts, or 256 when 512-position chunks would leave SMs without a
+// CTA (a short tail tile).
+int auto_split(int64_t ntok, int ctas_per_split, int ctas_per_sm) {
   const int sms = sm_count_current();
   if (sms <= 0) return -1;
-  const int64_t target = 2LL * sms;
+  const int64_t target = (int64_t)ctas_per_sm * sms;
   const int64_t by_occupancy = (target + ctas_per_split - 1) / ctas_per_split;
   int64_t n = std::min(by_occupancy, (ntok + 511) / 512);
   if (n * ctas_per_split < sms) n = std::min(by_occupancy, (ntok + 255) / 256);
@@ -234,6 +233,10 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
     return fail(QPS_ERR_INVALID_ARG, "attention: scale and softcap must be finite");
   if (is_tq(a->v.fmt) && !a->v_signs)
     return fail(QPS_ERR_INVALID_ARG, "attention: v_signs is required for a TurboQuant V");
+  if (a->reserved1 != 0) return fail(QPS_ERR_INVALID_ARG, "attention: reserved1 must be 0");
+  const int vblock = a->v_block == 0 ? a->d : a->v_block;
+  if (vblock < 32 || vblock > a->d || (vblock & (vblock - 1)))
+    return fail(QPS_ERR_INVALID_ARG, "attention: v_block must be 0 or a power of two in [32, head_dim]");
   if (a->n_split < 0) return fail(QPS_ERR_INVALID_ARG, "attention: n_split must be >= 0");
   const bool shared = a->k.batch_stride == 0 && a->batch > 1;
   if (shared && n_q > 1)
@@ -247,7 +250,7 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   const int ctas_per_split = a->hkv * (shared ? 1 : a->batch) * ((rows_per_cta + tile_rows - 1) / tile_rows);
   int n_split = a->n_split;
   if (n_split == 0) {
-    n_split = auto_split(ntok, ctas_per_split);
+    n_split = auto_split(ntok, ctas_per_split, mma_ctas_per_sm(a->d, tile_rows / 8, a->v.fmt));
     if (n_split < 0) return fail(QPS_ERR_CUDA, "attention: cannot query the current device's SM count");
   }
   if (n_split > 65535) return fail(QPS_ERR_INVALID_ARG, "attention: n_split must be <= 65535");
@@ -281,8 +284,12 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   p->q_pos = a->q_pos;
   p->rows_per_cta = rows_per_cta;
   p->rows_total = rows_total;
+  p->vblock = vblock;
+  p->v_out_scale = (float)(1.0 / std::sqrt((double)a->d * (double)vblock));
   if (is_tq(a->v.fmt)) {
     for (int i = 0; i < a->d / 32; ++i) p->vsigns[i] = a->v_signs[i];
+    if (a->v_signs2)
+      for (int i = 0; i < a->d / 32; ++i) p->vsigns2[i] = a->v_signs2[i];
     const Codebook* cb = tq_codebook(tq_bits(a->v.fmt));
     for (int i = 0; i < cb->n; ++i) p->tq_levels[i] = cb->levels[i];
   }
@@ -445,8 +452,28 @@ qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int64_t x_ro
   if (!lo2 || !hi1 || !norms) return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq3: an output plane is NULL");
   if (!aligned(x, 2) || !aligned(hi1, 4) || !aligned(norms, 2))
     return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq3: x / norms must be 2-byte and hi1 4-byte aligned");
-  return launch_quant_tq(3, reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs,
+  return launch_quant_tq(3, reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs, nullptr, d,
                          reinterpret_cast<uint8_t*>(lo2), reinterpret_cast<uint8_t*>(hi1),
+                         reinterpret_cast<__half*>(norms), reinterpret_cast<cudaStream_t>(stream));
+}
+
+qps_status qps_kv_quant_tq_rot(int32_t bits, const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                               const uint32_t* signs1, const uint32_t* signs2, int32_t block, void* plane0,
+                               void* plane1, void* norms, void* stream) {
+  if (bits < 2 || bits > 4) return fail(QPS_ERR_UNSUPPORTED, "kv_quant_tq_rot: bits must be 2, 3 or 4");
+  qps_status st = check_encoder(x, rows, d, x_row_stride, "kv_quant_tq_rot");
+  if (st != QPS_OK) return st;
+  if (!signs1) return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq_rot: signs1 is NULL");
+  const int g = block == 0 ? d : block;
+  if (g < 32 || g > d || (g & (g - 1)))
+    return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq_rot: block must be 0 or a power of two in [32, head_dim]");
+  if (rows == 0) return QPS_OK;
+  if (!plane0 || !norms || (bits == 3 && !plane1))
+    return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq_rot: an output plane is NULL");
+  if (!aligned(x, 2) || !aligned(norms, 2) || (bits == 3 && !aligned(plane1, 4)))
+    return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq_rot: x / norms must be 2-byte and plane1 4-byte aligned");
+  return launch_quant_tq(bits, reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs1, signs2, g,
+                         reinterpret_cast<uint8_t*>(plane0), bits == 3 ? reinterpret_cast<uint8_t*>(plane1) : nullptr,
                          reinterpret_cast<__half*>(norms), reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -462,7 +489,7 @@ static qps_status kv_quant_tq_fields(int bits, const char* name, const void* x, 
   if (!codes || !norms) return fail(QPS_ERR_INVALID_ARG, n + ": an output plane is NULL");
   if (!aligned(x, 2) || !aligned(norms, 2))
     return fail(QPS_ERR_INVALID_ARG, n + ": x / norms must be 2-byte aligned");
-  return launch_quant_tq(bits, reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs,
+  return launch_quant_tq(bits, reinterpret_cast<const __half*>(x), rows, d, x_row_stride, signs, nullptr, d,
                          reinterpret_cast<uint8_t*>(codes), nullptr, reinterpret_cast<__half*>(norms),
                          reinterpret_cast<cudaStream_t>(stream));
 }

@@ -139,8 +139,13 @@ struct PlaneG {
   static constexpr int BYTES = TT * RB;
 };
 
-template <int D, int KF, int VF, int TT_>
+// Stage bytes of one CTA when CTAS CTAs share an SM's 228 KB (less 1 KB reserved per
+// CTA, the barriers and the 1024-byte alignment slack).
+__host__ __device__ constexpr int stage_budget(int ctas) { return ctas >= 3 ? 74 * 1024 : 104 * 1024; }
+
+template <int D, int KF, int VF, int TT_, int CTAS_>
 struct GeoT {
+  static constexpr int CTAS = CTAS_;
   static constexpr int K_RB = KF == QPS_FMT_F16 ? 2 * D : D;          // K data bytes / token
   static constexpr int K_ARB = KF == QPS_FMT_Q8_0 ? D / 16 : 0;       // K scales bytes / token
   // V data: fp16 values, q8_0 codes, TQ2 / TQ3 2-bit fields or TQ4 4-bit fields; V aux:
@@ -171,8 +176,8 @@ struct GeoT {
   static constexpr int ARRIVALS = 1 + (SMALL ? 32 : 0);  // expect_tx + one per lane's cp.async
   // warps per CTA: 4, or 2 when two stages of 4 warps would not fit in shared memory
   static constexpr int NW = 4 * 2 * STAGE <= 200 * 1024 ? 4 : 2;
-  // ~104 KB of stages per CTA: two CTAs (8 warps) per SM within its 228 KB
-  static constexpr int STAGES_RAW = (104 * 1024) / (NW * STAGE);
+  // the stage budget of CTAS CTAs per SM
+  static constexpr int STAGES_RAW = stage_budget(CTAS) / (NW * STAGE);
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 6 ? 6 : STAGES_RAW);
   static constexpr int PIPE = NW * STAGES * STAGE;
   static constexpr int BARS = PIPE;                   // mbarriers after the stages
@@ -181,13 +186,13 @@ struct GeoT {
 
 // Tokens per stage: two 16-token MMA sub-tiles (independent chains for latency hiding,
 // one softmax update per 32 tokens) where registers allow (head_dim <= 128) and 4 warps
-// x 2 stages of 32 tokens still leave room for two CTAs per SM; else one.
-template <int D, int KF, int VF>
+// x 2 stages of 32 tokens still fit the stage budget; else one.
+template <int D, int KF, int VF, int CTAS>
 constexpr int stage_tokens() {
-  return (D <= 128 && 4 * 2 * GeoT<D, KF, VF, 32>::STAGE <= 104 * 1024) ? 32 : 16;
+  return (D <= 128 && 4 * 2 * GeoT<D, KF, VF, 32, CTAS>::STAGE <= stage_budget(CTAS)) ? 32 : 16;
 }
-template <int D, int KF, int VF>
-struct Geo : GeoT<D, KF, VF, stage_tokens<D, KF, VF>()> {};
+template <int D, int KF, int VF, int NTW>
+struct Geo : GeoT<D, KF, VF, stage_tokens<D, KF, VF, mma_ctas_per_sm(D, NTW, VF)>(), mma_ctas_per_sm(D, NTW, VF)> {};
 
 // Tensor maps of one launch, one per tensor-map plane (unused ones left empty).
 struct TmaSet {
@@ -273,9 +278,9 @@ __host__ __device__ constexpr int tq_col(int i, int hh) {
 // CAUSAL: the verify batch's causal limit (a separate instance, so that single-token
 // decode compiles without it).
 template <int D, int KF, int VF, int NTW, bool CAUSAL>
-__global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
+__global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, NTW>::CTAS)
     attn_mma_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ TmaSet maps) {
-  using G = Geo<D, KF, VF>;
+  using G = Geo<D, KF, VF, NTW>;
   constexpr int kWarps = G::NW;
   constexpr int ROWS = 8 * NTW;  // query rows per CTA
   constexpr int MT = D / 16;     // m-tiles of O^T, k-steps of S^T
@@ -927,13 +932,16 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) acc += ow[(w * ROWS + r) * D + dd] * wgt[w * ROWS + r];
+    if constexpr (is_tq(VF))  // the rotation's second sign vector
+      if ((p.vsigns2[dd >> 5] >> (dd & 31)) & 1u) acc = -acc;
     fin[idx] = acc;
   }
   __syncthreads();
-  if constexpr (is_tq(VF)) {  // inverse rotation x = s .* (H y) / D, in place
+  if constexpr (is_tq(VF)) {  // inverse rotation x = s1 .* blockdiag(H_G)(s2 .* y) / sqrt(D G), in place
 #pragma unroll
     for (int lh = 0; (1 << lh) < D; ++lh) {  // butterflies of span h = 2^lh
       const int h = 1 << lh;
+      if (h >= p.vblock) break;  // (uniform over the CTA)
 #pragma unroll 4
       for (int pid = threadIdx.x; pid < ROWS * (D / 2); pid += G::NW * 32) {
         const int r = pid / (D / 2), j = pid % (D / 2);
@@ -950,7 +958,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
     const float mx = rmx[r], den = rden[r];
     float val = fin[r * D + dd];
     if constexpr (is_tq(VF)) {
-      val *= 1.0f / (float)D;
+      val *= p.v_out_scale;
       if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) val = -val;
     }
     const int64_t row = orow[r];
@@ -963,7 +971,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF>::NW * 32, 2)
 
 template <int D, int KF, int VF, int NTW>
 constexpr size_t smem_bytes() {
-  using G = Geo<D, KF, VF>;
+  using G = Geo<D, KF, VF, NTW>;
   constexpr size_t pipe = (size_t)G::END;
   constexpr int ROWS = 8 * NTW;
   constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D) +
@@ -973,13 +981,14 @@ constexpr size_t smem_bytes() {
 
 template <int D, int KF, int VF, int NTW, bool CAUSAL>
 qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
-  using G = Geo<D, KF, VF>;
+  using G = Geo<D, KF, VF, NTW>;
   constexpr size_t smem = smem_bytes<D, KF, VF, NTW>();
   static_assert(smem <= 227 * 1024, "tile staging exceeds the 227 KB shared memory of one CTA");
-  // two CTAs per SM (the launch bound the registers are sized for: 228 KB less 1 KB
-  // reserved per CTA), unless the stages are already at their minimum of two (fp16
+  // G::CTAS CTAs per SM (the launch bound the registers are sized for: 228 KB less 1 KB
+  // reserved per CTA), unless two-CTA stages are already at their minimum of two (fp16
   // planes at head_dim >= 256, which then run one CTA per SM)
-  static_assert(2 * (smem + 1024) <= 228 * 1024 || G::STAGES == 2, "two CTAs per SM no longer fit");
+  static_assert(G::CTAS * (smem + 1024) <= 228 * 1024 || (G::CTAS == 2 && G::STAGES == 2),
+                "the CTAs per SM the instance is built for no longer fit");
   // tensor maps over each plane as [row bytes][tokens < kv_end][KV heads][batch]
   TmaSet maps;
   std::memset(&maps, 0, sizeof(maps));

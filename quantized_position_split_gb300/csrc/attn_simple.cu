@@ -213,13 +213,15 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
           if (mw != -INFINITY) acc += os[(w * RC + r) * D + dd] * __expf(mw - mx);
         }
       }
+      if constexpr (is_tq(VF))  // the rotation's second sign vector
+        if ((p.vsigns2[dd >> 5] >> (dd & 31)) & 1u) acc = -acc;
       qs[r * D + dd] = acc;  // the query rows are no longer needed
     }
     __syncthreads();
 
     if constexpr (is_tq(VF)) {
-      // inverse rotation of the accumulated rows: x = s .* (H y) / D
-      for (int h = 1; h < D; h *= 2) {
+      // inverse rotation of the accumulated rows: x = s1 .* blockdiag(H_G)(s2 .* y) / sqrt(D G)
+      for (int h = 1; h < p.vblock; h *= 2) {
         for (int pid = threadIdx.x; pid < nr * (D / 2); pid += blockDim.x) {
           const int r = pid / (D / 2), j = pid % (D / 2);
           const int i = (j / h) * 2 * h + (j % h);
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
       }
       float val = qs[r * D + dd];
       if constexpr (is_tq(VF)) {
-        val *= 1.0f / (float)D;
+        val *= p.v_out_scale;
         if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) val = -val;
       }
       const int rr = rc0 + r;

@@ -105,7 +105,10 @@ struct AttnParams {
   float* lse_parts;
   int part_offset;
   unsigned int* err;  // device word set non-zero when a bounded in-kernel wait gives up
-  uint32_t vsigns[kMaxSignWords];
+  uint32_t vsigns[kMaxSignWords];   // V rotation: s1
+  uint32_t vsigns2[kMaxSignWords];  // s2 (all 0: none)
+  int vblock;                       // Hadamard block width G (a power of two, <= d)
+  float v_out_scale;                // 1 / sqrt(d * G)
   float tq_levels[16];  // the V tier's codebook (ascending)
 };
 
@@ -118,6 +121,15 @@ inline int mma_tile_rows(int d, int rows_per_cta, bool shared) {
   return (rows_per_cta <= 16 || shared) ? 16 : 24;
 }
 
+// CTAs per SM a tensor-core instance is built for (its register cap and stage budget):
+// three for a TurboQuant V, whose decode chains leave the kernel latency-bound with 8
+// warps per SM, where the accumulators leave registers for 12 warps (head_dim 64 with
+// up to two n-tiles, 128 with one); else two (more CTAs did not help the fp16 / q8_0
+// kernels, which are bound by HBM).
+__host__ __device__ constexpr int mma_ctas_per_sm(int d, int ntw, int vfmt) {
+  return (is_tq(vfmt) && ((d <= 64 && ntw <= 2) || (d == 128 && ntw == 1))) ? 3 : 2;
+}
+
 // Validated, resolved form of qps_attn_args.
 qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split, size_t* ws_bytes);
 qps_status launch_attn(const AttnParams& p, cudaStream_t stream);
@@ -128,9 +140,10 @@ qps_status run_attn(const qps_attn_args* a, const AttnParams& p, int n_split, cu
 
 qps_status launch_quant_q8_0(const __half* x, int64_t rows, int d, int64_t stride,
                              int8_t* codes, __half* scales, cudaStream_t s);
-// TurboQuant encode at `bits` = 2, 3 or 4; plane1 is the TQ3 sign plane (unused otherwise)
+// TurboQuant encode at `bits` = 2, 3 or 4 with rotation diag(s2) blockdiag(H_block)
+// diag(s1) (signs2 NULL: none); plane1 is the TQ3 sign plane (unused otherwise)
 qps_status launch_quant_tq(int bits, const __half* x, int64_t rows, int d, int64_t stride,
-                           const uint32_t* signs, uint8_t* plane0, uint8_t* plane1, __half* norms,
-                           cudaStream_t s);
+                           const uint32_t* signs, const uint32_t* signs2, int block, uint8_t* plane0,
+                           uint8_t* plane1, __half* norms, cudaStream_t s);
 
 }  // namespace qps

@@ -11,6 +11,8 @@
 // The encoders are bit-exact contracts: every floating-point step is an explicitly
 // rounded IEEE float32 operation (__fmul_rn / __fadd_rn / __fdiv_rn / __fsqrt_rn) in a
 // fixed order, so that no contraction into FMA can change a code.
+#include <cmath>
+
 #include "internal.h"
 
 namespace qps {
@@ -68,12 +70,16 @@ __global__ void __launch_bounds__(256) quant_q8_0_kernel(const __half* __restric
 }
 
 struct TqConsts {
-  uint32_t signs[kMaxSignWords];
+  uint32_t signs[kMaxSignWords];   // s1
+  uint32_t signs2[kMaxSignWords];  // s2 (all 0: none)
   float thresholds[15];
+  float kappa;  // sqrtf(D / G), correctly rounded
+  int hreg;     // register FWHT stages run for H < hreg (= G / 32)
 };
 
 // One warp per row.  Lane L holds elements L + 32 e, e < D / 32, so the FWHT stages
-// h < 32 are lane shuffles and the stages h >= 32 stay inside a lane's registers.
+// h < 32 are lane shuffles and the stages 32 <= h < G stay inside a lane's registers
+// (stage h = 32 H pairs registers e and e + H).
 // BITS = 3: plane0 = magnitudes (2 bits), plane1 = signs (1 bit); BITS = 2 / 4: plane0 =
 // (sign << (BITS - 1)) | magnitude fields, plane1 unused.
 template <int D, int BITS>
@@ -126,6 +132,7 @@ __global__ void __launch_bounds__(256) quant_tq_kernel(const __half* __restrict_
     }
 #pragma unroll
     for (int H = 1; H < E; H *= 2) {
+      if (H >= c.hreg) break;  // the block width ends the transform
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         if ((e & H) == 0) {
@@ -134,6 +141,12 @@ __global__ void __launch_bounds__(256) quant_tq_kernel(const __half* __restrict_
           u[e + H] = __fsub_rn(a, b);
         }
       }
+    }
+    // the second sign vector and the block scale (kappa = 1 for G = D: exact)
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float v2 = ((c.signs2[e] >> lane) & 1u) ? -u[e] : u[e];
+      u[e] = __fmul_rn(v2, c.kappa);
     }
 
     // level index k (a zero row takes k = HALF - 1: sign 0, magnitude 0), then its
@@ -206,8 +219,8 @@ qps_status launch_quant_q8_0(const __half* x, int64_t rows, int d, int64_t strid
 }
 
 qps_status launch_quant_tq(int bits, const __half* x, int64_t rows, int d, int64_t stride,
-                           const uint32_t* signs, uint8_t* plane0, uint8_t* plane1, __half* norms,
-                           cudaStream_t s) {
+                           const uint32_t* signs, const uint32_t* signs2, int block, uint8_t* plane0,
+                           uint8_t* plane1, __half* norms, cudaStream_t s) {
   if (rows == 0) return QPS_OK;
   const Codebook* cb = tq_codebook(bits);
   if (!cb) return fail(QPS_ERR_UNSUPPORTED, "kv_quant_tq: bits must be 2, 3 or 4");
@@ -215,12 +228,18 @@ qps_status launch_quant_tq(int bits, const __half* x, int64_t rows, int d, int64
     return fail(QPS_ERR_UNSUPPORTED, "kv_quant_tq: head_dim must be 32, 64, 128, 256 or 512");
   TqConsts c{};
   for (int i = 0; i < d / 32; ++i) c.signs[i] = signs[i];
+  if (signs2)
+    for (int i = 0; i < d / 32; ++i) c.signs2[i] = signs2[i];
   for (int i = 0; i < cb->n - 1; ++i) c.thresholds[i] = cb->thresholds[i];
-  const int block = 256;
-  const int grid = grid_for(rows * 32, block);
-  if (bits == 2) launch_quant_tq_bits<2>(d, grid, block, s, x, rows, stride, c, plane0, plane1, norms);
-  else if (bits == 3) launch_quant_tq_bits<3>(d, grid, block, s, x, rows, stride, c, plane0, plane1, norms);
-  else launch_quant_tq_bits<4>(d, grid, block, s, x, rows, stride, c, plane0, plane1, norms);
+  if (block < 32 || block > d || (block & (block - 1)))
+    return fail(QPS_ERR_INVALID_ARG, "kv_quant_tq: block must be a power of two in [32, head_dim]");
+  c.kappa = std::sqrt((float)(d / block));  // IEEE square root: correctly rounded
+  c.hreg = block / 32;
+  const int threads = 256;
+  const int grid = grid_for(rows * 32, threads);
+  if (bits == 2) launch_quant_tq_bits<2>(d, grid, threads, s, x, rows, stride, c, plane0, plane1, norms);
+  else if (bits == 3) launch_quant_tq_bits<3>(d, grid, threads, s, x, rows, stride, c, plane0, plane1, norms);
+  else launch_quant_tq_bits<4>(d, grid, threads, s, x, rows, stride, c, plane0, plane1, norms);
   count_launch();
   QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;

@@ -23,6 +23,7 @@ from .gen import (
     outlier_channels,
     kv_f16,
     query_f16,
+    rotation_words,
     sign_bits,
 )
 
@@ -36,5 +37,6 @@ __all__ = [
     "outlier_channels",
     "kv_f16",
     "query_f16",
+    "rotation_words",
     "sign_bits",
 ]

@@ -33,6 +33,8 @@ class Workload:
     agents: int = 0  # fanout: number of agents sharing the prefix
     suffix_len: int = 0  # fanout: private fp16 suffix per agent
     sign_seed: int = 42
+    sign_seed2: Optional[int] = None  # TurboQuant second sign vector (None: none)
+    rot_block: int = 0  # TurboQuant Hadamard block width (0: head_dim)
     seed: int = 1234
 
     @property
@@ -184,6 +186,27 @@ CONFIGS = [
         k_outliers=4,
         ring_slots=3,
         tile_tokens=8192,
+    ),
+    # the Gemma-like global layers with the rotation the pages' fork runs at head_dim 512:
+    # four independent 128-wide Hadamard blocks between two sign vectors
+    Workload(
+        name="gemma_global_q8k_tq3v_r128",
+        kind="split",
+        layers=5,
+        batch=1,
+        hq=16,
+        hkv=2,
+        d=512,
+        n_kv=262144,
+        wc=131072,
+        k_fmt="q8_0",
+        v_fmt="tq3",
+        softcap=50.0,
+        k_outliers=4,
+        ring_slots=3,
+        tile_tokens=16384,
+        sign_seed2=43,
+        rot_block=128,
     ),
     Workload(
         name="fanout_prefix",

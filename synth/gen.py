@@ -71,6 +71,13 @@ def query_f16(cfg, layer: int, device="cpu", tag: str = "") -> torch.Tensor:
                      device=device)
 
 
+def rotation_words(cfg):
+    """A workload's TurboQuant rotation inputs: (sign words s1, sign words s2 or None,
+    Hadamard block width, 0 = head_dim)."""
+    w2 = None if cfg.sign_seed2 is None else sign_bits(cfg.d, cfg.sign_seed2)
+    return sign_bits(cfg.d, cfg.sign_seed), w2, cfg.rot_block
+
+
 def sign_bits(d: int, seed: int = 42) -> torch.Tensor:
     """The seeded sign diagonal as d/32 uint32 words (int64 tensor holding the words).
 

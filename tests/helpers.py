@@ -35,7 +35,21 @@ def assert_parity(o_gpu, lse_gpu, o_ref, lse_ref, tag=""):
 
 
 def signs_for(cfg):
-    return synth.sign_bits(cfg.d, cfg.sign_seed)
+    """The workload's TurboQuant sign words, or its Rotation, for the library."""
+    w1, w2, block = synth.rotation_words(cfg)
+    if w2 is None and block == 0:
+        return w1
+    import quantized_position_split_gb300 as qps
+    return qps.Rotation(w1, w2, block)
+
+
+def oracle_signs(cfg):
+    """The same rotation for the oracle."""
+    from oracle import turboquant
+    w1, w2, block = synth.rotation_words(cfg)
+    if w2 is None and block == 0:
+        return w1.numpy()
+    return turboquant.Rotation(w1.numpy(), None if w2 is None else w2.numpy(), block or None)
 
 
 def layer_inputs(cfg, layer, device):
@@ -49,10 +63,10 @@ def oracle_layer(cfg, q, k, v):
     if cfg.mixed:
         return pipeline.mixed_layer_reference(q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy(), cfg.wc,
                                               cfg.k_fmt, cfg.v_fmt, cfg.tk_fmt, cfg.tv_fmt, cfg.scale,
-                                              cfg.softcap, signs_for(cfg).numpy())
+                                              cfg.softcap, oracle_signs(cfg))
     return pipeline.layer_reference(q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy(),
                                     cfg.k_fmt, cfg.v_fmt, cfg.scale, cfg.softcap,
-                                    signs_for(cfg).numpy())
+                                    oracle_signs(cfg))
 
 
 def build_split_decoder(cfg, device="cuda", keep_inputs=(), **kw):
@@ -92,7 +106,7 @@ def fanout_inputs(cfg, device):
 def oracle_fanout(cfg, q, pk, pv, sk, sv):
     c = lambda t: t.cpu().numpy()  # noqa: E731
     return pipeline.fanout_reference(c(q), c(pk), c(pv), c(sk), c(sv), cfg.k_fmt, cfg.v_fmt,
-                                     cfg.scale, cfg.softcap, signs_for(cfg).numpy())
+                                     cfg.scale, cfg.softcap, oracle_signs(cfg))
 
 
 def cuda_ok():

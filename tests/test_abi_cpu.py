@@ -159,6 +159,16 @@ def test_attn_view_validation(lib):
         assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
         a.v.aux = 0  # no norms
         assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
+    for blk in (48, 16, 256):  # not a power of two, below 32, above head_dim 128
+        a = _args()
+        a.v_block = blk
+        assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
+    a = _args()
+    a.reserved1 = 1
+    assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
+    a = _args()
+    a.v_block = 64
+    assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_OK
     a = _args()
     a.v.fmt = 5  # unknown format
     assert lib.qps_attn_plan(ctypes.byref(a), None, None) == N.QPS_ERR_INVALID_ARG
@@ -172,6 +182,11 @@ def test_encoder_and_combine_validation(lib):
     assert lib.qps_kv_quant_q8_0(None, 4, 48, 48, None, None, None) == N.QPS_ERR_UNSUPPORTED
     assert lib.qps_kv_quant_q8_0(None, 0, 128, 128, None, None, None) == N.QPS_OK  # no-op
     assert lib.qps_kv_quant_tq3(None, 4, 128, 128, None, None, None, None, None) == N.QPS_ERR_INVALID_ARG
+    w = (ctypes.c_uint32 * 4)()
+    assert lib.qps_kv_quant_tq_rot(5, None, 4, 128, 128, w, None, 0, None, None, None, None) == N.QPS_ERR_UNSUPPORTED
+    assert lib.qps_kv_quant_tq_rot(3, None, 4, 128, 128, None, None, 0, None, None, None, None) == N.QPS_ERR_INVALID_ARG
+    assert lib.qps_kv_quant_tq_rot(3, None, 0, 128, 128, w, None, 96, None, None, None, None) == N.QPS_ERR_INVALID_ARG
+    assert lib.qps_kv_quant_tq_rot(4, None, 0, 128, 128, w, None, 32, None, None, None, None) == N.QPS_OK  # no-op
     for fn in (lib.qps_kv_quant_tq2, lib.qps_kv_quant_tq4):
         assert fn(None, 4, 128, 128, None, None, None, None) == N.QPS_ERR_INVALID_ARG
         assert fn(None, 4, 96, 96, None, None, None, None) == N.QPS_ERR_UNSUPPORTED

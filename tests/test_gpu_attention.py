@@ -7,6 +7,7 @@ import torch
 import synth
 from oracle import attention as oatt
 from oracle import pipeline
+from oracle import turboquant as otq
 from tests.helpers import assert_parity, parity_report
 
 pytestmark = pytest.mark.gpu
@@ -79,6 +80,33 @@ def test_window_attention_formats(qps, layout, d, kf, vf, softcap):
         o, lse = qps.attn_decode_window(a)
         assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq),
                       (layout, d, kf, vf, softcap, n_split))
+
+
+@pytest.mark.parametrize("layout", ["head", "token"])
+@pytest.mark.parametrize("d,g", [(512, 128), (256, 128), (128, 64)])
+@pytest.mark.parametrize("vf", ["tq2", "tq3", "tq4"])
+def test_window_attention_rotation(qps, layout, d, g, vf):
+    """A V encoded with the block-diagonal two-sign rotation, read back through the
+    attention's inverse transform (its block width and second sign vector)."""
+    hq, hkv, n = 8, 2, 700 + 11
+    q, k, v = _inputs(n, hq, hkv, d, seed=d + g + len(vf), outliers=True)
+    w1, w2 = synth.sign_bits(d, 42), synth.sign_bits(d, 43)
+    rot = qps.Rotation(w1, w2, g)
+    K = _encode(qps, layout, "q8_0", k, None)
+    V = _encode(qps, layout, vf, v, rot)
+    kh = pipeline.dequant("q8_0", k.numpy())
+    vh = pipeline.dequant(vf, v.numpy(), otq.Rotation(w1.numpy(), w2.numpy(), g))
+    ro, rl = oatt.gqa_decode(q.double().numpy(), kh, vh, 1.0 / np.sqrt(d), 30.0)
+    for n_split in (0, 3):
+        a = qps.attn_args(q.cuda(), K, V, scale=1.0 / np.sqrt(d), softcap=30.0, v_signs=rot, n_split=n_split)
+        assert qps.attn_path(a) == LAYOUT_PATH[layout]
+        o, lse = qps.attn_decode_window(a)
+        assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq),
+                      (layout, d, g, vf, n_split))
+    # the same cache read with the first form's transform is a different (wrong) answer
+    a = qps.attn_args(q.cuda(), K, V, scale=1.0 / np.sqrt(d), softcap=30.0, v_signs=w1)
+    o, _ = qps.attn_decode_window(a)
+    assert np.abs(o.cpu().numpy() - ro.reshape(hq, d)).max() > 1e-2
 
 
 @pytest.mark.parametrize("layout", ["head", "token"])

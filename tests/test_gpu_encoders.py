@@ -97,6 +97,19 @@ def test_tq_tier_bit_exact(qps, d, bits):
     assert not codes[3].any() and float(n[3]) == 0.0  # the zero row
 
 
+@pytest.mark.parametrize("d,g", [(512, 128), (256, 128), (128, 32), (64, 64)])
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_tq_rotation_bit_exact(qps, d, g, bits):
+    """The block-diagonal two-sign rotation: planes and norms equal the oracle's."""
+    x = _rows(1500 + 3, d, 300 + d + g + bits, outliers=(d != 64))
+    w1, w2 = synth.sign_bits(d, 42), synth.sign_bits(d, 43)
+    planes = qps.encode_kv(f"tq{bits}", x.cuda().reshape(-1, 1, d), qps.Rotation(w1, w2, g)).planes
+    rp, rn = otq.encode_tier(x.numpy(), otq.Rotation(w1.numpy(), w2.numpy(), g), bits)
+    assert np.array_equal(planes[-1].cpu().numpy().reshape(-1).view(np.uint16), rn.view(np.uint16))
+    for got, want in zip(planes[:-1], rp):
+        assert np.array_equal(got.cpu().numpy().reshape(want.shape), want)
+
+
 def test_tq3_sign_vector_changes_codes(qps):
     x = _rows(64, 128, 7, outliers=False).cuda()
     a = qps.kv_quant_tq3(x, synth.sign_bits(128, 42))[0]

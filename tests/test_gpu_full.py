@@ -29,6 +29,7 @@ def qps():
     ("qwen14b_f16_q8tail", (5,)),
     ("qwen14b_q8_tq3vtail", (40,)),
     ("qwen14b_q8_tq2vtail", (21,)),
+    ("gemma_global_q8k_tq3v_r128", (2,)),
 ])
 def test_full_size_split_workload(qps, name, sample):
     cfg = synth.by_name(name)

@@ -48,6 +48,9 @@ def parse_args(argv=None):
     ap.add_argument("--v-fmt", default="",
                     help="with --kernel-only: store the window's V in this format instead "
                          "(f16, q8_0, tq2, tq3, tq4)")
+    ap.add_argument("--k-fmt", default="",
+                    help="with --kernel-only: store the window's K in this format instead "
+                         "(f16, q8_0, or the V format's TurboQuant tier)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the window decode-attention kernel alone on one layer of every "
                          "workload (one JSON line per workload; not the benchmark line)")
@@ -503,8 +506,10 @@ def run_ours(args):
     return 0
 
 
-# kernel-only lines of a workload's window with V stored at another TurboQuant tier
-TIER_VARIANTS = {"qwen14b_q8": ("tq4", "tq2"), "gemma_global_q8k_tq3v": ("tq4", "tq2")}
+# kernel-only lines of a workload's window with (K, V) stored in other formats: V at the
+# other TurboQuant tiers, and K and V both TurboQuant (K read in the rotated domain)
+TIER_VARIANTS = {"qwen14b_q8": (("q8_0", "tq4"), ("q8_0", "tq2"), ("tq4", "tq4"), ("tq3", "tq3"), ("tq2", "tq2")),
+                 "gemma_global_q8k_tq3v": (("q8_0", "tq4"), ("q8_0", "tq2"), ("tq3", "tq3"))}
 
 
 def run_kernel_only(args):
@@ -527,9 +532,9 @@ def run_kernel_only(args):
     s = torch.cuda.current_stream()
     for name in names:
         cfg = synth.by_name(name)
-        if args.v_fmt:
-            cfg = cfg.replace(v_fmt=args.v_fmt)
-            name = f"{name} V={args.v_fmt}"
+        if args.v_fmt or args.k_fmt:
+            cfg = cfg.replace(v_fmt=args.v_fmt or cfg.v_fmt, k_fmt=args.k_fmt or cfg.k_fmt)
+            name = f"{name} K={cfg.k_fmt} V={cfg.v_fmt}"
         signs = _lib_signs(qps, synth, cfg)
         if cfg.kind == "split":
             q = synth.query_f16(cfg, 0, device=dev)
@@ -555,13 +560,14 @@ def run_kernel_only(args):
                 rows = cfg.batch * n_q * cfg.hq
             _time_window_launch(qps, torch, a, name if n_q == 1 else f"{name} verify n_q={n_q} causal",
                                 rows, cfg, K, V, dev, s, peak, peak_kind)
-        # the same window with V at the 2- and 4-bit TurboQuant tiers
-        for vf in (TIER_VARIANTS.get(name, ()) if not (args.layers or args.v_fmt) else ()):
-            del V
+        # the same window with (K, V) in the other formats
+        for kf, vf in (TIER_VARIANTS.get(name, ()) if not (args.layers or args.v_fmt or args.k_fmt) else ()):
+            del K, V
+            K = qps.encode_kv_head_major(kf, k, signs)
             V = qps.encode_kv_head_major(vf, v, signs)
             a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs)
-            _time_window_launch(qps, torch, a, f"{name} V={vf}", cfg.batch * cfg.hq, cfg.replace(v_fmt=vf),
-                                K, V, dev, s, peak, peak_kind)
+            _time_window_launch(qps, torch, a, f"{name} K={kf} V={vf}", cfg.batch * cfg.hq,
+                                cfg.replace(k_fmt=kf, v_fmt=vf), K, V, dev, s, peak, peak_kind)
         qps.device_status(reset=True)
     return 0
 

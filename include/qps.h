@@ -66,7 +66,8 @@
  *                 4(i%2)..4(i%2)+3 of byte i/2; aux: one fp16 norm (2 bytes).
  *                 k = sign ? 8 + mag : 7 - mag over the 16-level codebook; value as TQ3.
  *   TQ2 / TQ3 / TQ4 are the 2-, 3- and 4-bit rungs of one rotation + codebook scheme
- *   [POLY, "S2 — TurboQuant tier family"]; they are V formats only.
+ *   [POLY, "S2 — TurboQuant tier family"]: V formats, and K formats where V is in the
+ *   same tier.
  */
 #ifndef QPS_H
 #define QPS_H
@@ -193,7 +194,7 @@ QPS_API qps_status qps_kv_quant_tq4(const void* x, int64_t rows, int32_t d, int6
  * [POLY, "S1 — SharedKVPool"]); the attention then packs every batch entry's query
  * rows of a KV head into one tile so the shared rows are read once. */
 typedef struct qps_kv_view {
-  int32_t fmt;         /* qps_kv_format */
+  int32_t fmt;         /* qps_kv_format (TurboQuant: V, or K with V of the same tier) */
   int32_t reserved0;   /* must be 0 */
   const void* data;    /* device: F16 values | Q8_0 codes | TQ2/3/4 code plane; 16-byte aligned */
   const void* aux;     /* device: Q8_0 scales | TQ3 1-bit plane | TQ2/TQ4 norms; NULL for F16 */
@@ -227,7 +228,9 @@ typedef struct qps_attn_args {
   int64_t kv_begin, kv_end; /* 0 <= kv_begin <= kv_end; tokens of the views */
   float scale;
   float softcap;          /* <= 0: off */
-  const uint32_t* v_signs;/* host, D/32 sign words; required iff v.fmt is TQ2, TQ3 or TQ4 */
+  const uint32_t* v_signs;/* host, D/32 sign words of the cache's TurboQuant rotation;
+                           required iff v.fmt is TQ2, TQ3 or TQ4 (a TurboQuant K uses
+                           the same rotation, v_signs2 and v_block) */
   int32_t n_split;        /* > 0, or 0 = chosen by the library */
   int32_t part_offset;
   float* o_parts;
@@ -273,8 +276,10 @@ QPS_API qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out,
 QPS_API int32_t qps_attn_path(const qps_attn_args* a);
 
 /* Decode attention over device-resident KV (the window [0, wc), or any device part)
- * [RKV].  Supported: D in {64, 128, 256, 512}; K in {F16, Q8_0}; V in {F16, Q8_0, TQ2, TQ3, TQ4};
- * hq a multiple of hkv.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+ * [RKV].  Supported: D in {64, 128, 256, 512}; K in {F16, Q8_0} with V in {F16, Q8_0, TQ2,
+ * TQ3, TQ4}, or K and V in the same TurboQuant tier (TQ2 / TQ3 / TQ4: K is read in the
+ * rotated domain against the rotated query, [POLY, "S2 perf-path Level B"]); hq a
+ * multiple of hkv.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 QPS_API qps_status qps_attn_decode_window(const qps_attn_args* a, void* stream);
 
 /* LSE combine [RKV, item S2]: M = max_t lse_t, w_t = exp(lse_t - M),

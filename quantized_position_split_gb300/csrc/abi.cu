@@ -221,10 +221,12 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   const int n_q = a->n_q < 1 ? 1 : a->n_q;
   if (a->batch > 1 && (a->q_batch_stride < (int64_t)n_q * a->hq * a->d || a->q_batch_stride % 8))
     return fail(QPS_ERR_INVALID_ARG, "attention: q_batch_stride must be >= n_q*hq*d and a multiple of 8");
-  qps_status st = check_view(a->k, "attention k", false);
+  qps_status st = check_view(a->k, "attention k", true);
   if (st != QPS_OK) return st;
   st = check_view(a->v, "attention v", true);
   if (st != QPS_OK) return st;
+  if (is_tq(a->k.fmt) && a->v.fmt != a->k.fmt)
+    return fail(QPS_ERR_UNSUPPORTED, "attention: a TurboQuant K needs V in the same TurboQuant tier");
   if ((a->k.batch_stride == 0) != (a->v.batch_stride == 0))
     return fail(QPS_ERR_INVALID_ARG, "attention: k and v must both be shared (batch_stride 0) or both per-batch");
   if (a->kv_begin < 0 || a->kv_end < a->kv_begin)
@@ -232,7 +234,7 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   if (!std::isfinite(a->scale) || !std::isfinite(a->softcap))
     return fail(QPS_ERR_INVALID_ARG, "attention: scale and softcap must be finite");
   if (is_tq(a->v.fmt) && !a->v_signs)
-    return fail(QPS_ERR_INVALID_ARG, "attention: v_signs is required for a TurboQuant V");
+    return fail(QPS_ERR_INVALID_ARG, "attention: v_signs is required for a TurboQuant V (and K)");
   if (a->reserved1 != 0) return fail(QPS_ERR_INVALID_ARG, "attention: reserved1 must be 0");
   const int vblock = a->v_block == 0 ? a->d : a->v_block;
   if (vblock < 32 || vblock > a->d || (vblock & (vblock - 1)))
@@ -286,6 +288,8 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   p->rows_total = rows_total;
   p->vblock = vblock;
   p->v_out_scale = (float)(1.0 / std::sqrt((double)a->d * (double)vblock));
+  p->k_rot_scale = (float)(1.0 / std::sqrt((double)vblock));
+  p->k_norm_scale = (float)(1.0 / std::sqrt((double)a->d));
   if (is_tq(a->v.fmt)) {
     for (int i = 0; i < a->d / 32; ++i) p->vsigns[i] = a->v_signs[i];
     if (a->v_signs2)

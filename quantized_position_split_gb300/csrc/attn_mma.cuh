@@ -139,15 +139,25 @@ struct PlaneG {
   static constexpr int BYTES = TT * RB;
 };
 
-// Stage bytes of one CTA when CTAS CTAs share an SM's 228 KB (less 1 KB reserved per
-// CTA, the barriers and the 1024-byte alignment slack).
-__host__ __device__ constexpr int stage_budget(int ctas) { return ctas >= 3 ? 74 * 1024 : 104 * 1024; }
+// Stage bytes of one CTA when CTAS CTAs share an SM's 228 KB.  Three CTAs: 228 KB / 3
+// less 1 KB reserved per CTA, the 1024-byte alignment slack and up to 192 bytes of
+// barriers leaves 75584 bytes for the stages and what sits beside them; 75392 keeps
+// 192 more in hand.  Two CTAs: ~104 KB.
+__host__ __device__ constexpr int stage_budget(int ctas) { return ctas >= 3 ? 75392 : 104 * 1024; }
 
-template <int D, int KF, int VF, int TT_, int CTAS_>
+// Bytes of the rotated query fragments a TurboQuant-K CTA keeps in shared memory: per
+// n-tile, k-step and lane {hi b0, hi b1, lo b0, lo b1} (fp16 hi + lo = the fp32 value).
+template <int D, int KF, int NTW>
+constexpr int qf_bytes() { return is_tq(KF) ? NTW * (D / 16) * 32 * 16 : 0; }
+
+template <int D, int KF, int VF, int TT_, int CTAS_, int RES_>
 struct GeoT {
   static constexpr int CTAS = CTAS_;
-  static constexpr int K_RB = KF == QPS_FMT_F16 ? 2 * D : D;          // K data bytes / token
-  static constexpr int K_ARB = KF == QPS_FMT_Q8_0 ? D / 16 : 0;       // K scales bytes / token
+  // K data: fp16 values, q8_0 codes, TQ2 / TQ3 2-bit or TQ4 4-bit fields; K aux: q8_0
+  // scales, the TQ3 sign plane or the TQ2 / TQ4 norms; K aux2: the TQ3 norms
+  static constexpr int K_RB = KF == QPS_FMT_F16 ? 2 * D : KF == QPS_FMT_Q8_0 ? D : KF == QPS_FMT_TQ4 ? D / 2 : D / 4;
+  static constexpr int K_ARB = KF == QPS_FMT_Q8_0 ? D / 16 : KF == QPS_FMT_TQ3 ? D / 8 : is_tq(KF) ? 2 : 0;
+  static constexpr int K_A2RB = KF == QPS_FMT_TQ3 ? 2 : 0;
   // V data: fp16 values, q8_0 codes, TQ2 / TQ3 2-bit fields or TQ4 4-bit fields; V aux:
   // q8_0 scales, the TQ3 sign plane or the TQ2 / TQ4 norms; V aux2: the TQ3 norms
   static constexpr int V_RB = VF == QPS_FMT_F16 ? 2 * D : VF == QPS_FMT_Q8_0 ? D : VF == QPS_FMT_TQ4 ? D / 2 : D / 4;
@@ -156,28 +166,39 @@ struct GeoT {
   static constexpr int TT = TT_;
   static constexpr int SUB = TT / 16;
   using PK = PlaneG<K_RB, true, TT>;
-  using PKA = PlaneG<K_ARB, false, TT>;
+  using PKA = PlaneG<K_ARB, KF == QPS_FMT_TQ3, TT>;  // TQ3 sign planes are read like values
+  using PKA2 = PlaneG<K_A2RB, false, TT>;
   using PV = PlaneG<V_RB, true, TT>;
-  using PVA = PlaneG<V_ARB, VF == QPS_FMT_TQ3, TT>;  // the TQ3 sign plane is read like values
+  using PVA = PlaneG<V_ARB, VF == QPS_FMT_TQ3, TT>;
   using PVA2 = PlaneG<V_A2RB, false, TT>;
-  // swizzled planes first (each on a 1024-byte boundary), then the small ones
+  // swizzled planes first (each on a 1024-byte boundary), then the others (128-byte)
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = align_to(K_OFF + PK::BYTES, 1024);
-  static constexpr int AFTER_V = V_OFF + PV::BYTES;
-  static constexpr int KA_OFF = align_to(PVA::SW ? align_to(AFTER_V, 1024) + PVA::BYTES : AFTER_V, 128);
-  static constexpr int VA_OFF = PVA::SW ? align_to(AFTER_V, 1024) : align_to(KA_OFF + PKA::BYTES, 128);
-  static constexpr int VA2_OFF = align_to(PVA::SW ? KA_OFF + PKA::BYTES : VA_OFF + PVA::BYTES, 128);
-  static constexpr int NORM_OFF = VF == QPS_FMT_TQ3 ? VA2_OFF : VA_OFF;  // TurboQuant norms
+  static constexpr int END_V = V_OFF + PV::BYTES;
+  static constexpr int KA_SW_OFF = align_to(END_V, 1024);
+  static constexpr int END_KA_SW = PKA::SW ? KA_SW_OFF + PKA::BYTES : END_V;
+  static constexpr int VA_SW_OFF = align_to(END_KA_SW, 1024);
+  static constexpr int END_VA_SW = PVA::SW ? VA_SW_OFF + PVA::BYTES : END_KA_SW;
+  static constexpr int KA_PL_OFF = align_to(END_VA_SW, 128);
+  static constexpr int END_KA_PL = PKA::SW ? KA_PL_OFF : KA_PL_OFF + PKA::BYTES;
+  static constexpr int VA_PL_OFF = align_to(END_KA_PL, 128);
+  static constexpr int END_VA_PL = PVA::SW ? VA_PL_OFF : VA_PL_OFF + PVA::BYTES;
+  static constexpr int KA_OFF = PKA::SW ? KA_SW_OFF : KA_PL_OFF;
+  static constexpr int VA_OFF = PVA::SW ? VA_SW_OFF : VA_PL_OFF;
+  static constexpr int KA2_OFF = align_to(END_VA_PL, 128);
+  static constexpr int VA2_OFF = align_to(KA2_OFF + PKA2::BYTES, 128);
+  static constexpr int KNORM_OFF = KF == QPS_FMT_TQ3 ? KA2_OFF : KA_OFF;  // TurboQuant K norms
+  static constexpr int NORM_OFF = VF == QPS_FMT_TQ3 ? VA2_OFF : VA_OFF;   // TurboQuant V norms
   static constexpr int STAGE = align_to(VA2_OFF + PVA2::BYTES, 1024);
   // bytes the tensor-map boxes of one tile deliver
-  static constexpr int TX = PK::BYTES + (PKA::TMA ? PKA::BYTES : 0) + PV::BYTES + (PVA::TMA ? PVA::BYTES : 0) +
-                            (PVA2::TMA ? PVA2::BYTES : 0);
-  static constexpr bool SMALL = (K_ARB > 0 && !PKA::TMA) || (V_ARB > 0 && !PVA::TMA) || (V_A2RB > 0 && !PVA2::TMA);
+  static constexpr int TX = PK::BYTES + (PKA::TMA ? PKA::BYTES : 0) + PV::BYTES + (PVA::TMA ? PVA::BYTES : 0);
+  static_assert(!PKA2::TMA && !PVA2::TMA, "aux2 planes (norms) are staged by cp.async");
+  static constexpr bool SMALL = (K_ARB > 0 && !PKA::TMA) || (V_ARB > 0 && !PVA::TMA) || K_A2RB > 0 || V_A2RB > 0;
   static constexpr int ARRIVALS = 1 + (SMALL ? 32 : 0);  // expect_tx + one per lane's cp.async
   // warps per CTA: 4, or 2 when two stages of 4 warps would not fit in shared memory
   static constexpr int NW = 4 * 2 * STAGE <= 200 * 1024 ? 4 : 2;
-  // the stage budget of CTAS CTAs per SM
-  static constexpr int STAGES_RAW = stage_budget(CTAS) / (NW * STAGE);
+  // the stage budget of CTAS CTAs per SM, less RES_ bytes kept beside the stages
+  static constexpr int STAGES_RAW = (stage_budget(CTAS) - RES_) / (NW * STAGE);
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 6 ? 6 : STAGES_RAW);
   static constexpr int PIPE = NW * STAGES * STAGE;
   static constexpr int BARS = PIPE;                   // mbarriers after the stages
@@ -187,12 +208,13 @@ struct GeoT {
 // Tokens per stage: two 16-token MMA sub-tiles (independent chains for latency hiding,
 // one softmax update per 32 tokens) where registers allow (head_dim <= 128) and 4 warps
 // x 2 stages of 32 tokens still fit the stage budget; else one.
-template <int D, int KF, int VF, int CTAS>
+template <int D, int KF, int VF, int CTAS, int RES>
 constexpr int stage_tokens() {
-  return (D <= 128 && 4 * 2 * GeoT<D, KF, VF, 32, CTAS>::STAGE <= stage_budget(CTAS)) ? 32 : 16;
+  return (D <= 128 && 4 * 2 * GeoT<D, KF, VF, 32, CTAS, RES>::STAGE <= stage_budget(CTAS) - RES) ? 32 : 16;
 }
 template <int D, int KF, int VF, int NTW>
-struct Geo : GeoT<D, KF, VF, stage_tokens<D, KF, VF, mma_ctas_per_sm(D, NTW, VF)>(), mma_ctas_per_sm(D, NTW, VF)> {};
+struct Geo : GeoT<D, KF, VF, stage_tokens<D, KF, VF, mma_ctas_per_sm(D, NTW, VF), qf_bytes<D, KF, NTW>()>(),
+                  mma_ctas_per_sm(D, NTW, VF), qf_bytes<D, KF, NTW>()> {};
 
 // Tensor maps of one launch, one per tensor-map plane (unused ones left empty).
 struct TmaSet {
@@ -274,6 +296,15 @@ __host__ __device__ constexpr int tq_col(int i, int hh) {
   return DT >= 16 ? 16 * (i >> 3) + ((i >> 1) & 3) + 8 * (i & 1) + 4 * hh : i + 4 * hh;
 }
 
+// Head-dim index of B-operand element e (0, 1: register b0; 2, 3: b1) of lane group c at
+// k-step kk for a TurboQuant K.  Lane group c decodes the quarter [c D/4, (c+1) D/4) of
+// every K row, in the order its decode produces: TQ4 four consecutive dims per k-step;
+// TQ2 / TQ3 per 16-dim word w = kk / 4 the dims j, j + 4, j + 8, j + 12 (j = kk % 4).
+template <int D, int KF>
+__host__ __device__ constexpr int tqk_dim(int c, int kk, int e) {
+  return c * (D / 4) + (KF == QPS_FMT_TQ4 ? 4 * kk + e : 16 * (kk >> 2) + 4 * e + (kk & 3));
+}
+
 // ---- the kernel -------------------------------------------------------------------
 // CAUSAL: the verify batch's causal limit (a separate instance, so that single-token
 // decode compiles without it).
@@ -347,7 +378,10 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   }
 
   // ---- query fragments (B operand of S^T), one set per 8-row n-tile --------------
-  uint32_t qb[NTW][MT][2];
+  constexpr int QMT = is_tq(KF) ? 1 : MT;  // (a TurboQuant K reads them from shared memory)
+  uint32_t qb[NTW][QMT][2];
+  constexpr int QF_OFF = align_to(G::END, 16);
+  if constexpr (!is_tq(KF)) {
 #pragma unroll
   for (int nt = 0; nt < NTW; ++nt) {
     const int rr = row0 + nt * 8 + g;
@@ -373,11 +407,70 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
       qb[nt][kk][1] = valid ? *reinterpret_cast<const uint32_t*>(qrow + d1) : 0u;
     }
   }
+  }
+  if constexpr (is_tq(KF)) {
+    // A TurboQuant K is read in the rotated domain: q . x_hat = (n / sqrt(D)) (R q) . c, so
+    // the CTA's query rows are rotated once, R q = s2 .* blockdiag(H_G)(s1 .* q) / sqrt(G),
+    // in the stage memory (no tile is in flight yet), then split into fp16 hi + lo
+    // fragments in the lane order of the K decode.
+    static_assert(ROWS * D * 4 <= G::PIPE, "query rotation scratch must fit the stages");
+    float* qs = reinterpret_cast<float*>(pipe);
+    for (int idx = threadIdx.x; idx < ROWS * D; idx += G::NW * 32) {
+      const int r = idx / D, dd = idx % D, rr = row0 + r;
+      float v = 0.f;
+      if (rr < p.rows_per_cta) {
+        const int h = head * p.group + rr % p.group;
+        const __half* qrow = p.shared ? p.q + (int64_t)(rr / p.group) * p.q_bstride + (int64_t)h * D
+                                      : p.q + (int64_t)bz * p.q_bstride + ((int64_t)(rr / p.group) * p.hq + h) * D;
+        v = __half2float(qrow[dd]);
+        if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) v = -v;
+      }
+      qs[idx] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int lh = 0; (1 << lh) < D; ++lh) {
+      const int h = 1 << lh;
+      if (h >= p.vblock) break;  // (uniform over the CTA)
+      for (int pid = threadIdx.x; pid < ROWS * (D / 2); pid += G::NW * 32) {
+        const int r = pid / (D / 2), j = pid % (D / 2);
+        const int i = ((j >> lh) << (lh + 1)) | (j & (h - 1));
+        const float a = qs[r * D + i], b = qs[r * D + i + h];
+        qs[r * D + i] = a + b;
+        qs[r * D + i + h] = a - b;
+      }
+      __syncthreads();
+    }
+    uint4* qf = reinterpret_cast<uint4*>(smem + QF_OFF);
+    for (int f = threadIdx.x; f < NTW * MT * 32; f += G::NW * 32) {
+      const int ln = f & 31, kk = (f >> 5) % MT, nt = (f >> 5) / MT;
+      const int row = nt * 8 + (ln >> 2), cc = ln & 3;
+      uint32_t hv[2], lv[2];
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        float x[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int dd = tqk_dim<D, KF>(cc, kk, 2 * b + e);
+          const float v = qs[row * D + dd] * p.k_rot_scale;
+          x[e] = ((p.vsigns2[dd >> 5] >> (dd & 31)) & 1u) ? -v : v;
+        }
+        const uint32_t hi = pack_h2(x[0], x[1]);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        hv[b] = hi;
+        lv[b] = pack_h2(x[0] - hf.x, x[1] - hf.y);
+      }
+      qf[f] = make_uint4(hv[0], hv[1], lv[0], lv[1]);
+    }
+    // (the __syncthreads after the barrier set-up below orders these writes before every
+    // read, and the scratch before the first tile copies)
+  }
 
   // ---- plane bases of this (head, batch entry) -------------------------------------
   const int64_t krow = (p.shared ? 0 : (int64_t)bz * p.k.batch) + (int64_t)head * p.k.head;
   const int64_t vrow = (p.shared ? 0 : (int64_t)bz * p.v.batch) + (int64_t)head * p.v.head;
-  const uint8_t* ka = KQ ? reinterpret_cast<const uint8_t*>(p.k.aux) + krow * G::K_ARB : nullptr;
+  const uint8_t* ka = G::K_ARB ? reinterpret_cast<const uint8_t*>(p.k.aux) + krow * G::K_ARB : nullptr;
+  const uint8_t* ka2 = G::K_A2RB ? reinterpret_cast<const uint8_t*>(p.k.aux2) + krow * G::K_A2RB : nullptr;
   const uint8_t* va = G::V_ARB ? reinterpret_cast<const uint8_t*>(p.v.aux) + vrow * G::V_ARB : nullptr;
   const uint8_t* va2 = G::V_A2RB ? reinterpret_cast<const uint8_t*>(p.v.aux2) + vrow * G::V_A2RB : nullptr;
   const uint8_t* safe = reinterpret_cast<const uint8_t*>(p.k.data);
@@ -430,7 +523,9 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         stage_flat_zfill<G::PKA::BYTES>(st + G::KA_OFF, ka + tb * G::K_ARB, valid * G::K_ARB, lane, safe);
       if constexpr (G::V_ARB > 0 && !G::PVA::TMA)
         stage_flat_zfill<G::PVA::BYTES>(st + G::VA_OFF, va + tb * G::V_ARB, valid * G::V_ARB, lane, safe);
-      if constexpr (G::V_A2RB > 0 && !G::PVA2::TMA)
+      if constexpr (G::K_A2RB > 0)
+        stage_flat_zfill<G::PKA2::BYTES>(st + G::KA2_OFF, ka2 + tb * G::K_A2RB, valid * G::K_A2RB, lane, safe);
+      if constexpr (G::V_A2RB > 0)
         stage_flat_zfill<G::PVA2::BYTES>(st + G::VA2_OFF, va2 + tb * G::V_A2RB, valid * G::V_A2RB, lane, safe);
       cp_async_arrive_noinc(bar);
     }
@@ -459,7 +554,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
 #pragma unroll
     for (int i = 0; i < MT; ++i) o[i][nt][0] = o[i][nt][1] = o[i][nt][2] = o[i][nt][3] = 0.f;
   }
-  const float qk_scale = p.scale;
+  // (a TurboQuant K's logits also carry the 1 / sqrt(D) of its decode)
+  const float qk_scale = is_tq(KF) ? p.scale * p.k_norm_scale : p.scale;
   const float cap = p.softcap;
   const float cap_k = cap > 0.f ? 2.f * 1.4426950408889634f / cap : 0.f;  // 2 log2(e) / cap
 
@@ -520,7 +616,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[sb][nt][e] += sodd[sb][nt][e];
-    } else {
+    } else if constexpr (KF == QPS_FMT_Q8_0) {
       const uint8_t* kc = st + G::K_OFF;
       const __half* ks = reinterpret_cast<const __half*>(st + G::KA_OFF) + ks_lane;
 #pragma unroll
@@ -548,6 +644,141 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
             sacc[sb][nt][2] = fmaf(sg8, acc[2], sacc[sb][nt][2]);
             sacc[sb][nt][3] = fmaf(sg8, acc[3], sacc[sb][nt][3]);
           }
+        }
+      }
+    } else {
+      // TurboQuant K (the same tier as V): lane group c decodes the quarter [c D/4,
+      // (c+1) D/4) of tokens g and g + 8 into the A operand, the rotated query comes
+      // from shared memory as hi + lo fragments (two accumulator chains), and each
+      // token's logit is scaled by its norm at the end.
+      static_assert(is_tq(KF) && KF == VF, "a TurboQuant K pairs with V of the same tier");
+      constexpr int QB = G::K_RB / 4;           // bytes of a quarter row
+      constexpr int CH = QB >= 16 ? 16 : QB;    // bytes per read
+      const uint4* qf = reinterpret_cast<const uint4*>(smem + QF_OFF) + lane;
+      const uint8_t* kc = st + G::K_OFF;
+      float slo[SUB][NTW][4];
+#pragma unroll
+      for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) slo[sb][nt][0] = slo[sb][nt][1] = slo[sb][nt][2] = slo[sb][nt][3] = 0.f;
+      // one k-step: a = {token g pair 0, token g+8 pair 0, token g pair 1, token g+8 pair 1}
+      auto kstep = [&](int sb, int kk, const uint32_t (&a)[4]) {
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) {
+          const uint4 qv = qf[(nt * MT + kk) * 32];
+          mma16816(sacc[sb][nt], a, qv.x, qv.y);
+          mma16816(slo[sb][nt], a, qv.z, qv.w);
+        }
+      };
+#pragma unroll
+      for (int sb = 0; sb < SUB; ++sb) {
+        const int r0 = g + 16 * sb, r8 = r0 + 8;
+#pragma unroll
+        for (int q0 = 0; q0 < QB; q0 += CH) {
+          uint32_t w[2][CH / 4];  // words of tokens r0, r8
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint8_t* src = kc + soff<G::PK::IB, G::PK::SW, TT>(u ? r8 : r0, c * QB + q0);
+            if constexpr (CH == 16) {
+              const uint4 r = *reinterpret_cast<const uint4*>(src);
+              w[u][0] = r.x; w[u][1] = r.y; w[u][2] = r.z; w[u][3] = r.w;
+            } else if constexpr (CH == 8) {
+              const uint2 r = *reinterpret_cast<const uint2*>(src);
+              w[u][0] = r.x; w[u][1] = r.y;
+            } else {
+              w[u][0] = *reinterpret_cast<const uint32_t*>(src);
+            }
+          }
+          if constexpr (KF == QPS_FMT_TQ4) {
+            // a word holds 8 dims (4-bit fields): k-steps (q0 + 4 wi) / 2 and the next
+#pragma unroll
+            for (int wi = 0; wi < CH / 4; ++wi) {
+              uint32_t mg[2], w4[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                mg[u] = w[u][wi] & 0x77777777u;
+                w4[u] = w[u][wi] << 4;
+              }
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                uint32_t a[4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const uint32_t sel = hf ? mg[u] >> 16 : mg[u];
+                  const uint32_t lo = prmt(tq_lo, tq_hi, sel);
+                  const uint32_t pos = prmt(w[u][wi], w4[u], hf ? 0xBFAEu : 0x9D8Cu);
+                  const uint32_t hi = prmt(tq_lo2, tq_hi2, sel) | (~pos & 0x80808080u);
+                  a[u] = __byte_perm(lo, hi, 0x5140u);      // dims 4kk, 4kk + 1 of the quarter
+                  a[2 + u] = __byte_perm(lo, hi, 0x7362u);  // dims 4kk + 2, 4kk + 3
+                }
+                kstep(sb, (q0 + 4 * wi) / 2 + hf, a);
+              }
+            }
+          } else {
+            // a word holds 16 dims (2-bit fields); TQ3 signs: 16 bits per word, up to four
+            // words (8 sign bytes) per chunk
+            uint32_t sgw[2][2] = {{0u, 0u}, {0u, 0u}};
+            if constexpr (KF == QPS_FMT_TQ3) {
+              constexpr int SB = CH / 2;  // sign bytes of the chunk: 2, 4 or 8
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const uint8_t* src =
+                    st + G::KA_OFF + soff<G::PKA::IB, G::PKA::SW, TT>(u ? r8 : r0, c * (QB / 2) + q0 / 2);
+                if constexpr (SB == 8) {
+                  const uint2 r = *reinterpret_cast<const uint2*>(src);
+                  sgw[u][0] = r.x;
+                  sgw[u][1] = r.y;
+                } else if constexpr (SB == 4) {
+                  sgw[u][0] = *reinterpret_cast<const uint32_t*>(src);
+                } else {
+                  sgw[u][0] = *reinterpret_cast<const uint16_t*>(src);
+                }
+              }
+            }
+#pragma unroll
+            for (int wi = 0; wi < CH / 4; ++wi) {
+              const int wq = (q0 + 4 * wi) / 4;  // word of the quarter
+              uint32_t s1[2] = {0u, 0u}, s2[2] = {0u, 0u};
+              if constexpr (KF == QPS_FMT_TQ3) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const uint32_t sg16 = (sgw[u][wi >> 1] >> (16 * (wi & 1))) & 0xffffu;
+                  s1[u] = sg16 | (sg16 << 12);        // dims j, j + 4 at bits j, 16 + j
+                  s2[u] = (sg16 >> 8) | (sg16 << 4);  // dims j + 8, j + 12 at bits j, 16 + j
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t a[4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  // one code per byte (dims j, j+4, j+8, j+12), then table selectors
+                  const uint32_t sel = ((w[u][wi] >> (2 * j)) & 0x03030303u) * 0x22u + 0x10101010u;
+                  uint32_t m0 = __byte_perm(tq_lo, tq_hi, sel);
+                  uint32_t m1 = __byte_perm(tq_lo, tq_hi, sel >> 16);
+                  if constexpr (KF == QPS_FMT_TQ3) {  // a clear sign bit stores a negative level
+                    m0 |= ~(s1[u] << (15 - j)) & 0x80008000u;
+                    m1 |= ~(s2[u] << (15 - j)) & 0x80008000u;
+                  }
+                  a[u] = m0;
+                  a[2 + u] = m1;
+                }
+                kstep(sb, 4 * wq + j, a);
+              }
+            }
+          }
+        }
+      }
+      const __half* kn = reinterpret_cast<const __half*>(st + G::KNORM_OFF);
+#pragma unroll
+      for (int sb = 0; sb < SUB; ++sb) {
+        const float n0 = __half2float(kn[16 * sb + g]), n8 = __half2float(kn[16 * sb + g + 8]);
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) {
+          sacc[sb][nt][0] = (sacc[sb][nt][0] + slo[sb][nt][0]) * n0;
+          sacc[sb][nt][1] = (sacc[sb][nt][1] + slo[sb][nt][1]) * n0;
+          sacc[sb][nt][2] = (sacc[sb][nt][2] + slo[sb][nt][2]) * n8;
+          sacc[sb][nt][3] = (sacc[sb][nt][3] + slo[sb][nt][3]) * n8;
         }
       }
     }
@@ -972,7 +1203,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
 template <int D, int KF, int VF, int NTW>
 constexpr size_t smem_bytes() {
   using G = Geo<D, KF, VF, NTW>;
-  constexpr size_t pipe = (size_t)G::END;
+  // the stages and barriers, then a TurboQuant K's query fragments
+  constexpr size_t pipe = (size_t)align_to(G::END, 16) + qf_bytes<D, KF, NTW>();
   constexpr int ROWS = 8 * NTW;
   constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D) +
                            sizeof(int64_t) * ROWS + sizeof(float) * ((size_t)G::NW * ROWS + 2 * ROWS);
@@ -997,7 +1229,7 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
       !encode_plane_map(&maps.v, p.v.data, G::V_RB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PV::IB, G::PV::SW, G::TT))
     return QPS_ERR_CUDA;
   if constexpr (G::PKA::TMA)
-    if (!encode_plane_map(&maps.ka, p.k.aux, G::K_ARB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PKA::IB, 0, G::TT))
+    if (!encode_plane_map(&maps.ka, p.k.aux, G::K_ARB, p.end, p.hkv, p.k.head, nb, p.k.batch, G::PKA::IB, G::PKA::SW, G::TT))
       return QPS_ERR_CUDA;
   if constexpr (G::PVA::TMA)
     if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, G::PVA::SW, G::TT))
@@ -1014,9 +1246,10 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
 }
 
 // Every format pairing and n-tile count of one head_dim, with or without the causal
-// limit; TIERS selects the V formats: TQ2 / TQ4 (true) or F16 / Q8_0 / TQ3 (false).  The
-// halves live in separate translation units.
-template <int D, bool CAUSAL, bool TIERS>
+// limit; SET selects the pairings: 0 K F16 / Q8_0 with V F16 / Q8_0 / TQ3, 1 the same K
+// with V TQ2 / TQ4, 2 a TurboQuant K with V of the same tier.  The sets live in
+// separate translation units.
+template <int D, bool CAUSAL, int SET>
 qps_status launch_mma_d(const AttnParams& p, cudaStream_t s) {
   // 8-row n-tiles per warp: more only where the accumulators still fit in registers
   const int ntw = mma_tile_rows(D, p.rows_per_cta, p.shared != 0) / 8;
@@ -1026,7 +1259,11 @@ qps_status launch_mma_d(const AttnParams& p, cudaStream_t s) {
     if (ntw == 2) return launch_mma_t<D, KF, VF, (D <= 128 ? 2 : 1), CAUSAL>(p, s); \
     return launch_mma_t<D, KF, VF, 1, CAUSAL>(p, s);                                \
   }
-  if constexpr (TIERS) {
+  if constexpr (SET == 2) {
+    QPS_MMA_CASE(QPS_FMT_TQ2, QPS_FMT_TQ2)
+    QPS_MMA_CASE(QPS_FMT_TQ3, QPS_FMT_TQ3)
+    QPS_MMA_CASE(QPS_FMT_TQ4, QPS_FMT_TQ4)
+  } else if constexpr (SET == 1) {
     QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_TQ2)
     QPS_MMA_CASE(QPS_FMT_F16, QPS_FMT_TQ4)
     QPS_MMA_CASE(QPS_FMT_Q8_0, QPS_FMT_TQ2)

@@ -1,13 +1,15 @@
 // Tensor-core decode attention instances for head_dim 128 (see attn_mma.cuh); the
-// causal (verify-batch) instances are in attn_mma_d128_causal.cu and the TQ2 / TQ4 V
-// instances in attn_mma_d128_tiers.cu.
+// causal (verify-batch) instances are in attn_mma_d128_causal.cu, the TQ2 / TQ4 V
+// instances in attn_mma_d128_tiers.cu and the TurboQuant-K ones in attn_mma_d128_tqk.cu.
 #include "attn_mma.cuh"
 
 namespace qps {
 qps_status launch_attn_mma_d128_causal(const AttnParams& p, cudaStream_t s);
 qps_status launch_attn_mma_d128_tiers(const AttnParams& p, cudaStream_t s);
+qps_status launch_attn_mma_d128_tqk(const AttnParams& p, cudaStream_t s);
 qps_status launch_attn_mma_d128(const AttnParams& p, cudaStream_t s) {
+  if (is_tq(p.kfmt)) return launch_attn_mma_d128_tqk(p, s);
   if (p.vfmt == QPS_FMT_TQ2 || p.vfmt == QPS_FMT_TQ4) return launch_attn_mma_d128_tiers(p, s);
-  return p.causal ? launch_attn_mma_d128_causal(p, s) : mma::launch_mma_d<128, false, false>(p, s);
+  return p.causal ? launch_attn_mma_d128_causal(p, s) : mma::launch_mma_d<128, false, 0>(p, s);
 }
 }  // namespace qps

@@ -4,6 +4,6 @@
 
 namespace qps {
 qps_status launch_attn_mma_d512_causal(const AttnParams& p, cudaStream_t s) {
-  return mma::launch_mma_d<512, true, false>(p, s);
+  return mma::launch_mma_d<512, true, 0>(p, s);
 }
 }  // namespace qps

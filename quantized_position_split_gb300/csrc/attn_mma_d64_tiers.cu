@@ -4,6 +4,6 @@
 
 namespace qps {
 qps_status launch_attn_mma_d64_tiers(const AttnParams& p, cudaStream_t s) {
-  return p.causal ? mma::launch_mma_d<64, true, true>(p, s) : mma::launch_mma_d<64, false, true>(p, s);
+  return p.causal ? mma::launch_mma_d<64, true, 1>(p, s) : mma::launch_mma_d<64, false, 1>(p, s);
 }
 }  // namespace qps

@@ -1,4 +1,6 @@
-// Split-KV decode attention on CUDA cores (any supported format pairing).
+// Split-KV decode attention on CUDA cores (any supported format pairing).  A
+// TurboQuant K (with V in the same tier) is read in the rotated domain against the
+// rotated query ("F5 M6 — PolyKV", section "S2 perf-path Level B").
 //
 // Computes one part of the position-split decode of "F5 M7 — Rolling KV:
 // position-windowed KV residency" (section "Implementation decomposition, refined
@@ -157,6 +159,33 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
       qs[idx] = val;
     }
     __syncthreads();
+    if constexpr (is_tq(KF)) {
+      // a TurboQuant K is read in the rotated domain (norm x level), so the query rows
+      // become R q = s2 .* blockdiag(H_G)(s1 .* q) / sqrt(G); the logits then carry the
+      // decode's 1 / sqrt(D) (k_norm_scale)
+      for (int idx = threadIdx.x; idx < RC * D; idx += blockDim.x) {
+        const int dd = idx % D;
+        if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) qs[idx] = -qs[idx];
+      }
+      __syncthreads();
+      for (int h = 1; h < p.vblock; h *= 2) {
+        for (int pid = threadIdx.x; pid < RC * (D / 2); pid += blockDim.x) {
+          const int r = pid / (D / 2), j = pid % (D / 2);
+          const int i = (j / h) * 2 * h + (j % h);
+          const float a = qs[r * D + i], b = qs[r * D + i + h];
+          qs[r * D + i] = a + b;
+          qs[r * D + i + h] = a - b;
+        }
+        __syncthreads();
+      }
+      for (int idx = threadIdx.x; idx < RC * D; idx += blockDim.x) {
+        const int dd = idx % D;
+        const float v = qs[idx] * p.k_rot_scale;
+        qs[idx] = ((p.vsigns2[dd >> 5] >> (dd & 31)) & 1u) ? -v : v;
+      }
+      __syncthreads();
+    }
+    const float logit_scale = is_tq(KF) ? p.scale * p.k_norm_scale : p.scale;
 
     float m[RC], l[RC], o[RC][E];
 #pragma unroll
@@ -179,7 +208,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
         for (int e = 0; e < E; ++e) acc = fmaf(qr[e], kf[e], acc);
 #pragma unroll
         for (int h = 16; h >= 1; h /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, h);
-        float s = acc * p.scale;
+        float s = acc * logit_scale;
         if (p.softcap > 0.f) s = p.softcap * tanhf(s / p.softcap);
         const float mn = fmaxf(m[r], s);
         const float corr = __expf(m[r] - mn);
@@ -276,6 +305,11 @@ qps_status launch_simple_dkv(const AttnParams& p, cudaStream_t s) {
 
 template <int D>
 qps_status launch_simple_d(const AttnParams& p, cudaStream_t s) {
+  if (is_tq(p.kfmt) && p.vfmt == p.kfmt) {
+    if (p.kfmt == QPS_FMT_TQ2) return launch_simple_dkv<D, QPS_FMT_TQ2, QPS_FMT_TQ2>(p, s);
+    if (p.kfmt == QPS_FMT_TQ3) return launch_simple_dkv<D, QPS_FMT_TQ3, QPS_FMT_TQ3>(p, s);
+    return launch_simple_dkv<D, QPS_FMT_TQ4, QPS_FMT_TQ4>(p, s);
+  }
   if (p.kfmt == QPS_FMT_F16) {
     if (p.vfmt == QPS_FMT_F16) return launch_simple_dkv<D, QPS_FMT_F16, QPS_FMT_F16>(p, s);
     if (p.vfmt == QPS_FMT_Q8_0) return launch_simple_dkv<D, QPS_FMT_F16, QPS_FMT_Q8_0>(p, s);

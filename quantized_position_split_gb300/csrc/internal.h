@@ -109,6 +109,8 @@ struct AttnParams {
   uint32_t vsigns2[kMaxSignWords];  // s2 (all 0: none)
   int vblock;                       // Hadamard block width G (a power of two, <= d)
   float v_out_scale;                // 1 / sqrt(d * G)
+  float k_rot_scale;                // a TurboQuant K: 1 / sqrt(G) (the rotated query)
+  float k_norm_scale;               // and 1 / sqrt(d) (its decode)
   float tq_levels[16];  // the V tier's codebook (ascending)
 };
 

@@ -21,7 +21,7 @@ class Workload:
     d: int
     n_kv: int  # split: total positions; fanout: prefix length
     wc: int  # split: device window length; fanout: unused (= n_kv)
-    k_fmt: str  # "f16" | "q8_0"
+    k_fmt: str  # "f16" | "q8_0" | "tq2" | "tq3" | "tq4" (with V in the same tier)
     v_fmt: str  # "f16" | "q8_0" | "tq2" | "tq3" | "tq4"
     softcap: float = 0.0  # <= 0: off
     tail_k_fmt: Optional[str] = None  # split: the tail's K format (None: k_fmt)
@@ -183,6 +183,25 @@ CONFIGS = [
         v_fmt="q8_0",
         tail_k_fmt="q8_0",
         tail_v_fmt="tq2",
+        k_outliers=4,
+        ring_slots=3,
+        tile_tokens=8192,
+    ),
+    # a tail with K and V both at the 3-bit TurboQuant tier (K read in the rotated domain)
+    Workload(
+        name="qwen14b_q8_tq3kvtail",
+        kind="split",
+        layers=48,
+        batch=1,
+        hq=40,
+        hkv=8,
+        d=128,
+        n_kv=131072,
+        wc=98304,
+        k_fmt="q8_0",
+        v_fmt="q8_0",
+        tail_k_fmt="tq3",
+        tail_v_fmt="tq3",
         k_outliers=4,
         ring_slots=3,
         tile_tokens=8192,

@@ -110,17 +110,54 @@ def test_window_attention_rotation(qps, layout, d, g, vf):
 
 
 @pytest.mark.parametrize("layout", ["head", "token"])
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("tier", ["tq2", "tq3", "tq4"])
+@pytest.mark.parametrize("rot", ["first", "block"])
+def test_window_attention_turboquant_k(qps, layout, d, tier, rot):
+    """K and V in the same TurboQuant tier: K read in the rotated domain against the
+    rotated query, with either rotation form, softcap on, several split counts."""
+    hq, hkv, n = 8, 2, 900 + 13
+    q, k, v = _inputs(n, hq, hkv, d, seed=7 * d + len(tier) + len(rot), outliers=True)
+    w1, w2 = synth.sign_bits(d, 42), synth.sign_bits(d, 43)
+    g = min(d, 128) if rot == "block" else 0
+    lib_rot = qps.Rotation(w1, w2, g) if rot == "block" else w1
+    ora_rot = otq.Rotation(w1.numpy(), w2.numpy(), g) if rot == "block" else w1.numpy()
+    K = _encode(qps, layout, tier, k, lib_rot)
+    V = _encode(qps, layout, tier, v, lib_rot)
+    scale = 1.0 / np.sqrt(d)
+    ro, rl = pipeline.layer_reference(q.numpy(), k.numpy(), v.numpy(), tier, tier, scale, 30.0, ora_rot)
+    for n_split in (0, 1, 6):
+        a = qps.attn_args(q.cuda(), K, V, scale=scale, softcap=30.0, v_signs=lib_rot, n_split=n_split)
+        assert qps.attn_path(a) == LAYOUT_PATH[layout]
+        o, lse = qps.attn_decode_window(a)
+        assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq),
+                      (layout, d, tier, rot, n_split))
+
+
+def test_turboquant_k_needs_the_same_tier_for_v(qps):
+    d, n = 128, 64
+    q, k, v = _inputs(n, 4, 1, d, seed=1)
+    w = synth.sign_bits(d, 42)
+    for kf, vf in [("tq3", "q8_0"), ("tq3", "tq4"), ("tq2", "f16")]:
+        a = qps.attn_args(q.cuda(), qps.encode_kv_head_major(kf, k.cuda(), w),
+                          qps.encode_kv_head_major(vf, v.cuda(), w), scale=0.1, v_signs=w)
+        with pytest.raises(qps.QpsError):
+            qps.attn_decode_window(a)
+
+
+@pytest.mark.parametrize("layout", ["head", "token"])
 @pytest.mark.parametrize("begin,end", [(17, 211), (0, 16), (5, 6), (31, 300), (299, 300)])
-@pytest.mark.parametrize("d,vf", [(128, "f16"), (512, "tq3"), (64, "tq4"), (256, "tq2")])
-def test_ragged_ranges(qps, layout, begin, end, d, vf):
+@pytest.mark.parametrize("d,kf,vf", [(128, "q8_0", "f16"), (512, "q8_0", "tq3"), (64, "q8_0", "tq4"),
+                                     (256, "q8_0", "tq2"), (128, "tq4", "tq4"), (512, "tq3", "tq3")])
+def test_ragged_ranges(qps, layout, begin, end, d, kf, vf):
     """Sub-ranges whose ends cut 16-token tiles, single tokens and tiny chunks (at
     head_dim 512 several warps share each tile)."""
     hq, hkv, n = 5, 1, 300
     q, k, v = _inputs(n, hq, hkv, d, seed=begin * 7 + end)
     words = synth.sign_bits(d, 5) if vf.startswith("tq") else None
-    K = _encode(qps, layout, "q8_0", k, None)
+    K = _encode(qps, layout, kf, k, words)
     V = _encode(qps, layout, vf, v, words)
-    kh = pipeline.dequant("q8_0", k.numpy())
+    kh = pipeline.dequant(kf, k.numpy(), None if words is None else words.numpy())
     vh = pipeline.dequant(vf, v.numpy(), None if words is None else words.numpy())
     for n_split in (1, 3):
         a = qps.attn_args(q.cuda(), K, V, scale=0.1, kv_begin=begin, kv_end=end, n_split=n_split, v_signs=words)
@@ -178,8 +215,8 @@ def test_split_identity_every_window_length(qps):
 
 @pytest.mark.parametrize("layout", ["head", "token"])
 @pytest.mark.parametrize("b", [1, 2, 5])
-@pytest.mark.parametrize("vf", ["tq3", "tq4"])
-def test_gqa_and_shared_batch(qps, layout, b, vf):
+@pytest.mark.parametrize("kf,vf", [("q8_0", "tq3"), ("q8_0", "tq4"), ("tq3", "tq3")])
+def test_gqa_and_shared_batch(qps, layout, b, kf, vf):
     """A shared prefix (batch_stride 0) read by b batch entries (up to 40 query rows
     per KV head) equals each entry attending it alone."""
     d, hq, hkv, n = 128, 16, 2, 777
@@ -188,11 +225,11 @@ def test_gqa_and_shared_batch(qps, layout, b, vf):
     k = torch.randn((n, hkv, d), generator=g).half()
     v = torch.randn((n, hkv, d), generator=g).half()
     words = synth.sign_bits(d, 42)
-    K = _encode(qps, layout, "q8_0", k, None)
+    K = _encode(qps, layout, kf, k, words)
     V = _encode(qps, layout, vf, v, words)
     a = qps.attn_args(q.cuda(), K, V, scale=0.09, v_signs=words, shared=True)
     o, lse = qps.attn_decode_window(a)
-    kh = pipeline.dequant("q8_0", k.numpy())
+    kh = pipeline.dequant(kf, k.numpy(), words.numpy())
     vh = pipeline.dequant(vf, v.numpy(), words.numpy())
     ro, rl = oatt.gqa_decode(q.double().numpy(), kh, vh, 0.09)
     assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(b * hq, d), rl.reshape(b * hq))
@@ -200,7 +237,8 @@ def test_gqa_and_shared_batch(qps, layout, b, vf):
 
 MQ_FORMATS = [(128, "q8_0", "q8_0", 0.0), (128, "f16", "f16", 0.0), (512, "q8_0", "tq3", 50.0),
               (64, "f16", "tq3", 0.0), (256, "q8_0", "f16", 30.0), (128, "q8_0", "tq2", 0.0),
-              (256, "q8_0", "tq4", 0.0), (64, "q8_0", "tq4", 30.0), (512, "f16", "tq2", 0.0)]
+              (256, "q8_0", "tq4", 0.0), (64, "q8_0", "tq4", 30.0), (512, "f16", "tq2", 0.0),
+              (128, "tq3", "tq3", 0.0), (512, "tq4", "tq4", 50.0), (64, "tq2", "tq2", 0.0)]
 
 
 @pytest.mark.parametrize("d,kf,vf,softcap", MQ_FORMATS)

@@ -30,6 +30,7 @@ def qps():
     ("qwen14b_q8_tq3vtail", (40,)),
     ("qwen14b_q8_tq2vtail", (21,)),
     ("gemma_global_q8k_tq3v_r128", (2,)),
+    ("qwen14b_q8_tq3kvtail", (33,)),
 ])
 def test_full_size_split_workload(qps, name, sample):
     cfg = synth.by_name(name)

@@ -97,3 +97,22 @@ def test_block_width_must_divide_head_dim():
         tq.encode_tier(x, tq.Rotation(_words(128, 1), None, 96), 3)
     with pytest.raises(ValueError):
         tq.encode_tier(x, tq.Rotation(_words(128, 1), None, 256), 3)
+
+
+@pytest.mark.parametrize("d,g", ROTS)
+def test_rotated_query_identity(d, g):
+    """q . x_hat = (n / sqrt(D)) (R q) . c[k]: a TurboQuant K can be read in the rotated
+    domain against the rotated query (PolyKV page, "S2 perf-path Level B")."""
+    rng = np.random.default_rng(d * 3 + g)
+    k = rng.standard_normal((25, d)).astype(np.float16)
+    q = rng.standard_normal((4, d))
+    w1, w2 = _words(d, 12), _words(d, 13)
+    rot = tq.Rotation(w1, w2, g)
+    r = _dense_r(d, g, w1, w2)
+    for bits in (2, 3, 4):
+        planes, n = tq.encode_tier(k, rot, bits)
+        lv, _ = tq.codebook(1 << bits)
+        c = lv.astype(np.float64)[tq.codes_from_tier_planes(planes, d, bits)]
+        direct = q @ tq.decode_tier(planes, n, rot, d, bits).T
+        rotated = ((q @ r.T) @ c.T) * n.astype(np.float64)[None, :] / np.sqrt(d)
+        assert np.allclose(direct, rotated, rtol=0, atol=1e-11)

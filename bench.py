@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--k-fmt", default="",
                     help="with --kernel-only: store the window's K in this format instead "
                          "(f16, q8_0, or the V format's TurboQuant tier)")
+    ap.add_argument("--ring-copy", choices=["engine", "kernel"], default="kernel",
+                    help="how the ring moves tail tiles: the ring's copy kernel (default) or the copy engine")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the window decode-attention kernel alone on one layer of every "
                          "workload (one JSON line per workload; not the benchmark line)")
@@ -329,7 +331,7 @@ def run_ours(args):
                                n_kv=cfg.n_kv, wc=cfg.wc, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
                                scale=cfg.scale, softcap=cfg.softcap, signs=signs,
                                ring_slots=cfg.ring_slots, tile_tokens=cfg.tile_tokens, device=device,
-                               tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt)
+                               tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt, ring_copy=args.ring_copy)
     for layer in range(cfg.layers):
         q = synth.query_f16(cfg, layer, device=device)
         k = synth.kv_f16(cfg, layer, "k", cfg.n_kv, device=device)
@@ -480,7 +482,8 @@ def run_ours(args):
                    "hkv": cfg.hkv, "d": cfg.d, "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt,
                    "v_fmt": cfg.v_fmt, "tail_k_fmt": cfg.tk_fmt, "tail_v_fmt": cfg.tv_fmt,
                    "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
-                   "tile_tokens": cfg.tile_tokens, "ring_plan": ring_plan, "parallelism": f"replicas x{world}",
+                   "tile_tokens": cfg.tile_tokens, "ring_plan": ring_plan, "ring_copy": args.ring_copy,
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" %
                          (window_bytes / 1e9, tail_bytes / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -298,9 +298,11 @@ QPS_API qps_status qps_lse_combine(const float* o_parts, const float* lse_parts,
  * residency", section "Storage layer": per-layer KV lives in pinned host memory
  * allocated with cudaHostAlloc(cudaHostAllocPortable)).  One large arena holding every
  * tile of the tail keeps the copy engine's reads on few, large page-locked regions.
- *   bytes  > 0;  flags: 0 = cudaHostAlloc portable, 1 = portable | write-combined,
- *          2 = an anonymous mapping advised to use transparent huge pages, faulted in
- *          and registered with cudaHostRegister (portable);
+ *   bytes  > 0;  flags: 0 = cudaHostAlloc portable | mapped, 1 = portable | mapped |
+ *          write-combined, 2 = an anonymous mapping advised to use transparent huge
+ *          pages, faulted in and registered with cudaHostRegister (portable | mapped);
+ *          every allocation is mapped into the device's address space, so that the
+ *          ring's copy kernel can read it (below);
  *   out    receives the host pointer (256-byte aligned), owned by the caller until
  *          qps_host_free.
  * Errors: INVALID_ARG, CUDA (allocation failure). */
@@ -332,7 +334,9 @@ QPS_API qps_status qps_ring_destroy(qps_ring* ring);
  * planes.  The ring places each plane at the next 256-byte-aligned offset of the slot
  * (in that order); their total must fit in slot_bytes.  When the host planes already
  * sit at those offsets from the first K plane (a tail packed tile by tile), the whole
- * tile moves in one copy; otherwise each plane is its own copy. */
+ * tile moves in one copy; otherwise each plane is its own copy.  Copies run on the
+ * copy engine, or as the ring's copy kernel (64 small CTAs loading the mapped host
+ * memory, on the copy stream) under QPS_RING_COPY_KERNEL (qps_ring_set_copy_mode). */
 typedef struct qps_tile_desc {
   int32_t n_k_planes, n_v_planes;
   const void* host_k[3];
@@ -343,6 +347,19 @@ typedef struct qps_tile_desc {
   int64_t tok_stride;  /* rows; > 0 */
   int64_t head_stride; /* rows; >= 0 */
 } qps_tile_desc;
+
+/* How the ring moves tiles: QPS_RING_COPY_ENGINE (the default) uses the copy engine
+ * (cudaMemcpyAsync) for every tile, leaving the SMs to the attention;
+ * QPS_RING_COPY_KERNEL uses the ring's copy kernel for every tile whose planes lie in
+ * qps_host_alloc memory (each on a 16-byte boundary) and the copy engine for the
+ * others.  On GB300 hosts the copy engine's host-to-device transfers stall in bursts on
+ * some boxes (single 1.3 ms transfers taking up to 50 ms) where SM loads of the same
+ * memory do not; inside a decode step the copy kernel moves ~199 GB/s (the copy engine
+ * 208) and slows the attention running beside it.  Takes effect from the next
+ * qps_ring_begin_step.  Errors: STATE (invalid ring, open step), INVALID_ARG (mode). */
+#define QPS_RING_COPY_ENGINE 0
+#define QPS_RING_COPY_KERNEL 1
+QPS_API qps_status qps_ring_set_copy_mode(qps_ring* ring, int32_t mode);
 
 /* Start a step: copy the flat (layer, tile) schedule (host array, read during the
  * call) and enqueue the first n_slots tile copies on the copy stream; each copy

@@ -477,11 +477,16 @@ class HostArena:
             pass
 
 
+RING_COPY = {"engine": 0, "kernel": 1}  # QPS_RING_COPY_ENGINE / QPS_RING_COPY_KERNEL
+
+
 class Ring:
     """The tail-prefetch ring (``qps_ring_*``): device staging slots, a copy stream and
     pre-created copy_done / compute_done events, owned by the library."""
 
-    def __init__(self, n_slots: int, slot_bytes: int, device: Optional[int] = None):
+    def __init__(self, n_slots: int, slot_bytes: int, device: Optional[int] = None, copy: str = "engine"):
+        """``copy``: "engine" (cudaMemcpyAsync) or "kernel" (the ring's copy kernel for
+        tiles in ``HostArena`` / qps_host_alloc memory, the copy engine otherwise)."""
         dev = torch.cuda.current_device() if device is None else device
         h = ctypes.c_void_p()
         N.check(lib().qps_ring_create(n_slots, slot_bytes, dev, ctypes.byref(h)))
@@ -489,6 +494,9 @@ class Ring:
         self.n_slots = n_slots
         self.slot_bytes = slot_bytes
         self._tiles = None
+        if copy not in RING_COPY:
+            raise QpsError(N.QPS_ERR_INVALID_ARG, f"unknown ring copy mode {copy}")
+        N.check(lib().qps_ring_set_copy_mode(self.handle, RING_COPY[copy]))
 
     def begin_step(self, tiles: Sequence[N.TileDesc], stream=None):
         arr = (N.TileDesc * len(tiles))(*tiles)

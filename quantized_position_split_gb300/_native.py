@@ -134,6 +134,7 @@ SIGNATURES = [
     ("qps_host_free", c_int32, [c_void_p]),
     ("qps_ring_create", c_int32, [c_int32, c_size_t, c_int32, POINTER(c_void_p)]),
     ("qps_ring_destroy", c_int32, [c_void_p]),
+    ("qps_ring_set_copy_mode", c_int32, [c_void_p, c_int32]),
     ("qps_ring_begin_step", c_int32, [c_void_p, POINTER(TileDesc), c_int32, c_void_p]),
     ("qps_attn_decode_tail", c_int32, [c_void_p, c_int32, POINTER(AttnArgs), c_void_p]),
     ("qps_ring_end_step", c_int32, [c_void_p]),

@@ -145,10 +145,20 @@ struct PlaneG {
 // 192 more in hand.  Two CTAs: ~104 KB.
 __host__ __device__ constexpr int stage_budget(int ctas) { return ctas >= 3 ? 75392 : 104 * 1024; }
 
-// Bytes of the rotated query fragments a TurboQuant-K CTA keeps in shared memory: per
-// n-tile, k-step and lane {hi b0, hi b1, lo b0, lo b1} (fp16 hi + lo = the fp32 value).
-template <int D, int KF, int NTW>
-constexpr int qf_bytes() { return is_tq(KF) ? NTW * (D / 16) * 32 * 16 : 0; }
+// Query fragments kept in shared memory instead of registers: a TurboQuant K's rotated
+// fragments (per n-tile, k-step and lane {hi b0, hi b1, lo b0, lo b1}: fp16 hi + lo = the
+// fp32 value), and at head_dim 512 with a q8_0 K and a TQ3 / TQ2 V the plain fragments
+// {b0, b1}: 64 registers the accumulators and the V decode use better (the q8_0-K /
+// TQ3-V window 67.9 -> 66.0 us), in 8 KB that still leave two CTAs per SM (not so with
+// a TQ4 V, whose two stages already fill it, or an fp16 K, which runs one CTA per SM).
+template <int D, int KF, int VF>
+__host__ __device__ constexpr bool q_in_smem() {
+  return is_tq(KF) || (D >= 512 && KF == QPS_FMT_Q8_0 && (VF == QPS_FMT_TQ3 || VF == QPS_FMT_TQ2));
+}
+template <int D, int KF, int VF, int NTW>
+__host__ __device__ constexpr int qf_bytes() {
+  return is_tq(KF) ? NTW * (D / 16) * 32 * 16 : q_in_smem<D, KF, VF>() ? NTW * (D / 16) * 32 * 8 : 0;
+}
 
 template <int D, int KF, int VF, int TT_, int CTAS_, int RES_>
 struct GeoT {
@@ -213,8 +223,8 @@ constexpr int stage_tokens() {
   return (D <= 128 && 4 * 2 * GeoT<D, KF, VF, 32, CTAS, RES>::STAGE <= stage_budget(CTAS) - RES) ? 32 : 16;
 }
 template <int D, int KF, int VF, int NTW>
-struct Geo : GeoT<D, KF, VF, stage_tokens<D, KF, VF, mma_ctas_per_sm(D, NTW, VF), qf_bytes<D, KF, NTW>()>(),
-                  mma_ctas_per_sm(D, NTW, VF), qf_bytes<D, KF, NTW>()> {};
+struct Geo : GeoT<D, KF, VF, stage_tokens<D, KF, VF, mma_ctas_per_sm(D, NTW, VF), qf_bytes<D, KF, VF, NTW>()>(),
+                  mma_ctas_per_sm(D, NTW, VF), qf_bytes<D, KF, VF, NTW>()> {};
 
 // Tensor maps of one launch, one per tensor-map plane (unused ones left empty).
 struct TmaSet {
@@ -378,7 +388,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   }
 
   // ---- query fragments (B operand of S^T), one set per 8-row n-tile --------------
-  constexpr int QMT = is_tq(KF) ? 1 : MT;  // (a TurboQuant K reads them from shared memory)
+  constexpr bool QS = q_in_smem<D, KF, VF>();  // fragments in shared memory (see q_in_smem)
+  constexpr int QMT = QS ? 1 : MT;
   uint32_t qb[NTW][QMT][2];
   constexpr int QF_OFF = align_to(G::END, 16);
   if constexpr (!is_tq(KF)) {
@@ -403,11 +414,22 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         d0 = 16 * kk + 2 * c;
         d1 = d0 + 8;
       }
-      qb[nt][kk][0] = valid ? *reinterpret_cast<const uint32_t*>(qrow + d0) : 0u;
-      qb[nt][kk][1] = valid ? *reinterpret_cast<const uint32_t*>(qrow + d1) : 0u;
+      const uint32_t b0 = valid ? *reinterpret_cast<const uint32_t*>(qrow + d0) : 0u;
+      const uint32_t b1 = valid ? *reinterpret_cast<const uint32_t*>(qrow + d1) : 0u;
+      if constexpr (QS) {  // (each lane reads back only its own slots: no barrier needed)
+        reinterpret_cast<uint2*>(smem + QF_OFF)[(nt * MT + kk) * 32 + lane] = make_uint2(b0, b1);
+      } else {
+        qb[nt][kk][0] = b0;
+        qb[nt][kk][1] = b1;
+      }
     }
   }
   }
+  // query fragment {b0, b1} of n-tile nt, k-step kk (F16 / Q8_0 K)
+  auto qfrag = [&](int nt, int kk) -> uint2 {
+    if constexpr (QS) return reinterpret_cast<const uint2*>(smem + QF_OFF)[(nt * MT + kk) * 32 + lane];
+    else return make_uint2(qb[nt][kk][0], qb[nt][kk][1]);
+  };
   if constexpr (is_tq(KF)) {
     // A TurboQuant K is read in the rotated domain: q . x_hat = (n / sqrt(D)) (R q) . c, so
     // the CTA's query rows are rotated once, R q = s2 .* blockdiag(H_G)(s1 .* q) / sqrt(G),
@@ -605,8 +627,9 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
           ldsm_x4(a, kbase + soff<G::PK::IB, G::PK::SW, TT>(trow + 16 * sb, (2 * kk + (mi >> 1)) << 4));
 #pragma unroll
           for (int nt = 0; nt < NTW; ++nt) {
-            if (kk & 1) mma16816(sodd[sb][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-            else mma16816(sacc[sb][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+            const uint2 qv = qfrag(nt, kk);
+            if (kk & 1) mma16816(sodd[sb][nt], a, qv.x, qv.y);
+            else mma16816(sacc[sb][nt], a, qv.x, qv.y);
           }
         }
       }
@@ -637,8 +660,9 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
 #pragma unroll
           for (int nt = 0; nt < NTW; ++nt) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            mma16816(acc, a0, qb[nt][2 * j][0], qb[nt][2 * j][1]);
-            mma16816(acc, a1, qb[nt][2 * j + 1][0], qb[nt][2 * j + 1][1]);
+            const uint2 qv0 = qfrag(nt, 2 * j), qv1 = qfrag(nt, 2 * j + 1);
+            mma16816(acc, a0, qv0.x, qv0.y);
+            mma16816(acc, a1, qv1.x, qv1.y);
             sacc[sb][nt][0] = fmaf(sg, acc[0], sacc[sb][nt][0]);
             sacc[sb][nt][1] = fmaf(sg, acc[1], sacc[sb][nt][1]);
             sacc[sb][nt][2] = fmaf(sg8, acc[2], sacc[sb][nt][2]);
@@ -1204,7 +1228,7 @@ template <int D, int KF, int VF, int NTW>
 constexpr size_t smem_bytes() {
   using G = Geo<D, KF, VF, NTW>;
   // the stages and barriers, then a TurboQuant K's query fragments
-  constexpr size_t pipe = (size_t)align_to(G::END, 16) + qf_bytes<D, KF, NTW>();
+  constexpr size_t pipe = (size_t)align_to(G::END, 16) + qf_bytes<D, KF, VF, NTW>();
   constexpr int ROWS = 8 * NTW;
   constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D) +
                            sizeof(int64_t) * ROWS + sizeof(float) * ((size_t)G::NW * ROWS + 2 * ROWS);
@@ -1221,6 +1245,8 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
   // planes at head_dim >= 256, which then run one CTA per SM)
   static_assert(G::CTAS * (smem + 1024) <= 228 * 1024 || (G::CTAS == 2 && G::STAGES == 2),
                 "the CTAs per SM the instance is built for no longer fit");
+  static_assert(qf_bytes<D, KF, VF, NTW>() == 0 || G::CTAS * (smem + 1024) <= 228 * 1024,
+                "query fragments in shared memory must not cost a CTA per SM");
   // tensor maps over each plane as [row bytes][tokens < kv_end][KV heads][batch]
   TmaSet maps;
   std::memset(&maps, 0, sizeof(maps));

@@ -25,12 +25,14 @@
 #include "internal.h"
 
 namespace {
-// Every allocation made by qps_host_alloc: base -> (length, made by mmap).  qps_host_free
-// unregisters and unmaps the mappings (flags = 2) instead of calling cudaFreeHost, and
-// the ring copies a packed tile in one transfer only when it lies in one of them.
+// Every allocation made by qps_host_alloc: base -> (length, made by mmap, the device's
+// address of the base).  qps_host_free unregisters and unmaps the mappings (flags = 2)
+// instead of calling cudaFreeHost; the ring copies a packed tile in one transfer only when
+// it lies in one of them, and moves a tile with its copy kernel only when every plane does.
 struct HostAlloc {
   size_t bytes;
   bool mapped;
+  const char* dev;
 };
 std::mutex& host_map_mutex() {
   static std::mutex m;
@@ -40,15 +42,28 @@ std::map<uintptr_t, HostAlloc>& host_map() {
   static std::map<uintptr_t, HostAlloc> m;
   return m;
 }
-// True when [p, p + n) lies inside one qps_host_alloc allocation.
-bool in_one_host_alloc(const void* p, size_t n) {
+// The device's address of host byte p when [p, p + n) lies inside one qps_host_alloc
+// allocation, else nullptr.
+const char* host_alloc_dev(const void* p, size_t n) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
   std::lock_guard<std::mutex> lk(host_map_mutex());
   auto it = host_map().upper_bound(a);
-  if (it == host_map().begin()) return false;
+  if (it == host_map().begin()) return nullptr;
   --it;
-  return a - it->first <= it->second.bytes && n <= it->second.bytes - (a - it->first);
+  const size_t off = a - it->first;
+  if (off > it->second.bytes || n > it->second.bytes - off) return nullptr;
+  return it->second.dev + off;
 }
+bool in_one_host_alloc(const void* p, size_t n) { return host_alloc_dev(p, n) != nullptr; }
+
+// A tile moved by the copy kernel: up to six (device-visible host source, slot offset,
+// bytes) segments.
+struct KernelCopy {
+  const char* src[6];
+  size_t off[6];
+  size_t bytes[6];
+  int n;
+};
 }  // namespace
 
 struct qps_ring {
@@ -65,6 +80,8 @@ struct qps_ring {
   std::vector<qps_tile_desc> tiles;
   std::vector<size_t> offsets;  // per tile: 6 plane offsets within the slot
   std::vector<size_t> span;     // per tile: bytes of one copy covering every plane, or 0
+  std::vector<KernelCopy> kcopy;  // per tile: its copy-kernel segments (n = 0: cudaMemcpyAsync)
+  int copy_mode = QPS_RING_COPY_ENGINE;
   int next_consume = 0;
   bool open = false;
 };
@@ -90,13 +107,68 @@ qps_status check_pinned(const void* p, const char* what) {
   return QPS_OK;
 }
 
+// Host -> slot copy by SMs reading the pinned allocation through its device mapping
+// (QPS_RING_COPY_KERNEL).  On some GB300 hosts the copy engine's host-to-device transfers
+// stall in bursts (chunks of 1.3 ms taking up to 50 ms, seconds lost per 10 s of
+// streaming); the same transfers issued as loads by SMs ran at the same 211 GB/s without
+// them in every probe.
+// Every segment: n16 16-byte units (source and destination 16-byte aligned), then rem
+// bytes one by one.  Shape chosen by measuring the copy rate while window attention
+// runs back to back beside it (fp16 Qwen-like window, 28.6 us alone): 64 CTAs of 64
+// threads with sixteen 16-byte loads in flight per thread copy ~196 GB/s under that load
+// and leave the window at 33 us; the copy engine ~207 GB/s (when it does not stall) and
+// 41 us; 32 x 512 threads 197 GB/s and 58 us; 8 x 512 185 GB/s and 41 us.
+constexpr int kCopyCtas = 64, kCopyThreads = 64, kCopyUnroll = 16;
+
+struct CopySegs {
+  const uint4* src[6];
+  uint4* dst[6];
+  uint64_t n16[6];
+  uint32_t rem[6];
+  int n;
+};
+
+__global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const __grid_constant__ CopySegs s) {
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t step = (size_t)gridDim.x * blockDim.x;
+  for (int k = 0; k < s.n; ++k) {
+    const uint4* __restrict__ src = s.src[k];
+    uint4* __restrict__ dst = s.dst[k];
+    const size_t n = s.n16[k];
+    size_t i = tid;
+    for (; i + (kCopyUnroll - 1) * step < n; i += kCopyUnroll * step) {
+      uint4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) v[u] = src[i + u * step];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) dst[i + u * step] = v[u];
+    }
+    for (; i < n; i += step) dst[i] = src[i];
+    if (tid < s.rem[k])
+      reinterpret_cast<uint8_t*>(dst + n)[tid] = reinterpret_cast<const uint8_t*>(src + n)[tid];
+  }
+}
+
 qps_status issue_copy(qps_ring* r, int i) {
   const int slot = i % r->n_slots;
   const qps_tile_desc& t = r->tiles[i];
   if (r->compute_recorded[slot]) QPS_CUDA_TRY(cudaStreamWaitEvent(r->copy, r->compute_done[slot], 0));
   char* base = reinterpret_cast<char*>(r->slots[slot]);
   const size_t* off = &r->offsets[(size_t)i * 6];
-  if (r->span[i]) {  // the planes sit in host memory exactly as in the slot: one copy
+  if (r->kcopy[i].n > 0) {
+    const KernelCopy& kc = r->kcopy[i];
+    CopySegs cs{};
+    cs.n = kc.n;
+    for (int k = 0; k < kc.n; ++k) {
+      cs.src[k] = reinterpret_cast<const uint4*>(kc.src[k]);
+      cs.dst[k] = reinterpret_cast<uint4*>(base + kc.off[k]);
+      cs.n16[k] = kc.bytes[k] / 16;
+      cs.rem[k] = (uint32_t)(kc.bytes[k] % 16);
+    }
+    ring_copy_kernel<<<kCopyCtas, kCopyThreads, 0, r->copy>>>(cs);
+    count_launch();
+    QPS_CUDA_TRY(cudaGetLastError());
+  } else if (r->span[i]) {  // the planes sit in host memory exactly as in the slot: one copy
     QPS_CUDA_TRY(cudaMemcpyAsync(base, t.host_k[0], r->span[i], cudaMemcpyHostToDevice, r->copy));
   } else {
     for (int p = 0; p < t.n_k_planes; ++p)
@@ -215,20 +287,34 @@ qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out) {
     if (p == MAP_FAILED) return fail(QPS_ERR_CUDA, "host_alloc: mmap failed");
     madvise(p, n, MADV_HUGEPAGE);
     std::memset(p, 0, n);
-    cudaError_t e = cudaHostRegister(p, n, cudaHostRegisterPortable);
+    cudaError_t e = cudaHostRegister(p, n, cudaHostRegisterPortable | cudaHostRegisterMapped);
     if (e != cudaSuccess) {
       munmap(p, n);
       return cuda_fail(e, "host_alloc: cudaHostRegister");
     }
+    void* dev = nullptr;
+    e = cudaHostGetDevicePointer(&dev, p, 0);
+    if (e != cudaSuccess) {
+      cudaHostUnregister(p);
+      munmap(p, n);
+      return cuda_fail(e, "host_alloc: cudaHostGetDevicePointer");
+    }
     std::lock_guard<std::mutex> lk(host_map_mutex());
-    host_map()[reinterpret_cast<uintptr_t>(p)] = HostAlloc{n, true};
+    host_map()[reinterpret_cast<uintptr_t>(p)] = HostAlloc{n, true, reinterpret_cast<const char*>(dev)};
     *out = p;
     return QPS_OK;
   }
-  unsigned int f = cudaHostAllocPortable | (flags == 1 ? cudaHostAllocWriteCombined : 0u);
+  unsigned int f = cudaHostAllocPortable | cudaHostAllocMapped | (flags == 1 ? cudaHostAllocWriteCombined : 0u);
   QPS_CUDA_TRY(cudaHostAlloc(out, bytes, f));
+  void* dev = nullptr;
+  cudaError_t e = cudaHostGetDevicePointer(&dev, *out, 0);
+  if (e != cudaSuccess) {
+    cudaFreeHost(*out);
+    *out = nullptr;
+    return cuda_fail(e, "host_alloc: cudaHostGetDevicePointer");
+  }
   std::lock_guard<std::mutex> lk(host_map_mutex());
-  host_map()[reinterpret_cast<uintptr_t>(*out)] = HostAlloc{bytes, false};
+  host_map()[reinterpret_cast<uintptr_t>(*out)] = HostAlloc{bytes, false, reinterpret_cast<const char*>(dev)};
   return QPS_OK;
 }
 
@@ -265,6 +351,12 @@ qps_status qps_ring_create(int32_t n_slots, size_t slot_bytes, int32_t device, q
   r->slot_bytes = align_up(slot_bytes, kPlaneAlign);
   qps_status st = QPS_OK;
   cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
+  // The copy kernel needs no shared memory; asking for the largest shared carveout keeps
+  // an SM that runs one of its CTAs configured for the attention CTAs beside it (with
+  // the default an SM could pick an L1-heavy split and turn the attention CTAs away)
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ring_copy_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   for (int s = 0; s < n_slots && e == cudaSuccess; ++s) {
     e = cudaMalloc(&r->slots[s], r->slot_bytes);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->copy_done[s], cudaEventDisableTiming);
@@ -309,6 +401,15 @@ qps_status qps_ring_destroy(qps_ring* r) {
   return QPS_OK;
 }
 
+qps_status qps_ring_set_copy_mode(qps_ring* r, int32_t mode) {
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_set_copy_mode: invalid or destroyed ring");
+  if (mode != QPS_RING_COPY_ENGINE && mode != QPS_RING_COPY_KERNEL)
+    return fail(QPS_ERR_INVALID_ARG, "ring_set_copy_mode: unknown mode");
+  if (r->open) return fail(QPS_ERR_STATE, "ring_set_copy_mode: a step is open");
+  r->copy_mode = mode;
+  return QPS_OK;
+}
+
 qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t n_tiles,
                                void* compute_stream) {
   (void)compute_stream;
@@ -316,6 +417,7 @@ qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t 
   if (r->open) return fail(QPS_ERR_STATE, "ring_begin_step: the previous step is still open");
   if (n_tiles < 0 || (n_tiles > 0 && !tiles)) return fail(QPS_ERR_INVALID_ARG, "ring_begin_step: bad tile list");
   std::vector<size_t> offsets((size_t)n_tiles * 6, 0), span((size_t)n_tiles, 0);
+  std::vector<KernelCopy> kcopy((size_t)n_tiles);
   for (int i = 0; i < n_tiles; ++i) {
     const qps_tile_desc& t = tiles[i];
     if (t.n_k_planes < 1 || t.n_k_planes > 3 || t.n_v_planes < 1 || t.n_v_planes > 3 || t.tokens < 0)
@@ -357,6 +459,30 @@ qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t 
       end = offsets[(size_t)i * 6 + p] + b;
     }
     span[i] = contiguous && in_one_host_alloc(h0, end) ? end : 0;
+    // the copy kernel takes the tile when every segment lies in a qps_host_alloc
+    // allocation and starts on a 16-byte boundary (slot offsets are 256-byte aligned)
+    KernelCopy kc{};
+    bool ok = true;
+    auto add = [&](const void* h, size_t off, size_t b) {
+      if (!ok || b == 0) return;
+      const char* dev = host_alloc_dev(h, b);
+      if (!dev || (reinterpret_cast<uintptr_t>(dev) & 15)) {
+        ok = false;
+        return;
+      }
+      kc.src[kc.n] = dev;
+      kc.off[kc.n] = off;
+      kc.bytes[kc.n] = b;
+      ++kc.n;
+    };
+    if (span[i]) {
+      add(h0, 0, span[i]);
+    } else {
+      for (int p = 0; p < t.n_k_planes; ++p) add(t.host_k[p], offsets[(size_t)i * 6 + p], t.bytes_k[p]);
+      for (int p = 0; p < t.n_v_planes; ++p) add(t.host_v[p], offsets[(size_t)i * 6 + 3 + p], t.bytes_v[p]);
+    }
+    if (!ok || r->copy_mode != QPS_RING_COPY_KERNEL) kc.n = 0;
+    kcopy[i] = kc;
   }
   int prev = 0;
   cudaGetDevice(&prev);
@@ -364,6 +490,7 @@ qps_status qps_ring_begin_step(qps_ring* r, const qps_tile_desc* tiles, int32_t 
   r->tiles.assign(tiles, tiles + n_tiles);
   r->offsets.swap(offsets);
   r->span.swap(span);
+  r->kcopy.swap(kcopy);
   r->next_consume = 0;
   r->open = true;
   const int first = n_tiles < r->n_slots ? n_tiles : r->n_slots;

@@ -44,10 +44,16 @@ class PositionSplitDecoder:
                  k_fmt: str, v_fmt: str, scale: float, softcap: float = 0.0, signs=None,
                  ring_slots: int = 3, tile_tokens: int = 8192, n_split_window: int = 0,
                  n_split_tail: int = 0, device=None, host_alloc_flags: int = 2,
-                 tail_k_fmt: Optional[str] = None, tail_v_fmt: Optional[str] = None):
+                 tail_k_fmt: Optional[str] = None, tail_v_fmt: Optional[str] = None,
+                 ring_copy: str = "kernel"):
         if not 0 <= wc <= n_kv:
             raise ValueError("need 0 <= wc <= n_kv")
         self.host_alloc_flags = host_alloc_flags
+        # "kernel": the ring's copy kernel moves the tail (arena) tiles: the copy engine's
+        # host-to-device transfers stall in bursts on some GB300 hosts (steps of 31 ms
+        # taking up to 320 ms) where SM loads of the same memory do not; "engine":
+        # cudaMemcpyAsync (5% faster when nothing stalls, and no SMs taken)
+        self.ring_copy = ring_copy
         self.layers, self.batch, self.hq, self.hkv, self.d = layers, batch, hq, hkv, d
         self.n_kv, self.wc = n_kv, wc
         self.k_fmt, self.v_fmt = k_fmt, v_fmt
@@ -124,7 +130,7 @@ class PositionSplitDecoder:
                 need = sum((x + 255) // 256 * 256 for x in list(td.bytes_k) + list(td.bytes_v))
                 slot_bytes = max(slot_bytes, need)
         if tiles:
-            self.ring = Ring(self.ring_slots, slot_bytes, self.device.index)
+            self.ring = Ring(self.ring_slots, slot_bytes, self.device.index, copy=self.ring_copy)
         layers, wlayers = [], []
         self._keep = []
         self.window_args = []

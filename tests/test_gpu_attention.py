@@ -315,3 +315,41 @@ def test_multi_query_paths_that_refuse(qps):
 def test_zz_no_bounded_wait_gave_up(qps):
     """Every tensor-core launch above finished its tile waits within their bounds."""
     qps.device_status(reset=True)
+
+
+@pytest.mark.parametrize("flags", [0, 2])
+@pytest.mark.parametrize("tokens", [7, 64, 333])
+def test_ring_copy_kernel_and_copy_engine_paths(qps, flags, tokens):
+    """With the ring's copy kernel selected, a tail tile whose planes live in a
+    qps_host_alloc arena is moved by that kernel (one more launch; plane sizes with a
+    ragged byte tail), the same tile in torch-pinned memory by cudaMemcpyAsync; both give
+    the oracle's answer."""
+    d, hq, hkv = 64, 4, 1
+    q, k, v = _inputs(tokens, hq, hkv, d, seed=tokens + flags)
+    words = synth.sign_bits(d, 42)
+    K = qps.encode_kv_head_major("q8_0", k.cuda(), words, pad=1)
+    V = qps.encode_kv_head_major("tq3", v.cuda(), words, pad=1)
+    kh = pipeline.dequant("q8_0", k.numpy())
+    vh = pipeline.dequant("tq3", v.numpy(), words.numpy())
+    ro, rl = oatt.gqa_decode(q.double().numpy(), kh, vh, 0.125)
+    arena = qps.HostArena(2 << 20, flags)
+    launches = []
+    for host, mode in (("arena", "kernel"), ("torch", "kernel"), ("arena", "engine")):
+        kt = arena.copy_in(K) if host == "arena" else K.pinned_copy()
+        vt = arena.copy_in(V) if host == "arena" else V.pinned_copy()
+        torch.cuda.synchronize()
+        ring = qps.Ring(2, 1 << 20, copy=mode)
+        parts = (torch.zeros((4, hq, d), device="cuda"), torch.zeros((4, hq), device="cuda"))
+        qps.launch_count(reset=True)
+        ring.begin_step([qps.tile_desc(kt, vt)])
+        a = qps.attn_args(q.cuda(), kt, vt, scale=0.125, v_signs=words, n_split=1)
+        ring.decode_tail(0, a, parts=parts, part_offset=0)
+        ring.end_step()
+        ring.sync()
+        launches.append(qps.launch_count())
+        o, lse = qps.lse_combine(parts[0][:1], parts[1][:1])
+        assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(hq, d), rl.reshape(hq), (host, mode, flags, tokens))
+        ring.close()
+    arena.close()
+    assert launches[0] == launches[1] + 1  # the arena tile's copy kernel
+    assert launches[2] == launches[1]      # the copy engine: no kernel

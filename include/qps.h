@@ -354,8 +354,8 @@ typedef struct qps_tile_desc {
  * qps_host_alloc memory (each on a 16-byte boundary) and the copy engine for the
  * others.  On GB300 hosts the copy engine's host-to-device transfers stall in bursts on
  * some boxes (single 1.3 ms transfers taking up to 50 ms) where SM loads of the same
- * memory do not; inside a decode step the copy kernel moves ~199 GB/s (the copy engine
- * 208) and slows the attention running beside it.  Takes effect from the next
+ * memory do not; inside a decode step the copy kernel moves ~196 GB/s (the copy engine
+ * 208 when it does not stall).  Takes effect from the next
  * qps_ring_begin_step.  Errors: STATE (invalid ring, open step), INVALID_ARG (mode). */
 #define QPS_RING_COPY_ENGINE 0
 #define QPS_RING_COPY_KERNEL 1

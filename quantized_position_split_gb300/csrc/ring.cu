@@ -113,12 +113,12 @@ qps_status check_pinned(const void* p, const char* what) {
 // streaming); the same transfers issued as loads by SMs ran at the same 211 GB/s without
 // them in every probe.
 // Every segment: n16 16-byte units (source and destination 16-byte aligned), then rem
-// bytes one by one.  Shape chosen by measuring the copy rate while window attention
-// runs back to back beside it (fp16 Qwen-like window, 28.6 us alone): 64 CTAs of 64
-// threads with sixteen 16-byte loads in flight per thread copy ~196 GB/s under that load
-// and leave the window at 33 us; the copy engine ~207 GB/s (when it does not stall) and
-// 41 us; 32 x 512 threads 197 GB/s and 58 us; 8 x 512 185 GB/s and 41 us.
-constexpr int kCopyCtas = 64, kCopyThreads = 64, kCopyUnroll = 16;
+// bytes one by one.  Shape chosen inside the decode step (fp16 Qwen-like stack): 64
+// CTAs of 64 threads with four 16-byte loads in flight per thread stream the tail at
+// ~196 GB/s and leave each window attention at ~39 us (alone 28.6 us); pushing the copy
+// to ~199 GB/s (sixteen loads in flight, or 304 x 32 threads) gains 1-2% of step time
+// but slows every window launch beside it to ~95 us.
+constexpr int kCopyCtas = 64, kCopyThreads = 64, kCopyUnroll = 4;
 
 struct CopySegs {
   const uint4* src[6];

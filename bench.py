@@ -53,6 +53,9 @@ def parse_args(argv=None):
                          "(f16, q8_0, or the V format's TurboQuant tier)")
     ap.add_argument("--ring-copy", choices=["engine", "kernel"], default="kernel",
                     help="how the ring moves tail tiles: the ring's copy kernel (default) or the copy engine")
+    ap.add_argument("--n-q", type=int, default=1,
+                    help="query tokens per step: > 1 runs verify-batch steps (batch 1, causal, the "
+                         "query tokens at the cache's last positions)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time the window decode-attention kernel alone on one layer of every "
                          "workload (one JSON line per workload; not the benchmark line)")
@@ -331,9 +334,11 @@ def run_ours(args):
                                n_kv=cfg.n_kv, wc=cfg.wc, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
                                scale=cfg.scale, softcap=cfg.softcap, signs=signs,
                                ring_slots=cfg.ring_slots, tile_tokens=cfg.tile_tokens, device=device,
-                               tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt, ring_copy=args.ring_copy)
+                               tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt, ring_copy=args.ring_copy,
+                               n_q=args.n_q)
     for layer in range(cfg.layers):
-        q = synth.query_f16(cfg, layer, device=device)
+        q = (synth.query_f16(cfg, layer, device=device) if args.n_q == 1 else
+             synth.randn_f16((1, args.n_q, cfg.hq, cfg.d), cfg.seed, cfg.name, "verify", layer, device=device))
         k = synth.kv_f16(cfg, layer, "k", cfg.n_kv, device=device)
         v = synth.kv_f16(cfg, layer, "v", cfg.n_kv, device=device)
         dec.load_layer(layer, k, v, q)
@@ -446,7 +451,7 @@ def run_ours(args):
 
     # roofline of the dominant kernel: the window decode-attention launch
     per_launch_bytes = window_bytes / L
-    rows = cfg.batch * cfg.hq
+    rows = dec.rows
     n_split_w = qps.attn_plan(dec.window_args[0])[0]
     q_bytes = rows * cfg.d * 2
     part_bytes = n_split_w * rows * (cfg.d + 1) * 4
@@ -482,7 +487,7 @@ def run_ours(args):
                    "hkv": cfg.hkv, "d": cfg.d, "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt,
                    "v_fmt": cfg.v_fmt, "tail_k_fmt": cfg.tk_fmt, "tail_v_fmt": cfg.tv_fmt,
                    "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
-                   "tile_tokens": cfg.tile_tokens, "ring_plan": ring_plan, "ring_copy": args.ring_copy,
+                   "tile_tokens": cfg.tile_tokens, "ring_plan": ring_plan, "ring_copy": args.ring_copy, "n_q": args.n_q,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" %
                          (window_bytes / 1e9, tail_bytes / 1e9)},

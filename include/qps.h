@@ -79,7 +79,7 @@
 extern "C" {
 #endif
 
-#define QPS_ABI_VERSION 3
+#define QPS_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define QPS_API __attribute__((visibility("default")))
@@ -246,10 +246,11 @@ typedef struct qps_attn_args {
    * causal != 0: query token i sees only the view positions p <= q_pos + i (positions
    * counted like kv_begin / kv_end); a token that sees none of [kv_begin, kv_end) gets
    * O = 0 and lse = -inf.  n_q > 1 or causal needs the tensor-core path (see
-   * qps_attn_path) and per-entry KV rows (batch_stride != 0 or batch == 1); the
-   * decode-step ring (qps_attn_decode_tail, qps_decode_step tails) takes n_q > 1 but
-   * not causal, since its tiles carry no position.  Zero-initialised fields keep the
-   * single-token behaviour. */
+   * qps_attn_path) and per-entry KV rows (batch_stride != 0 or batch == 1); in the
+   * decode-step ring (qps_attn_decode_tail, qps_decode_step tails) q_pos is given in
+   * the coordinates of the tiles' pos0 (qps_tile_desc), so that the newest positions of
+   * a verify batch may lie in the tail.  Zero-initialised fields keep the single-token
+   * behaviour. */
   int32_t n_q;
   int32_t causal;
   int64_t q_pos;
@@ -346,6 +347,9 @@ typedef struct qps_tile_desc {
   int64_t tokens;
   int64_t tok_stride;  /* rows; > 0 */
   int64_t head_stride; /* rows; >= 0 */
+  int64_t pos0;        /* position of the tile's first token in the coordinates of the
+                          attention's q_pos (the causal limit of a verify batch whose
+                          newest positions lie in the tail); 0 when unused */
 } qps_tile_desc;
 
 /* How the ring moves tiles: QPS_RING_COPY_ENGINE (the default) uses the copy engine
@@ -375,8 +379,9 @@ QPS_API qps_status qps_ring_begin_step(qps_ring* ring, const qps_tile_desc* tile
  * runs on the slot (the k / v views' data pointers in `a` are ignored and replaced by
  * the slot's planes, their token / head strides by the tile's, their batch strides by
  * 0 (one tile serves every batch entry); their fmt is used; kv_begin / kv_end are
- * replaced by [0, tokens)), compute_done is recorded, and the copy of tile tile_index + n_slots
- * into the same slot is enqueued behind it.  Output modes as for
+ * replaced by [0, tokens); with the causal limit, q_pos - pos0 of the tile), compute_done
+ * is recorded, and the copy of tile tile_index + n_slots into the same slot is enqueued
+ * behind it.  Output modes as for
  * qps_attn_decode_window.  Errors: STATE (out of order, no open step), INVALID_ARG,
  * UNSUPPORTED, CUDA. */
 QPS_API qps_status qps_attn_decode_tail(qps_ring* ring, int32_t tile_index, const qps_attn_args* a,

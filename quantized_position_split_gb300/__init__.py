@@ -274,6 +274,7 @@ def attn_args(q: torch.Tensor, k: KV, v: KV, *, scale: float, softcap: float = 0
         if q.stride(1) != hq * d or q.stride(2) != d or q.stride(3) != 1:
             raise QpsError(N.QPS_ERR_INVALID_ARG, "q [batch, n_q, hq, D] must be contiguous per batch entry")
     a = N.AttnArgs()
+    a._tensors = (q, k, v)  # the struct holds raw pointers: keep what they point to alive
     a.q = q.data_ptr()
     a.q_batch_stride = q.stride(0)
     a.batch, a.hq, a.hkv, a.d = batch, hq, k.hkv, d
@@ -391,14 +392,17 @@ def encode_kv_head_major(fmt: str, x: torch.Tensor, signs=None, pad: int = 16, s
               batch_stride=hkv * tp if batched else 0)
 
 
-def tile_desc(k_host: KV, v_host: KV, t0: Optional[int] = None, t1: Optional[int] = None) -> N.TileDesc:
+def tile_desc(k_host: KV, v_host: KV, t0: Optional[int] = None, t1: Optional[int] = None,
+              pos0: int = 0) -> N.TileDesc:
     """Ring descriptor of a pinned host tile.
 
     With ``t0, t1`` given, a token-major cache (row = token * hkv + head) is sliced to
     positions [t0, t1).  Without them, the cache is one whole tile described as it is
-    stored (e.g. head-major, ``encode_kv_head_major``).
+    stored (e.g. head-major, ``encode_kv_head_major``).  ``pos0``: the position of the
+    tile's first token in the coordinates of a causal q_pos.
     """
     td = N.TileDesc()
+    td.pos0 = int(pos0)
     if t0 is None:
         if (v_host.tok_stride, v_host.head_stride) != (1, k_host.head_stride):
             raise QpsError(N.QPS_ERR_INVALID_ARG, "K and V of a tile need the same layout")

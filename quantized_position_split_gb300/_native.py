@@ -91,6 +91,7 @@ class TileDesc(ctypes.Structure):
         ("tokens", c_int64),
         ("tok_stride", c_int64),
         ("head_stride", c_int64),
+        ("pos0", c_int64),
     ]
 
 

@@ -194,13 +194,13 @@ qps_status tail_attend(qps_ring* r, int idx, const qps_attn_args* a_in, cudaStre
   if (!valid_ring(r)) return fail(QPS_ERR_STATE, "decode_tail: invalid or destroyed ring");
   if (!r->open) return fail(QPS_ERR_STATE, "decode_tail: no open step");
   if (!a_in) return fail(QPS_ERR_INVALID_ARG, "decode_tail: args is NULL");
-  if (a_in->causal) return fail(QPS_ERR_UNSUPPORTED, "decode_tail: ring tiles carry no position; causal is not supported");
   if (idx != r->next_consume)
     return fail(QPS_ERR_STATE, "decode_tail: tiles must be consumed in schedule order (expected " +
                                    std::to_string(r->next_consume) + ", got " + std::to_string(idx) + ")");
   const qps_tile_desc& t = r->tiles[idx];
   const int slot = idx % r->n_slots;
   qps_attn_args a = *a_in;
+  if (a.causal) a.q_pos -= t.pos0;  // the kernel counts positions from the tile's start
   a.k.tok_stride = a.v.tok_stride = t.tok_stride;
   a.k.head_stride = a.v.head_stride = t.head_stride;
   if (t.n_k_planes != plane_count(a.k.fmt) || t.n_v_planes != plane_count(a.v.fmt))

@@ -38,16 +38,28 @@ class PositionSplitDecoder:
     section "2026-07-12 — #582-P2 SHIPPED: position-axis mixed KV (compressed tail,
     -ctkt/-ctvt)"): the recent positions keep the window's formats on the device, the
     tail ships fewer bytes per step, and each part is read at its own format.  Unset,
-    the tail uses the window's formats."""
+    the tail uses the window's formats.
+
+    ``n_q`` > 1 makes each step a verify batch ("F5 M6 — PolyKV", section "S2 perf-path
+    — turbo-MMA verify kernel"): q is [batch = 1, n_q, hq, D], the n_q query tokens are
+    the cache's last n_q positions, and with ``causal`` token i sees the positions up to
+    n_kv - n_q + i (they lie in the tail when the tail is non-empty: each tile carries
+    its first position to the ring)."""
 
     def __init__(self, *, layers: int, batch: int, hq: int, hkv: int, d: int, n_kv: int, wc: int,
                  k_fmt: str, v_fmt: str, scale: float, softcap: float = 0.0, signs=None,
                  ring_slots: int = 3, tile_tokens: int = 8192, n_split_window: int = 0,
                  n_split_tail: int = 0, device=None, host_alloc_flags: int = 2,
                  tail_k_fmt: Optional[str] = None, tail_v_fmt: Optional[str] = None,
-                 ring_copy: str = "kernel"):
+                 ring_copy: str = "kernel", n_q: int = 1, causal: bool = True):
         if not 0 <= wc <= n_kv:
             raise ValueError("need 0 <= wc <= n_kv")
+        if n_q > 1 and batch != 1:
+            raise ValueError("a verify batch (n_q > 1) decodes one sequence (batch 1)")
+        if not 1 <= n_q <= min(64, max(n_kv, 1)):
+            raise ValueError("need 1 <= n_q <= min(64, n_kv)")
+        self.n_q = n_q
+        self.q_pos = n_kv - n_q if (n_q > 1 and causal) else None
         self.host_alloc_flags = host_alloc_flags
         # "kernel": the ring's copy kernel moves the tail (arena) tiles: the copy engine's
         # host-to-device transfers stall in bursts on some GB300 hosts (steps of 31 ms
@@ -63,8 +75,9 @@ class PositionSplitDecoder:
         self.ring_slots, self.tile_tokens = ring_slots, tile_tokens
         self.n_split_window, self.n_split_tail = n_split_window, n_split_tail
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-        self.rows = batch * hq
-        self.q = torch.zeros((layers, batch, hq, d), dtype=torch.float16, device=self.device)
+        self.rows = batch * n_q * hq
+        qshape = (layers, batch, hq, d) if n_q == 1 else (layers, batch, n_q, hq, d)
+        self.q = torch.zeros(qshape, dtype=torch.float16, device=self.device)
         self.o = torch.zeros((layers, self.rows, d), dtype=torch.float32, device=self.device)
         self.lse = torch.zeros((layers, self.rows), dtype=torch.float32, device=self.device)
         self.window: List[Optional[tuple]] = [None] * layers  # (K, V) on device
@@ -110,22 +123,22 @@ class PositionSplitDecoder:
         for a, b in ranges:
             kt = encode_kv_head_major(self.tail_k_fmt, k16[self.wc + a:self.wc + b], self.signs)
             vt = encode_kv_head_major(self.tail_v_fmt, v16[self.wc + a:self.wc + b], self.signs)
-            tiles.append((self.arena.copy_in(kt), self.arena.copy_in(vt)))
+            tiles.append((self.arena.copy_in(kt), self.arena.copy_in(vt), self.wc + a))
         self.tail[layer] = tiles
         if q16 is not None:
             self.q[layer].copy_(q16)
 
     def _args(self, layer, k: KV, v: KV, n_split: int):
         return attn_args(self.q[layer], k, v, scale=self.scale, softcap=self.softcap,
-                         v_signs=self.signs, n_split=n_split)
+                         v_signs=self.signs, n_split=n_split, q_pos=self.q_pos)
 
     def build(self):
         """Create the ring, the flat (layer, tile) schedule and the step plans."""
         tiles = []
         slot_bytes = 0
         for layer in range(self.layers):
-            for kt, vt in self.tail[layer]:
-                td = tile_desc(kt, vt)
+            for kt, vt, pos0 in self.tail[layer]:
+                td = tile_desc(kt, vt, pos0=pos0)
                 tiles.append(td)
                 need = sum((x + 255) // 256 * 256 for x in list(td.bytes_k) + list(td.bytes_v))
                 slot_bytes = max(slot_bytes, need)
@@ -143,7 +156,7 @@ class PositionSplitDecoder:
                 parts.append(wargs)
                 cap += attn_plan(wargs)[0]
             tail_tpl = None
-            for kt, vt in self.tail[layer]:
+            for kt, vt, _ in self.tail[layer]:
                 probe = self._args(layer, kt, vt, self.n_split_tail)
                 cap += attn_plan(probe)[0]
                 if tail_tpl is None:
@@ -174,7 +187,7 @@ class PositionSplitDecoder:
         return sum(kv.nbytes() for w in self.window if w is not None for kv in w)
 
     def tail_bytes(self) -> int:
-        return sum(kv.nbytes() for t in self.tail for tile in t for kv in tile)
+        return sum(kv.nbytes() for t in self.tail for tile in t for kv in tile[:2])
 
     def close(self):
         """Release the ring (after its copies finish), the plans and the host arena."""

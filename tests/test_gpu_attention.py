@@ -274,12 +274,10 @@ def test_multi_query_verify_batch(qps, d, kf, vf, softcap, n_q, batch):
 
 
 def test_multi_query_paths_that_refuse(qps):
-    """Multi-query needs the tensor-core path and per-entry KV; the ring refuses a
-    causal limit (its tiles carry no position)."""
+    """Multi-query needs the tensor-core path and per-entry KV."""
     from quantized_position_split_gb300 import _native as N
-    d, hq, hkv, n = 128, 4, 1, 64
-    q = torch.randn((1, 3, hq, d)).half().cuda()
-    k = torch.randn((n, hkv, d)).half().cuda()
+    d, hq, n = 128, 4, 64
+    k = torch.randn((n, 1, d)).half().cuda()
     k2 = torch.randn((n, 2, d)).half().cuda()  # token-major, 2 heads: not token-contiguous
     Kt2 = qps.encode_kv("f16", k2)
     a = qps.attn_args(torch.randn((1, 3, 2, d)).half().cuda(), Kt2, Kt2, scale=0.1)
@@ -292,24 +290,32 @@ def test_multi_query_paths_that_refuse(qps):
     with pytest.raises(N.QpsError) as e:
         qps.attn_plan(a)
     assert e.value.status == N.QPS_ERR_UNSUPPORTED
-    kh = Kh.pinned_copy()
+
+
+@pytest.mark.parametrize("pos0,q_pos", [(0, 10), (100, 130), (1000, 1061), (100, 50), (0, None)])
+def test_ring_tile_causal_limit_from_its_first_position(qps, pos0, q_pos):
+    """A tail tile whose first token sits at view position pos0: a causal q_pos in view
+    coordinates limits query token i to the tile positions <= q_pos + i - pos0 (none at
+    all when q_pos is before the tile)."""
+    d, hq, n, n_q = 128, 4, 64, 3
+    g = torch.Generator().manual_seed(pos0 + (q_pos or 0))
+    q = torch.randn((1, n_q, hq, d), generator=g).half()
+    k = torch.randn((n, 1, d), generator=g).half()
+    v = torch.randn((n, 1, d), generator=g).half()
+    kh = qps.encode_kv_head_major("f16", k.cuda()).pinned_copy()
+    vh = qps.encode_kv_head_major("f16", v.cuda()).pinned_copy()
     ring = qps.Ring(2, 1 << 20)
-    ring.begin_step([qps.tile_desc(kh, kh)])
-    ta = qps.attn_args(q, kh, kh, scale=0.1, q_pos=10)
-    parts = (torch.zeros((8, 3 * hq, d), device="cuda"), torch.zeros((8, 3 * hq), device="cuda"))
-    with pytest.raises(N.QpsError) as e:
-        ring.decode_tail(0, ta, parts=parts, part_offset=0)
-    assert e.value.status == N.QPS_ERR_UNSUPPORTED
-    ta = qps.attn_args(q, kh, kh, scale=0.1)  # n_q > 1 without the causal limit is fine
+    ring.begin_step([qps.tile_desc(kh, vh, pos0=pos0)])
+    ta = qps.attn_args(q.cuda(), kh, vh, scale=0.1, q_pos=q_pos, n_split=2)
+    parts = (torch.zeros((8, n_q * hq, d), device="cuda"), torch.zeros((8, n_q * hq), device="cuda"))
     ring.decode_tail(0, ta, parts=parts, part_offset=0)
     ring.end_step()
     ring.sync()
     ring.close()
-    n_split = qps.attn_plan(ta)[0]
-    o, lse = qps.lse_combine(parts[0][:n_split], parts[1][:n_split])
-    ro, rl = oatt.multi_query_decode(q[0].double().cpu().numpy(), k.double().cpu().numpy(),
-                                     k.double().cpu().numpy(), 0.1)
-    assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(3 * hq, d), rl.reshape(3 * hq))
+    o, lse = qps.lse_combine(parts[0][:2], parts[1][:2])
+    ro, rl = oatt.multi_query_decode(q[0].numpy(), k.double().numpy(), v.double().numpy(), 0.1,
+                                     q_pos=None if q_pos is None else q_pos - pos0)
+    assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(-1, d), rl.reshape(-1), (pos0, q_pos))
 
 
 def test_zz_no_bounded_wait_gave_up(qps):

@@ -39,6 +39,41 @@ def test_workload_step_parity(qps, name):
     dec.close()
 
 
+@pytest.mark.parametrize("name", ["qwen14b_q8", "qwen14b_q8_tq3vtail", "gemma_global_q8k_tq3v", "qwen14b_q8_tq3kvtail"])
+@pytest.mark.parametrize("n_q", [2, 5])
+@pytest.mark.parametrize("causal", [True, False])
+def test_verify_batch_through_the_split(qps, name, n_q, causal):
+    """A verify batch: n_q query tokens at the cache's last positions (in the host tail)
+    through window + ring tail + combine; with the causal limit each tile's first
+    position reaches the ring.  Small tiles put the limit inside the last tile."""
+    from quantized_position_split_gb300.decode import PositionSplitDecoder
+    from oracle import attention as oatt
+    from oracle import pipeline
+    cfg = synth.parity_scaled(synth.by_name(name), layers=1)
+    dec = PositionSplitDecoder(layers=1, batch=1, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d, n_kv=cfg.n_kv, wc=cfg.wc,
+                               k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt, scale=cfg.scale, softcap=cfg.softcap,
+                               signs=helpers.signs_for(cfg), ring_slots=3, tile_tokens=448,
+                               tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt, n_q=n_q, causal=causal)
+    q4 = synth.randn_f16((1, n_q, cfg.hq, cfg.d), cfg.seed, cfg.name, "verify", n_q, device="cuda")
+    k = synth.kv_f16(cfg, 0, "k", cfg.n_kv, device="cuda")
+    v = synth.kv_f16(cfg, 0, "v", cfg.n_kv, device="cuda")
+    dec.load_layer(0, k, v, q4)
+    dec.build()
+    for _ in range(2):
+        dec.step()
+        torch.cuda.synchronize()
+        sw = helpers.oracle_signs(cfg)
+        kn, vn = k.cpu().numpy(), v.cpu().numpy()
+        kh = np.concatenate([pipeline.dequant(cfg.k_fmt, kn[:cfg.wc], sw), pipeline.dequant(cfg.tk_fmt, kn[cfg.wc:], sw)])
+        vh = np.concatenate([pipeline.dequant(cfg.v_fmt, vn[:cfg.wc], sw), pipeline.dequant(cfg.tv_fmt, vn[cfg.wc:], sw)])
+        ro, rl = oatt.multi_query_decode(q4[0].cpu().numpy(), kh, vh, cfg.scale, cfg.softcap,
+                                         q_pos=cfg.n_kv - n_q if causal else None)
+        assert_parity(dec.o[0].cpu().numpy(), dec.lse[0].cpu().numpy(), ro.reshape(-1, cfg.d), rl.reshape(-1),
+                      (name, n_q, causal))
+    dec.ring.sync()
+    dec.close()
+
+
 def test_fanout_parity(qps):
     from quantized_position_split_gb300.decode import FanoutDecoder
     cfg = synth.parity_scaled(synth.by_name("fanout_prefix"))

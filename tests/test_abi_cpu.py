@@ -194,11 +194,28 @@ def test_encoder_and_combine_validation(lib):
     assert lib.qps_lse_combine(None, None, 2, 0, 128, None, None, None) == N.QPS_OK  # no rows
 
 
+def test_binding_tables_match_the_header():
+    """The binding's plane sizes and format / copy-mode numbers are the header's."""
+    import quantized_position_split_gb300 as qps
+    text = open(HEADER).read()
+    for name, val in (("QPS_FMT_TQ2", N.FMT_TQ2), ("QPS_FMT_TQ4", N.FMT_TQ4), ("QPS_FMT_TQ3", N.FMT_TQ3)):
+        assert re.search(r"%s = %d\b" % (name, val), text), name
+    for name, val in (("QPS_RING_COPY_ENGINE", qps.RING_COPY["engine"]), ("QPS_RING_COPY_KERNEL", qps.RING_COPY["kernel"])):
+        assert re.search(r"#define %s %d\b" % (name, val), text), name
+    d = 256
+    assert qps.plane_row_bytes("tq2", d) == [d // 4, 2] and qps.plane_row_bytes("tq4", d) == [d // 2, 2]
+    assert qps.plane_row_bytes("tq3", d) == [d // 4, d // 8, 2] and qps.plane_row_bytes("q8_0", d) == [d, d // 16]
+    from oracle import turboquant as tq
+    for bits, fmt in ((2, "tq2"), (3, "tq3"), (4, "tq4")):  # the binding's sizes are the oracle's bytes per value
+        assert (sum(qps.plane_row_bytes(fmt, d))) / d == tq.bytes_per_value(d, bits)
+
+
 def test_ring_and_step_state_errors(lib):
     assert lib.qps_ring_end_step(None) == N.QPS_ERR_STATE
     assert lib.qps_ring_sync(None, 10) == N.QPS_ERR_STATE
     assert lib.qps_attn_decode_tail(None, 0, None, None) == N.QPS_ERR_STATE
     assert lib.qps_ring_destroy(None) == N.QPS_OK
+    assert lib.qps_ring_set_copy_mode(None, 0) == N.QPS_ERR_STATE
     h = ctypes.c_void_p()
     assert lib.qps_ring_create(5, 1024, 0, ctypes.byref(h)) == N.QPS_ERR_INVALID_ARG
     # a step whose layers announce tiles but no ring is given

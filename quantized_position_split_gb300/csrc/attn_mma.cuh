@@ -336,6 +336,13 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint8_t* pipe = smem;
 
+  // Programmatic dependent launch: this grid may start while the previous kernel on
+  // the stream finishes (the launch sets the attribute); everything it reads or writes
+  // in global memory (q, the KV cache a preceding kernel may have appended to, the
+  // partial outputs) is touched only after the previous grid has completed.  The next
+  // grid is released once this CTA's tiles are done (after its main loop), so that its
+  // CTAs do not sit resident beside this grid's for the whole stream.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   // the row groups of one (chunk, KV head) are adjacent CTAs, so they stream the same
@@ -1118,6 +1125,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   }
   cp_async_wait<0>();
   __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" :::);
 
   // ---- merge the warps' states, then the chunk's partial ------------------------------
   float* mw = reinterpret_cast<float*>(smem);  // [kWarps][ROWS]
@@ -1261,11 +1269,32 @@ qps_status launch_mma_t(const AttnParams& p, cudaStream_t s) {
     if (!encode_plane_map(&maps.va, p.v.aux, G::V_ARB, p.end, p.hkv, p.v.head, nb, p.v.batch, G::PVA::IB, G::PVA::SW, G::TT))
       return QPS_ERR_CUDA;
   auto kern = attn_mma_kernel<D, KF, VF, NTW, CAUSAL>;
-  QPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  // Ask for enough shared memory that no more than G::CTAS CTAs fit on an SM: under
+  // programmatic launch the next grid's CTAs would otherwise take a spare slot early
+  // and pile three of them onto some SMs (the q8_0 Qwen-like window: 39.5 -> 45 us).
+  constexpr size_t kSmPerSm = 228 * 1024, kReserved = 1024;
+  constexpr size_t smem_floor = kSmPerSm / (G::CTAS + 1) - kReserved + 1;
+  constexpr size_t smem_launch = smem > smem_floor ? smem : smem_floor;
+  static_assert(G::CTAS * (smem_launch + kReserved) <= kSmPerSm || smem_launch == smem,
+                "the padding must not cost a CTA per SM");
+  QPS_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_launch));
   constexpr int ROWS = 8 * NTW;
   const int rgroups = (p.rows_per_cta + ROWS - 1) / ROWS;
   const dim3 grid(p.n_split * rgroups, p.hkv, p.shared ? 1 : p.batch);
-  kern<<<grid, G::NW * 32, smem, s>>>(p, maps);
+  // launched with programmatic stream serialization: overlaps this grid's launch with
+  // the end of the previous kernel on the stream (the kernel waits before any global
+  // memory access)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(G::NW * 32);
+  cfg.dynamicSmemBytes = smem_launch;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  QPS_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, p, maps));
   count_launch();
   QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;

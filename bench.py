@@ -62,6 +62,22 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
+def max_over_ranks(torch, value: float, world: int, device) -> float:
+    """The slowest rank's figure, on every rank (an all-reduce MAX over the job's process
+    group; the identity for one rank)."""
+    if world <= 1:
+        return value
+    tt = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_rate(world: int, bytes_per_rank: float, ms_per_step: float) -> float:
+    """Aggregate GB/s of the job: every rank (one replica of the workload) processes its
+    own bytes each step, timed by the slowest rank."""
+    return world * bytes_per_rank / (ms_per_step / 1e3) / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -412,11 +428,7 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     set_events(None)
-    step_ms = t0.elapsed_time(t1) / K
-    if world > 1:
-        tt = torch.tensor([step_ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(torch, t0.elapsed_time(t1) / K, world, device)
     win_ms = [ev[i][layer][0].elapsed_time(ev[i][layer][1]) for i in range(K) for layer in range(L)]
     win_launch_ms = statistics.mean(win_ms)
     per_step = [t0.elapsed_time(bounds[0])] + [bounds[i - 1].elapsed_time(bounds[i]) for i in range(1, K)]
@@ -442,10 +454,7 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / K
     h2d = q_host.numel() * q_host.element_size()
     d2h = o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size()
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(torch, e2e_ms, world, device)
 
     dec.ring.sync()
 
@@ -468,7 +477,7 @@ def run_ours(args):
         b, s, sample = time_oracle(cfg, oracle_layers_for(cfg, args.cpu_layers))
         cpu = {"value": b / s / 1e9, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                "sample": sample + f"; CPU {cpu_model()}"}
-    value = world * kv_bytes / (step_ms / 1e3) / 1e9
+    value = whole_job_rate(world, kv_bytes, step_ms)
     out = {
         "metric": METRIC,
         "value": value,
@@ -502,7 +511,7 @@ def run_ours(args):
                  "link_probe_gbs": link_gbs, "host_memcpy_1thread_gbs": host_memcpy_gbs,
                  "steps_per_s": 1000.0 / step_ms, "per_step": step_dist},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * kv_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+        "e2e": {"value": whole_job_rate(world, kv_bytes, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clk,

@@ -95,7 +95,7 @@ CONFIGS = [
         v_fmt="f16",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=8192,
+        tile_tokens=16384,
     ),
     Workload(
         name="qwen14b_q8",
@@ -111,7 +111,7 @@ CONFIGS = [
         v_fmt="q8_0",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=8192,
+        tile_tokens=16384,
     ),
     Workload(
         name="gemma_global_q8k_tq3v",
@@ -128,7 +128,7 @@ CONFIGS = [
         softcap=50.0,
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=16384,
+        tile_tokens=32768,
     ),
     # the same Qwen-like stacks with a more compressed tail than window (the tail's own
     # K / V storage formats)
@@ -148,7 +148,7 @@ CONFIGS = [
         tail_v_fmt="q8_0",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=8192,
+        tile_tokens=16384,
     ),
     Workload(
         name="qwen14b_q8_tq3vtail",
@@ -166,7 +166,7 @@ CONFIGS = [
         tail_v_fmt="tq3",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=8192,
+        tile_tokens=16384,
     ),
     # the smallest tail: V at the 2-bit TurboQuant tier
     Workload(
@@ -185,7 +185,7 @@ CONFIGS = [
         tail_v_fmt="tq2",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=8192,
+        tile_tokens=16384,
     ),
     # a tail with K and V both at the 3-bit TurboQuant tier (K read in the rotated domain)
     Workload(
@@ -204,7 +204,7 @@ CONFIGS = [
         tail_v_fmt="tq3",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=8192,
+        tile_tokens=16384,
     ),
     # the Gemma-like global layers with the rotation the pages' fork runs at head_dim 512:
     # four independent 128-wide Hadamard blocks between two sign vectors
@@ -223,7 +223,7 @@ CONFIGS = [
         softcap=50.0,
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=16384,
+        tile_tokens=32768,
         sign_seed2=43,
         rot_block=128,
     ),

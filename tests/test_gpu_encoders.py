@@ -127,3 +127,34 @@ def test_encoders_row_stride(qps):
     lo2, hi1, n = qps.kv_quant_tq3(x.cuda()[:, :128], words)
     rlo, rhi, rn = otq.encode(xs.contiguous().numpy(), words.numpy())
     assert np.array_equal(lo2.cpu().numpy(), rlo) and np.array_equal(hi1.cpu().numpy(), rhi)
+
+
+@pytest.mark.parametrize("d", [32, 128, 512])
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_tq_exact_ties_bit_exact(qps, d, bits):
+    """Rows whose rotated coordinates sit exactly on the middle threshold, 0: with
+    x = c s_i e_i + c s_j e_j the sign diagonal is undone, H (s * x) is +-2c at half the
+    coordinates and exactly 0 at the other half.  The oracle puts a coordinate on a
+    threshold in the upper cell; the GPU encoders must agree bit for bit."""
+    words = synth.sign_bits(d, 42)
+    s = otq.signs_from_words(words.numpy(), d)
+    rng = np.random.default_rng(1000 + d + bits)
+    x = np.zeros((64, d))
+    for r in range(64):
+        i, j = rng.choice(d, 2, replace=False)
+        c = 2.0 ** int(rng.integers(-6, 7))
+        x[r, i], x[r, j] = s[i] * c, s[j] * c
+    x16 = x.astype(np.float16)
+    planes, rn = otq.encode_tier(x16, words.numpy(), bits)
+    k = otq.codes_from_tier_planes(planes, d, bits)
+    assert (k == (1 << bits) // 2).sum() >= 64 * d // 2  # the ties took the upper cell
+    xt = torch.from_numpy(x16).cuda()
+    if bits == 3:
+        lo2, hi1, n = qps.kv_quant_tq3(xt, words)
+        got = (lo2.cpu().numpy(), hi1.cpu().numpy())
+    else:
+        codes, n = (qps.kv_quant_tq2 if bits == 2 else qps.kv_quant_tq4)(xt, words)
+        got = (codes.cpu().numpy(),)
+    assert np.array_equal(n.cpu().numpy().view(np.uint16), rn.view(np.uint16))
+    for g, want in zip(got, planes):
+        assert np.array_equal(g, want)

@@ -133,3 +133,24 @@ def test_bytes_per_value_matches_pages():
     row = [r for r in golden_rows("polykv_storage_and_roundtrip.txt")
            if r[0] == "bytes_per_value" and r[1] == "turbo3"][0]
     assert abs(tq.bytes_per_value(128) - float(row[2])) <= 0.5 * 10 ** -int(row[3])
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("d", [32, 128, 512])
+def test_exact_tie_takes_the_upper_cell(d, bits):
+    """With every sign +1, x = e_0 + e_1 gives H x = 2 at the even and exactly 0 at the
+    odd coordinates (column 0 of H is all ones, column 1 alternates in sign).  0 is the
+    threshold between the two middle levels of every symmetric codebook, so the odd
+    coordinates sit exactly on a threshold and must take the upper cell, index L / 2;
+    the even ones (z = sqrt 2, away from every threshold) take the nearest level."""
+    n_levels = 1 << bits
+    x16 = np.zeros((1, d), dtype=np.float16)
+    x16[0, :2] = 1.0
+    words = np.zeros(d // 32, dtype=np.uint32)  # s = +1 everywhere
+    levels, thr = tq.codebook(n_levels)
+    assert thr[n_levels // 2 - 1] == 0.0
+    planes, n16 = tq.encode_tier(x16, words, bits)
+    k = tq.codes_from_tier_planes(planes, d, bits)[0]
+    assert np.all(k[1::2] == n_levels // 2)
+    assert np.min(np.abs(thr.astype(np.float64) - np.sqrt(2.0))) > 1e-2
+    assert np.all(k[0::2] == np.argmin(np.abs(levels.astype(np.float64) - np.sqrt(2.0))))

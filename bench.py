@@ -78,6 +78,25 @@ def whole_job_rate(world: int, bytes_per_rank: float, ms_per_step: float) -> flo
     return world * bytes_per_rank / (ms_per_step / 1e3) / 1e9
 
 
+def step_distribution(per_step_ms):
+    """Distribution of the timed steps' durations: median, 10th / 90th percentiles
+    (linear interpolation between order statistics), extremes, and the number of
+    steps longer than 1.25 x the median."""
+    xs = sorted(float(x) for x in per_step_ms)
+    if not xs:
+        raise ValueError("no timed steps")
+
+    def pct(p):
+        pos = p * (len(xs) - 1)
+        lo = int(pos)
+        hi = min(lo + 1, len(xs) - 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (pos - lo)
+
+    p50 = statistics.median(xs)
+    return {"p50_ms": p50, "p10_ms": pct(0.10), "p90_ms": pct(0.90), "min_ms": xs[0], "max_ms": xs[-1],
+            "slow_steps": sum(1 for x in xs if x > 1.25 * p50)}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -92,14 +111,27 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_model() -> str:
-    try:
-        with open("/proc/cpuinfo") as f:
-            for line in f:
-                if line.lower().startswith(("model name", "cpu part")):
-                    return line.split(":", 1)[1].strip()
-    except OSError:
-        pass
+# Arm CPU part numbers (the "CPU part" field of /proc/cpuinfo on Arm Linux hosts)
+ARM_CPU_PARTS = {"0xd0c": "Arm Neoverse N1", "0xd40": "Arm Neoverse V1", "0xd49": "Arm Neoverse N2",
+                 "0xd4f": "Arm Neoverse V2"}
+
+
+def cpu_model(cpuinfo_text=None) -> str:
+    """The host CPU's name: x86 "model name", or the Arm "CPU part" number (named when
+    known)."""
+    if cpuinfo_text is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                cpuinfo_text = f.read()
+        except OSError:
+            return "unknown"
+    for line in cpuinfo_text.splitlines():
+        key = line.split(":", 1)[0].strip().lower()
+        if key == "model name":
+            return line.split(":", 1)[1].strip()
+        if key == "cpu part":
+            part = line.split(":", 1)[1].strip().lower()
+            return f"{ARM_CPU_PARTS[part]} (CPU part {part})" if part in ARM_CPU_PARTS else f"CPU part {part}"
     return "unknown"
 
 
@@ -432,9 +464,7 @@ def run_ours(args):
     win_ms = [ev[i][layer][0].elapsed_time(ev[i][layer][1]) for i in range(K) for layer in range(L)]
     win_launch_ms = statistics.mean(win_ms)
     per_step = [t0.elapsed_time(bounds[0])] + [bounds[i - 1].elapsed_time(bounds[i]) for i in range(1, K)]
-    p50 = statistics.median(per_step)
-    step_dist = {"p50_ms": p50, "min_ms": min(per_step), "max_ms": max(per_step),
-                 "slow_steps": sum(1 for x in per_step if x > 1.25 * p50)}
+    step_dist = step_distribution(per_step)
 
     # end to end through the public API with host buffers: q in, (o, lse) out each step
     q_host = torch.empty_like(dec.q, device="cpu").pin_memory()

@@ -79,7 +79,7 @@
 extern "C" {
 #endif
 
-#define QPS_ABI_VERSION 4
+#define QPS_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define QPS_API __attribute__((visibility("default")))
@@ -455,6 +455,15 @@ QPS_API qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, void* 
  * device's pending work to reach it on the legacy stream) and clears it if `reset`.
  * Errors: TIMEOUT (some wait gave up since the last reset), CUDA. */
 QPS_API qps_status qps_device_status(int32_t reset);
+
+/* Self-test of the bounded waits above (no counterpart on the pages: it exists so that
+ * the give-up path of a wait can be exercised on a GPU without any fault).  Enqueues on
+ * `stream` one CTA of one warp that waits, with the same bounded wait the attention
+ * kernels use on their tile copies, on a shared-memory barrier nothing ever arrives
+ * on; after 256 polls of at most ~1 ms it sets the device error word and exits.  A
+ * following qps_device_status then returns QPS_ERR_TIMEOUT (reset clears it).  The
+ * call itself returns QPS_OK once the launch is enqueued.  Errors: CUDA. */
+QPS_API qps_status qps_selftest_bounded_wait(void* stream);
 
 /* Number of kernel launches the calling thread has issued through this library
  * since the last reset (reset if `reset` is non-zero).  Host only. */

@@ -99,6 +99,13 @@ def device_status(reset: bool = True) -> None:
     N.check(lib().qps_device_status(1 if reset else 0))
 
 
+def selftest_bounded_wait(stream=None) -> None:
+    """Enqueue the library's self-test of its bounded in-kernel waits: one warp waits on
+    a barrier nothing arrives on, gives up after well under a second and sets the device
+    error word, so that the next ``device_status()`` raises QpsError(QPS_ERR_TIMEOUT)."""
+    N.check(lib().qps_selftest_bounded_wait(_stream(stream)))
+
+
 def tq3_codebook():
     """The library's fixed TQ3 codebook: (8 levels, 7 thresholds) as Python floats."""
     lv = (ctypes.c_float * 8)()

@@ -143,6 +143,7 @@ SIGNATURES = [
     ("qps_decode_step", c_int32, [c_void_p, POINTER(TileDesc), c_int32, POINTER(LayerStep), c_int32, c_void_p]),
     ("qps_attn_decode_window_noalloc", c_int32, [POINTER(AttnArgs), c_void_p]),
     ("qps_device_status", c_int32, [c_int32]),
+    ("qps_selftest_bounded_wait", c_int32, [c_void_p]),
     ("qps_launch_count", c_int64, [c_int32]),
     ("qps_plan_ring", c_int32, [c_double, c_double, c_double, c_double, POINTER(c_int32), POINTER(c_int32),
                                 POINTER(c_double), POINTER(c_double)]),

@@ -298,6 +298,25 @@ def attention_source_sha():
     return h.hexdigest()[:16]
 
 
+def window_signature(cfg):
+    """What decides the window launch's kernel and its bytes: shapes, window length,
+    formats, softcap and rotation (not the layer count or the tail's formats)."""
+    return (cfg.kind, cfg.batch, cfg.hq, cfg.hkv, cfg.d, cfg.wc, cfg.k_fmt, cfg.v_fmt, cfg.softcap,
+            cfg.sign_seed, cfg.sign_seed2, cfg.rot_block)
+
+
+def traffic_workload(cfg, configs) -> str:
+    """The workload whose window-kernel DRAM traffic file serves ``cfg``: ``cfg`` itself,
+    or the workload whose window launch is the same kernel on the same window (a
+    mixed-format tail changes only the tail's kernels)."""
+    if not cfg.mixed:
+        return cfg.name
+    for c in configs:
+        if not c.mixed and window_signature(c) == window_signature(cfg):
+            return c.name
+    return cfg.name
+
+
 def committed_traffic(workload: str):
     path = os.path.join(ROOT, "profiles", f"attn_window_{workload}_traffic.json")
     try:
@@ -531,7 +550,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" %
                          (window_bytes / 1e9, tail_bytes / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": committed_traffic(cfg.name),
+                     "frac": achieved / peak, "traffic": committed_traffic(traffic_workload(cfg, synth.CONFIGS)),
                      "kernel": "window decode attention (one launch per layer)",
                      "algorithmic_bytes_per_launch": algo_bytes, "launch_ms": win_launch_ms,
                      "peak_source": peak_kind},

@@ -34,3 +34,19 @@ def test_cpu_model_from_cpuinfo_text():
     assert bench.cpu_model("CPU part\t: 0xabc\n") == "CPU part 0xabc"
     assert bench.cpu_model("") == "unknown"
     assert bench.cpu_model() != ""
+
+
+def test_traffic_file_of_a_mixed_tail_is_its_window_kernels():
+    import synth
+    names = {c.name: bench.traffic_workload(c, synth.CONFIGS) for c in synth.CONFIGS if c.kind == "split"}
+    assert names["qwen14b_f16"] == "qwen14b_f16" and names["qwen14b_q8"] == "qwen14b_q8"
+    assert names["qwen14b_f16_q8tail"] == "qwen14b_f16"
+    for mixed in ("qwen14b_q8_tq3vtail", "qwen14b_q8_tq2vtail", "qwen14b_q8_tq3kvtail"):
+        assert names[mixed] == "qwen14b_q8"
+    # another rotation is another kernel: the two-sign block rotation keeps its own name
+    assert names["gemma_global_q8k_tq3v_r128"] == "gemma_global_q8k_tq3v_r128"
+    for c in synth.CONFIGS:
+        if c.kind == "split" and c.mixed:
+            w = synth.by_name(names[c.name])
+            assert (w.wc, w.hkv, w.d, w.k_fmt, w.v_fmt) == (c.wc, c.hkv, c.d, c.k_fmt, c.v_fmt)
+    assert bench.committed_traffic("qwen14b_q8") is not None  # the committed figure is current

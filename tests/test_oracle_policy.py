@@ -64,3 +64,14 @@ def test_ring_plan_boundaries():
     assert policy.ring_plan(2.0, 200.0, 10e9, 1e6)[0] == 4    # large budget: at most 4
     assert policy.ring_plan(2.0, 200.0, 1e9, 0)[1:3] == (0, 0)  # no tail: no tiles
     assert policy.ring_plan(2.0, 200.0, 1e9, 320e6)[1] == 1    # exactly one tile
+
+
+@pytest.mark.parametrize("tail", [1000e6 + 1, 999_999_999.0, 7.0, 641e6, 123_456_789.0])
+def test_ring_tiles_cover_a_tail_that_does_not_divide(tail):
+    """Brute force over tile counts: the plan takes the fewest equal tiles no larger
+    than the maximum, and those tiles (whole bytes) cover the whole tail."""
+    n, tiles, tb, tmax = policy.ring_plan(2.0, 200.0, 1e9, tail)
+    fewest = next(t for t in range(1, 10 ** 6) if tail / t <= tmax)
+    assert tiles == fewest
+    assert tb == int(tb) and tiles * tb >= tail and (tiles - 1) * tb < tail
+    assert tb <= tmax + 1

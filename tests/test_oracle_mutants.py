@@ -22,7 +22,7 @@ import pytest
 
 PINS = {
     "q8": ["tests.test_oracle_q8_0"],
-    "att": ["tests.test_oracle_attention"],
+    "att": ["tests.test_oracle_attention", "tests.test_oracle_pipeline"],
     "tq": ["tests.test_oracle_tq3", "tests.test_oracle_codebook", "tests.test_oracle_rotation",
            "tests.test_oracle_tqtiers"],
     "pol": ["tests.test_oracle_policy"],
@@ -159,6 +159,44 @@ MUTANTS = [
     ("tail_drop_in_seconds", "oracle.policy", "tail_bytes / (bw_eff_gbs * 1e9) * 1e3) / t_resident",
      "tail_bytes / (bw_eff_gbs * 1e9)) / t_resident", "pol"),
     ("tier_fit_strict", "oracle.policy", "if b <= budget_bytes + t_star:", "if b < budget_bytes + t_star:", "pol"),
+    # zero rows and blocks, bounds and masks, empty parts, the references' formats
+    ("q8_zero_block_not_zeroed", "oracle.q8_0", "q = np.where(dd == 0, 0.0, q)", "q = np.where(dd == 0, 1.0, q)", "q8"),
+    ("softcap_on_unscaled_logit", "oracle.attention",
+     "s = (np.asarray(q, dtype=np.float64) @ np.asarray(k, dtype=np.float64).T) * scale\n"
+     "    if softcap > 0:\n        s = softcap * np.tanh(s / softcap)",
+     "s = (np.asarray(q, dtype=np.float64) @ np.asarray(k, dtype=np.float64).T)\n"
+     "    if softcap > 0:\n        s = softcap * np.tanh(s / softcap)\n    s = s * scale", "att"),
+    ("causal_limit_ignores_begin", "oracle.attention", "min(end, max(begin, q_pos + i + 1))",
+     "min(end, q_pos + i + 1)", "att"),
+    ("all_empty_combine_lse_zero", "oracle.attention", "np.log(np.where(den > 0, den, 1.0)), -np.inf)",
+     "np.log(np.where(den > 0, den, 1.0)), 0.0)", "att"),
+    ("mixed_v_tail_read_at_window_format", "oracle.pipeline", "dequant(tail_v_fmt, v16[wc:], sign_words)",
+     "dequant(v_fmt, v16[wc:], sign_words)", "att"),
+    ("fanout_prefix_k_not_dequantised", "oracle.pipeline", "kp = dequant(k_fmt, prefix_k16, sign_words)",
+     "kp = np.asarray(prefix_k16, dtype=np.float64)", "att"),
+    ("fanout_prefix_v_not_dequantised", "oracle.pipeline", "vp = dequant(v_fmt, prefix_v16, sign_words)",
+     "vp = np.asarray(prefix_v16, dtype=np.float64)", "att"),
+    ("q8_0_read_without_quantisation", "oracle.pipeline", "return q8_0.decode(*q8_0.encode(x16))",
+     "return x16.astype(np.float64)", "att"),
+    ("tier_read_without_quantisation", "oracle.pipeline",
+     "return turboquant.decode_tier(planes, n, sign_words, d, bits)", "return x16.astype(np.float64)", "att"),
+    ("zero_row_stores_sign_one", "oracle.turboquant", "k = np.where(zero, levels // 2 - 1, k)",
+     "k = np.where(zero, levels // 2, k)", "tq"),
+    ("kappa_without_sqrt", "oracle.turboquant", "kappa = np.sqrt(np.float32(d // g), dtype=np.float32)",
+     "kappa = np.float32(d // g)", "tq"),
+    ("tq4_magnitude_mask_2bit", "oracle.turboquant", "sign, mag = f >> 3, f & 7", "sign, mag = f >> 3, f & 3", "tq"),
+    ("unpack_mask_one_bit_wide", "oracle.turboquant", "mask = (1 << width) - 1", "mask = (1 << width)", "tq"),
+    ("lloyd_stops_early", "oracle.turboquant", "tol: float = 1e-14", "tol: float = 1e-3", "tq"),
+    ("mse_integral_truncated", "oracle.turboquant", "[[-12.0], np.asarray(thresholds, dtype=np.float64), [12.0]]",
+     "[[-3.0], np.asarray(thresholds, dtype=np.float64), [3.0]]", "tq"),
+    ("decode_sign_order_swapped", "oracle.turboquant", "return np.where(sign == 1, half + mag, half - 1 - mag)",
+     "return np.where(sign == 1, half - 1 - mag, half + mag)", "tq"),
+    ("slots_ceil", "oracle.policy", "math.floor(slot_budget_bytes / tile_bytes_max)",
+     "math.ceil(slot_budget_bytes / tile_bytes_max)", "pol"),
+    ("tile_bytes_floor", "oracle.policy", "tile_bytes = int(math.ceil(per_layer_tail_bytes / tiles))",
+     "tile_bytes = int(per_layer_tail_bytes // tiles)", "pol"),
+    ("t_star_negative_kept", "oracle.policy", "return max(0.0, t)", "return t", "pol"),
+    ("no_tier_fits_takes_first", "oracle.policy", "return len(kv_bytes_per_tier) - 1", "return 0", "pol"),
 ]
 
 

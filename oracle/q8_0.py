@@ -9,8 +9,9 @@ int8 codes.
 
 Readings taken where the pages are silent:
   * the code of x is round(x / d16) where d16 is the STORED fp16 scale (so that the
-    round-trip error is at most d16 / 2), rounding half away from zero, clamped to
-    [-127, 127];
+    round-trip error is at most d16 / 2 whenever d16 is a normal fp16 number; a
+    subnormal d16 can round far enough that x / d16 reaches 128 and the clamp costs a
+    whole step), rounding half away from zero, clamped to [-127, 127];
   * every step is IEEE float32: d32 = f32(absmax) / 127 (correctly rounded), d16 =
     fp16 round-to-nearest-even of d32, then f32(x) / f32(d16) (correctly rounded);
   * a block whose d16 is zero stores all-zero codes.

@@ -44,7 +44,9 @@ def test_q8_0_every_fp16_value_for_fixed_amax(qps):
     31 values plus the amax element."""
     allv = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
     allv = allv[np.isfinite(allv)]
-    for amax in [1.0, 3.140625, 0.0009765625, 65504.0]:
+    # 2^-17: the scale rounds to the smallest subnormal and the codes clamp at +-127;
+    # 2^-20: the scale rounds to zero and the block stores zeros
+    for amax in [1.0, 3.140625, 0.0009765625, 65504.0, 2.0 ** -17, 2.0 ** -20]:
         vals = allv[np.abs(allv.astype(np.float64)) <= amax]
         pad = (-len(vals)) % 31
         vals = np.concatenate([vals, np.zeros(pad, dtype=np.float16)]).reshape(-1, 31)

@@ -160,6 +160,7 @@ MUTANTS = [
      "tail_bytes / (bw_eff_gbs * 1e9)) / t_resident", "pol"),
     ("tier_fit_strict", "oracle.policy", "if b <= budget_bytes + t_star:", "if b < budget_bytes + t_star:", "pol"),
     # zero rows and blocks, bounds and masks, empty parts, the references' formats
+    ("q8_clamp_allows_minus_128", "oracle.q8_0", "np.clip(q, -127, 127)", "np.clip(q, -128, 127)", "q8"),
     ("q8_zero_block_not_zeroed", "oracle.q8_0", "q = np.where(dd == 0, 0.0, q)", "q = np.where(dd == 0, 1.0, q)", "q8"),
     ("softcap_on_unscaled_logit", "oracle.attention",
      "s = (np.asarray(q, dtype=np.float64) @ np.asarray(k, dtype=np.float64).T) * scale\n"

@@ -89,3 +89,23 @@ def test_bytes_per_value_matches_pages():
             if r[0] == "bytes_per_value"}
     val, dec = rows["q8_0"]
     assert abs(q8_0.bytes_per_value(128) - val) <= 0.5 * 10 ** -dec + 1e-12
+
+
+def test_scales_at_the_bottom_of_the_fp16_range():
+    """absmax / 127 below half the smallest fp16 subnormal (2^-25) rounds to a zero
+    scale: the block stores zero codes and decodes to zeros, so its error is |x| itself
+    (< 127 * 2^-25), not d16 / 2.  With absmax = 2^-17 the scale rounds up to the
+    smallest subnormal, 2^-24, so x / d16 = +-128: the codes clamp to +-127 (never
+    -128), and the error, one d16, exceeds d16 / 2.  The d16 / 2 bound needs a normal
+    d16, whose rounding moves it by at most 2^-11 relative."""
+    tiny = np.float16(2.0 ** -20)  # absmax / 127 ~ 7.5e-9 < 2^-25 ~ 3.0e-8
+    blk = np.zeros((2, 32), dtype=np.float16)
+    blk[0, 0], blk[0, 7] = tiny, -tiny / np.float16(2)
+    blk[1, 0], blk[1, 1] = np.float16(2.0 ** -17), np.float16(-(2.0 ** -17))
+    codes, scales = q8_0.encode(blk)
+    assert float(scales[0, 0]) == 0.0 and not codes[0].any()
+    assert np.all(q8_0.decode(codes, scales)[0] == 0.0)
+    assert float(scales[1, 0]) == 2.0 ** -24
+    assert codes[1, 0] == 127 and codes[1, 1] == -127
+    err = np.abs(q8_0.decode(codes, scales)[1, :2] - blk[1, :2].astype(np.float64))
+    assert np.all(err == 2.0 ** -24)

@@ -225,7 +225,8 @@ typedef struct qps_attn_args {
   int64_t q_batch_stride; /* elements between batch entries (>= hq*D, multiple of 8) */
   int32_t batch, hq, hkv, d;
   qps_kv_view k, v;
-  int64_t kv_begin, kv_end; /* 0 <= kv_begin <= kv_end; tokens of the views */
+  int64_t kv_begin, kv_end; /* 0 <= kv_begin <= kv_end < 2^31 - 64 (else UNSUPPORTED);
+                               tokens of the views */
   float scale;
   float softcap;          /* <= 0: off */
   const uint32_t* v_signs;/* host, D/32 sign words of the cache's TurboQuant rotation;

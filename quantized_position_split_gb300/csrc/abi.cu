@@ -231,6 +231,9 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
     return fail(QPS_ERR_INVALID_ARG, "attention: k and v must both be shared (batch_stride 0) or both per-batch");
   if (a->kv_begin < 0 || a->kv_end < a->kv_begin)
     return fail(QPS_ERR_INVALID_ARG, "attention: need 0 <= kv_begin <= kv_end");
+  // the tensor-core kernels address tiles by 32-bit token coordinates (tensor maps)
+  if (a->kv_end > (int64_t)0x7fffffff - 64)
+    return fail(QPS_ERR_UNSUPPORTED, "attention: kv_end must be below 2^31 - 64 positions");
   if (!std::isfinite(a->scale) || !std::isfinite(a->softcap))
     return fail(QPS_ERR_INVALID_ARG, "attention: scale and softcap must be finite");
   if (is_tq(a->v.fmt) && !a->v_signs)

@@ -126,6 +126,7 @@ def test_attn_plan_host_only(lib):
     ("hkv", 3, N.QPS_ERR_INVALID_ARG),       # hq not a multiple of hkv
     ("d", 96, N.QPS_ERR_UNSUPPORTED),
     ("kv_end", -1, N.QPS_ERR_INVALID_ARG),
+    ("kv_end", 2 ** 31, N.QPS_ERR_UNSUPPORTED),  # beyond 32-bit token coordinates
     ("n_split", -2, N.QPS_ERR_INVALID_ARG),
     ("q", 4098, N.QPS_ERR_INVALID_ARG),      # misaligned
     ("q", None, N.QPS_ERR_INVALID_ARG),

@@ -3,6 +3,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -32,15 +33,15 @@ qps_status cuda_fail(cudaError_t err, const char* what) {
 void count_launch(int n) { g_launches += n; }
 
 int sm_count_current() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // zero-initialised; any thread may fill an entry
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 // ---- tensor maps (driver entry point looked up once through the runtime) -----------

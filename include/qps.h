@@ -105,14 +105,17 @@ typedef enum qps_kv_format {
   QPS_FMT_TQ4 = 4
 } qps_kv_format;
 
-/* ABI version of the loaded library (QPS_ABI_VERSION it was built with). */
+/* ABI version of the loaded library (QPS_ABI_VERSION it was built with).  Library
+ * utility, no counterpart on the pages.  Never fails. */
 QPS_API int32_t qps_abi_version(void);
 
 /* Message of the last failing call on this thread ("" if none).  The pointer stays
- * valid until the next failing call on the same thread. */
+ * valid until the next failing call on the same thread.  Library utility, no
+ * counterpart on the pages.  Never fails. */
 QPS_API const char* qps_last_error(void);
 
-/* Constant name of a status code ("QPS_OK", ...). */
+/* Constant name of a status code ("QPS_OK", ...; "QPS_UNKNOWN_STATUS" for any other
+ * value).  Library utility, no counterpart on the pages.  Never fails. */
 QPS_API const char* qps_status_name(int32_t status);
 
 /* The fixed TQ3 codebook [POLY, "S2 — TurboQuant tier family"]: the 8-level Lloyd-Max
@@ -158,7 +161,8 @@ QPS_API qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int6
                             const uint32_t* signs, void* lo2, void* hi1, void* norms,
                             void* stream);
 
-/* TQ2 / TQ4 encode: the TQ3 steps above with the 4- or 16-level codebook
+/* TQ2 / TQ4 encode [POLY, "S2 — TurboQuant tier family"]: the TQ3 steps above with
+ * the 4- or 16-level codebook
  * (qps_tq_codebook(2 or 4, ...)), storing one sign-magnitude field per element
  * (QPS_FMT_TQ2 / QPS_FMT_TQ4 above) and fp16(n).  A zero row stores zero fields and a
  * zero norm.
@@ -168,6 +172,11 @@ QPS_API qps_status qps_kv_quant_tq3(const void* x, int64_t rows, int32_t d, int6
  *   norms   device, fp16 [rows]; 2-byte aligned (so is x).
  * D in {32, 64, 128, 256, 512}.  rows == 0 is a no-op.
  * Errors: INVALID_ARG, UNSUPPORTED (D), CUDA. */
+QPS_API qps_status qps_kv_quant_tq2(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* codes, void* norms, void* stream);
+QPS_API qps_status qps_kv_quant_tq4(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
+                            const uint32_t* signs, void* codes, void* norms, void* stream);
+
 /* TurboQuant encode at any tier and with either rotation form [POLY, "S2 —
  * TurboQuant tier family", "S2 perf-path Level B"]: R = diag(s2) blockdiag(H_G)
  * diag(s1) / sqrt(G).  Per row, in IEEE float32 with a fixed order: the norm as for
@@ -183,10 +192,6 @@ QPS_API qps_status qps_kv_quant_tq_rot(int32_t bits, const void* x, int64_t rows
                                const uint32_t* signs2, int32_t block, void* plane0,
                                void* plane1, void* norms, void* stream);
 
-QPS_API qps_status qps_kv_quant_tq2(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
-                            const uint32_t* signs, void* codes, void* norms, void* stream);
-QPS_API qps_status qps_kv_quant_tq4(const void* x, int64_t rows, int32_t d, int64_t x_row_stride,
-                            const uint32_t* signs, void* codes, void* norms, void* stream);
 
 /* A K or V cache (or one of its parts) as seen by the attention calls.  Row of
  * (token t, KV head h, batch entry b) = b*batch_stride + t*tok_stride + h*head_stride.
@@ -266,15 +271,18 @@ typedef struct qps_attn_args {
   int32_t reserved1;      /* must be 0 */
 } qps_attn_args;
 
-/* Resolve the split count and the workspace the args need (host only, no launch).
- * n_split_out / workspace_bytes_out may be NULL.  Errors: INVALID_ARG, UNSUPPORTED. */
+/* Resolve the split count and the workspace the args need (host only, no launch):
+ * the split-KV partition of [RKV] item S2 chosen for this GPU (no counterpart on the
+ * pages for the choice itself).  n_split_out / workspace_bytes_out may be NULL.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA (the SM count of an automatic split). */
 QPS_API qps_status qps_attn_plan(const qps_attn_args* a, int32_t* n_split_out,
                          size_t* workspace_bytes_out);
 
 /* Which kernel the args select (host only): 1 = tensor-core path (every K / V plane
  * token-contiguous, tok_stride == 1, with 16-byte-aligned bases and head / batch
  * offsets), 0 = CUDA-core path (any other strides), negative = the args are invalid
- * (a qps_status, negated).  Both paths compute the same attention. */
+ * (a qps_status, negated).  Both paths compute the same attention.  Library utility,
+ * no counterpart on the pages.  Errors: as the negated return value. */
 QPS_API int32_t qps_attn_path(const qps_attn_args* a);
 
 /* Decode attention over device-resident KV (the window [0, wc), or any device part)
@@ -310,21 +318,22 @@ QPS_API qps_status qps_lse_combine(const float* o_parts, const float* lse_parts,
  * Errors: INVALID_ARG, CUDA (allocation failure). */
 QPS_API qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out);
 
-/* Free memory from qps_host_alloc (NULL is a no-op).  Errors: CUDA. */
+/* Free memory from qps_host_alloc (NULL is a no-op); the pinned tail of [RKV]
+ * "Storage layer".  Errors: CUDA. */
 QPS_API qps_status qps_host_free(void* p);
 
 /* ---- Tail-prefetch ring [RING] ------------------------------------------------ */
 
 typedef struct qps_ring qps_ring;
 
-/* Create a ring of n_slots (2..4) device staging slots of slot_bytes each on `device`,
+/* [RING] Create a ring of n_slots (2..4) device staging slots of slot_bytes each on `device`,
  * a non-blocking copy stream and pre-created copy_done / compute_done events (timing
  * disabled).  The library owns these until qps_ring_destroy.  Makes `device` current.
  * Errors: INVALID_ARG, CUDA (allocation). */
 QPS_API qps_status qps_ring_create(int32_t n_slots, size_t slot_bytes, int32_t device,
                            qps_ring** out);
 
-/* Wait (bounded, 10 s) for the ring's copies, then free slots, events and the stream.
+/* [RING] Wait (bounded, 10 s) for the ring's copies, then free slots, events and the stream.
  * NULL is a no-op.  Errors: TIMEOUT (resources leaked rather than freed in use). */
 QPS_API qps_status qps_ring_destroy(qps_ring* ring);
 
@@ -353,7 +362,7 @@ typedef struct qps_tile_desc {
                           newest positions lie in the tail); 0 when unused */
 } qps_tile_desc;
 
-/* How the ring moves tiles: QPS_RING_COPY_ENGINE (the default) uses the copy engine
+/* [RING] How the ring moves tiles: QPS_RING_COPY_ENGINE (the default) uses the copy engine
  * (cudaMemcpyAsync) for every tile, leaving the SMs to the attention;
  * QPS_RING_COPY_KERNEL uses the ring's copy kernel for every tile whose planes lie in
  * qps_host_alloc memory (each on a 16-byte boundary) and the copy engine for the
@@ -366,7 +375,7 @@ typedef struct qps_tile_desc {
 #define QPS_RING_COPY_KERNEL 1
 QPS_API qps_status qps_ring_set_copy_mode(qps_ring* ring, int32_t mode);
 
-/* Start a step: copy the flat (layer, tile) schedule (host array, read during the
+/* [RING] Start a step: copy the flat (layer, tile) schedule (host array, read during the
  * call) and enqueue the first n_slots tile copies on the copy stream; each copy
  * first waits for the compute_done event of the slot's previous user (which may
  * belong to the previous step).  Every host plane must be pinned.
@@ -388,11 +397,11 @@ QPS_API qps_status qps_ring_begin_step(qps_ring* ring, const qps_tile_desc* tile
 QPS_API qps_status qps_attn_decode_tail(qps_ring* ring, int32_t tile_index, const qps_attn_args* a,
                                 void* compute_stream);
 
-/* Close the step (every tile must have been consumed).  Does not wait for the
+/* [RING] Close the step (every tile must have been consumed).  Does not wait for the
  * device.  Errors: STATE. */
 QPS_API qps_status qps_ring_end_step(qps_ring* ring);
 
-/* Wait until every copy and every tail attention issued by the ring has completed,
+/* [RING] Wait until every copy and every tail attention issued by the ring has completed,
  * polling with a deadline of timeout_ms (never blocks longer).  Errors: TIMEOUT,
  * CUDA. */
 QPS_API qps_status qps_ring_sync(qps_ring* ring, int32_t timeout_ms);
@@ -446,10 +455,12 @@ QPS_API qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, i
  *     word (a synchronising step); make that first call before any stream capture.
  *   - A bounded in-kernel wait that gives up marks the array's error word instead of
  *     hanging and leaves the outputs invalid; this call does not read the word back.
- * Supported shapes, formats and other errors as qps_attn_decode_window. */
+ * Supported shapes and formats as qps_attn_decode_window.  Errors: INVALID_ARG (above,
+ * or o_parts set, or o / lse NULL), and otherwise as qps_attn_decode_window. */
 QPS_API qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, void* stream);
 
-/* Device-side status of the current device.  Kernels that wait on their own
+/* Device-side status of the current device (failure detection; no counterpart on the
+ * pages).  Kernels that wait on their own
  * asynchronous tile copies bound every wait; a wait that runs out sets a
  * library-owned device word instead of hanging, and the kernel returns early with
  * invalid outputs.  This call reads that word synchronously (it waits for the
@@ -467,7 +478,8 @@ QPS_API qps_status qps_device_status(int32_t reset);
 QPS_API qps_status qps_selftest_bounded_wait(void* stream);
 
 /* Number of kernel launches the calling thread has issued through this library
- * since the last reset (reset if `reset` is non-zero).  Host only. */
+ * since the last reset (reset if `reset` is non-zero).  Host only.  Library utility,
+ * no counterpart on the pages.  Never fails. */
 QPS_API int64_t qps_launch_count(int32_t reset);
 
 /* ---- Residency and ring sizing policy (host arithmetic only) ------------------- */

@@ -120,13 +120,13 @@ SIGNATURES = [
     ("qps_kv_quant_q8_0", c_int32, [c_void_p, c_int64, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
     ("qps_kv_quant_tq3", c_int32,
      [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p, c_void_p]),
-    ("qps_kv_quant_tq_rot", c_int32,
-     [c_int32, c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), POINTER(c_uint32), c_int32, c_void_p,
-      c_void_p, c_void_p, c_void_p]),
     ("qps_kv_quant_tq2", c_int32,
      [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p]),
     ("qps_kv_quant_tq4", c_int32,
      [c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), c_void_p, c_void_p, c_void_p]),
+    ("qps_kv_quant_tq_rot", c_int32,
+     [c_int32, c_void_p, c_int64, c_int32, c_int64, POINTER(c_uint32), POINTER(c_uint32), c_int32, c_void_p,
+      c_void_p, c_void_p, c_void_p]),
     ("qps_attn_plan", c_int32, [POINTER(AttnArgs), POINTER(c_int32), POINTER(c_size_t)]),
     ("qps_attn_path", c_int32, [POINTER(AttnArgs)]),
     ("qps_attn_decode_window", c_int32, [POINTER(AttnArgs), c_void_p]),

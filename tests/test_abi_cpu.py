@@ -225,3 +225,18 @@ def test_ring_and_step_state_errors(lib):
     st[0].tail = ctypes.pointer(_args())
     assert lib.qps_decode_step(None, None, 1, st, 1, None) == N.QPS_ERR_INVALID_ARG
     assert lib.qps_decode_step(None, None, 0, st, 1, None) == N.QPS_ERR_INVALID_ARG  # count mismatch
+
+
+def test_every_declaration_cites_its_source_and_states_its_errors():
+    """Each call's comment names the passage it follows (a source tag or a page title)
+    or says it has no counterpart on the pages, and states its errors (or that it
+    never fails)."""
+    text = open(HEADER).read()
+    decls = re.findall(r"(/\*(?:(?!\*/).)*\*/)\s*(?:#define[^\n]*\n\s*)*QPS_API\s+[\w\s\*]+?\b(qps_\w+)\(",
+                       text, flags=re.S)
+    named = {n for _, n in decls}
+    assert named == set(declared_functions()) - {"qps_kv_quant_tq4"}  # shares qps_kv_quant_tq2's comment
+    for comment, name in decls:
+        cites = re.search(r"\[(RKV|RING|POLY|TSTAR)\b", comment) or "counterpart" in comment or '"F5 M' in comment
+        assert cites, name
+        assert "Errors" in comment or "Never fails" in comment, name

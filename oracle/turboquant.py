@@ -73,6 +73,7 @@ LEVELS = 8
 
 
 def _phi(x):
+    """Standard normal density."""
     return np.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)
 
 
@@ -221,6 +222,8 @@ def level_index(x: np.ndarray, sign_words, levels: int = LEVELS):
 
 
 def _sign_magnitude(k, levels):
+    """Split a level index k into (sign, magnitude): sign = k >= L/2, magnitude counts
+    outward from the middle of the codebook on each side."""
     half = levels // 2
     sign = k >= half
     mag = np.where(sign, k - half, half - 1 - k)
@@ -296,6 +299,7 @@ def pack_bits(vals: np.ndarray, width: int) -> np.ndarray:
 
 
 def unpack_bits(packed: np.ndarray, width: int, d: int) -> np.ndarray:
+    """Inverse of ``pack_bits``: the ``d`` fields of ``width`` bits of each row."""
     per = 8 // width
     p = np.asarray(packed).astype(np.uint32)
     mask = (1 << width) - 1

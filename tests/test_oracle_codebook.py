@@ -84,3 +84,14 @@ def test_threshold_count_rule_equals_nearest_level():
     nearest = np.argmin(np.abs(z[:, None].astype(np.float64) - levels[None, :].astype(np.float64)), axis=1)
     assert np.array_equal(k, nearest)
     assert math.isclose(float(thr[3]), 0.0, abs_tol=0.0)
+
+
+def test_every_oracle_function_is_documented_and_every_module_cites_its_pages():
+    import inspect
+
+    from oracle import attention, pipeline, policy, q8_0
+    for m in (attention, q8_0, tq, pipeline, policy):
+        assert '"F5 M' in m.__doc__ or '"T*-aware' in m.__doc__ or '"Rolling-KV' in m.__doc__, m.__name__
+        for name, f in vars(m).items():
+            if inspect.isfunction(f) and f.__module__ == m.__name__:
+                assert f.__doc__, f"{m.__name__}.{name}"

@@ -50,3 +50,25 @@ def test_traffic_file_of_a_mixed_tail_is_its_window_kernels():
             w = synth.by_name(names[c.name])
             assert (w.wc, w.hkv, w.d, w.k_fmt, w.v_fmt) == (c.wc, c.hkv, c.d, c.k_fmt, c.v_fmt)
     assert bench.committed_traffic("qwen14b_q8") is not None  # the committed figure is current
+
+
+def test_reference_arm_line_carries_the_contract_keys(capsys, monkeypatch):
+    """The reference arm (the CPU oracle) on the tiny workload, one step: one JSON line
+    with the benchmark's keys, its own cpu_baseline and an e2e entry without copies."""
+    import json
+
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "0"]) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in j, key
+    assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == bench.UNIT
+    assert j["value"] > 0 and j["n_gpus"] == 1 and j["steps"] == 1 and j["higher_is_better"] is True
+    assert j["config"]["workload"] == "tiny"
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == j["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

@@ -54,3 +54,21 @@ def test_policy_argument_errors(qps):
         qps.choose_tier([], 1.0, 0.0)
     with pytest.raises(N.QpsError):
         qps.choose_tier([1.0], 1.0, -1.0)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 5, 7])
+def test_exact_boundaries_match_oracle(qps, k):
+    """Budgets and tails that are exact multiples of the largest tile, and a tier whose
+    bytes equal budget + T*: the floors, ceilings and the <= of both sides agree."""
+    c, bw = 2.0, 200.0  # 320e6-byte tiles, exactly
+    tmax = policy.ring_plan(c, bw, 1e9, 1.0)[3]
+    for budget in (k * tmax, k * tmax * (1 - 1e-15), k * tmax * (1 + 1e-15)):
+        for tail in (k * tmax, k * tmax + 1, k * tmax - 1):
+            got = qps.plan_ring(c, bw, budget, tail)
+            n, tiles, tb, tm = policy.ring_plan(c, bw, budget, tail)
+            assert (got["n_slots"], got["tiles_per_layer"], got["tile_bytes"], got["tile_bytes_max"]) == \
+                (n, tiles, tb, tm)
+    t = qps.tail_band(50.0, 1.0, 200.0, 0.2)
+    budget = 1e9
+    tiers = [budget + t + 1.0, budget + t, budget + t - 1.0]
+    assert qps.choose_tier(tiers, budget, t) == policy.choose_tier(tiers, budget, t) == 1

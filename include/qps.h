@@ -446,8 +446,9 @@ QPS_API qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, i
  * counterpart there.  It allocates nothing: instead of a caller workspace, the split
  * partials live in a fixed 8 MiB file-scope device array that every GPU which loads
  * the library holds until the process exits.  `workspace` is ignored.
- *   - Requests whose partials exceed the array (n_split * batch * hq * (D + 1) floats,
- *     plus alignment) fail with QPS_ERR_INVALID_ARG; pass a smaller n_split.
+ *   - o / lse hold batch * n_q * hq rows ([rows][D] and [rows] f32, n_q >= 1).
+ *   - Requests whose partials exceed the array (n_split * batch * n_q * hq * (D + 1)
+ *     floats, plus alignment) fail with QPS_ERR_INVALID_ARG; pass a smaller n_split.
  *   - All calls on a device share the array and leave their partials in it (each call
  *     rewrites everything it reads); calls that overlap on the GPU race on it, so
  *     serialise them (one stream, or events between streams).
@@ -455,8 +456,10 @@ QPS_API qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, i
  *     word (a synchronising step); make that first call before any stream capture.
  *   - A bounded in-kernel wait that gives up marks the array's error word instead of
  *     hanging and leaves the outputs invalid; this call does not read the word back.
- * Supported shapes and formats as qps_attn_decode_window.  Errors: INVALID_ARG (above,
- * or o_parts set, or o / lse NULL), and otherwise as qps_attn_decode_window. */
+ * Supported shapes and formats as qps_attn_decode_window (multi-query and causal decode
+ * only on the tensor-core path).  Errors: INVALID_ARG (above, or o_parts set, or o / lse
+ * NULL), UNSUPPORTED (n_q > 1 or causal with planes the tensor-core path cannot
+ * stage), and otherwise as qps_attn_decode_window. */
 QPS_API qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, void* stream);
 
 /* Device-side status of the current device (failure detection; no counterpart on the

@@ -360,8 +360,15 @@ def attn_decode_window(a: N.AttnArgs, *, o=None, lse=None, parts=None, part_offs
 def attn_decode_window_noalloc(a: N.AttnArgs, o: torch.Tensor, lse: torch.Tensor, stream=None):
     """Merged-output decode attention that allocates no device memory: the split
     partials go to the library's fixed device scratch instead of a workspace.  For
-    callers that cannot allocate on the call path; ``o`` [batch*hq, D] and ``lse``
-    [batch*hq] (f32, CUDA) must be given.  Calls sharing a device must not overlap."""
+    callers that cannot allocate on the call path; ``o`` [batch*n_q*hq, D] and ``lse``
+    [batch*n_q*hq] (f32, CUDA, contiguous) must be given.  Calls sharing a device must
+    not overlap."""
+    rows = a.batch * max(1, a.n_q) * a.hq
+    for t, n, what in ((o, rows * a.d, "o"), (lse, rows, "lse")):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.numel() != n:
+            raise QpsError(N.QPS_ERR_INVALID_ARG,
+                           f"attn_decode_window_noalloc: {what} must be a contiguous f32 CUDA tensor of "
+                           f"{n} elements (batch*n_q*hq rows)")
     a.o_parts = a.lse_parts = None
     a.o, a.lse = o.data_ptr(), lse.data_ptr()
     a.workspace, a.workspace_bytes = None, 0

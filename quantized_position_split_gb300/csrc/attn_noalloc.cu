@@ -97,6 +97,11 @@ extern "C" qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, voi
   p.part_offset = 0;
   p.err = reinterpret_cast<unsigned int*>(base + kErrOffset);
   if (!attn_uses_mma(p)) {
+    // the CUDA-core kernel decodes one query token per row and has no causal limit:
+    // refuse what it cannot compute, exactly as qps_attn_decode_window does
+    if (p.n_q > 1 || p.causal)
+      return fail(QPS_ERR_UNSUPPORTED, "attn_decode_window_noalloc: multi-query / causal decode needs the "
+                                       "tensor-core path (token-contiguous planes, see qps_attn_path)");
     st = launch_attn_simple(p, s);
   } else {
     switch (p.d) {

@@ -273,13 +273,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity: false after 256 polls of at most
-// ~1 ms each, i.e. well under a second.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int it = 0; it < 256; ++it)
+// Bounded wait for the phase with the given parity: false after `polls` polls of at
+// most ~1 ms each (by default 256, well under a second).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int polls = 256) {
+  for (int it = 0; it < polls; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// The longer bound of the drain after a give-up: copies already issued get ~1 s more.
+constexpr int kDrainPolls = 1024;
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
@@ -398,7 +400,9 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   constexpr bool QS = q_in_smem<D, KF, VF>();  // fragments in shared memory (see q_in_smem)
   constexpr int QMT = QS ? 1 : MT;
   uint32_t qb[NTW][QMT][2];
-  constexpr int QF_OFF = align_to(G::END, 16);
+  // the CTA's give-up flag sits right after the barriers, the query fragments after it
+  constexpr int ABORT_OFF = G::END;
+  constexpr int QF_OFF = align_to(G::END + 16, 16);
   if constexpr (!is_tq(KF)) {
 #pragma unroll
   for (int nt = 0; nt < NTW; ++nt) {
@@ -510,7 +514,10 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   uint8_t* wpipe = pipe + warp * G::STAGES * G::STAGE;
 
   const uint32_t bars = smem_addr(smem + G::BARS) + warp * G::STAGES * 8;
-  bool timed_out = false;
+  // Set (to 1) by the first warp whose bounded wait gives up: from then on no warp of the
+  // CTA issues another tile copy.  Read by lane 0 and broadcast, so warp-uniform.
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + ABORT_OFF);
+  int n_issued = 0;  // this warp's tiles whose copies were issued (warp-uniform)
 
   // The warp's k-th tile -> stage k % STAGES.  Lane 0 announces the tensor-map bytes; lanes issue one box each; small planes go by
   // zero-filling cp.async from every lane, each lane then arriving on the same mbarrier
@@ -518,6 +525,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   auto issue = [&](int k) {
     const int tile = warp + k * kWarps;
     if (tile >= ntiles) return;
+    if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) return;  // a warp gave up: no new copies
+    n_issued = k + 1;  // (tiles are issued in order, so every earlier one was too)
     uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
     const int64_t tb = tile0 + (int64_t)tile * TT;
     const int tok = (int)tb;
@@ -560,18 +569,9 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     }
   };
 
-  // Wait until the warp's k-th tile is in shared memory.
-  auto await = [&](int k) {
-    if (!mbar_wait(bars + (k % G::STAGES) * 8, (uint32_t)((k / G::STAGES) & 1))) {
-      // record the failure, then give the copies still in flight (tiles k..k+S-2 of
-      // this warp) a second bounded wait before the stage memory is reused
-      timed_out = true;
-      if (lane == 0) atomicOr(p.err, 1u);
-      for (int j = k; j < k + G::STAGES - 1 && warp + j * kWarps < ntiles; ++j)
-        mbar_wait(bars + (j % G::STAGES) * 8, (uint32_t)((j / G::STAGES) & 1));
-    }
-    __syncwarp();
-  };
+  // Barrier address and phase parity of the warp's k-th tile (stage k % STAGES).
+  auto bar_of = [&](int k) { return bars + (k % G::STAGES) * 8; };
+  auto par_of = [&](int k) { return (uint32_t)((k / G::STAGES) & 1); };
 
   // ---- running softmax state (log2 domain) and the O^T accumulators ---------------
   float m[NTW][2], l[NTW][2];
@@ -592,7 +592,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     for (int s = 0; s < G::STAGES; ++s) mbar_init(bars + s * 8, G::ARRIVALS);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  __syncthreads();  // the barriers are ready
+  if (threadIdx.x == 0) *abort_flag = 0;
+  __syncthreads();  // the barriers and the flag are ready
 
   // ---- per-tile work ------------------------------------------------------------------
 
@@ -1110,21 +1111,43 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   };
 
   // ---- the warp's tiles: a private pipeline, no cross-warp traffic ---------------------
+  // The loop consumes exactly the tiles whose copies were issued: after a give-up in any
+  // warp of the CTA no new copies start, the tiles already in flight are consumed (or,
+  // in the warp that gave up, drained), and the CTA returns without an epilogue.
 #pragma unroll 1
   for (int s = 0; s < G::STAGES - 1; ++s) issue(s);
+  int k_fail = -1;  // the tile whose wait gave up (warp-uniform)
 #pragma unroll 1
-  for (int k = 0; warp + k * kWarps < ntiles; ++k) {
+  for (int k = 0; k < n_issued; ++k) {
     issue(k + G::STAGES - 1);  // stage (k - 1) % STAGES is free
-    await(k);
-    if (timed_out) break;  // the error word tells the host; the outputs are not valid
+    if (!mbar_wait(bar_of(k), par_of(k))) {
+      k_fail = k;
+      break;
+    }
+    __syncwarp();
     const uint8_t* st = wpipe + (k % G::STAGES) * G::STAGE;
     float sacc[SUB][NTW][4];
     k_part(st, sacc);
     attend_tile(st, tile0 + (int64_t)(warp + k * kWarps) * TT, sacc);
     __syncwarp();
   }
+  if (k_fail >= 0) {
+    // Record the failure (the host reads it through qps_device_status), stop every warp's
+    // further copies, then give each copy this warp still has in flight (tiles k_fail ..
+    // n_issued - 1, at most STAGES, so one per stage) a longer bounded wait, so that no
+    // tensor-map write lands in shared memory after the CTA has exited.  Should one of
+    // those also run out, the CTA exits with that copy still outstanding.
+    if (lane == 0) {
+      atomicOr(p.err, 1u);
+      *abort_flag = 1;
+    }
+    for (int j = k_fail; j < n_issued; ++j) mbar_wait(bar_of(j), par_of(j), kDrainPolls);
+    __syncwarp();
+  }
   cp_async_wait<0>();
-  __syncthreads();
+  // every warp's outstanding copies are done (or drained); a CTA in which any wait gave
+  // up writes no partial (the error word marks the launch's outputs invalid)
+  if (__syncthreads_or(k_fail >= 0)) return;
   asm volatile("griddepcontrol.launch_dependents;" :::);
 
   // ---- merge the warps' states, then the chunk's partial ------------------------------
@@ -1235,8 +1258,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
 template <int D, int KF, int VF, int NTW>
 constexpr size_t smem_bytes() {
   using G = Geo<D, KF, VF, NTW>;
-  // the stages and barriers, then a TurboQuant K's query fragments
-  constexpr size_t pipe = (size_t)align_to(G::END, 16) + qf_bytes<D, KF, VF, NTW>();
+  // the stages and barriers, the give-up flag, then query fragments kept in shared memory
+  constexpr size_t pipe = (size_t)align_to(G::END + 16, 16) + qf_bytes<D, KF, VF, NTW>();
   constexpr int ROWS = 8 * NTW;
   constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D) +
                            sizeof(int64_t) * ROWS + sizeof(float) * ((size_t)G::NW * ROWS + 2 * ROWS);

@@ -255,16 +255,17 @@ def by_name(name: str) -> Workload:
 def parity_scaled(cfg: Workload, layers: Optional[int] = None) -> Workload:
     """A copy of ``cfg`` small enough for the float64 oracle to finish in seconds.
 
-    Head counts, head_dim, formats and softcap are kept; positions are cut to a few
-    thousand with deliberately ragged window / tile boundaries so that the GPU path
-    crosses several split chunks, several ring tiles and a partial last tile.
+    Head counts, head_dim, formats, softcap and (unless ``layers`` is given) the layer
+    count are kept; positions are cut to a few thousand with deliberately ragged window
+    / tile boundaries so that the GPU path crosses several split chunks, several ring
+    tiles and a partial last tile.
     """
     if cfg.kind == "fanout":
         return cfg.replace(n_kv=1000, wc=1000, suffix_len=77, agents=min(cfg.agents, 15))
     n = 3000 + 37 if cfg.d <= 128 else 2000 + 21
     wc = 1101 if cfg.d <= 128 else 777
     return cfg.replace(
-        layers=layers if layers is not None else min(cfg.layers, 2),
+        layers=layers if layers is not None else cfg.layers,
         n_kv=n,
         wc=wc,
         tile_tokens=512,

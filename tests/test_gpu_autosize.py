@@ -37,7 +37,7 @@ def test_probes_are_sane(qps):
 def test_planned_decoder_matches_oracle(qps):
     from quantized_position_split_gb300 import autosize
     from quantized_position_split_gb300.decode import PositionSplitDecoder
-    cfg = synth.parity_scaled(synth.by_name("qwen14b_f16"))
+    cfg = synth.parity_scaled(synth.by_name("qwen14b_f16"), layers=2)
     tiers = [("f16", "f16"), ("q8_0", "q8_0"), ("q8_0", "tq3")]
     per_tok_f16 = cfg.hkv * 2 * (2 * cfg.d)
     budget = 0.6 * cfg.layers * cfg.n_kv * per_tok_f16

@@ -1,5 +1,6 @@
 """Whole decode steps (window + ring tail + combine) vs the oracle, ring invariances
-and the ring's host-side error paths, at parity-sized copies of every workload."""
+and the ring's host-side error paths, at parity-sized copies of every workload (every
+layer of each), including the step runner's degenerate splits wc = 0 and wc = n_kv."""
 
 import numpy as np
 import pytest
@@ -28,6 +29,8 @@ def test_workload_step_parity(qps, name):
     cfg = synth.parity_scaled(synth.by_name(name))
     dec, kept = helpers.build_split_decoder(cfg, keep_inputs=range(cfg.layers))
     assert dec.n_tiles == cfg.layers * len(dec.tile_ranges()) and len(dec.tile_ranges()) >= 3
+    import bench
+    assert bench.split_kv_bytes(cfg) == (dec.window_bytes(), dec.tail_bytes())  # the bench's byte counts
     for _ in range(2):  # the second step reuses slots whose events belong to step one
         dec.step()
         torch.cuda.synchronize()
@@ -36,6 +39,34 @@ def test_workload_step_parity(qps, name):
             assert_parity(dec.o[layer].cpu().numpy(), dec.lse[layer].cpu().numpy(),
                           ro.reshape(-1, cfg.d), rl.reshape(-1), (name, layer))
     dec.ring.sync()
+    dec.close()
+
+
+@pytest.mark.parametrize("name", SPLIT_CONFIGS)
+@pytest.mark.parametrize("edge", ["no_window", "no_tail"])
+def test_step_edge_splits(qps, name, edge):
+    """The combine identity at the ends of the split ("F5 M7 — Rolling KV:
+    position-windowed KV residency", section "Implementation decomposition, refined
+    (S1 -> S2 -> S3)", item S2): with wc = 0 every position is a tail tile and no layer
+    has a device part; with wc = n_kv there are no tiles and no ring.  Both equal plain
+    attention over every position."""
+    base = synth.parity_scaled(synth.by_name(name))
+    cfg = base.replace(wc=0 if edge == "no_window" else base.n_kv)
+    dec, kept = helpers.build_split_decoder(cfg, keep_inputs=range(cfg.layers))
+    assert (dec.ring is None) == (edge == "no_tail")
+    if edge == "no_window":
+        assert dec.window_plan is None and dec.n_tiles == cfg.layers * len(dec.tile_ranges()) >= cfg.layers * 3
+    else:
+        assert dec.n_tiles == 0
+    for _ in range(2):
+        dec.step()
+        torch.cuda.synchronize()
+        for layer, (q, k, v) in kept.items():
+            ro, rl = helpers.oracle_layer(cfg, q, k, v)
+            assert_parity(dec.o[layer].cpu().numpy(), dec.lse[layer].cpu().numpy(),
+                          ro.reshape(-1, cfg.d), rl.reshape(-1), (name, edge, layer))
+    if dec.ring is not None:
+        dec.ring.sync()
     dec.close()
 
 

@@ -4,8 +4,16 @@
 A step is one pass of the whole hot path over every layer of the workload: the
 quantised-KV decode attention of the device window, the tail streamed from pinned
 host memory through the prefetch ring, and the per-layer LSE combine.  The default
-workload is the Qwen2.5-14B-like layer stack (48 layers, 40 q / 8 KV heads, head_dim
-128, n_kv 65536, window 32768, fp16 K with 4 outlier channels per head, 3-slot ring).
+workload is the largest single-GPU configuration, the Qwen2.5-14B-like layer stack
+with K and V at q8_0 (48 layers, 40 q / 8 KV heads, head_dim 128, n_kv 131072, window
+98304 on the device, a 32768-position compressed tail streamed through a 3-slot ring).
+
+The same JSON line carries one sub-record per other workload (``--sub-configs``): the
+fp16 Qwen-like stack, the Gemma-like global layers (q8_0 K / 3-bit TurboQuant V,
+head_dim 512, softcap 50) and the shared-prefix fan-out.  Every record is checked: the
+device error word of the bounded in-kernel waits after the timed and the end-to-end
+steps (a wait that gave up exits non-zero), and the outputs of sampled layers against
+the float64 CPU oracle on the same inputs, whose timing is the ``cpu_baseline``.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU oracle on a
 bounded sample of the same workload instead.
@@ -16,6 +24,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -29,6 +38,12 @@ if ROOT not in sys.path:
 
 METRIC = "decode-attn effective KV GB/s & % HBM peak; tail-hidden step ms vs max(compute,DMA)"
 UNIT = "GB/s"
+DEFAULT_CONFIG = "qwen14b_q8"
+SUB_CONFIGS = "qwen14b_f16,gemma_global_q8k_tq3v,fanout_prefix"
+# the bar every output is held to: per query row rel-L2 and max-abs of O, |dLSE|
+PARITY_BAR = {"rel_l2": 1e-3, "max_abs": 2e-3, "dlse": 1e-4}
+L2_BYTES = 129e6
+DATA = "synthetic (seeded N(0,1) fp16, 4 outlier K channels per head x20)"
 
 
 def parse_args(argv=None):
@@ -37,7 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="qwen14b_f16")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--sub-configs", default=SUB_CONFIGS,
+                    help="comma-separated workloads measured as sub-records of the same line ('' for none)")
     ap.add_argument("--cpu-layers", type=int, default=0, help="layers in the oracle sample (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
@@ -45,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--auto-ring", action="store_true",
                     help="size the ring (slots, tile tokens) from the measured link and attention time "
                          "instead of the workload's fixed values")
+    ap.add_argument("--n-split-window", type=int, default=0,
+                    help="split count of the window launches (0 = the library's automatic choice)")
     ap.add_argument("--v-fmt", default="",
                     help="with --kernel-only: store the window's V in this format instead "
                          "(f16, q8_0, tq2, tq3, tq4)")
@@ -136,7 +155,55 @@ def cpu_model(cpuinfo_text=None) -> str:
 
 
 # ---------------------------------------------------------------------------------
-# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# workload description shared by both arms
+# ---------------------------------------------------------------------------------
+# bytes per stored row of each plane of a format (data, aux, aux2), head_dim d
+ROW_BYTES = {"f16": lambda d: [2 * d], "q8_0": lambda d: [d, d // 16], "tq3": lambda d: [d // 4, d // 8, 2],
+             "tq2": lambda d: [d // 4, 2], "tq4": lambda d: [d // 2, 2]}
+
+
+def _pad16(n: int) -> int:
+    return (n + 15) // 16 * 16
+
+
+def split_kv_bytes(cfg):
+    """(window, tail) bytes one step reads: every stored plane of every layer, each KV
+    head's positions padded to 16 rows as the decoder stores them (head-major)."""
+    row = lambda fk, fv: sum(ROW_BYTES[fk](cfg.d)) + sum(ROW_BYTES[fv](cfg.d))  # noqa: E731
+    window = cfg.layers * cfg.hkv * _pad16(cfg.wc) * row(cfg.k_fmt, cfg.v_fmt) if cfg.wc > 0 else 0
+    tail = 0
+    for a in range(0, cfg.tail_len, cfg.tile_tokens):
+        n = min(cfg.tile_tokens, cfg.tail_len - a)
+        tail += cfg.hkv * _pad16(n) * row(cfg.tk_fmt, cfg.tv_fmt)
+    return window, tail * cfg.layers
+
+
+def bench_config(cfg, args, ring_plan=None) -> dict:
+    """The line's ``config``: the workload and the launch configuration timed (the same
+    dict on both arms for the same arguments)."""
+    if cfg.kind == "fanout":
+        pre = cfg.hkv * _pad16(cfg.n_kv) * (sum(ROW_BYTES[cfg.k_fmt](cfg.d)) + sum(ROW_BYTES[cfg.v_fmt](cfg.d)))
+        suf = cfg.agents * cfg.hkv * _pad16(cfg.suffix_len) * 2 * 2 * cfg.d
+        return {"workload": cfg.name, "layers": cfg.layers, "agents": cfg.agents, "hq": cfg.hq, "hkv": cfg.hkv,
+                "d": cfg.d, "prefix_len": cfg.n_kv, "suffix_len": cfg.suffix_len, "k_fmt": cfg.k_fmt,
+                "v_fmt": cfg.v_fmt, "suffix_fmt": "f16", "softcap": cfg.softcap,
+                "parallelism": f"replicas x{args.gpus}",
+                "l2": "inputs smaller than L2 (prefix %.2f MB + suffixes %.2f MB): L2 flushed (256 MB "
+                      "write) before every timed step" % (pre / 1e6, suf / 1e6)}
+    window, tail = split_kv_bytes(cfg)
+    return {"workload": cfg.name, "layers": cfg.layers, "batch": cfg.batch, "hq": cfg.hq,
+            "hkv": cfg.hkv, "d": cfg.d, "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt,
+            "v_fmt": cfg.v_fmt, "tail_k_fmt": cfg.tk_fmt, "tail_v_fmt": cfg.tv_fmt,
+            "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
+            "tile_tokens": cfg.tile_tokens, "ring_plan": ring_plan, "ring_copy": args.ring_copy, "n_q": args.n_q,
+            "n_split_window": args.n_split_window or "auto",
+            "parallelism": f"replicas x{args.gpus}",
+            "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" % (window / 1e9, tail / 1e9)}
+
+
+# ---------------------------------------------------------------------------------
+# CPU oracle: timing (the reference arm and the cpu_baseline leg) and the check of the
+# GPU outputs
 # ---------------------------------------------------------------------------------
 def _lib_signs(qps, synth, cfg):
     """The workload's TurboQuant sign words, or its Rotation, for the library."""
@@ -144,44 +211,85 @@ def _lib_signs(qps, synth, cfg):
     return w1 if w2 is None and block == 0 else qps.Rotation(w1, w2, block)
 
 
-def time_oracle(cfg, n_layers: int):
-    """Time the oracle's layer computation on ``n_layers`` layers of ``cfg`` (CPU).
+def _oracle_signs(synth, cfg):
+    from oracle import turboquant
+    w1, w2, block = synth.rotation_words(cfg)
+    return w1.numpy() if w2 is None and block == 0 else turboquant.Rotation(
+        w1.numpy(), None if w2 is None else w2.numpy(), block or None)
 
-    Returns (KV bytes processed, seconds, sample description).  The bytes are the
-    stored KV planes of those layers, the same unit as the GPU figure."""
+
+def parity_figures(o_gpu, lse_gpu, o_ref, lse_ref) -> dict:
+    """Worst per-row rel-L2 and max-abs of O and |dLSE| of one layer (float64); rows
+    empty on one side only count as a failure."""
     import numpy as np
 
+    o_gpu = np.asarray(o_gpu, dtype=np.float64).reshape(o_ref.shape)
+    lse_gpu = np.asarray(lse_gpu, dtype=np.float64).reshape(lse_ref.shape)
+    diff = o_gpu - o_ref
+    den = np.linalg.norm(o_ref, axis=-1)
+    rel = np.linalg.norm(diff, axis=-1) / np.where(den > 0, den, 1.0)
+    fin = np.isfinite(lse_ref)
+    dl = np.abs(lse_gpu[fin] - lse_ref[fin])
+    bad = not np.array_equal(fin, np.isfinite(lse_gpu))
+    return {"rel_l2": float(rel.max()), "max_abs": float(np.abs(diff).max()),
+            "dlse": float("inf") if bad else (float(dl.max()) if dl.size else 0.0)}
+
+
+def merge_parity(figs) -> dict:
+    out = {k: max(f[k] for f in figs) for k in PARITY_BAR}
+    out["pass"] = all(out[k] <= PARITY_BAR[k] for k in PARITY_BAR)
+    out["bar"] = dict(PARITY_BAR)
+    return out
+
+
+def time_oracle(cfg, layers, device="cpu", gpu_outputs=None):
+    """Time the oracle's layer computation on the given ``layers`` of ``cfg`` (CPU).
+
+    Inputs are drawn from the seeded generators on ``device`` (the device the GPU path
+    drew them on, so that they are the same values) and copied to host before the
+    clock starts.  ``gpu_outputs(layer)`` -> (O, lse) host arrays of the GPU path:
+    when given, each oracle layer is compared with it.  Returns (KV bytes processed,
+    seconds, sample description, parity figures or None).  The bytes are the stored
+    KV planes of those layers, the same unit as the GPU figure."""
     import synth
     from oracle import pipeline
 
-    from oracle import turboquant
-    w1, w2, block = synth.rotation_words(cfg)
-    signs = w1.numpy() if w2 is None and block == 0 else turboquant.Rotation(
-        w1.numpy(), None if w2 is None else w2.numpy(), block or None)
+    signs = _oracle_signs(synth, cfg)
     nbytes = 0
     elapsed = 0.0
-    for layer in range(n_layers):
-        q = synth.query_f16(cfg, layer).numpy()
-        k = synth.kv_f16(cfg, layer, "k", cfg.n_kv).numpy()
-        v = synth.kv_f16(cfg, layer, "v", cfg.n_kv).numpy()
+    figs = []
+    for layer in layers:
+        q = synth.query_f16(cfg, layer, device=device).cpu().numpy()
+        k = synth.kv_f16(cfg, layer, "k", cfg.n_kv, device=device).cpu().numpy()
+        v = synth.kv_f16(cfg, layer, "v", cfg.n_kv, device=device).cpu().numpy()
         t0 = time.perf_counter()
-        pipeline.mixed_layer_reference(q, k, v, cfg.wc, cfg.k_fmt, cfg.v_fmt, cfg.tk_fmt, cfg.tv_fmt,
-                                       cfg.scale, cfg.softcap, signs)
+        ro, rl = pipeline.mixed_layer_reference(q, k, v, cfg.wc, cfg.k_fmt, cfg.v_fmt, cfg.tk_fmt, cfg.tv_fmt,
+                                                cfg.scale, cfg.softcap, signs)
         elapsed += time.perf_counter() - t0
         for fmt, x in ((cfg.k_fmt, k[:cfg.wc]), (cfg.v_fmt, v[:cfg.wc]), (cfg.tk_fmt, k[cfg.wc:]),
                        (cfg.tv_fmt, v[cfg.wc:])):
             if x.shape[0]:
                 nbytes += sum(p.nbytes for p in pipeline.encode(fmt, x[:1], signs)) * x.shape[0]
+        if gpu_outputs is not None:
+            o, lse = gpu_outputs(layer)
+            figs.append(parity_figures(o, lse, ro.reshape(-1, cfg.d), rl.reshape(-1)))
         del q, k, v
-    sample = (f"{n_layers} of {cfg.layers} layers of {cfg.name}, all {cfg.hq} query heads over all "
+    sample = (f"layers {list(layers)} of {cfg.layers} of {cfg.name}, all {cfg.hq} query heads over all "
               f"{cfg.n_kv} positions (window + tail), float64")
-    return nbytes, elapsed, sample
+    par = None
+    if figs:
+        par = merge_parity(figs)
+        par["layers"] = list(layers)
+    return nbytes, elapsed, sample, par
 
 
-def oracle_layers_for(cfg, requested: int) -> int:
-    if requested > 0:
-        return min(requested, cfg.layers)
-    return min(cfg.layers, 4 if cfg.d <= 128 else 1)
+def oracle_layers_for(cfg, requested: int):
+    """The oracle sample: the first and the last layer plus evenly spaced ones between
+    (4 layers at head_dim <= 128, 1 at 512, or ``requested``)."""
+    n = min(requested, cfg.layers) if requested > 0 else min(cfg.layers, 4 if cfg.d <= 128 else 1)
+    if n <= 1:
+        return [cfg.layers - 1]
+    return sorted({round(i * (cfg.layers - 1) / (n - 1)) for i in range(n)})
 
 
 def run_reference(args):
@@ -191,14 +299,20 @@ def run_reference(args):
     import synth
 
     cfg = synth.by_name(args.config)
+    if args.layers > 0:
+        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
+    if cfg.kind != "split":
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the position-split "
+                          "workloads only"}), flush=True)
+        return 0
     steps = max(1, args.steps)
     layers = oracle_layers_for(cfg, args.cpu_layers)
     for _ in range(max(0, min(args.warmup, 1))):
-        time_oracle(cfg, 1)
+        time_oracle(cfg, layers[:1])
     total_b, total_s = 0, 0.0
     sample = ""
     for _ in range(steps):
-        b, s, sample = time_oracle(cfg, layers)
+        b, s, sample, _ = time_oracle(cfg, layers)
         total_b += b
         total_s += s
     value = total_b / total_s / 1e9
@@ -215,9 +329,8 @@ def run_reference(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
-        "data": "synthetic (seeded N(0,1), outlier K channels)",
-        "config": {"workload": cfg.name, "layers": cfg.layers, "hq": cfg.hq, "hkv": cfg.hkv, "d": cfg.d,
-                   "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt, "v_fmt": cfg.v_fmt},
+        "data": DATA,
+        "config": bench_config(cfg, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                          "sample": sample + f", per step; CPU {cpu_model()}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -288,8 +401,8 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
-def attention_source_sha():
-    csrc = os.path.join(ROOT, "quantized_position_split_gb300", "csrc")
+def attention_source_sha(root=None):
+    csrc = os.path.join(root or ROOT, "quantized_position_split_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
         if name.startswith("attn") or name.endswith((".h", ".cuh")):
@@ -317,14 +430,17 @@ def traffic_workload(cfg, configs) -> str:
     return cfg.name
 
 
-def committed_traffic(workload: str):
-    path = os.path.join(ROOT, "profiles", f"attn_window_{workload}_traffic.json")
+def committed_traffic(workload: str, root=None):
+    """DRAM bytes per window launch from the committed ncu capture of ``workload``, or
+    None when there is none or it was taken on another version of the kernels."""
+    root = root or ROOT
+    path = os.path.join(root, "profiles", f"attn_window_{workload}_traffic.json")
     try:
         with open(path) as f:
             j = json.load(f)
     except (OSError, ValueError):
         return None
-    if j.get("kernel_source_sha") != attention_source_sha():
+    if j.get("kernel_source_sha") != attention_source_sha(root):
         return None  # counters were taken on another version of the kernel
     return j.get("dram_bytes_per_launch")
 
@@ -357,70 +473,48 @@ def measure_link(torch, device, nbytes=1 << 30):
     return best, host
 
 
-def run_ours(args):
-    import torch
+class DeviceCheckFailed(RuntimeError):
+    pass
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    device = torch.device("cuda", torch.cuda.current_device())
+def check_device(qps, where: str):
+    """Raise if a kernel's bounded wait gave up since the last reset: the outputs of
+    the steps just timed are invalid, and so is any figure taken from them."""
+    from quantized_position_split_gb300 import _native as N
+    try:
+        qps.device_status(reset=False)
+    except N.QpsError as e:
+        raise DeviceCheckFailed(f"device status after {where}: {e}") from e
 
-    import synth
-    import quantized_position_split_gb300 as qps
-    from quantized_position_split_gb300 import build as qbuild
+
+def build_split(torch, qps, synth, cfg, args, device, n_q=1):
+    """A PositionSplitDecoder with every layer of ``cfg`` loaded from the seeded
+    generators on ``device`` (the oracle check draws the same values there)."""
     from quantized_position_split_gb300.decode import PositionSplitDecoder
 
-    qbuild.build()
-    cfg = synth.by_name(args.config)
-    if args.layers > 0:
-        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
-    if cfg.kind != "split":
-        raise SystemExit("bench.py times the position-split workloads")
-    signs = _lib_signs(qps, synth, cfg)
-    ring_plan = None
-    if args.auto_ring:
-        from quantized_position_split_gb300 import autosize
-        link, host = autosize.measure_link(device)
-        bw_eff = link  # pinned host -> device through the copy engine: the tail's own path
-        att_ms = autosize.attention_ms(cfg.k_fmt, cfg.v_fmt, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
-                                       n_kv=cfg.n_kv, scale=cfg.scale, softcap=cfg.softcap, signs=signs,
-                                       device=device)
-        ptb = cfg.hkv * (sum(qps.plane_row_bytes(cfg.tk_fmt, cfg.d)) + sum(qps.plane_row_bytes(cfg.tv_fmt, cfg.d)))
-        slot_budget = 4.0 * (1 << 30)  # device memory set aside for the ring's slots
-        rp = qps.plan_ring(att_ms, bw_eff, slot_budget, float(cfg.tail_len * ptb))
-        tile_tokens = max(16, int(rp["tile_bytes"] // ptb) // 16 * 16)
-        ring_plan = dict(rp, link_gbs=link, host_memcpy_gbs=host, bw_eff_gbs=bw_eff, attention_ms=att_ms,
-                         slot_budget_bytes=slot_budget, tile_tokens=tile_tokens)
-        cfg = cfg.replace(ring_slots=rp["n_slots"], tile_tokens=tile_tokens)
     dec = PositionSplitDecoder(layers=cfg.layers, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
                                n_kv=cfg.n_kv, wc=cfg.wc, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
-                               scale=cfg.scale, softcap=cfg.softcap, signs=signs,
+                               scale=cfg.scale, softcap=cfg.softcap, signs=_lib_signs(qps, synth, cfg),
                                ring_slots=cfg.ring_slots, tile_tokens=cfg.tile_tokens, device=device,
                                tail_k_fmt=cfg.tail_k_fmt, tail_v_fmt=cfg.tail_v_fmt, ring_copy=args.ring_copy,
-                               n_q=args.n_q)
+                               n_q=n_q, n_split_window=args.n_split_window)
     for layer in range(cfg.layers):
-        q = (synth.query_f16(cfg, layer, device=device) if args.n_q == 1 else
-             synth.randn_f16((1, args.n_q, cfg.hq, cfg.d), cfg.seed, cfg.name, "verify", layer, device=device))
+        q = (synth.query_f16(cfg, layer, device=device) if n_q == 1 else
+             synth.randn_f16((1, n_q, cfg.hq, cfg.d), cfg.seed, cfg.name, "verify", layer, device=device))
         k = synth.kv_f16(cfg, layer, "k", cfg.n_kv, device=device)
         v = synth.kv_f16(cfg, layer, "v", cfg.n_kv, device=device)
         dec.load_layer(layer, k, v, q)
         del q, k, v
     dec.build()
     torch.cuda.synchronize()
+    return dec
 
-    link_gbs, host_memcpy_gbs = measure_link(torch, device)
-    stream = torch.cuda.current_stream()
-    window_bytes = dec.window_bytes()
-    tail_bytes = dec.tail_bytes()
-    kv_bytes = window_bytes + tail_bytes
 
-    # per-layer timing events around the window part, one pair per (step, layer)
-    K, W, L = args.steps, args.warmup, cfg.layers
+def time_split_steps(torch, qps, dec, K, W, stream, world, device, gpu_id):
+    """Warm-up, the window-only steps, the timed steps (per-layer events around the
+    window part, clocks sampled) and the end-to-end steps through host buffers; the
+    device error word is checked after each."""
+    L = dec.layers
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
           for _ in range(K)]
     for row in ev:
@@ -450,13 +544,8 @@ def run_ours(args):
     w1.record(stream)
     torch.cuda.synchronize()
     window_step_ms = w0.elapsed_time(w1) / K
+    check_device(qps, "the warm-up and window-only steps")
 
-    # the timed region
-    gpu_id = None
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        gpu_id = None
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -479,11 +568,10 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     set_events(None)
+    check_device(qps, "the timed steps")
     step_ms = max_over_ranks(torch, t0.elapsed_time(t1) / K, world, device)
     win_ms = [ev[i][layer][0].elapsed_time(ev[i][layer][1]) for i in range(K) for layer in range(L)]
-    win_launch_ms = statistics.mean(win_ms)
     per_step = [t0.elapsed_time(bounds[0])] + [bounds[i - 1].elapsed_time(bounds[i]) for i in range(1, K)]
-    step_dist = step_distribution(per_step)
 
     # end to end through the public API with host buffers: q in, (o, lse) out each step
     q_host = torch.empty_like(dec.q, device="cpu").pin_memory()
@@ -500,84 +588,334 @@ def run_ours(args):
         lse_host.copy_(dec.lse, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
-    h2d = q_host.numel() * q_host.element_size()
-    d2h = o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size()
-    e2e_ms = max_over_ranks(torch, e2e_ms, world, device)
+    check_device(qps, "the end-to-end steps")
+    e2e_ms = max_over_ranks(torch, e0.elapsed_time(e1) / K, world, device)
+    if dec.ring is not None:
+        dec.ring.sync()
+    return {"step_ms": step_ms, "window_step_ms": window_step_ms, "win_launch_ms": statistics.mean(win_ms),
+            "win_launch_p50_ms": statistics.median(win_ms), "per_step": step_distribution(per_step),
+            "launches": launches, "clocks": clk, "e2e_ms": e2e_ms,
+            "h2d": q_host.numel() * q_host.element_size(),
+            "d2h": o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size(),
+            "o_host": o_host, "lse_host": lse_host}
 
-    dec.ring.sync()
 
-    # roofline of the dominant kernel: the window decode-attention launch
-    per_launch_bytes = window_bytes / L
+def _copy_args(a):
+    """An independent copy of an AttnArgs struct (its Python-side references stay with
+    the original, which must outlive the copy)."""
+    return type(a).from_buffer_copy(a)
+
+
+def time_window_rotating(torch, qps, args_list, rows, d, stream, n=48):
+    """Mean duration of back-to-back window launches that cycle through ``args_list``
+    (distinct layers' windows, so that no launch finds the previous one's KV in L2)."""
+    n_split = max(qps.attn_plan(a)[0] for a in args_list)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    parts = (torch.empty((n_split, rows, d), device=dev), torch.empty((n_split, rows), device=dev))
+    copies = [_copy_args(a) for a in args_list]
+    for a in copies[:3]:
+        qps.attn_decode_window(a, parts=parts, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        qps.attn_decode_window(copies[i % len(copies)], parts=parts, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def split_record(torch, qps, synth, cfg, args, dec, m, link_gbs, host_memcpy_gbs, peak, peak_kind, stream,
+                 world, ring_plan=None):
+    """The figures of one split workload's measurement ``m``."""
+    window_bytes, tail_bytes = dec.window_bytes(), dec.tail_bytes()
+    kv_bytes = window_bytes + tail_bytes
+    L = cfg.layers
     rows = dec.rows
-    n_split_w = qps.attn_plan(dec.window_args[0])[0]
-    q_bytes = rows * cfg.d * 2
-    part_bytes = n_split_w * rows * (cfg.d + 1) * 4
-    algo_bytes = per_launch_bytes + q_bytes + part_bytes
-    peak, peak_kind = measured_hbm_peak()
-    achieved = algo_bytes / (win_launch_ms / 1e3) / 1e9
+    rec = {"value": whole_job_rate(world, kv_bytes, m["step_ms"]), "unit": UNIT, "ms_per_step": m["step_ms"],
+           "dtype": ("f16" if cfg.k_fmt == "f16" and cfg.v_fmt == "f16" else f"{cfg.k_fmt}/{cfg.v_fmt}") +
+                    (f" window, {cfg.tk_fmt}/{cfg.tv_fmt} tail" if cfg.mixed else ""),
+           "config": bench_config(cfg, args, ring_plan)}
+    if dec.window_args:
+        n_split_w = qps.attn_plan(dec.window_args[0])[0]
+        algo = window_bytes / L + rows * cfg.d * 2 + n_split_w * rows * (cfg.d + 1) * 4
+        achieved = algo / (m["win_launch_ms"] / 1e3) / 1e9
+        rec["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                           "frac": achieved / peak, "traffic": committed_traffic(traffic_workload(cfg, synth.CONFIGS)),
+                           "kernel": "window decode attention (one launch per layer), inside the step",
+                           "algorithmic_bytes_per_launch": algo, "launch_ms": m["win_launch_ms"],
+                           "launch_p50_ms": m["win_launch_p50_ms"], "n_split": n_split_w,
+                           "peak_source": peak_kind}
+        # the same launches alone: back to back, cycling through the layers' windows
+        iso_ms = time_window_rotating(torch, qps, dec.window_args, rows, cfg.d, stream)
+        check_device(qps, "the isolated window launches")
+        iso = algo / (iso_ms / 1e3) / 1e9
+        rec["roofline_isolated"] = {"bound": "hbm", "achieved": iso, "peak": peak, "unit": "GB/s",
+                                    "frac": iso / peak, "launch_ms": iso_ms,
+                                    "kernel": "window decode attention alone (48 back-to-back launches "
+                                              "cycling through the layers' windows: no L2 reuse)",
+                                    "peak_source": peak_kind}
     tail_dma_ms = tail_bytes / (link_gbs * 1e9) * 1e3
-    bound_ms = max(window_step_ms, tail_dma_ms)
+    bound_ms = max(m["window_step_ms"], tail_dma_ms)
+    if tail_bytes:
+        rec["roofline_tail"] = {"bound": "host link", "achieved": tail_bytes / (m["step_ms"] / 1e3) / 1e9,
+                                "peak": link_gbs, "unit": "GB/s",
+                                "frac": tail_bytes / (m["step_ms"] / 1e3) / 1e9 / link_gbs,
+                                "kernel": ("ring copy kernel" if args.ring_copy == "kernel" else "copy engine") +
+                                          " (tail tiles, pinned host -> ring slot)",
+                                "achieved_source": "tail bytes per step / step time",
+                                "peak_source": "pinned 1 GiB host-to-device cudaMemcpyAsync, best of 4, this run"}
+    rec["step"] = {"ms": m["step_ms"], "window_only_ms": m["window_step_ms"], "tail_dma_ms": tail_dma_ms,
+                   "bound_ms": bound_ms, "ratio_to_bound": m["step_ms"] / bound_ms,
+                   "tail_stream_gbs": tail_bytes / (m["step_ms"] / 1e3) / 1e9,
+                   "window_only_gbs": window_bytes / (m["window_step_ms"] / 1e3) / 1e9,
+                   "link_probe_gbs": link_gbs, "host_memcpy_1thread_gbs": host_memcpy_gbs,
+                   "steps_per_s": 1000.0 / m["step_ms"], "per_step": m["per_step"]}
+    rec["e2e"] = {"value": whole_job_rate(world, kv_bytes, m["e2e_ms"]), "unit": UNIT,
+                  "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"], "ms_per_step": m["e2e_ms"]}
+    rec["gpu_launches"] = m["launches"]
+    rec["clocks"] = m["clocks"]
+    return rec
 
+
+def gpu_outputs_of(m, cfg):
+    """(O, lse) host arrays of one layer from the last end-to-end step's host buffers."""
+    def get(layer):
+        return m["o_host"][layer].numpy(), m["lse_host"][layer].numpy()
+    return get
+
+
+def run_split(torch, qps, synth, cfg, args, device, stream, world, rank, gpu_id, link, peak, peak_kind,
+              val_layers, cpu_baseline: bool, ring_plan=None):
+    dec = build_split(torch, qps, synth, cfg, args, device, n_q=args.n_q)
+    try:
+        m = time_split_steps(torch, qps, dec, args.steps, args.warmup, stream, world, device, gpu_id)
+        rec = split_record(torch, qps, synth, cfg, args, dec, m, link[0], link[1], peak, peak_kind, stream, world,
+                           ring_plan)
+    finally:
+        dec.close()
+        del dec
+        torch.cuda.empty_cache()
+    if rank == 0 and args.n_q == 1 and val_layers:
+        b, s, sample, par = time_oracle(cfg, val_layers, device=device, gpu_outputs=gpu_outputs_of(m, cfg))
+        rec["validation"] = dict(par, against="float64 CPU oracle on the same seeded inputs",
+                                 outputs="last end-to-end step")
+        if cpu_baseline:
+            rec["cpu_baseline"] = {"value": b / s / 1e9, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                                   "sample": sample + f"; CPU {cpu_model()}"}
+    return rec
+
+
+def run_fanout(torch, qps, synth, cfg, args, device, stream, world, rank, gpu_id, peak, peak_kind):
+    """The shared-prefix fan-out as a whole step: one compressed prefix read once for
+    every agent, private fp16 suffixes, the per-agent LSE combine; q in, (O, lse) out."""
+    import numpy as np
+
+    from quantized_position_split_gb300.decode import FanoutDecoder
+
+    signs = _lib_signs(qps, synth, cfg)
+    q = synth.randn_f16((cfg.agents, cfg.hq, cfg.d), cfg.seed, cfg.name, "q", device=device)
+    pk = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "k", device=device)
+    pv = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "v", device=device)
+    sk = synth.randn_f16((cfg.agents, cfg.suffix_len, cfg.hkv, cfg.d), cfg.seed, cfg.name, "suffix", "k",
+                         device=device)
+    sv = synth.randn_f16((cfg.agents, cfg.suffix_len, cfg.hkv, cfg.d), cfg.seed, cfg.name, "suffix", "v",
+                         device=device)
+    fd = FanoutDecoder(agents=cfg.agents, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d, k_fmt=cfg.k_fmt, v_fmt=cfg.v_fmt,
+                       scale=cfg.scale, softcap=cfg.softcap, signs=signs).load(q, pk, pv, sk, sv).build()
+    K, W = args.steps, args.warmup
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > L2: evicts the KV between steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for _ in range(W):
+        flush.fill_(0)
+        fd.step(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    qps.launch_count(reset=True)
+    for i in range(K):
+        flush.fill_(i & 255)
+        ev[i][0].record(stream)
+        fd.step(stream)
+        ev[i][1].record(stream)
+    launches = qps.launch_count()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    check_device(qps, "the timed fan-out steps")
+    per_step = [a.elapsed_time(b) for a, b in ev]
+    step_ms = max_over_ranks(torch, statistics.mean(per_step), world, device)
+    # end to end: q from pinned host memory in, (O, lse) out, every step
+    q_host = fd.q.cpu().pin_memory()
+    o_host = torch.empty_like(fd.o, device="cpu").pin_memory()
+    lse_host = torch.empty_like(fd.lse, device="cpu").pin_memory()
+    e2e = []
+    for i in range(K):
+        flush.fill_(i & 255)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fd.q.copy_(q_host, non_blocking=True)
+        fd.step(stream)
+        o_host.copy_(fd.o, non_blocking=True)
+        lse_host.copy_(fd.lse, non_blocking=True)
+        b.record(stream)
+        e2e.append((a, b))
+    torch.cuda.synchronize()
+    check_device(qps, "the end-to-end fan-out steps")
+    e2e_ms = max_over_ranks(torch, statistics.mean(a.elapsed_time(b) for a, b in e2e), world, device)
+    prefix, suffix = fd.prefix_bytes(), fd.suffix_bytes()
+    read_once = prefix + suffix
+    naive = cfg.agents * prefix + suffix
+    rows = cfg.agents * cfg.hq
+    n_parts = qps.attn_plan(fd.pre)[0] + qps.attn_plan(fd.suf)[0]
+    algo = read_once + rows * cfg.d * 2 + n_parts * rows * (cfg.d + 1) * 4 * 2 + rows * (cfg.d + 1) * 4
+    achieved = algo / (step_ms / 1e3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "fanout_prefix_traffic.json")) as f:
+            tj = json.load(f)
+        if tj.get("kernel_source_sha") == attention_source_sha():
+            traffic = tj.get("dram_bytes_per_step")
+    except (OSError, ValueError):
+        pass
+    rec = {"value": whole_job_rate(world, read_once, step_ms), "unit": UNIT, "ms_per_step": step_ms,
+           "dtype": f"{cfg.k_fmt}/{cfg.v_fmt} prefix, f16 suffixes", "config": bench_config(cfg, args),
+           "bytes": {"prefix_read_once": prefix, "suffixes": suffix, "read_once_total": read_once,
+                     "naive_per_agent_prefix_reads": naive,
+                     "naive_equivalent_gbs": naive / (step_ms / 1e3) / 1e9},
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "traffic": traffic,
+                        "kernel": "whole fan-out step (prefix part, suffix part, combine), L2 flushed before",
+                        "algorithmic_bytes_per_step": algo, "peak_source": peak_kind},
+           "step": {"ms": step_ms, "per_step": step_distribution(per_step), "steps_per_s": 1000.0 / step_ms},
+           "e2e": {"value": whole_job_rate(world, read_once, e2e_ms), "unit": UNIT,
+                   "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+                   "d2h_bytes_per_step": o_host.numel() * o_host.element_size() + lse_host.numel() * 4,
+                   "ms_per_step": e2e_ms},
+           "gpu_launches": launches, "clocks": clk}
+    if rank == 0:
+        from oracle import pipeline
+        c = lambda t: t.cpu().numpy()  # noqa: E731
+        t0 = time.perf_counter()
+        ro, rl = pipeline.fanout_reference(c(q), c(pk), c(pv), c(sk), c(sv), cfg.k_fmt, cfg.v_fmt, cfg.scale,
+                                           cfg.softcap, _oracle_signs(synth, cfg))
+        secs = time.perf_counter() - t0
+        par = merge_parity([parity_figures(o_host.numpy(), lse_host.numpy(), ro.reshape(-1, cfg.d), rl.reshape(-1))])
+        rec["validation"] = dict(par, against="float64 CPU oracle on the same seeded inputs",
+                                 outputs="last end-to-end step", oracle_s=secs)
+    del fd, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+
+    import synth
+    import quantized_position_split_gb300 as qps
+    from quantized_position_split_gb300 import build as qbuild
+
+    qbuild.build()
+    qps.device_status(reset=True)
+    cfg = synth.by_name(args.config)
+    if args.layers > 0:
+        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
+    if cfg.kind != "split":
+        raise SystemExit("the benchmark line times a position-split workload (the fan-out is a sub-record)")
+    ring_plan = None
+    if args.auto_ring:
+        from quantized_position_split_gb300 import autosize
+        signs = _lib_signs(qps, synth, cfg)
+        link, host = autosize.measure_link(device)
+        bw_eff = link  # pinned host -> device through the copy engine: the tail's own path
+        att_ms = autosize.attention_ms(cfg.k_fmt, cfg.v_fmt, batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, d=cfg.d,
+                                       n_kv=cfg.n_kv, scale=cfg.scale, softcap=cfg.softcap, signs=signs,
+                                       device=device)
+        ptb = cfg.hkv * (sum(qps.plane_row_bytes(cfg.tk_fmt, cfg.d)) + sum(qps.plane_row_bytes(cfg.tv_fmt, cfg.d)))
+        slot_budget = 4.0 * (1 << 30)  # device memory set aside for the ring's slots
+        rp = qps.plan_ring(att_ms, bw_eff, slot_budget, float(cfg.tail_len * ptb))
+        tile_tokens = max(16, int(rp["tile_bytes"] // ptb) // 16 * 16)
+        ring_plan = dict(rp, link_gbs=link, host_memcpy_gbs=host, bw_eff_gbs=bw_eff, attention_ms=att_ms,
+                         slot_budget_bytes=slot_budget, tile_tokens=tile_tokens)
+        cfg = cfg.replace(ring_slots=rp["n_slots"], tile_tokens=tile_tokens)
+
+    link = measure_link(torch, device)
+    stream = torch.cuda.current_stream()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = None
+    peak, peak_kind = measured_hbm_peak()
+    # the oracle sample of the main workload: its timing is the cpu_baseline (rank 0 at
+    # N = 1); at N > 1 rank 0 still checks one layer of its replica
+    main_layers = oracle_layers_for(cfg, args.cpu_layers) if world == 1 else [cfg.layers - 1]
+    failed = None
+    try:
+        main = run_split(torch, qps, synth, cfg, args, device, stream, world, rank, gpu_id, link, peak, peak_kind,
+                         main_layers, cpu_baseline=(world == 1 and not args.no_cpu_baseline), ring_plan=ring_plan)
+        subs = {}
+        for name in [s for s in args.sub_configs.split(",") if s.strip()]:
+            sc = synth.by_name(name.strip())
+            if sc.name == cfg.name:
+                continue
+            if sc.kind == "fanout":
+                subs[sc.name] = run_fanout(torch, qps, synth, sc, args, device, stream, world, rank, gpu_id, peak,
+                                           peak_kind)
+            else:
+                val = [sc.layers - 1] if sc.d > 128 or world > 1 else [0, sc.layers - 1]
+                subs[sc.name] = run_split(torch, qps, synth, sc, args, device, stream, world, rank, gpu_id, link,
+                                          peak, peak_kind, val, cpu_baseline=False)
+    except DeviceCheckFailed as e:
+        failed = str(e)
+    if failed:
+        print(f"bench.py: {failed}; the figures of this run are not valid", file=sys.stderr, flush=True)
+        return 3
     if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
         return 0
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        b, s, sample = time_oracle(cfg, oracle_layers_for(cfg, args.cpu_layers))
-        cpu = {"value": b / s / 1e9, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-               "sample": sample + f"; CPU {cpu_model()}"}
-    value = whole_job_rate(world, kv_bytes, step_ms)
     out = {
         "metric": METRIC,
-        "value": value,
+        "value": main["value"],
         "unit": UNIT,
         "n_gpus": world,
-        "steps": K,
-        "warmup": W,
-        "ms_per_step": step_ms,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": main["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("f16" if cfg.k_fmt == "f16" and cfg.v_fmt == "f16" else f"{cfg.k_fmt}/{cfg.v_fmt}") +
-                 (f" window, {cfg.tk_fmt}/{cfg.tv_fmt} tail" if cfg.mixed else ""),
-        "data": "synthetic (seeded N(0,1) fp16, 4 outlier K channels per head x20)",
-        "config": {"workload": cfg.name, "layers": cfg.layers, "batch": cfg.batch, "hq": cfg.hq,
-                   "hkv": cfg.hkv, "d": cfg.d, "n_kv": cfg.n_kv, "wc": cfg.wc, "k_fmt": cfg.k_fmt,
-                   "v_fmt": cfg.v_fmt, "tail_k_fmt": cfg.tk_fmt, "tail_v_fmt": cfg.tv_fmt,
-                   "softcap": cfg.softcap, "ring_slots": cfg.ring_slots,
-                   "tile_tokens": cfg.tile_tokens, "ring_plan": ring_plan, "ring_copy": args.ring_copy, "n_q": args.n_q,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (window %.2f GB + tail %.2f GB per step)" %
-                         (window_bytes / 1e9, tail_bytes / 1e9)},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": committed_traffic(traffic_workload(cfg, synth.CONFIGS)),
-                     "kernel": "window decode attention (one launch per layer)",
-                     "algorithmic_bytes_per_launch": algo_bytes, "launch_ms": win_launch_ms,
-                     "peak_source": peak_kind},
-        # the ring's tail transfer: most of the step's GPU time goes to the ring copy
-        # kernel (or the copy engine), bound by the host link rather than by HBM
-        "roofline_tail": {"bound": "host link", "achieved": tail_bytes / (step_ms / 1e3) / 1e9,
-                          "peak": link_gbs, "unit": "GB/s",
-                          "frac": tail_bytes / (step_ms / 1e3) / 1e9 / link_gbs,
-                          "kernel": ("ring copy kernel" if args.ring_copy == "kernel" else "copy engine") +
-                                    " (tail tiles, pinned host -> ring slot)",
-                          "achieved_source": "tail bytes per step / step time",
-                          "peak_source": "pinned 1 GiB host-to-device cudaMemcpyAsync, best of 4, this run"},
-        "step": {"ms": step_ms, "window_only_ms": window_step_ms, "tail_dma_ms": tail_dma_ms,
-                 "bound_ms": bound_ms, "ratio_to_bound": step_ms / bound_ms,
-                 "tail_stream_gbs": tail_bytes / (step_ms / 1e3) / 1e9,
-                 "link_probe_gbs": link_gbs, "host_memcpy_1thread_gbs": host_memcpy_gbs,
-                 "steps_per_s": 1000.0 / step_ms, "per_step": step_dist},
-        "cpu_baseline": cpu,
-        "e2e": {"value": whole_job_rate(world, kv_bytes, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": launches,
-        "clocks": clk,
+        "dtype": main["dtype"],
+        "data": DATA,
+        "config": main["config"],
+        "roofline": main["roofline"],
+        "roofline_isolated": main.get("roofline_isolated"),
+        "roofline_tail": main.get("roofline_tail"),
+        "step": main["step"],
+        "cpu_baseline": main.get("cpu_baseline"),
+        "validation": main.get("validation"),
+        "e2e": main["e2e"],
+        "gpu_launches": main["gpu_launches"],
+        "clocks": main["clocks"],
+        "sub_records": subs,
     }
     print(json.dumps(out), flush=True)
-    dec.close()
     if world > 1:
         torch.distributed.destroy_process_group()
+    bad = [n for n, r in [(cfg.name, main)] + list(subs.items())
+           if r.get("validation") is not None and not r["validation"]["pass"]]
+    if bad:
+        print(f"bench.py: outputs outside the parity bar for {bad}", file=sys.stderr, flush=True)
+        return 4
     return 0
 
 
@@ -589,8 +927,10 @@ TIER_VARIANTS = {"qwen14b_q8": (("q8_0", "tq4"), ("q8_0", "tq2"), ("tq4", "tq4")
 
 def run_kernel_only(args):
     """Per-launch time of the window decode-attention kernel on one layer of each
-    workload (or of --config), timed back to back with CUDA events; inputs > L2 except
-    the tiny and fan-out workloads (flagged)."""
+    workload (or of --config), timed back to back with CUDA events.  The launches cycle
+    through enough copies of the window (each at its own address) that together they
+    exceed 3 x L2, so no launch reads the previous one's KV from L2; the fan-out
+    prefix is flagged as L2-sized."""
     import torch
 
     import synth
@@ -601,7 +941,7 @@ def run_kernel_only(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     # (the mixed-tail workloads share their window kernel with the uniform ones)
-    names = [args.config] if args.config != "qwen14b_f16" or args.layers else [
+    names = [args.config] if args.config != DEFAULT_CONFIG or args.layers else [
         c.name for c in synth.CONFIGS if not c.mixed]
     peak, peak_kind = measured_hbm_peak()
     s = torch.cuda.current_stream()
@@ -615,60 +955,50 @@ def run_kernel_only(args):
             q = synth.query_f16(cfg, 0, device=dev)
             k = synth.kv_f16(cfg, 0, "k", cfg.wc, device=dev)
             v = synth.kv_f16(cfg, 0, "v", cfg.wc, device=dev)
-            K = qps.encode_kv_head_major(cfg.k_fmt, k, signs)
-            V = qps.encode_kv_head_major(cfg.v_fmt, v, signs)
-            a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs)
+            shared = False
             rows = cfg.batch * cfg.hq
         else:
             q = synth.randn_f16((cfg.agents, cfg.hq, cfg.d), cfg.seed, cfg.name, "q", device=dev)
-            pk = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "k", device=dev)
-            pv = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "v", device=dev)
-            K = qps.encode_kv_head_major(cfg.k_fmt, pk, signs)
-            V = qps.encode_kv_head_major(cfg.v_fmt, pv, signs)
-            a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs, shared=True)
+            k = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "k", device=dev)
+            v = synth.randn_f16((cfg.n_kv, cfg.hkv, cfg.d), cfg.seed, cfg.name, "prefix", "v", device=dev)
+            shared = True
             rows = cfg.agents * cfg.hq
-        for n_q in ([1, 4] if name == "qwen14b_q8" and cfg.kind == "split" else [1]):
+
+        def windows(kf, vf, qq, **kw):
+            first = (qps.encode_kv_head_major(kf, k, signs), qps.encode_kv_head_major(vf, v, signs))
+            kvb = first[0].nbytes() + first[1].nbytes()
+            n_copies = 1 if cfg.kind != "split" else max(1, min(8, math.ceil(3 * L2_BYTES / kvb)))
+            kvs = [first] + [(qps.encode_kv_head_major(kf, k, signs), qps.encode_kv_head_major(vf, v, signs))
+                             for _ in range(n_copies - 1)]
+            return kvs, [qps.attn_args(qq, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs,
+                                       shared=shared, **kw) for K, V in kvs]
+
+        variants = [(cfg.k_fmt, cfg.v_fmt, 1)]
+        if name == DEFAULT_CONFIG and cfg.kind == "split":
+            variants.append((cfg.k_fmt, cfg.v_fmt, 4))
+        if not (args.layers or args.v_fmt or args.k_fmt):
+            variants += [(kf, vf, 1) for kf, vf in TIER_VARIANTS.get(name, ())]
+        for kf, vf, n_q in variants:
             if n_q > 1:  # a verify batch: 4 query tokens at the end of the window, causal
-                q4 = synth.randn_f16((cfg.batch, n_q, cfg.hq, cfg.d), cfg.seed, cfg.name, "verify", device=dev)
-                a = qps.attn_args(q4, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs,
-                                  q_pos=cfg.wc - n_q)
-                rows = cfg.batch * n_q * cfg.hq
-            _time_window_launch(qps, torch, a, name if n_q == 1 else f"{name} verify n_q={n_q} causal",
-                                rows, cfg, K, V, dev, s, peak, peak_kind)
-        # the same window with (K, V) in the other formats
-        for kf, vf in (TIER_VARIANTS.get(name, ()) if not (args.layers or args.v_fmt or args.k_fmt) else ()):
-            del K, V
-            K = qps.encode_kv_head_major(kf, k, signs)
-            V = qps.encode_kv_head_major(vf, v, signs)
-            a = qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs)
-            _time_window_launch(qps, torch, a, f"{name} K={kf} V={vf}", cfg.batch * cfg.hq,
-                                cfg.replace(k_fmt=kf, v_fmt=vf), K, V, dev, s, peak, peak_kind)
+                qq = synth.randn_f16((cfg.batch, n_q, cfg.hq, cfg.d), cfg.seed, cfg.name, "verify", device=dev)
+                kvs, alist = windows(kf, vf, qq, q_pos=cfg.wc - n_q)
+                label = f"{name} verify n_q={n_q} causal"
+            else:
+                kvs, alist = windows(kf, vf, q)
+                label = name if (kf, vf) == (cfg.k_fmt, cfg.v_fmt) else f"{name} K={kf} V={vf}"
+            r = rows * n_q
+            us = time_window_rotating(torch, qps, alist, r, cfg.d, s, n=50) * 1e3
+            n_split = qps.attn_plan(alist[0])[0]
+            kv = kvs[0][0].nbytes() + kvs[0][1].nbytes()
+            algo = kv + r * cfg.d * 2 + n_split * r * (cfg.d + 1) * 4
+            print(json.dumps({"kernel": "attn_decode_window", "workload": label, "path": qps.attn_path(alist[0]),
+                              "n_split": n_split, "launch_us": us, "kv_bytes": kv, "algorithmic_bytes": algo,
+                              "achieved_gbs": algo / us / 1e3, "frac_of_hbm": algo / us / 1e3 / peak,
+                              "peak_gbs": peak, "peak_source": peak_kind, "window_copies": len(kvs),
+                              "l2_resident": kv < L2_BYTES and len(kvs) == 1}), flush=True)
+            del kvs, alist
         qps.device_status(reset=True)
     return 0
-
-
-def _time_window_launch(qps, torch, a, label, rows, cfg, K, V, dev, s, peak, peak_kind):
-    """Per-launch time of one window attention (50 launches back to back, CUDA events)."""
-    n_split, _ = qps.attn_plan(a)
-    parts = (torch.empty((n_split, rows, cfg.d), device=dev), torch.empty((n_split, rows), device=dev))
-    for _ in range(3):
-        qps.attn_decode_window(a, parts=parts)
-    n = 50
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(s)
-    for _ in range(n):
-        qps.attn_decode_window(a, parts=parts)
-    e1.record(s)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) / n * 1e3
-    kv = K.nbytes() + V.nbytes()
-    algo = kv + rows * cfg.d * 2 + n_split * rows * (cfg.d + 1) * 4
-    print(json.dumps({"kernel": "attn_decode_window", "workload": label, "path": qps.attn_path(a),
-                      "n_split": n_split, "launch_us": us, "kv_bytes": kv, "algorithmic_bytes": algo,
-                      "achieved_gbs": algo / us / 1e3, "frac_of_hbm": algo / us / 1e3 / peak,
-                      "peak_gbs": peak, "peak_source": peak_kind,
-                      "l2_resident": kv < 129e6}), flush=True)
 
 
 def main(argv=None):

@@ -228,10 +228,13 @@ class FanoutDecoder:
         return self
 
     def build(self):
-        pre = attn_args(self.q, self.pk, self.pv, scale=self.scale, softcap=self.softcap,
-                        v_signs=self.signs, n_split=self.n_split_prefix, shared=True)
-        suf = attn_args(self.q, self.sk, self.sv, scale=self.scale, softcap=self.softcap,
-                        n_split=self.n_split_suffix)
+        """The step plan: the prefix part (every agent's rows in one pass over the shared
+        prefix), the suffix part (each agent its own rows) and the combine; ``pre`` and
+        ``suf`` keep the two parts' arguments."""
+        self.pre = pre = attn_args(self.q, self.pk, self.pv, scale=self.scale, softcap=self.softcap,
+                                   v_signs=self.signs, n_split=self.n_split_prefix, shared=True)
+        self.suf = suf = attn_args(self.q, self.sk, self.sv, scale=self.scale, softcap=self.softcap,
+                                   n_split=self.n_split_suffix)
         cap = attn_plan(pre)[0] + attn_plan(suf)[0]
         self.o_parts, self.lse_parts = _parts_buffers(cap, self.rows, self.d, self.device)
         self.plan = StepPlan([dict(device_parts=[pre, suf], tail=None, n_tiles=0,

@@ -1,6 +1,8 @@
 """Host-side helpers of bench.py (no GPU): the step-time distribution and the host
 CPU description."""
 
+import os
+
 import numpy as np
 import pytest
 
@@ -49,7 +51,54 @@ def test_traffic_file_of_a_mixed_tail_is_its_window_kernels():
         if c.kind == "split" and c.mixed:
             w = synth.by_name(names[c.name])
             assert (w.wc, w.hkv, w.d, w.k_fmt, w.v_fmt) == (c.wc, c.hkv, c.d, c.k_fmt, c.v_fmt)
-    assert bench.committed_traffic("qwen14b_q8") is not None  # the committed figure is current
+
+
+def test_committed_traffic_is_dropped_once_the_kernels_change(tmp_path):
+    """A DRAM-traffic figure counts only for the kernel sources it was captured on."""
+    import json
+    import shutil
+
+    src = os.path.join(bench.ROOT, "quantized_position_split_gb300", "csrc")
+    shutil.copytree(src, tmp_path / "quantized_position_split_gb300" / "csrc")
+    (tmp_path / "profiles").mkdir()
+    rec = {"kernel_source_sha": bench.attention_source_sha(str(tmp_path)), "dram_bytes_per_launch": 123.0}
+    (tmp_path / "profiles" / "attn_window_w_traffic.json").write_text(json.dumps(rec))
+    assert bench.committed_traffic("w", root=str(tmp_path)) == 123.0
+    assert bench.committed_traffic("absent", root=str(tmp_path)) is None
+    with open(tmp_path / "quantized_position_split_gb300" / "csrc" / "attn_mma.cuh", "a") as f:
+        f.write("// edited\n")
+    assert bench.committed_traffic("w", root=str(tmp_path)) is None
+
+
+def test_both_arms_describe_the_workload_with_the_same_config():
+    import synth
+    args = bench.parse_args([])
+    for name in ("qwen14b_q8", "qwen14b_f16", "gemma_global_q8k_tq3v", "fanout_prefix"):
+        cfg = synth.by_name(name)
+        assert bench.bench_config(cfg, args) == bench.bench_config(cfg, bench.parse_args(["--impl", "reference"]))
+    assert bench.parse_args([]).config == "qwen14b_q8"  # the largest single-GPU workload by default
+    w, t = bench.split_kv_bytes(synth.by_name("qwen14b_q8"))
+    assert abs(w / 1e9 - 10.27) < 0.01 and abs(t / 1e9 - 3.42) < 0.01  # 48 layers x 8 heads x 272 B
+
+
+def test_oracle_sample_spans_the_stack():
+    import synth
+    assert bench.oracle_layers_for(synth.by_name("qwen14b_q8"), 0) == [0, 16, 31, 47]
+    assert bench.oracle_layers_for(synth.by_name("gemma_global_q8k_tq3v"), 0) == [4]
+    assert bench.oracle_layers_for(synth.by_name("tiny"), 0) == [0]
+    assert bench.oracle_layers_for(synth.by_name("qwen14b_f16"), 2) == [0, 47]
+
+
+def test_parity_figures_and_the_bar():
+    import numpy as np
+    ro = np.ones((3, 8))
+    rl = np.array([0.0, 1.0, -np.inf])
+    ro[2] = 0.0
+    f = bench.parity_figures(ro + 1e-4, rl + 5e-5, ro, rl)
+    assert f["max_abs"] == pytest.approx(1e-4) and f["dlse"] == pytest.approx(5e-5)
+    assert bench.merge_parity([f])["pass"]
+    g = bench.parity_figures(ro, np.array([0.0, 1.0, 0.0]), ro, rl)  # an empty row that is not
+    assert g["dlse"] == float("inf") and not bench.merge_parity([f, g])["pass"]
 
 
 def test_reference_arm_line_carries_the_contract_keys(capsys, monkeypatch):

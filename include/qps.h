@@ -79,7 +79,7 @@
 extern "C" {
 #endif
 
-#define QPS_ABI_VERSION 5
+#define QPS_ABI_VERSION 6
 
 #if defined(__GNUC__)
 #define QPS_API __attribute__((visibility("default")))
@@ -406,6 +406,43 @@ QPS_API qps_status qps_ring_end_step(qps_ring* ring);
  * CUDA. */
 QPS_API qps_status qps_ring_sync(qps_ring* ring, int32_t timeout_ms);
 
+/* Guard regions of the ring's slots (failure detection; no counterpart on the pages:
+ * the pages found their ring's write-after-read hazard only by byte-identity checks,
+ * and this is the check for the other way a slot can be corrupted, a write outside
+ * it).  Every slot is allocated with 256 guard bytes before and after it, filled with
+ * a fixed per-slot pattern at qps_ring_create.  This call waits (bounded by
+ * timeout_ms, as qps_ring_sync) until the ring's copies and tail attention are done,
+ * reads both guards of every slot back (synchronous) and compares them with the
+ * pattern.  bad_slot: host, may be NULL; set to -1, or to the first slot whose guard
+ * changed.  The ring's device must be current.  Errors: INTERNAL (a guard changed:
+ * something wrote outside its slot; the message names slot and side), TIMEOUT, STATE,
+ * INVALID_ARG, CUDA. */
+QPS_API qps_status qps_ring_check_guards(qps_ring* ring, int32_t timeout_ms, int32_t* bad_slot);
+
+/* Device address and usable size (slot_bytes rounded up to 256) of ring slot `slot`,
+ * for inspection and tests; the ring keeps owning the memory.  Library utility, no
+ * counterpart on the pages.  data / bytes: host, either may be NULL.
+ * Errors: STATE (invalid ring), INVALID_ARG (slot out of range). */
+QPS_API qps_status qps_ring_slot(qps_ring* ring, int32_t slot, void** data, size_t* bytes);
+
+/* Host-side fault injection for tests of the ring's error paths (no counterpart on the
+ * pages; it exists so that a failed or late tile copy can be exercised without any GPU
+ * fault).  Arms a one-shot fault on the next copy of schedule index tile_index, in
+ * this or a later step:
+ *   QPS_RING_FAULT_COPY_FAIL  the copy is not issued and the call issuing it
+ *                             (qps_ring_begin_step, qps_attn_decode_tail or
+ *                             qps_decode_step) returns QPS_ERR_CUDA, as a failed
+ *                             cudaMemcpyAsync would; the step is closed;
+ *   QPS_RING_FAULT_COPY_LATE  a host function that sleeps delay_ms (0..5000) runs on
+ *                             the copy stream just before the copy, so the tile lands
+ *                             late; the compute stream waits for it as for any tile;
+ *   QPS_RING_FAULT_NONE       disarms.
+ * Errors: STATE (invalid ring), INVALID_ARG (mode, tile_index < 0, delay_ms). */
+#define QPS_RING_FAULT_NONE 0
+#define QPS_RING_FAULT_COPY_FAIL 1
+#define QPS_RING_FAULT_COPY_LATE 2
+QPS_API qps_status qps_ring_inject_fault(qps_ring* ring, int32_t tile_index, int32_t mode, int32_t delay_ms);
+
 /* ---- Native step runner -------------------------------------------------------- */
 
 /* One layer of a decode step: device-resident parts (the window; for a shared-prefix
@@ -468,17 +505,48 @@ QPS_API qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, void* 
  * library-owned device word instead of hanging, and the kernel returns early with
  * invalid outputs.  This call reads that word synchronously (it waits for the
  * device's pending work to reach it on the legacy stream) and clears it if `reset`.
- * Errors: TIMEOUT (some wait gave up since the last reset), CUDA. */
+ * Errors: INTERNAL (a bounds check of the checked build failed since the last reset;
+ * see qps_build_checked), TIMEOUT (some wait gave up since the last reset), CUDA. */
 QPS_API qps_status qps_device_status(int32_t reset);
+
+/* The device error word and the record of the first bounded wait that gave up since
+ * the last reset (failure detection; no counterpart on the pages), copied synchronously
+ * into `words` (host, n words; words past the record are zeroed):
+ *   [0] status bits (1: a wait gave up, 2: a bounds check failed), [1] number of waits
+ *   that gave up, [2..4] that CTA's block index x / y / z, [5] its warp, [6] the warp's
+ *   tile whose wait ran out, [7] tiles the warp had issued, [8] tiles the warp owns,
+ *   [9] positions in the CTA's chunk, [10] ns the drain wait of that tile took,
+ *   [11] 1 if the tile's copy completed during it, [12] ns of the last
+ *   qps_selftest_bounded_wait's full bounded wait.
+ * qps_device_status with reset clears all of it.  Errors: INVALID_ARG, CUDA. */
+QPS_API qps_status qps_device_wait_record(uint32_t* words, int32_t n);
 
 /* Self-test of the bounded waits above (no counterpart on the pages: it exists so that
  * the give-up path of a wait can be exercised on a GPU without any fault).  Enqueues on
  * `stream` one CTA of one warp that waits, with the same bounded wait the attention
  * kernels use on their tile copies, on a shared-memory barrier nothing ever arrives
- * on; after 256 polls of at most ~1 ms it sets the device error word and exits.  A
+ * on; once one second of the GPU's global timer has passed it sets the device error
+ * word (and records the wait's duration, qps_device_wait_record word 12) and exits.  A
  * following qps_device_status then returns QPS_ERR_TIMEOUT (reset clears it).  The
  * call itself returns QPS_OK once the launch is enqueued.  Errors: CUDA. */
 QPS_API qps_status qps_selftest_bounded_wait(void* stream);
+
+/* 1 when this library is the bounds-checked build (libqps_checked.so, compiled with
+ * QPS_CHECK_BOUNDS=1), else 0.  In that build every kernel tests each staged or
+ * addressed access (tensor-map boxes and zero-filling copies into a tile stage, the
+ * rows of a view, q, the partial outputs, the combine's outputs, the ring copy kernel's
+ * writes into its slot) against the extent it must stay in; a failing access is
+ * skipped and marks the device error word, which qps_device_status then reports as
+ * QPS_ERR_INTERNAL.  A debug aid with no counterpart on the pages.  Never fails. */
+QPS_API int32_t qps_build_checked(void);
+
+/* Self-test of those bounds checks (no counterpart on the pages: it exercises the
+ * checker's report without any out-of-bounds access).  Enqueues on `stream` one warp
+ * that guards a store one past a 4-element shared array with the kernels' check; the
+ * check fails, the store is skipped, and a following qps_device_status returns
+ * QPS_ERR_INTERNAL (reset clears it).  Errors: UNSUPPORTED (not the checked build),
+ * CUDA. */
+QPS_API qps_status qps_selftest_bounds_check(void* stream);
 
 /* Number of kernel launches the calling thread has issued through this library
  * since the last reset (reset if `reset` is non-zero).  Host only.  Library utility,

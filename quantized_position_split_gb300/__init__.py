@@ -99,6 +99,14 @@ def device_status(reset: bool = True) -> None:
     N.check(lib().qps_device_status(1 if reset else 0))
 
 
+def device_wait_record() -> List[int]:
+    """The device error word and the record of the first bounded wait that gave up
+    (``qps_device_wait_record``: 16 words, synchronous)."""
+    arr = (ctypes.c_uint32 * 16)()
+    N.check(lib().qps_device_wait_record(arr, 16))
+    return list(arr)
+
+
 def selftest_bounded_wait(stream=None) -> None:
     """Enqueue the library's self-test of its bounded in-kernel waits: one warp waits on
     a barrier nothing arrives on, gives up after well under a second and sets the device
@@ -531,6 +539,26 @@ class Ring:
 
     def sync(self, timeout_ms: int = 10000):
         N.check(lib().qps_ring_sync(self.handle, timeout_ms))
+
+    def check_guards(self, timeout_ms: int = 10000) -> None:
+        """Wait for the ring's work, then compare the guard regions around every slot
+        with their pattern (``qps_ring_check_guards``); raises QpsError(INTERNAL) if
+        something wrote outside a slot."""
+        bad = ctypes.c_int32(-1)
+        N.check(lib().qps_ring_check_guards(self.handle, timeout_ms, ctypes.byref(bad)))
+
+    def slot(self, index: int):
+        """(device address, usable bytes) of slot ``index``."""
+        p, n = ctypes.c_void_p(), ctypes.c_size_t()
+        N.check(lib().qps_ring_slot(self.handle, index, ctypes.byref(p), ctypes.byref(n)))
+        return p.value, n.value
+
+    FAULTS = {"none": 0, "copy_fail": 1, "copy_late": 2}
+
+    def inject_fault(self, tile_index: int, mode: str, delay_ms: int = 0) -> None:
+        """Arm a one-shot host-side fault on the next copy of schedule index
+        ``tile_index`` (``qps_ring_inject_fault``): "copy_fail", "copy_late" or "none"."""
+        N.check(lib().qps_ring_inject_fault(self.handle, tile_index, self.FAULTS[mode], delay_ms))
 
     def close(self):
         if self.handle:

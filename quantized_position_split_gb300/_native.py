@@ -2,6 +2,8 @@
 
 The shared library is built in-tree by ``quantized_position_split_gb300.build``; if it
 is missing, loading fails loudly: there is no other implementation to fall back to.
+``QPS_LIB_VARIANT=checked`` in the environment loads the bounds-checked variant
+(``libqps_checked.so``, same ABI) instead.
 """
 
 from __future__ import annotations
@@ -11,7 +13,18 @@ import os
 import threading
 from ctypes import POINTER, c_char_p, c_double, c_float, c_int32, c_int64, c_size_t, c_uint32, c_void_p
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqps.so")
+LIB_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib")
+LIB_PATHS = {"default": os.path.join(LIB_DIR, "libqps.so"), "checked": os.path.join(LIB_DIR, "libqps_checked.so")}
+LIB_PATH = LIB_PATHS["default"]
+
+
+def variant() -> str:
+    """The library variant this process loads: "default", or "checked" (bounds checks
+    in every kernel) when QPS_LIB_VARIANT=checked."""
+    v = os.environ.get("QPS_LIB_VARIANT", "default") or "default"
+    if v not in LIB_PATHS:
+        raise ImportError(f"QPS_LIB_VARIANT={v!r}: expected one of {sorted(LIB_PATHS)}")
+    return v
 
 QPS_OK = 0
 QPS_ERR_INVALID_ARG = 1
@@ -140,10 +153,16 @@ SIGNATURES = [
     ("qps_attn_decode_tail", c_int32, [c_void_p, c_int32, POINTER(AttnArgs), c_void_p]),
     ("qps_ring_end_step", c_int32, [c_void_p]),
     ("qps_ring_sync", c_int32, [c_void_p, c_int32]),
+    ("qps_ring_check_guards", c_int32, [c_void_p, c_int32, POINTER(c_int32)]),
+    ("qps_ring_slot", c_int32, [c_void_p, c_int32, POINTER(c_void_p), POINTER(c_size_t)]),
+    ("qps_ring_inject_fault", c_int32, [c_void_p, c_int32, c_int32, c_int32]),
     ("qps_decode_step", c_int32, [c_void_p, POINTER(TileDesc), c_int32, POINTER(LayerStep), c_int32, c_void_p]),
     ("qps_attn_decode_window_noalloc", c_int32, [POINTER(AttnArgs), c_void_p]),
     ("qps_device_status", c_int32, [c_int32]),
+    ("qps_device_wait_record", c_int32, [POINTER(c_uint32), c_int32]),
     ("qps_selftest_bounded_wait", c_int32, [c_void_p]),
+    ("qps_build_checked", c_int32, []),
+    ("qps_selftest_bounds_check", c_int32, [c_void_p]),
     ("qps_launch_count", c_int64, [c_int32]),
     ("qps_plan_ring", c_int32, [c_double, c_double, c_double, c_double, POINTER(c_int32), POINTER(c_int32),
                                 POINTER(c_double), POINTER(c_double)]),
@@ -155,12 +174,14 @@ _lib = None
 _lock = threading.Lock()
 
 
-def load(path: str = LIB_PATH):
-    """Load the shared library once and declare every function's signature."""
+def load(path: str = None):
+    """Load the shared library (the variant ``variant()`` names) once and declare every
+    function's signature."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
+        path = path or LIB_PATHS[variant()]
         if not os.path.exists(path):
             raise ImportError(
                 f"CUDA library not built: {path} is missing; run "

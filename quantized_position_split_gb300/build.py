@@ -2,9 +2,12 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into one shared
 library against the shared CUDA runtime.  IEEE division and square root are kept
-(no fast-math): the encoders are bit-exact contracts.
+(no fast-math): the encoders are bit-exact contracts.  ``variant="checked"`` builds the
+same sources with ``-DQPS_CHECK_BOUNDS=1`` into ``_lib/libqps_checked.so``: every
+kernel then tests its staged and addressed accesses against their extents (a debug
+build; loaded with ``QPS_LIB_VARIANT=checked``).
 
-Usage: ``python -m quantized_position_split_gb300.build [--force] [-j N]``.
+Usage: ``python -m quantized_position_split_gb300.build [--force] [-j N] [--checked]``.
 """
 
 from __future__ import annotations
@@ -22,9 +25,13 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
-LIB = os.path.join(LIBDIR, "libqps.so")
+VARIANTS = {  # build directory, library, extra compiler flags
+    "default": (os.path.join(PKG, "_build"), os.path.join(LIBDIR, "libqps.so"), []),
+    "checked": (os.path.join(PKG, "_build_checked"), os.path.join(LIBDIR, "libqps_checked.so"),
+                ["-DQPS_CHECK_BOUNDS=1"]),
+}
+BUILD, LIB, _ = VARIANTS["default"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [
@@ -69,10 +76,10 @@ def _headers():
     return hs
 
 
-def compile_one(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def compile_one(src: str, verbose: bool, build_dir: str = BUILD, extra=()) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     stamp = obj + ".sha"
-    flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC]
+    flags = ARCH + NVCC_FLAGS + list(extra) + ["-I", INCLUDE, "-I", CSRC]
     key = _digest([src] + _headers(), flags)
     if os.path.exists(obj) and os.path.exists(stamp) and open(stamp).read() == key:
         return obj
@@ -89,17 +96,19 @@ def compile_one(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, jobs: int = 0, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, jobs: int = 0, verbose: bool = False, variant: str = "default") -> str:
+    build_dir, lib_path, extra = VARIANTS[variant]
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     if force:
-        for f in os.listdir(BUILD):
-            os.remove(os.path.join(BUILD, f))
+        for f in os.listdir(build_dir):
+            os.remove(os.path.join(build_dir, f))
     srcs = sources()
     jobs = jobs or min(len(srcs), os.cpu_count() or 4)
     with concurrent.futures.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: compile_one(s, verbose), srcs))
+        objs = list(ex.map(lambda s: compile_one(s, verbose, build_dir, extra), srcs))
     key = _digest(objs, ["link"])
+    LIB = lib_path
     stamp = LIB + ".sha"
     if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == key:
         return LIB
@@ -119,8 +128,9 @@ def main(argv=None):
     ap.add_argument("--force", action="store_true")
     ap.add_argument("-j", "--jobs", type=int, default=0)
     ap.add_argument("-v", "--verbose", action="store_true")
+    ap.add_argument("--checked", action="store_true", help="build the bounds-checked variant")
     args = ap.parse_args(argv)
-    print(build(args.force, args.jobs, args.verbose))
+    print(build(args.force, args.jobs, args.verbose, "checked" if args.checked else "default"))
 
 
 if __name__ == "__main__":

@@ -100,8 +100,8 @@ unsigned int* device_error_word() {
   std::lock_guard<std::mutex> lk(mu);
   if (!words[dev]) {
     unsigned int* w = nullptr;
-    if (cudaMalloc(&w, sizeof(unsigned int)) != cudaSuccess) return nullptr;
-    if (cudaMemset(w, 0, sizeof(unsigned int)) != cudaSuccess) return nullptr;
+    if (cudaMalloc(&w, kErrWords * sizeof(unsigned int)) != cudaSuccess) return nullptr;
+    if (cudaMemset(w, 0, kErrWords * sizeof(unsigned int)) != cudaSuccess) return nullptr;
     words[dev] = w;
   }
   return words[dev];
@@ -290,6 +290,19 @@ qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split_out,
   p->q_pos = a->q_pos;
   p->rows_per_cta = rows_per_cta;
   p->rows_total = rows_total;
+  // the extents the checked build tests accesses against
+  {
+    const int nb = shared ? 1 : a->batch;
+    auto view_rows = [&](const qps_kv_view& v) -> int64_t {
+      if (a->kv_end == 0) return 0;
+      return (int64_t)(nb - 1) * v.batch_stride + (a->kv_end - 1) * v.tok_stride +
+             (int64_t)(a->hkv - 1) * v.head_stride + 1;
+    };
+    p->k_rows = view_rows(a->k);
+    p->v_rows = view_rows(a->v);
+    p->q_elems = (int64_t)(a->batch - 1) * p->q_bstride + (int64_t)n_q * a->hq * a->d;
+    p->parts_cap = n_split;  // run_attn sets the real capacity
+  }
   p->vblock = vblock;
   p->v_out_scale = (float)(1.0 / std::sqrt((double)a->d * (double)vblock));
   p->k_rot_scale = (float)(1.0 / std::sqrt((double)vblock));
@@ -332,15 +345,15 @@ bool attn_uses_mma(const AttnParams& p) {
 }
 
 qps_status launch_attn(const AttnParams& p_in, cudaStream_t s) {
+  AttnParams p = p_in;
+  p.err = device_error_word();
+  if (!p.err) return fail(QPS_ERR_CUDA, "attention: cannot allocate the device error word");
   if (!attn_uses_mma(p_in)) {
     if (p_in.n_q > 1 || p_in.causal)
       return fail(QPS_ERR_UNSUPPORTED, "attention: multi-query / causal decode needs the tensor-core path "
                                        "(token-contiguous planes, see qps_attn_path)");
-    return launch_attn_simple(p_in, s);
+    return launch_attn_simple(p, s);
   }
-  AttnParams p = p_in;
-  p.err = device_error_word();
-  if (!p.err) return fail(QPS_ERR_CUDA, "attention: cannot allocate the device error word");
   switch (p.d) {
     case 64: return launch_attn_mma_d64(p, s);
     case 128: return launch_attn_mma_d128(p, s);
@@ -350,7 +363,8 @@ qps_status launch_attn(const AttnParams& p_in, cudaStream_t s) {
   }
 }
 
-qps_status run_attn(const qps_attn_args* a, const AttnParams& p_in, int n_split, cudaStream_t s) {
+qps_status run_attn(const qps_attn_args* a, const AttnParams& p_in, int n_split, cudaStream_t s,
+                    int64_t parts_capacity) {
   AttnParams p = p_in;
   if (a->o_parts) {
     if (!a->lse_parts) return fail(QPS_ERR_INVALID_ARG, "attention: lse_parts is NULL");
@@ -358,6 +372,8 @@ qps_status run_attn(const qps_attn_args* a, const AttnParams& p_in, int n_split,
     p.o_parts = a->o_parts;
     p.lse_parts = a->lse_parts;
     p.part_offset = a->part_offset;
+    // a caller's buffers hold at least the parts this call writes
+    p.parts_cap = parts_capacity >= 0 ? parts_capacity : (int64_t)a->part_offset + n_split;
     return launch_attn(p, s);
   }
   if (!a->o || !a->lse) return fail(QPS_ERR_INVALID_ARG, "attention: o / lse are NULL and no o_parts given");
@@ -371,9 +387,10 @@ qps_status run_attn(const qps_attn_args* a, const AttnParams& p_in, int n_split,
   p.o_parts = ws;
   p.lse_parts = ws + (size_t)n_split * rows * p.d;
   p.part_offset = 0;
+  p.parts_cap = n_split;
   qps_status st = launch_attn(p, s);
   if (st != QPS_OK) return st;
-  return launch_combine(p.o_parts, p.lse_parts, n_split, rows, p.d, a->o, a->lse, s);
+  return launch_combine(p.o_parts, p.lse_parts, n_split, rows, p.d, a->o, a->lse, s, device_error_word());
 }
 
 }  // namespace qps
@@ -404,8 +421,22 @@ qps_status qps_device_status(int32_t reset) {
   if (!w) return fail(QPS_ERR_CUDA, "device_status: no device error word");
   unsigned int v = 0;
   QPS_CUDA_TRY(cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost));
-  if (v && reset) QPS_CUDA_TRY(cudaMemset(w, 0, sizeof(v)));
+  if (reset) QPS_CUDA_TRY(cudaMemset(w, 0, kErrWords * sizeof(unsigned int)));
+  if (v & kErrBounds)
+    return fail(QPS_ERR_INTERNAL, std::string("device_status: a bounds check of the checked build failed (the access "
+                                              "was skipped; outputs are not valid)") +
+                                      ((v & kErrTimeout) ? "; a bounded wait also gave up" : ""));
   if (v) return fail(QPS_ERR_TIMEOUT, "device_status: a kernel's bounded wait for its tile copies gave up");
+  return QPS_OK;
+}
+
+qps_status qps_device_wait_record(uint32_t* words, int32_t n) {
+  if (!words || n < 0) return fail(QPS_ERR_INVALID_ARG, "device_wait_record: need words and n >= 0");
+  unsigned int* w = device_error_word();
+  if (!w) return fail(QPS_ERR_CUDA, "device_wait_record: no device error word");
+  const int m = n < kErrWords ? n : kErrWords;
+  if (m > 0) QPS_CUDA_TRY(cudaMemcpy(words, w, m * sizeof(unsigned int), cudaMemcpyDeviceToHost));
+  for (int i = m; i < n; ++i) words[i] = 0;
   return QPS_OK;
 }
 
@@ -552,7 +583,8 @@ qps_status qps_lse_combine(const float* o_parts, const float* lse_parts, int32_t
   if (rows == 0) return QPS_OK;
   if (!o_parts || !lse_parts || !o || !lse) return fail(QPS_ERR_INVALID_ARG, "lse_combine: NULL pointer");
   if (!aligned(o_parts, 4) || !aligned(o, 4)) return fail(QPS_ERR_INVALID_ARG, "lse_combine: misaligned pointer");
-  return launch_combine(o_parts, lse_parts, n_parts, rows, d, o, lse, reinterpret_cast<cudaStream_t>(stream));
+  return launch_combine(o_parts, lse_parts, n_parts, rows, d, o, lse, reinterpret_cast<cudaStream_t>(stream),
+                        device_error_word());
 }
 
 }  // extern "C"

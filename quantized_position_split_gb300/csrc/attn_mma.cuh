@@ -263,7 +263,8 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const TensorMap* map, 
       : "memory");
 }
 // One poll that suspends the warp (instead of spinning on issue slots) until the phase
-// completes or about a millisecond passes.
+// completes or a hardware time limit passes.  The 1 ms hint is an upper bound only: on
+// GB300 one poll returns after about 4 us, so waits are bounded by the global timer.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -273,31 +274,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity: false after `polls` polls of at
-// most ~1 ms each (by default 256, well under a second).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int polls = 256) {
-  for (int it = 0; it < polls; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
-// The longer bound of the drain after a give-up: copies already issued get ~1 s more.
-constexpr int kDrainPolls = 1024;
+// Bounded wait for the phase with the given parity: false once `limit_ns` of the GPU's
+// global timer have passed without it (the clock is read only after a first poll
+// fails).  A tile copy lands in microseconds; the bound, one second, only has to end a
+// wait that would otherwise never end.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 >= limit_ns) return false;
+  }
+}
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 // A small plane's 16-token tile by 16-byte cp.async; bytes past `valid_bytes` are
-// zero-filled without being read.
+// zero-filled without being read.  The checked build also tests each chunk's source
+// against the plane's addressed bytes [lo, hi) and its destination against the stage
+// region of BYTES bytes; a failing chunk reads nothing (zero-filled).
 template <int BYTES>
 __device__ __forceinline__ void stage_flat_zfill(uint8_t* dst, const uint8_t* src, int valid_bytes, int lane,
-                                                 const uint8_t* safe) {
+                                                 const uint8_t* safe, const uint8_t* lo, const uint8_t* hi,
+                                                 unsigned int* err) {
   constexpr int CHUNKS = (BYTES + 15) / 16;
+  static_assert(BYTES % 16 == 0, "small-plane stage regions are whole 16-byte chunks");
   const uint32_t base = smem_addr(dst);
   for (int ch = lane; ch < CHUNKS; ch += 32) {
     int nb = valid_bytes - ch * 16;
     nb = nb < 0 ? 0 : (nb > 16 ? 16 : nb);
+    if (nb > 0 && !in_bounds(src + ch * 16 >= lo && src + ch * 16 + nb <= hi, err)) nb = 0;
     cp_async16(base + ch * 16, nb > 0 ? (const void*)(src + ch * 16) : (const void*)safe, nb);
   }
+  (void)lo;
+  (void)hi;
 }
 
 // Output column (within a lane group's DT columns) of row g (hh = 0) or g + 8 (hh = 1)
@@ -316,6 +333,15 @@ template <int D, int KF>
 __host__ __device__ constexpr int tqk_dim(int c, int kk, int e) {
   return c * (D / 4) + (KF == QPS_FMT_TQ4 ? 4 * kk + e : 16 * (kk >> 2) + 4 * e + (kk & 3));
 }
+
+// The warps' partial rows are merged through shared memory in a padded layout: one
+// extra float after every D/8 columns (a lane group's output columns) and a row stride
+// of D + 20 floats, so that the 32 lanes' stores of one accumulator register (rows 2c,
+// 2c + 1, column base g * D/8 or 16 i + g) fall into 32 different banks.
+template <int D>
+__host__ __device__ constexpr int ow_stride() { return D + 20; }
+template <int D>
+__host__ __device__ constexpr int ow_col(int col) { return col + col / (D / 8); }
 
 // ---- the kernel -------------------------------------------------------------------
 // CAUSAL: the verify batch's causal limit (a separate instance, so that single-token
@@ -370,6 +396,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     for (int idx = threadIdx.x; idx < nrows * D; idx += G::NW * 32) {
       const int r = idx / D, dd = idx % D;
       const int64_t row = out_row(row0 + r);
+      if (!in_bounds(part < p.parts_cap && row >= 0 && row < p.rows_total, p.err)) continue;
       p.o_parts[((int64_t)part * p.rows_total + row) * D + dd] = 0.f;
       if (dd == 0) p.lse_parts[(int64_t)part * p.rows_total + row] = -INFINITY;
     }
@@ -409,10 +436,12 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     const int rr = row0 + nt * 8 + g;
     const bool valid = rr < p.rows_per_cta;
     const __half* qrow = nullptr;
+    bool valid_q = valid;
     if (valid) {
       const int h = head * p.group + rr % p.group;
       qrow = p.shared ? p.q + (int64_t)(rr / p.group) * p.q_bstride + (int64_t)h * D
                       : p.q + (int64_t)bz * p.q_bstride + ((int64_t)(rr / p.group) * p.hq + h) * D;
+      valid_q = in_bounds((int64_t)(qrow - p.q) + D <= p.q_elems, p.err);
     }
 #pragma unroll
     for (int kk = 0; kk < MT; ++kk) {
@@ -425,8 +454,8 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         d0 = 16 * kk + 2 * c;
         d1 = d0 + 8;
       }
-      const uint32_t b0 = valid ? *reinterpret_cast<const uint32_t*>(qrow + d0) : 0u;
-      const uint32_t b1 = valid ? *reinterpret_cast<const uint32_t*>(qrow + d1) : 0u;
+      const uint32_t b0 = valid_q ? *reinterpret_cast<const uint32_t*>(qrow + d0) : 0u;
+      const uint32_t b1 = valid_q ? *reinterpret_cast<const uint32_t*>(qrow + d1) : 0u;
       if constexpr (QS) {  // (each lane reads back only its own slots: no barrier needed)
         reinterpret_cast<uint2*>(smem + QF_OFF)[(nt * MT + kk) * 32 + lane] = make_uint2(b0, b1);
       } else {
@@ -455,7 +484,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         const int h = head * p.group + rr % p.group;
         const __half* qrow = p.shared ? p.q + (int64_t)(rr / p.group) * p.q_bstride + (int64_t)h * D
                                       : p.q + (int64_t)bz * p.q_bstride + ((int64_t)(rr / p.group) * p.hq + h) * D;
-        v = __half2float(qrow[dd]);
+        if (in_bounds((int64_t)(qrow - p.q) + dd < p.q_elems, p.err)) v = __half2float(qrow[dd]);
         if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) v = -v;
       }
       qs[idx] = v;
@@ -542,29 +571,51 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     if (lane < NBOX) {
       const TensorMap* mp = &maps.k;
       int dst = G::K_OFF + lane * (TT * G::PK::IB), x = lane * G::PK::IB;
+      int rb = G::K_RB, ib = G::PK::IB;  // the plane's row bytes and the box width
       if (lane >= NKB && lane < NKB + NVB) {
         mp = &maps.v;
         dst = G::V_OFF + (lane - NKB) * (TT * G::PV::IB);
         x = (lane - NKB) * G::PV::IB;
+        rb = G::V_RB;
+        ib = G::PV::IB;
       } else if (lane >= NKB + NVB) {
         const bool ka = G::PKA::TMA && lane == NKB + NVB;
         mp = ka ? &maps.ka : &maps.va;
         dst = ka ? G::KA_OFF : G::VA_OFF;
         x = 0;
+        rb = ka ? G::K_ARB : G::V_ARB;
+        ib = ka ? G::PKA::IB : G::PVA::IB;
       }
-      tma_load_4d(sbase + dst, mp, x, tok, head, bcoord, bar);
+      // the box stays inside its plane's row, tensor and this warp's stage
+      const int stage_off = (int)(st - pipe);
+      if (in_bounds(x >= 0 && x + ib <= rb && tb >= 0 && head < p.hkv && bcoord < (p.shared ? 1 : p.batch) &&
+                        dst + TT * ib <= G::STAGE && stage_off >= 0 && stage_off + G::STAGE <= G::PIPE,
+                    p.err))
+        tma_load_4d(sbase + dst, mp, x, tok, head, bcoord, bar);
+      (void)rb;
+      (void)ib;
+      (void)stage_off;
     }
     if constexpr (G::SMALL) {
       // rows past the view's end (kv_end) are zero-filled, like the tensor-map boxes
       const int valid = (int)max((int64_t)0, min((int64_t)TT, p.end - tb));
+      // each plane's addressed bytes: rows [0, k_rows) / [0, v_rows) of the view
+      const uint8_t* k_aux = reinterpret_cast<const uint8_t*>(p.k.aux);
+      const uint8_t* v_aux = reinterpret_cast<const uint8_t*>(p.v.aux);
+      const uint8_t* k_aux2 = reinterpret_cast<const uint8_t*>(p.k.aux2);
+      const uint8_t* v_aux2 = reinterpret_cast<const uint8_t*>(p.v.aux2);
       if constexpr (G::K_ARB > 0 && !G::PKA::TMA)
-        stage_flat_zfill<G::PKA::BYTES>(st + G::KA_OFF, ka + tb * G::K_ARB, valid * G::K_ARB, lane, safe);
+        stage_flat_zfill<G::PKA::BYTES>(st + G::KA_OFF, ka + tb * G::K_ARB, valid * G::K_ARB, lane, safe, k_aux,
+                                        k_aux + p.k_rows * G::K_ARB, p.err);
       if constexpr (G::V_ARB > 0 && !G::PVA::TMA)
-        stage_flat_zfill<G::PVA::BYTES>(st + G::VA_OFF, va + tb * G::V_ARB, valid * G::V_ARB, lane, safe);
+        stage_flat_zfill<G::PVA::BYTES>(st + G::VA_OFF, va + tb * G::V_ARB, valid * G::V_ARB, lane, safe, v_aux,
+                                        v_aux + p.v_rows * G::V_ARB, p.err);
       if constexpr (G::K_A2RB > 0)
-        stage_flat_zfill<G::PKA2::BYTES>(st + G::KA2_OFF, ka2 + tb * G::K_A2RB, valid * G::K_A2RB, lane, safe);
+        stage_flat_zfill<G::PKA2::BYTES>(st + G::KA2_OFF, ka2 + tb * G::K_A2RB, valid * G::K_A2RB, lane, safe,
+                                         k_aux2, k_aux2 + p.k_rows * G::K_A2RB, p.err);
       if constexpr (G::V_A2RB > 0)
-        stage_flat_zfill<G::PVA2::BYTES>(st + G::VA2_OFF, va2 + tb * G::V_A2RB, valid * G::V_A2RB, lane, safe);
+        stage_flat_zfill<G::PVA2::BYTES>(st + G::VA2_OFF, va2 + tb * G::V_A2RB, valid * G::V_A2RB, lane, safe,
+                                         v_aux2, v_aux2 + p.v_rows * G::V_A2RB, p.err);
       cp_async_arrive_noinc(bar);
     }
   };
@@ -607,6 +658,11 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     for (int u = 0; u < 4; ++u) {
       tq_off2[u] = soff<G::PV::IB, G::PV::SW, TT>(tk0[u], g * (DT / 4));
       if constexpr (VF == QPS_FMT_TQ3) tq_sgn[u] = soff<G::PVA::IB, G::PVA::SW, TT>(tk0[u], g * (DT / 8));
+      // the decode reads up to DT / 4 (DT / 8) bytes from here, in every sub-tile
+      in_bounds(tq_off2[u] >= 0 && tq_off2[u] + 16 * (SUB - 1) * G::PV::IB + DT / 4 <= G::PV::BYTES, p.err);
+      if constexpr (VF == QPS_FMT_TQ3)
+        in_bounds(tq_sgn[u] >= 0 && tq_sgn[u] + 16 * (SUB - 1) * G::PVA::IB + DT / 8 <= G::PVA::BYTES,
+                  p.err);
     }
   }
 
@@ -1134,14 +1190,34 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   if (k_fail >= 0) {
     // Record the failure (the host reads it through qps_device_status), stop every warp's
     // further copies, then give each copy this warp still has in flight (tiles k_fail ..
-    // n_issued - 1, at most STAGES, so one per stage) a longer bounded wait, so that no
+    // n_issued - 1, at most STAGES, so one per stage) one more bounded wait, so that no
     // tensor-map write lands in shared memory after the CTA has exited.  Should one of
     // those also run out, the CTA exits with that copy still outstanding.
+    bool first = false;
     if (lane == 0) {
       atomicOr(p.err, 1u);
       *abort_flag = 1;
+      first = atomicAdd(p.err + 1, 1u) == 0;  // this CTA's record is the launch's first
+      if (first) {
+        unsigned int* r = p.err + 2;
+        r[0] = blockIdx.x;
+        r[1] = blockIdx.y;
+        r[2] = blockIdx.z;
+        r[3] = warp;
+        r[4] = k_fail;
+        r[5] = n_issued;
+        r[6] = (unsigned)((ntiles - warp + kWarps - 1) / kWarps);
+        r[7] = (unsigned)(t1 - t0);
+      }
     }
-    for (int j = k_fail; j < n_issued; ++j) mbar_wait(bar_of(j), par_of(j), kDrainPolls);
+    for (int j = k_fail; j < n_issued; ++j) {
+      const uint64_t w0 = global_ns();
+      const bool done = mbar_wait(bar_of(j), par_of(j));
+      if (first && j == k_fail) {
+        p.err[10] = (unsigned)min((uint64_t)0xffffffffu, global_ns() - w0);
+        p.err[11] = done ? 1u : 0u;
+      }
+    }
     __syncwarp();
   }
   cp_async_wait<0>();
@@ -1151,10 +1227,11 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
   asm volatile("griddepcontrol.launch_dependents;" :::);
 
   // ---- merge the warps' states, then the chunk's partial ------------------------------
+  constexpr int OWS = ow_stride<D>();
   float* mw = reinterpret_cast<float*>(smem);  // [kWarps][ROWS]
   float* lw = mw + kWarps * ROWS;              // [kWarps][ROWS]
-  float* ow = lw + kWarps * ROWS;              // [kWarps][ROWS][D]
-  float* fin = ow + kWarps * ROWS * D;         // [ROWS][D]
+  float* ow = lw + kWarps * ROWS;              // [kWarps][ROWS][OWS], columns at ow_col
+  float* fin = ow + kWarps * ROWS * OWS;       // [ROWS][D]
   int64_t* orow = reinterpret_cast<int64_t*>(fin + ROWS * D);  // [ROWS] output row index
   float* wgt = reinterpret_cast<float*>(orow + ROWS);             // [kWarps][ROWS] warp weights
   float* rmx = wgt + kWarps * ROWS;                                // [ROWS] row maximum (log2)
@@ -1186,11 +1263,11 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         d0 = 16 * i + g;
         d1 = d0 + 8;
       }
-      float* base = ow + (warp * ROWS + nt * 8 + 2 * c) * D;
-      base[d0] = o[i][nt][0];
-      base[D + d0] = o[i][nt][1];
-      base[d1] = o[i][nt][2];
-      base[D + d1] = o[i][nt][3];
+      float* base = ow + (warp * ROWS + nt * 8 + 2 * c) * OWS;
+      base[ow_col<D>(d0)] = o[i][nt][0];
+      base[OWS + ow_col<D>(d0)] = o[i][nt][1];
+      base[ow_col<D>(d1)] = o[i][nt][2];
+      base[OWS + ow_col<D>(d1)] = o[i][nt][3];
     }
   }
   __syncthreads();
@@ -1217,7 +1294,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     const int r = idx / D, dd = idx % D;
     float acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) acc += ow[(w * ROWS + r) * D + dd] * wgt[w * ROWS + r];
+    for (int w = 0; w < kWarps; ++w) acc += ow[(w * ROWS + r) * OWS + ow_col<D>(dd)] * wgt[w * ROWS + r];
     if constexpr (is_tq(VF))  // the rotation's second sign vector
       if ((p.vsigns2[dd >> 5] >> (dd & 31)) & 1u) acc = -acc;
     fin[idx] = acc;
@@ -1249,6 +1326,7 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     }
     const int64_t row = orow[r];
     const bool empty = !(den > 0.f);
+    if (!in_bounds(part < p.parts_cap && row >= 0 && row < p.rows_total, p.err)) continue;
     p.o_parts[((int64_t)part * p.rows_total + row) * D + dd] = empty ? 0.f : val / den;
     if (dd == 0)
       p.lse_parts[(int64_t)part * p.rows_total + row] = empty ? -INFINITY : (mx + log2f(den)) * 0.6931471805599453f;
@@ -1261,7 +1339,8 @@ constexpr size_t smem_bytes() {
   // the stages and barriers, the give-up flag, then query fragments kept in shared memory
   constexpr size_t pipe = (size_t)align_to(G::END + 16, 16) + qf_bytes<D, KF, VF, NTW>();
   constexpr int ROWS = 8 * NTW;
-  constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * D + (size_t)ROWS * D) +
+  constexpr size_t merge = sizeof(float) * ((size_t)2 * G::NW * ROWS + (size_t)G::NW * ROWS * ow_stride<D>() +
+                                           (size_t)ROWS * D) +
                            sizeof(int64_t) * ROWS + sizeof(float) * ((size_t)G::NW * ROWS + 2 * ROWS);
   return (pipe > merge ? pipe : merge) + 1024;  // + slack for the 1024-byte base alignment
 }

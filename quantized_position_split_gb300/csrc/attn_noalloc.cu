@@ -95,6 +95,7 @@ extern "C" qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, voi
   p.o_parts = reinterpret_cast<float*>(base + kPartsOffset);
   p.lse_parts = reinterpret_cast<float*>(base + lse_off);
   p.part_offset = 0;
+  p.parts_cap = n_split;
   p.err = reinterpret_cast<unsigned int*>(base + kErrOffset);
   if (!attn_uses_mma(p)) {
     // the CUDA-core kernel decodes one query token per row and has no causal limit:
@@ -113,5 +114,5 @@ extern "C" qps_status qps_attn_decode_window_noalloc(const qps_attn_args* a, voi
     }
   }
   if (st != QPS_OK) return st;
-  return launch_combine(p.o_parts, p.lse_parts, n_split, p.rows_total, p.d, a->o, a->lse, s);
+  return launch_combine(p.o_parts, p.lse_parts, n_split, p.rows_total, p.d, a->o, a->lse, s, p.err);
 }

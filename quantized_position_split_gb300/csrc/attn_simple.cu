@@ -154,7 +154,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
         const int rr = rc0 + r;
         const int b = p.shared ? rr / p.group : bz;
         const int h = g * p.group + (p.shared ? rr % p.group : rr);
-        val = __half2float(p.q[(int64_t)b * p.q_bstride + (int64_t)h * D + dd]);
+        const int64_t qi = (int64_t)b * p.q_bstride + (int64_t)h * D + dd;
+        if (in_bounds(qi >= 0 && qi < p.q_elems, p.err)) val = __half2float(p.q[qi]);
       }
       qs[idx] = val;
     }
@@ -198,8 +199,21 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
 
     for (int64_t t = t0 + warp; t < t1; t += kWarps) {
       float kf[E], vf[E];
-      load_row<KF, D>(p.k, kbase + t * p.k.tok + (int64_t)g * p.k.head, lane, levels, kf);
-      load_row<VF, D>(p.v, vbase + t * p.v.tok + (int64_t)g * p.v.head, lane, levels, vf);
+      const int64_t krow = kbase + t * p.k.tok + (int64_t)g * p.k.head;
+      const int64_t vrow = vbase + t * p.v.tok + (int64_t)g * p.v.head;
+      // (warp-uniform: a row outside its view reads as zeros in the checked build)
+      if (in_bounds(krow >= 0 && krow < p.k_rows, p.err)) {
+        load_row<KF, D>(p.k, krow, lane, levels, kf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) kf[e] = 0.f;
+      }
+      if (in_bounds(vrow >= 0 && vrow < p.v_rows, p.err)) {
+        load_row<VF, D>(p.v, vrow, lane, levels, vf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) vf[e] = 0.f;
+      }
 #pragma unroll
       for (int r = 0; r < RC; ++r) {
         const float* qr = qs + r * D + lane * E;
@@ -283,6 +297,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simple_kernel(const AttnPara
       const int h = g * p.group + (p.shared ? rr % p.group : rr);
       const int64_t row = (int64_t)b * p.hq + h;
       const bool empty = !(den > 0.f);
+      if (!in_bounds(part < p.parts_cap && row >= 0 && row < p.rows_total, p.err)) continue;
       p.o_parts[((int64_t)part * p.rows_total + row) * D + dd] = empty ? 0.f : val / den;
       if (dd == 0) p.lse_parts[(int64_t)part * p.rows_total + row] = empty ? -INFINITY : mx + __logf(den);
     }

@@ -23,7 +23,7 @@ constexpr int kCombineU = 8;  // parts in flight per warp
 
 __global__ void __launch_bounds__(kCombineWarps * 32) lse_combine_kernel(
     const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int n_parts, int64_t rows, int d,
-    float* __restrict__ o, float* __restrict__ lse) {
+    float* __restrict__ o, float* __restrict__ lse, unsigned int* err) {
   constexpr int U = kCombineU;
   __shared__ float wm[kCombineWarps], wd[kCombineWarps], wacc[kCombineWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) lse_combine_kernel(
     }
   }
   const bool empty = !(dt > 0.f);
+  if (!in_bounds(row < rows && col < d, err)) return;
   o[row * d + col] = empty ? 0.f : s / dt;
   if (blockIdx.y == 0 && lane == 0) lse[row] = empty ? -INFINITY : mx + __logf(dt);
 }
@@ -80,13 +81,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) lse_combine_kernel(
 }  // namespace
 
 qps_status launch_combine(const float* o_parts, const float* lse_parts, int n_parts,
-                          int64_t rows, int d, float* o, float* lse, cudaStream_t s) {
+                          int64_t rows, int d, float* o, float* lse, cudaStream_t s, unsigned int* err) {
   if (rows == 0) return QPS_OK;
   if (rows > 0x7fffffffLL) return fail(QPS_ERR_UNSUPPORTED, "lse_combine: too many rows");
   if (d < 32 || d > 1024 || (d & (d - 1)))
     return fail(QPS_ERR_UNSUPPORTED, "lse_combine: head_dim must be 32, 64, 128, 256, 512 or 1024");
   const dim3 grid((unsigned)rows, (unsigned)(d / 32));
-  lse_combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o_parts, lse_parts, n_parts, rows, d, o, lse);
+  lse_combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o_parts, lse_parts, n_parts, rows, d, o, lse, err);
   count_launch();
   QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;

@@ -36,7 +36,34 @@ bool encode_plane_map(TensorMap* map, const void* base, int row_bytes, int64_t t
 // ---- device facts -----------------------------------------------------------------
 int sm_count_current();
 // The current device's error word (library-owned, allocated on first use, zeroed).
+// Bits: kErrTimeout, a bounded in-kernel wait gave up; kErrBounds, a bounds check of the
+// checked build failed and its access was skipped.
+// The word is the first of kErrWords: [1] counts bounded waits that gave up, [2..11]
+// record the first of them (block x / y / z, warp, the tile k whose wait ran out, tiles
+// issued, the warp's tiles, the chunk's positions, the ns the drain wait of that tile
+// took, 1 if it then completed), [12] the ns of the self-test's full bounded wait.
 unsigned int* device_error_word();
+constexpr unsigned int kErrTimeout = 1u, kErrBounds = 2u;
+constexpr int kErrWords = 16;
+
+// ---- the checked build ----------------------------------------------------------------
+// Compiled with -DQPS_CHECK_BOUNDS=1 (the library variant libqps_checked.so), the kernels
+// test every staged or addressed global / shared access against the extent it must stay
+// in; a failing access is skipped and sets kErrBounds in the error word passed (none if
+// NULL).  In the normal build the test is the constant true and compiles away.
+#ifndef QPS_CHECK_BOUNDS
+#define QPS_CHECK_BOUNDS 0
+#endif
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned int* err) {
+#if QPS_CHECK_BOUNDS
+  if (!ok && err) atomicOr(err, kErrBounds);
+  return ok;
+#else
+  (void)ok;
+  (void)err;
+  return true;
+#endif
+}
 
 // ---- TurboQuant codebooks (computed once on the host from the Gaussian density) ----
 struct Codebook {
@@ -104,6 +131,11 @@ struct AttnParams {
   float* o_parts;
   float* lse_parts;
   int part_offset;
+  // extents the checked build tests accesses against: rows a view addresses (the
+  // largest row index of [0, end) x heads x batch entries, + 1), q elements, and the
+  // parts the o_parts / lse_parts buffers hold
+  int64_t k_rows, v_rows, q_elems;
+  int64_t parts_cap;
   unsigned int* err;  // device word set non-zero when a bounded in-kernel wait gives up
   uint32_t vsigns[kMaxSignWords];   // V rotation: s1
   uint32_t vsigns2[kMaxSignWords];  // s2 (all 0: none)
@@ -136,9 +168,12 @@ __host__ __device__ constexpr int mma_ctas_per_sm(int d, int ntw, int vfmt) {
 qps_status resolve_attn(const qps_attn_args* a, AttnParams* p, int* n_split, size_t* ws_bytes);
 qps_status launch_attn(const AttnParams& p, cudaStream_t stream);
 qps_status launch_combine(const float* o_parts, const float* lse_parts, int n_parts,
-                          int64_t rows, int d, float* o, float* lse, cudaStream_t stream);
-// Runs a resolved attention in whichever output mode the args ask for.
-qps_status run_attn(const qps_attn_args* a, const AttnParams& p, int n_split, cudaStream_t s);
+                          int64_t rows, int d, float* o, float* lse, cudaStream_t stream,
+                          unsigned int* err = nullptr);
+// Runs a resolved attention in whichever output mode the args ask for; parts_capacity
+// (if >= 0) is the number of parts the caller's o_parts / lse_parts buffers hold.
+qps_status run_attn(const qps_attn_args* a, const AttnParams& p, int n_split, cudaStream_t s,
+                    int64_t parts_capacity = -1);
 
 qps_status launch_quant_q8_0(const __half* x, int64_t rows, int d, int64_t stride,
                              int8_t* codes, __half* scales, cudaStream_t s);

@@ -72,7 +72,8 @@ struct qps_ring {
   int device = 0;
   int n_slots = 0;
   size_t slot_bytes = 0;
-  void* slots[4] = {nullptr, nullptr, nullptr, nullptr};
+  void* alloc[4] = {nullptr, nullptr, nullptr, nullptr};  // guard + slot + guard
+  void* slots[4] = {nullptr, nullptr, nullptr, nullptr};  // alloc + kGuardBytes
   cudaStream_t copy = nullptr;
   cudaEvent_t copy_done[4] = {};
   cudaEvent_t compute_done[4] = {};
@@ -84,14 +85,39 @@ struct qps_ring {
   int copy_mode = QPS_RING_COPY_ENGINE;
   int next_consume = 0;
   bool open = false;
+  // one-shot host-side fault of the next copy of schedule index fault_tile (tests)
+  int fault_tile = -1;
+  int fault_mode = QPS_RING_FAULT_NONE;
+  int fault_delay_ms = 0;
 };
 
 namespace qps {
 namespace {
 
 constexpr size_t kPlaneAlign = 256;
+// Guard regions before and after every slot, filled with a fixed pattern at creation
+// and compared by qps_ring_check_guards: a write outside its slot changes one of them.
+constexpr size_t kGuardBytes = 256;
+constexpr size_t kGuardWords = kGuardBytes / 4;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Pattern word i of the guard before (side 0) or after (side 1) slot `slot`.
+uint32_t guard_word(int slot, int side, size_t i) {
+  uint32_t x = 0x9E3779B9u * (uint32_t)(i + 1) ^ (side ? 0xC0DEC0DEu : 0x5EED5EEDu) ^ (uint32_t)slot << 24;
+  x ^= x >> 15;
+  return x * 0x2C1B3C6Du;
+}
+
+void guard_pattern(int slot, int side, uint32_t* out) {
+  for (size_t i = 0; i < kGuardWords; ++i) out[i] = guard_word(slot, side, i);
+}
+
+// Stand-in for a late tile copy: runs on the copy stream before the copy (a host
+// function: it sleeps, calls no CUDA API).
+void CUDART_CB late_copy_host_fn(void* ms) {
+  std::this_thread::sleep_for(std::chrono::milliseconds(*static_cast<const int*>(ms)));
+}
 
 bool valid_ring(const qps_ring* r) { return r && r->magic == qps_ring::kMagic; }
 
@@ -126,11 +152,20 @@ struct CopySegs {
   uint64_t n16[6];
   uint32_t rem[6];
   int n;
+  // the slot's bytes [slot_lo, slot_hi): the checked build tests every write against them
+  const uint8_t* slot_lo;
+  const uint8_t* slot_hi;
+  unsigned int* err;
 };
 
 __global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const __grid_constant__ CopySegs s) {
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t step = (size_t)gridDim.x * blockDim.x;
+  // a 16-byte (or, for the byte tail, one-byte) write at q stays inside the slot
+  auto in_slot = [&](const void* q, size_t bytes) {
+    const uint8_t* b = static_cast<const uint8_t*>(q);
+    return in_bounds(b >= s.slot_lo && b + bytes <= s.slot_hi, s.err);
+  };
   for (int k = 0; k < s.n; ++k) {
     const uint4* __restrict__ src = s.src[k];
     uint4* __restrict__ dst = s.dst[k];
@@ -141,10 +176,12 @@ __global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const __grid_co
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) v[u] = src[i + u * step];
 #pragma unroll
-      for (int u = 0; u < kCopyUnroll; ++u) dst[i + u * step] = v[u];
+      for (int u = 0; u < kCopyUnroll; ++u)
+        if (in_slot(dst + i + u * step, 16)) dst[i + u * step] = v[u];
     }
-    for (; i < n; i += step) dst[i] = src[i];
-    if (tid < s.rem[k])
+    for (; i < n; i += step)
+      if (in_slot(dst + i, 16)) dst[i] = src[i];
+    if (tid < s.rem[k] && in_slot(reinterpret_cast<uint8_t*>(dst + n) + tid, 1))
       reinterpret_cast<uint8_t*>(dst + n)[tid] = reinterpret_cast<const uint8_t*>(src + n)[tid];
   }
 }
@@ -152,6 +189,15 @@ __global__ void __launch_bounds__(kCopyThreads) ring_copy_kernel(const __grid_co
 qps_status issue_copy(qps_ring* r, int i) {
   const int slot = i % r->n_slots;
   const qps_tile_desc& t = r->tiles[i];
+  if (i == r->fault_tile) {  // an armed test fault: one shot
+    const int mode = r->fault_mode;
+    r->fault_tile = -1;
+    r->fault_mode = QPS_RING_FAULT_NONE;
+    if (mode == QPS_RING_FAULT_COPY_FAIL)
+      return fail(QPS_ERR_CUDA, "ring: injected failure of the copy of tile " + std::to_string(i));
+    if (mode == QPS_RING_FAULT_COPY_LATE)
+      QPS_CUDA_TRY(cudaLaunchHostFunc(r->copy, late_copy_host_fn, &r->fault_delay_ms));
+  }
   if (r->compute_recorded[slot]) QPS_CUDA_TRY(cudaStreamWaitEvent(r->copy, r->compute_done[slot], 0));
   char* base = reinterpret_cast<char*>(r->slots[slot]);
   const size_t* off = &r->offsets[(size_t)i * 6];
@@ -159,6 +205,9 @@ qps_status issue_copy(qps_ring* r, int i) {
     const KernelCopy& kc = r->kcopy[i];
     CopySegs cs{};
     cs.n = kc.n;
+    cs.slot_lo = reinterpret_cast<const uint8_t*>(base);
+    cs.slot_hi = reinterpret_cast<const uint8_t*>(base) + r->slot_bytes;
+    cs.err = QPS_CHECK_BOUNDS ? device_error_word() : nullptr;
     for (int k = 0; k < kc.n; ++k) {
       cs.src[k] = reinterpret_cast<const uint4*>(kc.src[k]);
       cs.dst[k] = reinterpret_cast<uint4*>(base + kc.off[k]);
@@ -235,7 +284,7 @@ qps_status tail_attend(qps_ring* r, int idx, const qps_attn_args* a_in, cudaStre
   if (a.o_parts && (int64_t)a.part_offset + n_split > parts_capacity)
     return fail(QPS_ERR_INVALID_ARG, "decode_tail: parts capacity exceeded");
   QPS_CUDA_TRY(cudaStreamWaitEvent(compute, r->copy_done[slot], 0));
-  st = run_attn(&a, p, n_split, compute);
+  st = run_attn(&a, p, n_split, compute, parts_capacity == INT64_MAX ? -1 : parts_capacity);
   if (st != QPS_OK) return st;
   QPS_CUDA_TRY(cudaEventRecord(r->compute_done[slot], compute));
   r->compute_recorded[slot] = true;
@@ -358,14 +407,23 @@ qps_status qps_ring_create(int32_t n_slots, size_t slot_bytes, int32_t device, q
     e = cudaFuncSetAttribute(ring_copy_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   for (int s = 0; s < n_slots && e == cudaSuccess; ++s) {
-    e = cudaMalloc(&r->slots[s], r->slot_bytes);
+    e = cudaMalloc(&r->alloc[s], kGuardBytes + r->slot_bytes + kGuardBytes);
+    if (e == cudaSuccess) {
+      r->slots[s] = static_cast<char*>(r->alloc[s]) + kGuardBytes;
+      uint32_t pat[kGuardWords];
+      guard_pattern(s, 0, pat);
+      e = cudaMemcpy(r->alloc[s], pat, kGuardBytes, cudaMemcpyHostToDevice);
+      guard_pattern(s, 1, pat);
+      if (e == cudaSuccess)
+        e = cudaMemcpy(static_cast<char*>(r->slots[s]) + r->slot_bytes, pat, kGuardBytes, cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->copy_done[s], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->compute_done[s], cudaEventDisableTiming);
   }
   if (e != cudaSuccess) {
     st = cuda_fail(e, "ring_create");
     for (int s = 0; s < 4; ++s) {
-      if (r->slots[s]) cudaFree(r->slots[s]);
+      if (r->alloc[s]) cudaFree(r->alloc[s]);
       if (r->copy_done[s]) cudaEventDestroy(r->copy_done[s]);
       if (r->compute_done[s]) cudaEventDestroy(r->compute_done[s]);
     }
@@ -390,7 +448,7 @@ qps_status qps_ring_destroy(qps_ring* r) {
     return st;
   }
   for (int s = 0; s < r->n_slots; ++s) {
-    cudaFree(r->slots[s]);
+    cudaFree(r->alloc[s]);
     cudaEventDestroy(r->copy_done[s]);
     cudaEventDestroy(r->compute_done[s]);
   }
@@ -528,6 +586,52 @@ qps_status qps_ring_sync(qps_ring* r, int32_t timeout_ms) {
   return ring_sync(r, timeout_ms);
 }
 
+qps_status qps_ring_check_guards(qps_ring* r, int32_t timeout_ms, int32_t* bad_slot) {
+  if (bad_slot) *bad_slot = -1;
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_check_guards: invalid or destroyed ring");
+  if (timeout_ms < 0) return fail(QPS_ERR_INVALID_ARG, "ring_check_guards: timeout_ms must be >= 0");
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (prev != r->device) return fail(QPS_ERR_INVALID_ARG, "ring_check_guards: the ring's device is not current");
+  qps_status st = ring_sync(r, timeout_ms);  // every writer of the slots (the copies) is done
+  if (st != QPS_OK) return st;
+  uint32_t got[kGuardWords], want[kGuardWords];
+  for (int s = 0; s < r->n_slots; ++s) {
+    for (int side = 0; side < 2; ++side) {
+      const char* g = side ? static_cast<const char*>(r->slots[s]) + r->slot_bytes : static_cast<const char*>(r->alloc[s]);
+      QPS_CUDA_TRY(cudaMemcpy(got, g, kGuardBytes, cudaMemcpyDeviceToHost));
+      guard_pattern(s, side, want);
+      if (std::memcmp(got, want, kGuardBytes) != 0) {
+        if (bad_slot) *bad_slot = s;
+        return fail(QPS_ERR_INTERNAL, "ring_check_guards: the guard " + std::string(side ? "after" : "before") +
+                                          " slot " + std::to_string(s) + " was overwritten");
+      }
+    }
+  }
+  return QPS_OK;
+}
+
+qps_status qps_ring_slot(qps_ring* r, int32_t slot, void** data, size_t* bytes) {
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_slot: invalid or destroyed ring");
+  if (slot < 0 || slot >= r->n_slots) return fail(QPS_ERR_INVALID_ARG, "ring_slot: slot out of range");
+  if (data) *data = r->slots[slot];
+  if (bytes) *bytes = r->slot_bytes;
+  return QPS_OK;
+}
+
+qps_status qps_ring_inject_fault(qps_ring* r, int32_t tile_index, int32_t mode, int32_t delay_ms) {
+  if (!valid_ring(r)) return fail(QPS_ERR_STATE, "ring_inject_fault: invalid or destroyed ring");
+  if (mode != QPS_RING_FAULT_NONE && mode != QPS_RING_FAULT_COPY_FAIL && mode != QPS_RING_FAULT_COPY_LATE)
+    return fail(QPS_ERR_INVALID_ARG, "ring_inject_fault: unknown mode");
+  if (tile_index < 0) return fail(QPS_ERR_INVALID_ARG, "ring_inject_fault: tile_index must be >= 0");
+  if (mode == QPS_RING_FAULT_COPY_LATE && (delay_ms < 0 || delay_ms > 5000))
+    return fail(QPS_ERR_INVALID_ARG, "ring_inject_fault: delay_ms must be in [0, 5000]");
+  r->fault_tile = mode == QPS_RING_FAULT_NONE ? -1 : tile_index;
+  r->fault_mode = mode;
+  r->fault_delay_ms = delay_ms;
+  return QPS_OK;
+}
+
 qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n_tiles,
                            const qps_layer_step* layers, int32_t n_layers, void* stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -573,7 +677,7 @@ qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n
       }
       rows = p.rows_total;
       d = p.d;
-      st = run_attn(&a, p, n, s);
+      st = run_attn(&a, p, n, s, L.parts_capacity);
       off += n;
     }
     if (st == QPS_OK && L.part_events[1]) {
@@ -597,7 +701,7 @@ qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n
       st = fail(QPS_ERR_INVALID_ARG, "decode_step: o / lse are NULL");
       break;
     }
-    st = launch_combine(L.o_parts, L.lse_parts, off, rows, d, L.o, L.lse, s);
+    st = launch_combine(L.o_parts, L.lse_parts, off, rows, d, L.o, L.lse, s, device_error_word());
   }
   if (ring) {
     if (st != QPS_OK) {

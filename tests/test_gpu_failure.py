@@ -1,8 +1,9 @@
 """Failure detection on the GPU without a fault: a bounded in-kernel wait that runs
 out.  The library's self-test kernel waits, with the attention kernels' own bounded
-wait, on a barrier that nothing arrives on; it must give up in well under a second,
-leave the timeout in the device error word for qps_device_status to report, and leave
-the context usable for the next decode."""
+wait, on a barrier that nothing arrives on; it must give up after one second of the
+GPU's global timer (the recorded duration pins the bound), leave the timeout in the
+device error word for qps_device_status to report, and leave the context usable for
+the next decode."""
 
 import time
 
@@ -29,10 +30,14 @@ def test_bounded_wait_gives_up_and_reports_timeout(qps):
     qps.device_status(reset=True)  # start from a clear error word
     t0 = time.perf_counter()
     qps.selftest_bounded_wait()
+    torch.cuda.synchronize()
+    rec = qps.device_wait_record()
     with pytest.raises(N.QpsError) as e:
         qps.device_status(reset=True)  # synchronous: waits for the self-test kernel
     assert e.value.status == N.QPS_ERR_TIMEOUT
+    assert rec[0] == 1 and 1.0e9 <= rec[12] < 1.2e9, rec  # the wait ran its full second, no more
     assert time.perf_counter() - t0 < 5.0
+    assert qps.device_wait_record() == [0] * 16  # the reset cleared the word and the record
     qps.device_status(reset=True)  # the reset cleared it
     # the context still computes: a small decode against the oracle
     cfg = synth.by_name("tiny").replace(n_kv=700, wc=700)

@@ -34,6 +34,7 @@ def test_workload_step_parity(qps, name):
     for _ in range(2):  # the second step reuses slots whose events belong to step one
         dec.step()
         torch.cuda.synchronize()
+        dec.ring.check_guards()  # nothing wrote outside a slot
         for layer, (q, k, v) in kept.items():
             ro, rl = helpers.oracle_layer(cfg, q, k, v)
             assert_parity(dec.o[layer].cpu().numpy(), dec.lse[layer].cpu().numpy(),
@@ -61,6 +62,8 @@ def test_step_edge_splits(qps, name, edge):
     for _ in range(2):
         dec.step()
         torch.cuda.synchronize()
+        if dec.ring is not None:
+            dec.ring.check_guards()
         for layer, (q, k, v) in kept.items():
             ro, rl = helpers.oracle_layer(cfg, q, k, v)
             assert_parity(dec.o[layer].cpu().numpy(), dec.lse[layer].cpu().numpy(),

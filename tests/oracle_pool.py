@@ -31,13 +31,14 @@ def _mem_available() -> int:
 
 
 def workers_for(bytes_per_layer: int, cap: int = 0) -> int:
-    """Worker count: the host's cores, bounded so that the workers' working sets (about
-    20 x one layer's fp16 K + V bytes each) stay within half of the available memory."""
+    """Worker count: the host's cores, bounded so that the workers' working sets (at most
+    about 10 x one layer's fp16 K + V bytes each: float64 copies of both plus the
+    encoders' float32 temporaries) stay within half of the available memory."""
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
         cores = os.cpu_count() or 1
-    by_mem = int(0.5 * _mem_available() // max(1, 20 * bytes_per_layer))
+    by_mem = int(0.5 * _mem_available() // max(1, 10 * bytes_per_layer))
     n = max(1, min(cores, by_mem))
     return min(n, cap) if cap > 0 else n
 

@@ -51,7 +51,7 @@ def test_step_edge_splits(qps, name, edge):
     (S1 -> S2 -> S3)", item S2): with wc = 0 every position is a tail tile and no layer
     has a device part; with wc = n_kv there are no tiles and no ring.  Both equal plain
     attention over every position."""
-    base = synth.parity_scaled(synth.by_name(name))
+    base = synth.parity_scaled(synth.by_name(name), layers=min(4, synth.by_name(name).layers))
     cfg = base.replace(wc=0 if edge == "no_window" else base.n_kv)
     dec, kept = helpers.build_split_decoder(cfg, keep_inputs=range(cfg.layers))
     assert (dec.ring is None) == (edge == "no_tail")

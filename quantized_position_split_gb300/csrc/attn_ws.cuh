@@ -175,9 +175,10 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
     const uint8_t* safe = reinterpret_cast<const uint8_t*>(p.k.data);
     const int bcoord = p.shared ? 0 : bz;
     int n_issued = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t % NS;
-      if (t >= NS && !mbar_wait(bar_empty + 8 * s, (uint32_t)(((t / NS) - 1) & 1))) {
+    int s = 0;         // stage of tile t: t mod NS
+    uint32_t ph = 0;   // its use: (t / NS) mod 2
+    for (int t = 0; t < ntiles; ++t, s = s + 1 == NS ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+      if (t >= NS && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) {
         give_up(t, n_issued);
         break;
       }
@@ -257,10 +258,11 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
         qb[kk][1] = ok ? *reinterpret_cast<const uint32_t*>(qrow + d0 + 2) : 0u;
       }
     }
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t % NS;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int t = 0; t < ntiles; ++t, s = s + 1 == NS ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
       if (aborted()) break;
-      if (!mbar_wait(bar_full + 8 * s, (uint32_t)((t / NS) & 1))) {
+      if (!mbar_wait(bar_full + 8 * s, ph)) {
         give_up(t, -1);
         break;
       }
@@ -306,9 +308,9 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
     const float cap = p.softcap;
     const float cap_k = cap > 0.f ? 2.f * LOG2E / cap : 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows 2c, 2c + 1 (log2 domain)
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t % NS;
-      const uint32_t par = (uint32_t)((t / NS) & 1);
+    int s = 0;
+    uint32_t par = 0;
+    for (int t = 0; t < ntiles; ++t, s = s + 1 == NS ? 0 : s + 1, par ^= s == 0 ? 1u : 0u) {
       if (aborted()) break;
       if (!mbar_wait(bar_sready + 8 * s, par)) {
         give_up(t, -3);
@@ -409,68 +411,60 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
                     offs[u] + 2 <= G::VA_OFF + G::PVA::BYTES,
                 p.err);
     }
-    bool stop = false;
-    for (int tp = 0; tp < ntiles && !stop; tp += KW) {
-#pragma unroll
-      for (int q = 0; q < KW; ++q) {  // (one softmax state: q = 0)
-        const int t = tp + q;
-        if (stop || t >= ntiles) break;
-        const int s = t % NS;
-        const uint32_t par = (uint32_t)((t / NS) & 1);
-        if (aborted()) {
-          stop = true;
-          break;
-        }
-        if (!mbar_wait(bar_pready + 8 * s, par)) {
-          give_up(t, -2);
-          stop = true;
-          break;
-        }
-        mbar_wait(bar_full + 8 * s, par);  // complete already: makes the tile's bytes visible here
-        __syncwarp();
-        const uint8_t* st = smem + s * W::STAGE;
-        const uint8_t* pbs = smem + W::PB_OFF + s * W::PB_BYTES;
-        const uint2 pb = reinterpret_cast<const uint2*>(pbs)[lane];
-        const float cr0 = reinterpret_cast<const float*>(pbs + 256)[2 * c];
-        const float cr1 = reinterpret_cast<const float*>(pbs + 256)[2 * c + 1];
-        if (__any_sync(ALL, cr0 != 1.f || cr1 != 1.f)) {
-#pragma unroll
-          for (int i = 0; i < MTV; ++i) {
-            o[q][i][0] *= cr0;
-            o[q][i][1] *= cr1;
-            o[q][i][2] *= cr0;
-            o[q][i][3] *= cr1;
-          }
-        }
-        uint32_t L[4], H[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          L[u] = *reinterpret_cast<const uint32_t*>(st + off2[u]);
-          H[u] = *reinterpret_cast<const uint16_t*>(st + offs[u]);
-        }
-        const uint32_t hab[2] = {H[0] | (H[1] << 16), H[2] | (H[3] << 16)};  // token a bits 0..15, b 16..31
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t ysel = h ? 0x7362u : 0x5140u;
-          const uint32_t y[2] = {__byte_perm(L[0], L[1], ysel), __byte_perm(L[2], L[3], ysel)};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int e0 = j + 8 * h, e1 = e0 + 4;
-            uint32_t a[4];
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-              const uint32_t sel = ((y[pr] >> (2 * j)) & 0x03030303u) * 0x22u + 0x10101010u;
-              const uint32_t mg0 = __byte_perm(tq_lo, tq_hi, sel);
-              const uint32_t mg1 = __byte_perm(tq_lo, tq_hi, sel >> 16);
-              a[2 * pr] = mg0 | (~(hab[pr] << (15 - e0)) & 0x80008000u);  // a clear sign bit: negative level
-              a[2 * pr + 1] = mg1 | (~(hab[pr] << (15 - e1)) & 0x80008000u);
-            }
-            mma16816(o[q][2 * j + h], a, pb.x, pb.y);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    static_assert(KW == 1, "one softmax state");
+    constexpr int q = 0;
+    int s = 0;
+    uint32_t par = 0;
+    for (int t = 0; t < ntiles; ++t, s = s + 1 == NS ? 0 : s + 1, par ^= s == 0 ? 1u : 0u) {
+      if (aborted()) break;
+      if (!mbar_wait(bar_pready + 8 * s, par)) {
+        give_up(t, -2);
+        break;
       }
+      mbar_wait(bar_full + 8 * s, par);  // complete already: makes the tile's bytes visible here
+      __syncwarp();
+      const uint8_t* st = smem + s * W::STAGE;
+      const uint8_t* pbs = smem + W::PB_OFF + s * W::PB_BYTES;
+      const uint2 pb = reinterpret_cast<const uint2*>(pbs)[lane];
+      const float cr0 = reinterpret_cast<const float*>(pbs + 256)[2 * c];
+      const float cr1 = reinterpret_cast<const float*>(pbs + 256)[2 * c + 1];
+      if (__any_sync(ALL, cr0 != 1.f || cr1 != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < MTV; ++i) {
+          o[q][i][0] *= cr0;
+          o[q][i][1] *= cr1;
+          o[q][i][2] *= cr0;
+          o[q][i][3] *= cr1;
+        }
+      }
+      uint32_t L[4], H[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        L[u] = *reinterpret_cast<const uint32_t*>(st + off2[u]);
+        H[u] = *reinterpret_cast<const uint16_t*>(st + offs[u]);
+      }
+      const uint32_t hab[2] = {H[0] | (H[1] << 16), H[2] | (H[3] << 16)};  // token a bits 0..15, b 16..31
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t ysel = h ? 0x7362u : 0x5140u;
+        const uint32_t y[2] = {__byte_perm(L[0], L[1], ysel), __byte_perm(L[2], L[3], ysel)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e0 = j + 8 * h, e1 = e0 + 4;
+          uint32_t a[4];
+#pragma unroll
+          for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t sel = ((y[pr] >> (2 * j)) & 0x03030303u) * 0x22u + 0x10101010u;
+            const uint32_t mg0 = __byte_perm(tq_lo, tq_hi, sel);
+            const uint32_t mg1 = __byte_perm(tq_lo, tq_hi, sel >> 16);
+            a[2 * pr] = mg0 | (~(hab[pr] << (15 - e0)) & 0x80008000u);  // a clear sign bit: negative level
+            a[2 * pr + 1] = mg1 | (~(hab[pr] << (15 - e1)) & 0x80008000u);
+          }
+          mma16816(o[q][2 * j + h], a, pb.x, pb.y);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
   }
 
@@ -503,38 +497,83 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
     if (r < nrows) orow[r] = out_row(r);
   }
   __syncthreads();
+  // Inverse rotation x = s1 .* blockdiag(H_G)(s2 .* y) / sqrt(D G).  Lane group g of
+  // V-warp v holds columns 128 v + 16 g + x (x = 0..15) of rows 2c and 2c + 1, so the
+  // butterflies of span 1..8 pair values of one lane, spans 16..64 pair lane groups (lane
+  // bits 2..4: shuffles) and spans 128, 256 pair V-warps (through shared memory).
   if (warp > W::S_WARP) {
+    float v[2][16];  // [row parity][x]
 #pragma unroll
     for (int i = 0; i < MTV; ++i) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int row = 2 * c + (e & 1);
         // m-tile i = 2 j + h holds columns j + 8 h (e < 2) and j + 8 h + 4 of the lane's 16
-        const int col = 128 * vw + 16 * g + ((i >> 1) & 3) + 8 * (i & 1) + 4 * (e >> 1);
+        const int x = ((i >> 1) & 3) + 8 * (i & 1) + 4 * (e >> 1);
+        const int row = 2 * c + (e & 1), col = 128 * vw + 16 * g + x;
         float acc = 0.f;
 #pragma unroll
         for (int q = 0; q < KW; ++q) acc += o[q][i][e] * wk[q * 8 + row];
         if ((p.vsigns2[col >> 5] >> (col & 31)) & 1u) acc = -acc;  // the rotation's second sign vector
-        fin[row * FS + ow_col<D>(col)] = acc;
+        v[e & 1][x] = acc;
       }
+    }
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {  // spans 1..8: inside the lane
+      if (h >= p.vblock) break;          // (uniform)
+#pragma unroll
+      for (int rp = 0; rp < 2; ++rp)
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          if (!(x & h)) {
+            const float a = v[rp][x], b = v[rp][x + h];
+            v[rp][x] = a + b;
+            v[rp][x + h] = a - b;
+          }
+    }
+#pragma unroll
+    for (int h = 16; h < 128; h <<= 1) {  // spans 16..64: lane groups g ^ (h / 16)
+      if (h >= p.vblock) break;
+      const int mask = 4 * (h / 16);
+      const bool upper = (lane & mask) != 0;
+#pragma unroll
+      for (int rp = 0; rp < 2; ++rp)
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const float other = __shfl_xor_sync(ALL, v[rp][x], mask, 32);
+          v[rp][x] = upper ? other - v[rp][x] : v[rp][x] + other;
+        }
+    }
+#pragma unroll
+    for (int rp = 0; rp < 2; ++rp)
+#pragma unroll
+      for (int x = 0; x < 16; ++x) fin[(2 * c + rp) * FS + ow_col<D>(128 * vw + 16 * g + x)] = v[rp][x];
+  }
+  // spans 128 and 256: the V-warps' column blocks v ^ 1 and v ^ 2, through shared memory
+  for (int h = 128; h < D; h <<= 1) {
+    if (h >= p.vblock) break;  // (uniform over the CTA)
+    __syncthreads();
+    float nv[2][16];
+    if (warp > W::S_WARP) {
+      const bool upper = (vw & (h / 128)) != 0;
+#pragma unroll
+      for (int rp = 0; rp < 2; ++rp)
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int col = 128 * vw + 16 * g + x;
+          const float mine = fin[(2 * c + rp) * FS + ow_col<D>(col)];
+          const float other = fin[(2 * c + rp) * FS + ow_col<D>(col ^ h)];
+          nv[rp][x] = upper ? other - mine : mine + other;
+        }
+    }
+    __syncthreads();
+    if (warp > W::S_WARP) {
+#pragma unroll
+      for (int rp = 0; rp < 2; ++rp)
+#pragma unroll
+        for (int x = 0; x < 16; ++x) fin[(2 * c + rp) * FS + ow_col<D>(128 * vw + 16 * g + x)] = nv[rp][x];
     }
   }
   __syncthreads();
-  // inverse rotation x = s1 .* blockdiag(H_G)(s2 .* y) / sqrt(D G), in place
-#pragma unroll
-  for (int lh = 0; (1 << lh) < D; ++lh) {
-    const int h = 1 << lh;
-    if (h >= p.vblock) break;  // (uniform over the CTA)
-    for (int pid = threadIdx.x; pid < 8 * (D / 2); pid += W::THREADS) {
-      const int r = pid / (D / 2), j = pid % (D / 2);
-      const int i = ((j >> lh) << (lh + 1)) | (j & (h - 1));
-      float* fr = fin + r * FS;
-      const float a = fr[ow_col<D>(i)], b = fr[ow_col<D>(i + h)];
-      fr[ow_col<D>(i)] = a + b;
-      fr[ow_col<D>(i + h)] = a - b;
-    }
-    __syncthreads();
-  }
   for (int idx = threadIdx.x; idx < nrows * D; idx += W::THREADS) {
     const int r = idx / D, dd = idx % D;
     const float den = rden[r];

@@ -8,11 +8,14 @@
 // rounding.  Parts with lse = -inf weigh nothing.
 //
 // Grid: one CTA per (output row, 32-column slice), so a step's few dozen rows still
-// spread over the SMs; its warps stride over the parts, U parts in flight per warp
-// (the rows' parts are independent, so the loads overlap), and lane L of a warp owns
-// column 32 * blockIdx.y + L, so each part's slice is one coalesced 128-byte read.
-// Every slice of a row merges the same lse values in the same order, so all of them
-// agree on the row's weights.
+// spread over the SMs; its warps (one per U parts, at most kCombineWarps: a combine of
+// few parts launches few warps) stride over the parts, U parts in flight per warp (the
+// rows' parts are independent, so the loads overlap), and lane L of a warp owns column
+// 32 * blockIdx.y + L, so each part's slice is one coalesced 128-byte read.  Every
+// slice of a row merges the same lse values in the same order, so all of them agree on
+// the row's weights.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace qps {
@@ -27,10 +30,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) lse_combine_kernel(
   constexpr int U = kCombineU;
   __shared__ float wm[kCombineWarps], wd[kCombineWarps], wacc[kCombineWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;  // warps of this launch (<= kCombineWarps)
   const int64_t row = blockIdx.x;
   const int col = blockIdx.y * 32 + lane;
   float m = -INFINITY, den = 0.f, acc = 0.f;
-  for (int t0 = warp * U; t0 < n_parts; t0 += kCombineWarps * U) {
+  for (int t0 = warp * U; t0 < n_parts; t0 += nw * U) {
     float lt[U], v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -60,12 +64,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) lse_combine_kernel(
   __syncthreads();
   if (warp != 0) return;
   float mx = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) mx = fmaxf(mx, wm[w]);
+  for (int w = 0; w < nw; ++w) mx = fmaxf(mx, wm[w]);
   float dt = 0.f, s = 0.f;
   if (mx != -INFINITY) {
-#pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       if (wm[w] == -INFINITY) continue;
       const float f = __expf(wm[w] - mx);
       dt += wd[w] * f;
@@ -87,7 +89,8 @@ qps_status launch_combine(const float* o_parts, const float* lse_parts, int n_pa
   if (d < 32 || d > 1024 || (d & (d - 1)))
     return fail(QPS_ERR_UNSUPPORTED, "lse_combine: head_dim must be 32, 64, 128, 256, 512 or 1024");
   const dim3 grid((unsigned)rows, (unsigned)(d / 32));
-  lse_combine_kernel<<<grid, kCombineWarps * 32, 0, s>>>(o_parts, lse_parts, n_parts, rows, d, o, lse, err);
+  const int warps = std::min(kCombineWarps, std::max(1, (n_parts + kCombineU - 1) / kCombineU));
+  lse_combine_kernel<<<grid, warps * 32, 0, s>>>(o_parts, lse_parts, n_parts, rows, d, o, lse, err);
   count_launch();
   QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;

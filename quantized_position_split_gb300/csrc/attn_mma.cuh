@@ -263,14 +263,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const TensorMap* map, 
       : "memory");
 }
 // One poll that suspends the warp (instead of spinning on issue slots) until the phase
-// completes or a hardware time limit passes.  The 1 ms hint is an upper bound only: on
-// GB300 one poll returns after about 4 us, so waits are bounded by the global timer.
+// completes or a system-dependent time limit passes; waits are bounded by the global
+// timer around it.  (With an explicit 1 ms suspend hint one poll returned after about
+// 4 us on GB300, and the windows ran 0.3-1.2% slower than with the default limit.)
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -706,6 +707,31 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
     } else if constexpr (KF == QPS_FMT_Q8_0) {
       const uint8_t* kc = st + G::K_OFF;
       const __half* ks = reinterpret_cast<const __half*>(st + G::KA_OFF) + ks_lane;
+      // at head_dim <= 128 a row's D / 32 block scales come in one 4- or 8-byte load
+      constexpr bool VEC_SCALES = (D == 64 || D == 128) && NTW <= 2;  // (three n-tiles leave no registers)
+      float scv[SUB][2][VEC_SCALES ? D / 32 : 1];
+      if constexpr (VEC_SCALES) {
+#pragma unroll
+        for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const __half* src = ks + (16 * sb + 8 * u) * (D / 32);
+            uint32_t w[2];
+            if constexpr (D == 128) {
+              const uint2 r = *reinterpret_cast<const uint2*>(src);
+              w[0] = r.x;
+              w[1] = r.y;
+            } else {
+              w[0] = w[1] = *reinterpret_cast<const uint32_t*>(src);
+            }
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[h]));
+              scv[sb][u][2 * h] = f.x;
+              scv[sb][u][2 * h + 1] = f.y;
+            }
+          }
+      }
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         const int x = 2 * j + (c >> 1), sub = 8 * (c & 1);
@@ -719,8 +745,14 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
           i8x4_to_h2x2(wg8.x, a0[1], a0[3]);
           i8x4_to_h2x2(wg.y, a1[0], a1[2]);
           i8x4_to_h2x2(wg8.y, a1[1], a1[3]);
-          const float sg = __half2float(ks[16 * sb * (D / 32) + j]);
-          const float sg8 = __half2float(ks[(16 * sb + 8) * (D / 32) + j]);
+          float sg, sg8;
+          if constexpr (VEC_SCALES) {
+            sg = scv[sb][0][j];
+            sg8 = scv[sb][1][j];
+          } else {
+            sg = __half2float(ks[16 * sb * (D / 32) + j]);
+            sg8 = __half2float(ks[(16 * sb + 8) * (D / 32) + j]);
+          }
 #pragma unroll
           for (int nt = 0; nt < NTW; ++nt) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};

@@ -64,10 +64,12 @@ struct WsGeo {
   static constexpr int FLAG_OFF = BAR_OFF + 32 * NS;
   static constexpr int KS_OFF = align_to(FLAG_OFF + 16, 16);  // the K-warps' final (max, sum) per row
   static constexpr int END = KS_OFF + 2 * KW * 8 * 4;
-  // the epilogue, over the stages once every tile is consumed: merged rows [8][FS]
-  // (padded like the per-warp kernel's merge), per-row weights, maximum, denominator
-  // and output row
-  static constexpr int FS = ow_stride<D>();
+  // the epilogue, over the stages once every tile is consumed: merged rows [8][FS],
+  // per-row weights, maximum, denominator and output row.  Column x of a row sits at
+  // x + x / 16 and rows are FS = 8 (mod 32) floats apart, so the V-warps' stores of
+  // (row 2c + rp, column 16 g + x) from the 32 lanes hit 32 distinct banks.
+  static constexpr int FS = D + D / 16 + 8;
+  static_assert(FS % 32 == 8, "row stride 8 mod 32 banks");
   static constexpr int FIN_OFF = 0;
   static constexpr int WK_OFF = FIN_OFF + 8 * FS * 4;
   static constexpr int RMX_OFF = WK_OFF + KW * 8 * 4;
@@ -273,6 +275,19 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
       const uint8_t* kc = st + G::K_OFF;
       const __half* ks = reinterpret_cast<const __half*>(st + G::KA_OFF) + ks_lane;
+      // this quarter's four block scales of tokens g and g + 8: one 8-byte load each
+      static_assert(KB == 4, "four q8_0 blocks per K-warp");
+      float sc[2][KB];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint2 s4 = *reinterpret_cast<const uint2*>(ks + u * 8 * (D / 32) + KB * kq);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&s4.x));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&s4.y));
+        sc[u][0] = f01.x;
+        sc[u][1] = f01.y;
+        sc[u][2] = f23.x;
+        sc[u][3] = f23.y;
+      }
 #pragma unroll
       for (int jj = 0; jj < KB; ++jj) {
         const int j = KB * kq + jj;
@@ -284,8 +299,7 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
         i8x4_to_h2x2(wg8.x, a0[1], a0[3]);
         i8x4_to_h2x2(wg.y, a1[0], a1[2]);
         i8x4_to_h2x2(wg8.y, a1[1], a1[3]);
-        const float sg = __half2float(ks[j]);
-        const float sg8 = __half2float(ks[8 * (D / 32) + j]);
+        const float sg = sc[0][jj], sg8 = sc[1][jj];
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816(acc, a0, qb[2 * jj][0], qb[2 * jj][1]);
         mma16816(acc, a1, qb[2 * jj + 1][0], qb[2 * jj + 1][1]);
@@ -474,7 +488,8 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
 
   // ---- epilogue: merge the K-warps' states, inverse rotation, the partial -------------
   constexpr int FS = W::FS;
-  float* fin = reinterpret_cast<float*>(smem + W::FIN_OFF);  // [8][FS], columns at ow_col
+  float* fin = reinterpret_cast<float*>(smem + W::FIN_OFF);  // [8][FS], column x at fcol(x)
+  auto fcol = [](int x) { return x + (x >> 4); };
   float* wk = reinterpret_cast<float*>(smem + W::WK_OFF);    // [KW][8] state weights
   float* rmx = reinterpret_cast<float*>(smem + W::RMX_OFF);
   float* rden = reinterpret_cast<float*>(smem + W::RDEN_OFF);
@@ -546,7 +561,7 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
 #pragma unroll
     for (int rp = 0; rp < 2; ++rp)
 #pragma unroll
-      for (int x = 0; x < 16; ++x) fin[(2 * c + rp) * FS + ow_col<D>(128 * vw + 16 * g + x)] = v[rp][x];
+      for (int x = 0; x < 16; ++x) fin[(2 * c + rp) * FS + fcol(128 * vw + 16 * g + x)] = v[rp][x];
   }
   // spans 128 and 256: the V-warps' column blocks v ^ 1 and v ^ 2, through shared memory
   for (int h = 128; h < D; h <<= 1) {
@@ -560,8 +575,8 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int col = 128 * vw + 16 * g + x;
-          const float mine = fin[(2 * c + rp) * FS + ow_col<D>(col)];
-          const float other = fin[(2 * c + rp) * FS + ow_col<D>(col ^ h)];
+          const float mine = fin[(2 * c + rp) * FS + fcol(col)];
+          const float other = fin[(2 * c + rp) * FS + fcol(col ^ h)];
           nv[rp][x] = upper ? other - mine : mine + other;
         }
     }
@@ -570,14 +585,14 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
 #pragma unroll
       for (int rp = 0; rp < 2; ++rp)
 #pragma unroll
-        for (int x = 0; x < 16; ++x) fin[(2 * c + rp) * FS + ow_col<D>(128 * vw + 16 * g + x)] = nv[rp][x];
+        for (int x = 0; x < 16; ++x) fin[(2 * c + rp) * FS + fcol(128 * vw + 16 * g + x)] = nv[rp][x];
     }
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < nrows * D; idx += W::THREADS) {
     const int r = idx / D, dd = idx % D;
     const float den = rden[r];
-    float val = fin[r * FS + ow_col<D>(dd)] * p.v_out_scale;
+    float val = fin[r * FS + fcol(dd)] * p.v_out_scale;
     if ((p.vsigns[dd >> 5] >> (dd & 31)) & 1u) val = -val;
     const int64_t row = orow[r];
     const bool empty = !(den > 0.f);

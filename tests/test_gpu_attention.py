@@ -32,10 +32,11 @@ def _inputs(n, hq, hkv, d, seed, outliers=True):
     return q, k.half(), v
 
 
-@pytest.mark.parametrize("n_parts,d", [(7, 128), (1, 32), (201, 512), (64, 1024)])
+@pytest.mark.parametrize("n_parts,d", [(7, 128), (1, 32), (10, 128), (38, 256), (201, 512), (64, 1024)])
 def test_lse_combine(qps, n_parts, d):
-    """Several part counts around the 64 parts a CTA has in flight, every head_dim slice
-    count, an empty part and a row whose parts are all empty."""
+    """Part counts that launch one, two, five and eight warps per CTA (one per eight
+    parts), eight of them striding over 201 parts, every head_dim slice count, an empty
+    part and a row whose parts are all empty."""
     g = torch.Generator().manual_seed(n_parts * 7 + d)
     o = torch.randn((n_parts, 33, d), generator=g)
     l = torch.randn((n_parts, 33), generator=g) * 5

@@ -1,5 +1,5 @@
 """The bounds-checked build (``libqps_checked.so``, QPS_CHECK_BOUNDS=1): the stand-in for
-a memory checker on a pool where compute-sanitizer is closed.
+a memory checker where compute-sanitizer cannot be run.
 
 Every kernel of that build tests each staged or addressed access (tensor-map boxes
 and zero-filling copies into a tile stage, the rows of a view, q, the partial and

@@ -470,8 +470,11 @@ typedef struct qps_layer_step {
 /* Run one decode step over n_layers layers on `stream` [RKV, RING]: begin the ring
  * step with `tiles` (the concatenation of every layer's tiles, in layer order; ring
  * may be NULL when no layer has tiles), then for each layer its device parts, its
- * tiles and its combine, then close the ring step.  Nothing waits for the device.
- * Errors: as the calls it makes. */
+ * tiles and its combine, then close the ring step.  A layer's first device part runs
+ * on `stream`; any further ones (e.g. the private suffixes beside a shared prefix) run
+ * on library-owned side streams forked from `stream` by an event and joined back to it
+ * before the layer's tiles, so independent parts overlap on the GPU.  Nothing waits for
+ * the device.  Errors: as the calls it makes. */
 QPS_API qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n_tiles,
                            const qps_layer_step* layers, int32_t n_layers, void* stream);
 

@@ -295,6 +295,39 @@ qps_status tail_attend(qps_ring* r, int idx, const qps_attn_args* a_in, cudaStre
   return QPS_OK;
 }
 
+// Side streams of the step runner: a layer with several device parts (the fan-out's
+// shared prefix and private suffixes) launches its first part on the step's stream and
+// the others on these, forked from and joined back to the step's stream by events.  The
+// parts read independent inputs and write disjoint partial slots, so they may overlap.
+// Created once per device and kept for the process; `m` serialises the fork / join
+// enqueues of concurrent callers (the events are re-recorded per layer).
+constexpr int kSideStreams = 3;
+struct SideStreams {
+  std::mutex m;
+  bool ok = false;
+  cudaStream_t st[kSideStreams] = {};
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join[kSideStreams] = {};
+};
+SideStreams* side_streams() {
+  static std::mutex mu;
+  static SideStreams* pools[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!pools[dev]) {
+    SideStreams* sp = new SideStreams();
+    cudaError_t e = cudaEventCreateWithFlags(&sp->fork, cudaEventDisableTiming);
+    for (int i = 0; i < kSideStreams && e == cudaSuccess; ++i) {
+      e = cudaStreamCreateWithFlags(&sp->st[i], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sp->join[i], cudaEventDisableTiming);
+    }
+    sp->ok = e == cudaSuccess;
+    pools[dev] = sp;
+  }
+  return pools[dev]->ok ? pools[dev] : nullptr;
+}
+
 qps_status ring_sync(qps_ring* r, int timeout_ms) {
   const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
   for (;;) {
@@ -662,6 +695,12 @@ qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n
       cudaError_t e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(L.part_events[0]), s);
       if (e != cudaSuccess) st = cuda_fail(e, "decode_step: cudaEventRecord");
     }
+    // the device parts: every one resolved first (its partial slots follow the previous
+    // part's), then the first launched on the step's stream and the others on side
+    // streams forked from it and joined back before the layer's tiles
+    std::vector<qps_attn_args> pa;
+    std::vector<AttnParams> pp;
+    std::vector<int> pn;
     for (int i = 0; i < L.n_device_parts && st == QPS_OK; ++i) {
       qps_attn_args a = L.device_parts[i];
       a.o_parts = L.o_parts;
@@ -677,8 +716,43 @@ qps_status qps_decode_step(qps_ring* ring, const qps_tile_desc* tiles, int32_t n
       }
       rows = p.rows_total;
       d = p.d;
-      st = run_attn(&a, p, n, s, L.parts_capacity);
+      pa.push_back(a);
+      pp.push_back(p);
+      pn.push_back(n);
       off += n;
+    }
+    if (st == QPS_OK && !pa.empty()) {
+      SideStreams* side = pa.size() > 1 ? side_streams() : nullptr;
+      std::unique_lock<std::mutex> lk;
+      int used = 0;  // side streams forked in this layer
+      if (side) {
+        lk = std::unique_lock<std::mutex>(side->m);
+        cudaError_t e = cudaEventRecord(side->fork, s);
+        if (e != cudaSuccess) st = cuda_fail(e, "decode_step: cudaEventRecord");
+      }
+      for (size_t i = 0; i < pa.size() && st == QPS_OK; ++i) {
+        cudaStream_t si = s;
+        if (side && i > 0) {
+          const int k = (int)((i - 1) % kSideStreams);
+          si = side->st[k];
+          if (k >= used) {
+            cudaError_t e = cudaStreamWaitEvent(si, side->fork, 0);
+            if (e != cudaSuccess) {
+              st = cuda_fail(e, "decode_step: cudaStreamWaitEvent");
+              break;
+            }
+            used = k + 1;
+          }
+        }
+        st = run_attn(&pa[i], pp[i], pn[i], si, L.parts_capacity);
+      }
+      // join every forked stream, also after an error, so that nothing enqueued on the
+      // step's stream afterwards can overtake a part still running beside it
+      for (int k = 0; k < used; ++k) {
+        cudaError_t e = cudaEventRecord(side->join[k], side->st[k]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->join[k], 0);
+        if (e != cudaSuccess && st == QPS_OK) st = cuda_fail(e, "decode_step: joining a side stream");
+      }
     }
     if (st == QPS_OK && L.part_events[1]) {
       cudaError_t e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(L.part_events[1]), s);

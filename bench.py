@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--auto-ring", action="store_true",
                     help="size the ring (slots, tile tokens) from the measured link and attention time "
                          "instead of the workload's fixed values")
+    ap.add_argument("--tile-tokens", type=int, default=0,
+                    help="positions per ring tile of the line's workload (0 = the workload's)")
     ap.add_argument("--n-split-window", type=int, default=0,
                     help="split count of the window launches (0 = the library's automatic choice)")
     ap.add_argument("--v-fmt", default="",
@@ -849,6 +851,8 @@ def run_ours(args):
         ring_plan = dict(rp, link_gbs=link, host_memcpy_gbs=host, bw_eff_gbs=bw_eff, attention_ms=att_ms,
                          slot_budget_bytes=slot_budget, tile_tokens=tile_tokens)
         cfg = cfg.replace(ring_slots=rp["n_slots"], tile_tokens=tile_tokens)
+    if args.tile_tokens > 0:
+        cfg = cfg.replace(tile_tokens=args.tile_tokens)
 
     link = measure_link(torch, device)
     stream = torch.cuda.current_stream()

@@ -95,7 +95,7 @@ CONFIGS = [
         v_fmt="f16",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=16384,
+        tile_tokens=32768,
     ),
     Workload(
         name="qwen14b_q8",
@@ -111,7 +111,7 @@ CONFIGS = [
         v_fmt="q8_0",
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=16384,
+        tile_tokens=32768,
     ),
     Workload(
         name="gemma_global_q8k_tq3v",
@@ -128,7 +128,7 @@ CONFIGS = [
         softcap=50.0,
         k_outliers=4,
         ring_slots=3,
-        tile_tokens=32768,
+        tile_tokens=131072,
     ),
     # the same Qwen-like stacks with a more compressed tail than window (the tail's own
     # K / V storage formats)

@@ -922,6 +922,23 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         n_g8[sb] = __half2float(nrm[16 * sb + g + 8]);
       }
     }
+    // The reference maximum of the online softmax is raised only when a tile's maximum
+    // exceeds it by more than `lazy` (log2 units): P then stays <= 2^lazy, the running
+    // sum and O carry the same reference, and the rescale of O (a multiply per
+    // accumulator) is skipped on most tiles.  A TurboQuant V folds its norms into the
+    // fp16 P, so there lazy is 8 only while the tile's norms stay <= 255 (P x norm stays
+    // finite in fp16), else 0 (P <= 1, the exact maximum).  Three n-tiles keep the exact
+    // maximum: there the test's registers made the kernel spill (4-token verify batch
+    // 64.5 -> 66.8 us).
+    float lazy = NTW >= 3 ? 0.f : 8.f;
+    if constexpr (is_tq(VF) && NTW < 3) {
+      float nmx = 0.f;
+#pragma unroll
+      for (int sb = 0; sb < SUB; ++sb) nmx = fmaxf(nmx, fmaxf(fabsf(n_g[sb]), fabsf(n_g8[sb])));
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) nmx = fmaxf(nmx, __shfl_xor_sync(0xffffffffu, nmx, off));
+      lazy = nmx <= 255.f ? 8.f : 0.f;
+    }
     uint32_t pb[SUB][NTW][2];
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt) {
@@ -957,7 +974,14 @@ __global__ void __launch_bounds__(Geo<D, KF, VF, NTW>::NW * 32, Geo<D, KF, VF, N
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
-      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+      float mn0, mn1;
+      if constexpr (NTW >= 3) {
+        mn0 = fmaxf(m[nt][0], mx0);
+        mn1 = fmaxf(m[nt][1], mx1);
+      } else {
+        mn0 = mx0 - m[nt][0] > lazy ? mx0 : m[nt][0];  // (NaN if both are -inf: keeps -inf)
+        mn1 = mx1 - m[nt][1] > lazy ? mx1 : m[nt][1];
+      }
       const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
       const float cr0 = exp2f(m[nt][0] - ms0), cr1 = exp2f(m[nt][1] - ms1);
       float sum0 = 0.f, sum1 = 0.f;

@@ -364,7 +364,14 @@ __global__ void __launch_bounds__(WsGeo<D, KF, VF>::THREADS, 2)
         mx0 = fmaxf(mx0, __shfl_xor_sync(ALL, mx0, off));
         mx1 = fmaxf(mx1, __shfl_xor_sync(ALL, mx1, off));
       }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // the reference maximum is raised only when the tile's exceeds it by more than 8
+      // (log2 units) while the tile's norms stay <= 255, so P x norm stays finite in
+      // fp16 (else by any amount): most tiles then need no rescale of O in the V-warps
+      float nmx = fmaxf(fabsf(ng), fabsf(ng8));
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) nmx = fmaxf(nmx, __shfl_xor_sync(ALL, nmx, off));
+      const float lazy = nmx <= 255.f ? 8.f : 0.f;
+      const float mn0 = mx0 - m0 > lazy ? mx0 : m0, mn1 = mx1 - m1 > lazy ? mx1 : m1;  // (both -inf: NaN, keeps m)
       const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
       const float cr0 = exp2f(m0 - ms0), cr1 = exp2f(m1 - ms1);
       const float p0 = exp2f(xv[0] - ms0), p1 = exp2f(xv[1] - ms1);

@@ -63,7 +63,8 @@ def parse_args(argv=None):
                     help="size the ring (slots, tile tokens) from the measured link and attention time "
                          "instead of the workload's fixed values")
     ap.add_argument("--tile-tokens", type=int, default=0,
-                    help="positions per ring tile of the line's workload (0 = the workload's)")
+                    help="positions per ring tile of the line's workload (0 = the workload's; "
+                         "--auto-ring sizes it instead)")
     ap.add_argument("--n-split-window", type=int, default=0,
                     help="split count of the window launches (0 = the library's automatic choice)")
     ap.add_argument("--v-fmt", default="",
@@ -178,6 +179,17 @@ def split_kv_bytes(cfg):
         n = min(cfg.tile_tokens, cfg.tail_len - a)
         tail += cfg.hkv * _pad16(n) * row(cfg.tk_fmt, cfg.tv_fmt)
     return window, tail * cfg.layers
+
+
+def line_workload(synth, args):
+    """The workload the line times, as both arms build it: ``--config`` cut to
+    ``--layers`` and with ``--tile-tokens`` positions per ring tile."""
+    cfg = synth.by_name(args.config)
+    if args.layers > 0:
+        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
+    if args.tile_tokens > 0:
+        cfg = cfg.replace(tile_tokens=args.tile_tokens)
+    return cfg
 
 
 def bench_config(cfg, args, ring_plan=None) -> dict:
@@ -300,9 +312,7 @@ def run_reference(args):
         return 0
     import synth
 
-    cfg = synth.by_name(args.config)
-    if args.layers > 0:
-        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
+    cfg = line_workload(synth, args)
     if cfg.kind != "split":
         print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the position-split "
                           "workloads only"}), flush=True)
@@ -830,9 +840,7 @@ def run_ours(args):
 
     qbuild.build()
     qps.device_status(reset=True)
-    cfg = synth.by_name(args.config)
-    if args.layers > 0:
-        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
+    cfg = line_workload(synth, args)
     if cfg.kind != "split":
         raise SystemExit("the benchmark line times a position-split workload (the fan-out is a sub-record)")
     ring_plan = None
@@ -851,8 +859,6 @@ def run_ours(args):
         ring_plan = dict(rp, link_gbs=link, host_memcpy_gbs=host, bw_eff_gbs=bw_eff, attention_ms=att_ms,
                          slot_budget_bytes=slot_budget, tile_tokens=tile_tokens)
         cfg = cfg.replace(ring_slots=rp["n_slots"], tile_tokens=tile_tokens)
-    if args.tile_tokens > 0:
-        cfg = cfg.replace(tile_tokens=args.tile_tokens)
 
     link = measure_link(torch, device)
     stream = torch.cuda.current_stream()

@@ -81,6 +81,20 @@ def test_both_arms_describe_the_workload_with_the_same_config():
     assert abs(w / 1e9 - 10.27) < 0.01 and abs(t / 1e9 - 3.42) < 0.01  # 48 layers x 8 heads x 272 B
 
 
+def test_both_arms_time_the_same_cut_of_the_workload():
+    import synth
+    for argv in ([], ["--layers", "3"], ["--tile-tokens", "4096"], ["--config", "qwen14b_f16", "--layers", "2",
+                                                                       "--tile-tokens", "16384"]):
+        ours = bench.line_workload(synth, bench.parse_args(argv))
+        ref = bench.line_workload(synth, bench.parse_args(argv + ["--impl", "reference"]))
+        assert ours == ref
+        args = bench.parse_args(argv)
+        assert bench.bench_config(ours, args) == bench.bench_config(ref, bench.parse_args(argv + ["--impl", "reference"]))
+    cut = bench.line_workload(synth, bench.parse_args(["--layers", "3", "--tile-tokens", "4096"]))
+    assert (cut.layers, cut.tile_tokens) == (3, 4096)
+    assert bench.line_workload(synth, bench.parse_args([])) == synth.by_name("qwen14b_q8")
+
+
 def test_oracle_sample_spans_the_stack():
     import synth
     assert bench.oracle_layers_for(synth.by_name("qwen14b_q8"), 0) == [0, 16, 31, 47]

@@ -585,23 +585,24 @@ def time_split_steps(torch, qps, dec, K, W, stream, world, device, gpu_id):
     win_ms = [ev[i][layer][0].elapsed_time(ev[i][layer][1]) for i in range(K) for layer in range(L)]
     per_step = [t0.elapsed_time(bounds[0])] + [bounds[i - 1].elapsed_time(bounds[i]) for i in range(1, K)]
 
-    # end to end through the public API with host buffers: q in, (o, lse) out each step
-    q_host = torch.empty_like(dec.q, device="cpu").pin_memory()
+    # end to end through the public API with host buffers: q in, (o, lse) out each step,
+    # moved by the library's SM copies between page-locked host memory and the device
+    arena, (q_host, o_host, lse_host) = host_buffers(qps, dec.q, dec.o, dec.lse)
     q_host.copy_(dec.q.cpu())
-    o_host = torch.empty_like(dec.o, device="cpu").pin_memory()
-    lse_host = torch.empty_like(dec.lse, device="cpu").pin_memory()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        dec.q.copy_(q_host, non_blocking=True)
+        qps.copy_host(dec.q, q_host, stream)
         dec.step(stream)
-        o_host.copy_(dec.o, non_blocking=True)
-        lse_host.copy_(dec.lse, non_blocking=True)
+        qps.copy_host(o_host, dec.o, stream)
+        qps.copy_host(lse_host, dec.lse, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     check_device(qps, "the end-to-end steps")
     e2e_ms = max_over_ranks(torch, e0.elapsed_time(e1) / K, world, device)
+    o_host, lse_host = o_host.clone(), lse_host.clone()
+    arena.close()
     if dec.ring is not None:
         dec.ring.sync()
     return {"step_ms": step_ms, "window_step_ms": window_step_ms, "win_launch_ms": statistics.mean(win_ms),
@@ -610,6 +611,13 @@ def time_split_steps(torch, qps, dec, K, W, stream, world, device, gpu_id):
             "h2d": q_host.numel() * q_host.element_size(),
             "d2h": o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size(),
             "o_host": o_host, "lse_host": lse_host}
+
+
+def host_buffers(qps, *like):
+    """Page-locked, device-mapped host tensors shaped like the given device tensors, in
+    one library host arena (returned with them; close it when done)."""
+    arena = qps.HostArena(sum(t.numel() * t.element_size() + 256 for t in like))
+    return arena, tuple(arena.take(t.shape, t.dtype) for t in like)
 
 
 def _copy_args(a):
@@ -758,19 +766,18 @@ def run_fanout(torch, qps, synth, cfg, args, device, stream, world, rank, gpu_id
     check_device(qps, "the timed fan-out steps")
     per_step = [a.elapsed_time(b) for a, b in ev]
     step_ms = max_over_ranks(torch, statistics.mean(per_step), world, device)
-    # end to end: q from pinned host memory in, (O, lse) out, every step
-    q_host = fd.q.cpu().pin_memory()
-    o_host = torch.empty_like(fd.o, device="cpu").pin_memory()
-    lse_host = torch.empty_like(fd.lse, device="cpu").pin_memory()
+    # end to end: q from page-locked host memory in, (O, lse) out, every step (SM copies)
+    arena, (q_host, o_host, lse_host) = host_buffers(qps, fd.q, fd.o, fd.lse)
+    q_host.copy_(fd.q.cpu())
     e2e = []
     for i in range(K):
         flush.fill_(i & 255)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        fd.q.copy_(q_host, non_blocking=True)
+        qps.copy_host(fd.q, q_host, stream)
         fd.step(stream)
-        o_host.copy_(fd.o, non_blocking=True)
-        lse_host.copy_(fd.lse, non_blocking=True)
+        qps.copy_host(o_host, fd.o, stream)
+        qps.copy_host(lse_host, fd.lse, stream)
         b.record(stream)
         e2e.append((a, b))
     torch.cuda.synchronize()

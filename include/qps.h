@@ -79,7 +79,7 @@
 extern "C" {
 #endif
 
-#define QPS_ABI_VERSION 6
+#define QPS_ABI_VERSION 7
 
 #if defined(__GNUC__)
 #define QPS_API __attribute__((visibility("default")))
@@ -321,6 +321,17 @@ QPS_API qps_status qps_host_alloc(size_t bytes, int32_t flags, void** out);
 /* Free memory from qps_host_alloc (NULL is a no-op); the pinned tail of [RKV]
  * "Storage layer".  Errors: CUDA. */
 QPS_API qps_status qps_host_free(void* p);
+
+/* Copy `bytes` between device memory and qps_host_alloc memory with SM loads and stores
+ * on `stream` (the ring's copy kernel; the copy engine is not used).  Exactly one of
+ * dst / src lies inside one qps_host_alloc allocation and is reached through its device
+ * mapping; the other is device memory.  Both 16-byte aligned; bytes == 0 is a no-op.
+ * For a decode loop's per-step query upload and output readback: on GB300 hosts the
+ * copy engine's transfers stall in bursts on some boxes (tens of ms) where SM loads of
+ * the same memory do not (see qps_ring_set_copy_mode).  No counterpart on the pages.
+ * Errors: INVALID_ARG (NULL, misaligned, neither or both in qps_host_alloc memory, or the
+ * host span leaving its allocation), CUDA. */
+QPS_API qps_status qps_copy_host(void* dst, const void* src, size_t bytes, void* stream);
 
 /* ---- Tail-prefetch ring [RING] ------------------------------------------------ */
 

@@ -39,6 +39,7 @@ __all__ = [
     "attn_decode_window",
     "lse_combine",
     "HostArena",
+    "copy_host",
     "Ring",
     "tile_desc",
     "StepPlan",
@@ -501,6 +502,22 @@ class HostArena:
             self.close()
         except Exception:
             pass
+
+
+def copy_host(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """``qps_copy_host``: copy ``src`` into ``dst`` (same byte size, contiguous) where one
+    is a CUDA tensor and the other a CPU tensor inside a ``HostArena`` (qps_host_alloc
+    memory), by SM loads and stores on ``stream`` instead of the copy engine."""
+    for t, what in ((dst, "dst"), (src, "src")):
+        if not t.is_contiguous():
+            raise QpsError(N.QPS_ERR_INVALID_ARG, f"copy_host: {what} must be contiguous")
+    if dst.is_cuda == src.is_cuda:
+        raise QpsError(N.QPS_ERR_INVALID_ARG, "copy_host: one of dst / src must be a CUDA tensor, the other host")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise QpsError(N.QPS_ERR_INVALID_ARG, "copy_host: dst and src differ in size")
+    N.check(lib().qps_copy_host(dst.data_ptr(), src.data_ptr(), nbytes, _stream(stream)))
+    return dst
 
 
 RING_COPY = {"engine": 0, "kernel": 1}  # QPS_RING_COPY_ENGINE / QPS_RING_COPY_KERNEL

@@ -146,6 +146,7 @@ SIGNATURES = [
     ("qps_lse_combine", c_int32, [c_void_p, c_void_p, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p]),
     ("qps_host_alloc", c_int32, [c_size_t, c_int32, POINTER(c_void_p)]),
     ("qps_host_free", c_int32, [c_void_p]),
+    ("qps_copy_host", c_int32, [c_void_p, c_void_p, c_size_t, c_void_p]),
     ("qps_ring_create", c_int32, [c_int32, c_size_t, c_int32, POINTER(c_void_p)]),
     ("qps_ring_destroy", c_int32, [c_void_p]),
     ("qps_ring_set_copy_mode", c_int32, [c_void_p, c_int32]),

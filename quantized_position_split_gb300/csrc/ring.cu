@@ -15,6 +15,7 @@
 // deadline; nothing here can block forever.
 #include <sys/mman.h>
 
+#include <algorithm>
 #include <chrono>
 #include <cstring>
 #include <mutex>
@@ -662,6 +663,36 @@ qps_status qps_ring_inject_fault(qps_ring* r, int32_t tile_index, int32_t mode, 
   r->fault_tile = mode == QPS_RING_FAULT_NONE ? -1 : tile_index;
   r->fault_mode = mode;
   r->fault_delay_ms = delay_ms;
+  return QPS_OK;
+}
+
+qps_status qps_copy_host(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return QPS_OK;
+  if (!dst || !src) return fail(QPS_ERR_INVALID_ARG, "copy_host: NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15)
+    return fail(QPS_ERR_INVALID_ARG, "copy_host: dst and src must be 16-byte aligned");
+  const char* src_dev = host_alloc_dev(src, bytes);
+  const char* dst_dev = host_alloc_dev(dst, bytes);
+  if ((src_dev != nullptr) == (dst_dev != nullptr))
+    return fail(QPS_ERR_INVALID_ARG,
+                "copy_host: exactly one of dst / src must lie (whole) inside qps_host_alloc memory");
+  uint8_t* d = dst_dev ? reinterpret_cast<uint8_t*>(const_cast<char*>(dst_dev)) : static_cast<uint8_t*>(dst);
+  const uint8_t* sp = src_dev ? reinterpret_cast<const uint8_t*>(src_dev) : static_cast<const uint8_t*>(src);
+  CopySegs cs{};
+  cs.n = 1;
+  cs.src[0] = reinterpret_cast<const uint4*>(sp);
+  cs.dst[0] = reinterpret_cast<uint4*>(d);
+  cs.n16[0] = bytes / 16;
+  cs.rem[0] = (uint32_t)(bytes % 16);
+  cs.slot_lo = d;
+  cs.slot_hi = d + bytes;
+  cs.err = QPS_CHECK_BOUNDS ? device_error_word() : nullptr;
+  // as many CTAs as the copy has 4-vector rounds of one CTA, at most the ring's 64
+  const size_t per_cta = (size_t)kCopyThreads * kCopyUnroll;
+  const int ctas = (int)std::min<size_t>(kCopyCtas, std::max<size_t>(1, (cs.n16[0] + per_cta - 1) / per_cta));
+  ring_copy_kernel<<<ctas, kCopyThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(cs);
+  count_launch();
+  QPS_CUDA_TRY(cudaGetLastError());
   return QPS_OK;
 }
 

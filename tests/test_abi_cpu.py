@@ -240,3 +240,17 @@ def test_every_declaration_cites_its_source_and_states_its_errors():
         cites = re.search(r"\[(RKV|RING|POLY|TSTAR)\b", comment) or "counterpart" in comment or '"F5 M' in comment
         assert cites, name
         assert "Errors" in comment or "Never fails" in comment, name
+
+
+def test_copy_host_argument_checks(lib):
+    """qps_copy_host rejects, before any device call, NULL or misaligned pointers and a
+    pair of which not exactly one lies in qps_host_alloc memory; zero bytes is a no-op."""
+    a = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(a) + 255) // 256 * 256
+    assert lib.qps_copy_host(None, base, 64, None) == N.QPS_ERR_INVALID_ARG
+    assert lib.qps_copy_host(base, None, 64, None) == N.QPS_ERR_INVALID_ARG
+    assert lib.qps_copy_host(base + 8, base + 1024, 64, None) == N.QPS_ERR_INVALID_ARG  # misaligned
+    # neither pointer lies in qps_host_alloc memory (ordinary host memory both)
+    assert lib.qps_copy_host(base, base + 1024, 64, None) == N.QPS_ERR_INVALID_ARG
+    assert "qps_host_alloc" in lib.qps_last_error().decode()
+    assert lib.qps_copy_host(base, base + 1024, 0, None) == N.QPS_OK

@@ -591,23 +591,26 @@ def time_split_steps(torch, qps, dec, K, W, stream, world, device, gpu_id):
     q_host.copy_(dec.q.cpu())
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_bounds = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e0.record(stream)
-    for _ in range(K):
+    for i in range(K):
         qps.copy_host(dec.q, q_host, stream)
         dec.step(stream)
         qps.copy_host(o_host, dec.o, stream)
         qps.copy_host(lse_host, dec.lse, stream)
+        e_bounds[i].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     check_device(qps, "the end-to-end steps")
     e2e_ms = max_over_ranks(torch, e0.elapsed_time(e1) / K, world, device)
+    e2e_per_step = [e0.elapsed_time(e_bounds[0])] + [e_bounds[i - 1].elapsed_time(e_bounds[i]) for i in range(1, K)]
     o_host, lse_host = o_host.clone(), lse_host.clone()
     arena.close()
     if dec.ring is not None:
         dec.ring.sync()
     return {"step_ms": step_ms, "window_step_ms": window_step_ms, "win_launch_ms": statistics.mean(win_ms),
             "win_launch_p50_ms": statistics.median(win_ms), "per_step": step_distribution(per_step),
-            "launches": launches, "clocks": clk, "e2e_ms": e2e_ms,
+            "launches": launches, "clocks": clk, "e2e_ms": e2e_ms, "e2e_per_step": step_distribution(e2e_per_step),
             "h2d": q_host.numel() * q_host.element_size(),
             "d2h": o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size(),
             "o_host": o_host, "lse_host": lse_host}
@@ -692,7 +695,8 @@ def split_record(torch, qps, synth, cfg, args, dec, m, link_gbs, host_memcpy_gbs
                    "link_probe_gbs": link_gbs, "host_memcpy_1thread_gbs": host_memcpy_gbs,
                    "steps_per_s": 1000.0 / m["step_ms"], "per_step": m["per_step"]}
     rec["e2e"] = {"value": whole_job_rate(world, kv_bytes, m["e2e_ms"]), "unit": UNIT,
-                  "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"], "ms_per_step": m["e2e_ms"]}
+                  "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"], "ms_per_step": m["e2e_ms"],
+                  "per_step": m["e2e_per_step"]}
     rec["gpu_launches"] = m["launches"]
     rec["clocks"] = m["clocks"]
     return rec

@@ -181,6 +181,10 @@ def split_kv_bytes(cfg):
     return window, tail * cfg.layers
 
 
+# host time the reference arm's oracle sample may take over a whole run (seconds)
+REFERENCE_BUDGET_S = 150.0
+
+
 def line_workload(synth, args):
     """The workload the line times, as both arms build it: ``--config`` cut to
     ``--layers`` and with ``--tile-tokens`` positions per ring tile."""
@@ -319,14 +323,22 @@ def run_reference(args):
         return 0
     steps = max(1, args.steps)
     layers = oracle_layers_for(cfg, args.cpu_layers)
-    for _ in range(max(0, min(args.warmup, 1))):
-        time_oracle(cfg, layers[:1])
+    # one untimed layer warms up and gives the wall time of a layer (inputs included);
+    # each step then takes as many of the sample layers, in turn, as keep the whole run
+    # near REFERENCE_BUDGET_S of host time
+    t_w = time.perf_counter()
+    time_oracle(cfg, layers[:1])
+    per_layer = max(time.perf_counter() - t_w, 1e-3)
+    per_step = max(1, min(len(layers), int(REFERENCE_BUDGET_S / steps / per_layer)))
     total_b, total_s = 0, 0.0
     sample = ""
-    for _ in range(steps):
-        b, s, sample, _ = time_oracle(cfg, layers)
+    for i in range(steps):
+        pick = [layers[(i * per_step + j) % len(layers)] for j in range(per_step)]
+        b, s, sample, _ = time_oracle(cfg, pick)
         total_b += b
         total_s += s
+    if per_step < len(layers):
+        sample += f" (each step {per_step} of the layers {layers} in turn)"
     value = total_b / total_s / 1e9
     out = {
         "impl": "reference",

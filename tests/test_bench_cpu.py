@@ -135,3 +135,17 @@ def test_reference_arm_line_carries_the_contract_keys(capsys, monkeypatch):
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == j["value"] and cb["cores"] >= 1 and cb["sample"]
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_keeps_its_host_time_bounded(capsys, monkeypatch):
+    """With a small budget each step samples fewer of the oracle layers, in turn."""
+    import json
+
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 1e-6)
+    monkeypatch.setattr(bench, "oracle_layers_for", lambda cfg, n: [0, 0, 0])
+    assert bench.main(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "0"]) == 0
+    j = json.loads([ln for ln in capsys.readouterr().out.splitlines() if ln.strip()][-1])
+    assert "each step 1 of the layers [0, 0, 0] in turn" in j["cpu_baseline"]["sample"]
+    assert j["value"] > 0 and j["steps"] == 2

@@ -121,6 +121,38 @@ def test_fanout_parity(qps):
     assert_parity(fd.o.cpu().numpy(), fd.lse.cpu().numpy(), ro.reshape(-1, cfg.d), rl.reshape(-1))
 
 
+@pytest.mark.parametrize("name", ["qwen14b_q8", "gemma_global_q8k_tq3v"])
+def test_layer_of_several_device_parts_on_side_streams(qps, name):
+    """A layer whose positions are cut into five device parts (ragged, one a single
+    position) runs its first part on the step's stream and the other four on the
+    library's three side streams (one reused); after the join the combine sees every
+    part.  Twice in a row, against the oracle over all positions."""
+    from quantized_position_split_gb300.decode import _parts_buffers
+    cfg = synth.parity_scaled(synth.by_name(name), layers=1)
+    q, k, v = helpers.layer_inputs(cfg, 0, "cuda")
+    signs = helpers.signs_for(cfg)
+    K = qps.encode_kv_head_major(cfg.k_fmt, k, signs)
+    V = qps.encode_kv_head_major(cfg.v_fmt, v, signs)
+    n = cfg.n_kv
+    cuts = [0, 500, 1201, 1202, 1900, n]
+    parts = [qps.attn_args(q, K, V, scale=cfg.scale, softcap=cfg.softcap, v_signs=signs, kv_begin=a, kv_end=b)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    cap = sum(qps.attn_plan(a)[0] for a in parts)
+    rows = cfg.batch * cfg.hq
+    o_parts, lse_parts = _parts_buffers(cap, rows, cfg.d, q.device)
+    o = torch.zeros((rows, cfg.d), dtype=torch.float32, device=q.device)
+    lse = torch.zeros((rows,), dtype=torch.float32, device=q.device)
+    plan = qps.StepPlan([dict(device_parts=parts, tail=None, n_tiles=0, o_parts=o_parts, lse_parts=lse_parts,
+                              o=o, lse=lse)])
+    ro, rl = helpers.oracle_layer(cfg, q, k, v)
+    for _ in range(2):
+        o.zero_()
+        plan.run()
+        torch.cuda.synchronize()
+        assert_parity(o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(rows, cfg.d), rl.reshape(rows), name)
+    qps.device_status(reset=True)
+
+
 def test_ring_depth_and_tile_invariance(qps):
     cfg = synth.parity_scaled(synth.by_name("qwen14b_q8"), layers=2)
     outs = {}

@@ -6,8 +6,8 @@ and zero-filling copies into a tile stage, the rows of a view, q, the partial an
 merged outputs, the ring copy kernel's writes into its slot) against its extent,
 skips a failing access and marks the device error word (QPS_ERR_INTERNAL).  The
 tensor-core window parity over every format pairing and head_dim, whole decode steps
-of three workloads and the ring's fault tests run under it in a child process: they
-must pass, and no check may fail.  The
+of three workloads, the ring's fault tests and the host copies run under it in a child
+process: they must pass, and no check may fail.  The
 checker's own report is exercised by its self-test, which guards a store one past a
 small shared array (the store is skipped; no access leaves the array)."""
 
@@ -33,12 +33,13 @@ def checked_lib():
 def test_parity_suites_pass_under_the_checked_build(checked_lib):
     env = dict(os.environ, QPS_LIB_VARIANT="checked")
     # every format pairing and head_dim of the tensor-core window, the split steps of three
-    # workloads (fp16, q8_0, the head_dim-512 q8_0-K / TQ3-V one), the ring under faults
+    # workloads (fp16, q8_0, the head_dim-512 q8_0-K / TQ3-V one), the ring under faults,
+    # the host copies by the ring's copy kernel
     steps = [f"tests/test_gpu_step.py::test_workload_step_parity[{n}]"
              for n in ("qwen14b_f16", "qwen14b_q8", "gemma_global_q8k_tq3v")]
     cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider",
            "tests/test_gpu_checked.py", "tests/test_gpu_attention.py::test_window_attention_formats",
-           *steps, "tests/test_gpu_ring_faults.py", "-k", "not token"]
+           *steps, "tests/test_gpu_ring_faults.py", "tests/test_gpu_copy_host.py", "-k", "not token"]
     res = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     tail = (res.stdout + res.stderr)[-4000:]
     assert res.returncode == 0, tail

@@ -48,7 +48,7 @@ class PositionSplitDecoder:
 
     def __init__(self, *, layers: int, batch: int, hq: int, hkv: int, d: int, n_kv: int, wc: int,
                  k_fmt: str, v_fmt: str, scale: float, softcap: float = 0.0, signs=None,
-                 ring_slots: int = 3, tile_tokens: int = 8192, n_split_window: int = 0,
+                 ring_slots: int = 3, tile_tokens: int = 0, n_split_window: int = 0,
                  n_split_tail: int = 0, device=None, host_alloc_flags: int = 2,
                  tail_k_fmt: Optional[str] = None, tail_v_fmt: Optional[str] = None,
                  ring_copy: str = "kernel", n_q: int = 1, causal: bool = True):
@@ -92,7 +92,10 @@ class PositionSplitDecoder:
         return self.n_kv - self.wc
 
     def tile_ranges(self):
-        t = self.tile_tokens
+        """The tail's ring tiles: ``tile_tokens`` positions each, or with 0 (the default)
+        one tile per layer's tail — every copy launch costs the link ~11 us, and on
+        GB300 one tile per layer ran the Qwen-like q8_0 step 3% faster than two."""
+        t = self.tile_tokens if self.tile_tokens > 0 else max(self.tail_len, 1)
         return [(a, min(a + t, self.tail_len)) for a in range(0, self.tail_len, t)]
 
     def _arena_bytes(self) -> int:

@@ -24,6 +24,14 @@ def test_tail_tiles_partition_the_tail(n_kv, wc, tile):
     assert all(b - a == tile for a, b in r[:-1])  # only the last tile is ragged
 
 
+@pytest.mark.parametrize("n_kv,wc", [(1000, 333), (1000, 0), (1000, 1000), (17, 16)])
+def test_default_tile_is_the_whole_tail_of_a_layer(n_kv, wc):
+    args = dict(layers=2, batch=1, hq=8, hkv=2, d=128, n_kv=n_kv, wc=wc, k_fmt="q8_0", v_fmt="q8_0",
+                scale=0.1, device="cpu")
+    dec = PositionSplitDecoder(**args)  # tile_tokens left at its default
+    assert dec.tile_ranges() == ([(0, n_kv - wc)] if n_kv > wc else [])
+
+
 def test_arena_holds_every_tiles_planes_256_aligned():
     dec = _dec(tail_k_fmt="q8_0", tail_v_fmt="tq2")
     want = 0

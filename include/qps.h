@@ -329,8 +329,8 @@ QPS_API qps_status qps_host_free(void* p);
  * For a decode loop's per-step query upload and output readback: on GB300 hosts the
  * copy engine's transfers stall in bursts on some boxes (tens of ms) where SM loads of
  * the same memory do not (see qps_ring_set_copy_mode).  No counterpart on the pages.
- * Errors: INVALID_ARG (NULL, misaligned, neither or both in qps_host_alloc memory, or the
- * host span leaving its allocation), CUDA. */
+ * Errors: INVALID_ARG (NULL, misaligned, neither or both in qps_host_alloc memory, the
+ * host span leaving its allocation, or the other side not device memory), CUDA. */
 QPS_API qps_status qps_copy_host(void* dst, const void* src, size_t bytes, void* stream);
 
 /* ---- Tail-prefetch ring [RING] ------------------------------------------------ */

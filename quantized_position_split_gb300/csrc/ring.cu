@@ -676,6 +676,15 @@ qps_status qps_copy_host(void* dst, const void* src, size_t bytes, void* stream)
   if ((src_dev != nullptr) == (dst_dev != nullptr))
     return fail(QPS_ERR_INVALID_ARG,
                 "copy_host: exactly one of dst / src must lie (whole) inside qps_host_alloc memory");
+  // the other side must be device memory: a plain host pointer there would be a wild
+  // address for the kernel
+  cudaPointerAttributes attr{};
+  const void* dev_side = src_dev ? dst : src;
+  if (cudaPointerGetAttributes(&attr, dev_side) != cudaSuccess ||
+      (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)) {
+    cudaGetLastError();  // clear a sticky error of the query itself
+    return fail(QPS_ERR_INVALID_ARG, "copy_host: the side not in qps_host_alloc memory must be device memory");
+  }
   uint8_t* d = dst_dev ? reinterpret_cast<uint8_t*>(const_cast<char*>(dst_dev)) : static_cast<uint8_t*>(dst);
   const uint8_t* sp = src_dev ? reinterpret_cast<const uint8_t*>(src_dev) : static_cast<const uint8_t*>(src);
   CopySegs cs{};

@@ -54,6 +54,10 @@ def test_typed_tensors_and_argument_errors(qps):
                 qps.copy_host(dst, src)
         with pytest.raises(N.QpsError):
             qps.copy_host(d[:20], h)
+        # ordinary (not qps_host_alloc) host memory as the device side is refused
+        plain = torch.empty((40, 128), dtype=torch.float32)
+        rc = qps.lib().qps_copy_host(plain.data_ptr(), h.data_ptr(), h.numel() * 4, None)
+        assert rc == N.QPS_ERR_INVALID_ARG
         # a host span that leaves its allocation is refused by the library
         lib = qps.lib()
         end = arena.ptr + arena.nbytes
